@@ -1,0 +1,370 @@
+"""Pins for the CPU oracle, checked against things other than the oracle itself:
+the values the pages print (E4M3 range +-448), the OCP format facts they cite,
+hand-worked roundings, a library codec (torch float8_e4m3fn), a second encoder
+written differently, closed forms, invariants and brute force on tiny inputs.
+CPU only."""
+import math
+import multiprocessing as mp
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _torch_decode_all():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    return codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def _torch_encode(x32):
+    """Library encode, valid for |x| <= 448 (torch does not saturate)."""
+    t = torch.from_numpy(np.ascontiguousarray(x32, np.float32))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _read_table(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            a, b = line.split()[:2]
+            rows.append((a, b))
+    return rows
+
+
+# ---------------------------------------------------------------- E4M3 codec
+
+def test_decode_landmarks_from_pages_and_spec():
+    for code, val in _read_table("e4m3_landmarks.txt"):
+        got = O.lib().oracle_e4m3_decode(int(code, 16))
+        if val == "nan":
+            assert math.isnan(got)
+        else:
+            assert got == float(val), code
+            assert math.copysign(1.0, got) == math.copysign(1.0, float(val))
+
+
+def test_decode_matches_library_codec_all_256():
+    ours = O.e4m3_decode(np.arange(256))
+    lib = _torch_decode_all()
+    nan = np.isnan(lib)
+    assert (np.isnan(ours) == nan).all()
+    assert (ours[~nan] == lib[~nan]).all()
+    assert (np.signbit(ours[~nan]) == np.signbit(lib[~nan])).all()
+    assert np.nanmax(ours) == 448.0 and np.nanmin(ours) == -448.0
+
+
+def test_encode_roundtrip_254_codes():
+    for c in range(256):
+        if c in (0x7F, 0xFF):
+            continue
+        v = O.lib().oracle_e4m3_decode(c)
+        assert O.e4m3_encode_scalar(v) == c, hex(c)
+        assert O.e4m3_encode_bits_scalar(v) == c, hex(c)
+
+
+def test_encode_hand_rounding():
+    for x, code in _read_table("e4m3_hand_rounding.txt"):
+        v = float(np.float32(float(x)))
+        assert O.e4m3_encode_scalar(v) == int(code, 16), x
+        assert O.e4m3_encode_bits_scalar(v) == int(code, 16), x
+
+
+def _band_check(args):
+    start, count = args
+    import oracle as O2
+    return O2.e4m3_cross_check(start, count)
+
+
+def test_encoders_agree_exhaustive_band():
+    """Encoder A (grid search) vs encoder B (bit fields) on every positive
+    binary32 in [2^-12, 512), where all the rounding decisions are, and on a
+    stride through everything else (both signs, NaNs skipped)."""
+    lo = np.float32(2.0 ** -12).view(np.uint32).item()
+    hi = np.float32(512.0).view(np.uint32).item()
+    chunk = 1 << 22
+    jobs = [(s, min(chunk, hi - s)) for s in range(lo, hi, chunk)]
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(min(8, os.cpu_count() or 1)) as pool:
+        res = pool.map(_band_check, jobs)
+    bad = sum(r[0] for r in res)
+    assert bad == 0, [r for r in res if r[0]][:3]
+    # everything else: 4096-pattern windows spread over all 2^32 patterns
+    for off in range(0, 1 << 32, 1 << 22):
+        b, first = O.e4m3_cross_check(off, 4096)
+        assert b == 0, hex(first)
+
+
+def test_encoder_matches_library_in_range():
+    """Against torch's float8_e4m3fn conversion for |x| <= 448: every E4M3
+    rounding midpoint and its +-3 ulp neighbours, plus a dense random sample."""
+    grid = O.e4m3_decode(np.arange(0, 127))
+    mids = ((grid[:-1] + grid[1:]) / 2).astype(np.float32)  # exact in binary32
+    assert (mids.astype(np.float64) == (grid[:-1] + grid[1:]) / 2).all()
+    bits = mids.view(np.uint32).astype(np.int64)
+    near = (bits[:, None] + np.arange(-3, 4)[None, :]).reshape(-1).astype(np.uint32)
+    rng = np.random.default_rng(0)
+    rand = (rng.standard_normal(2_000_000) * rng.choice([1e-3, 1e-1, 1, 30, 200], 2_000_000))
+    x = np.concatenate([near.view(np.float32), rand.astype(np.float32), grid.astype(np.float32)])
+    x = np.concatenate([x, -x])
+    x = x[np.abs(x) <= 448]
+    assert (O.e4m3_encode(x) == _torch_encode(x)).all()
+
+
+def test_encode_monotone_and_saturating():
+    x = np.sort(np.random.default_rng(1).uniform(-600, 600, 500_000).astype(np.float32))
+    v = O.e4m3_decode(O.e4m3_encode(x))
+    assert (np.diff(v) >= 0).all()
+    assert v.max() == 448 and v.min() == -448
+    assert (O.e4m3_encode(np.array([np.inf, -np.inf], np.float32)) == [0x7E, 0xFE]).all()
+
+
+# ------------------------------------------------------------------- scales
+
+def test_scale_closed_forms():
+    assert O.scale_from_amax(448.0) == 1.0
+    assert O.scale_from_amax(896.0) == 2.0
+    assert O.scale_from_amax(0.0) == 1.0
+    assert O.scale_from_amax(3.5) == np.float32(3.5) / np.float32(448.0)
+    amax = np.abs(np.random.default_rng(2).standard_normal(10000)).astype(np.float32) * 100
+    s = np.array([O.scale_from_amax(a) for a in amax], np.float32)
+    back = (s.astype(np.float64) * 448.0)
+    ulp = np.spacing(amax).astype(np.float64)
+    assert (np.abs(back - amax) <= ulp).all()
+
+
+# --------------------------------------------------------------- quantizers
+
+def _bf16(x):
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _f32(bits):
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def _library_quantize(xbits, br, bc):
+    """The quantizer restated with library routines only: numpy for amax and
+    the binary32 division, torch float8_e4m3fn for the rounding (after the
+    saturation the pages' range implies)."""
+    x = _f32(xbits)
+    rows, cols = x.shape
+    nbr, nbc = -(-rows // br), -(-cols // bc)
+    q = np.zeros((rows, cols), np.uint8)
+    s = np.zeros((nbr, nbc), np.float32)
+    for bi in range(nbr):
+        for bj in range(nbc):
+            blk = x[bi * br:(bi + 1) * br, bj * bc:(bj + 1) * bc]
+            amax = np.float32(np.abs(blk).max()) if blk.size else np.float32(0)
+            sc = np.float32(1) if amax == 0 else np.float32(amax / np.float32(448))
+            s[bi, bj] = sc
+            t = (blk / sc).astype(np.float32)
+            t = np.clip(t, -448, 448)
+            q[bi * br:(bi + 1) * br, bj * bc:(bj + 1) * bc] = _torch_encode(t).reshape(blk.shape)
+    return q, s
+
+
+@pytest.mark.parametrize("shape,br,bc", [((256, 384), 128, 128), ((200, 300), 128, 128),
+                                          ((7, 333), 1, 128), ((1, 1000), 1, 1000),
+                                          ((130, 129), 128, 128), ((0, 5), 1, 128)])
+def test_quantizer_matches_library_restatement(shape, br, bc):
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal(shape).astype(np.float32)
+    if x.size:
+        x.reshape(-1)[rng.choice(x.size, max(1, x.size // 1000), replace=False)] *= 50
+    xb = _bf16(x)
+    q, s = O.quantize_blocks(xb, br, bc)
+    q2, s2 = _library_quantize(xb, br, bc)
+    assert (s == s2).all()
+    assert (q == q2).all()
+
+
+def test_hand_blocks_scale_one_and_two():
+    rng = np.random.default_rng(4)
+    w = rng.uniform(-400, 400, (128, 256)).astype(np.float32)
+    w[5, 7] = 448.0     # block 0: amax 448 -> S = 1, q = enc(x)
+    w[9, 200] = -896.0  # block 1: amax 896 -> S = 2, q = enc(x / 2) (exact halves)
+    wb = _bf16(w)
+    q, s = O.quantize_weight_blockwise(wb)
+    assert s.tolist() == [[1.0, 2.0]]
+    x = _f32(wb)
+    assert (q[:, :128] == _torch_encode(x[:, :128])).all()
+    assert (q[:, 128:] == _torch_encode(x[:, 128:] / 2)).all()
+    assert q[5, 7] == 0x7E and q[9, 200] == 0xFE
+
+
+def test_all_zero_block_and_signed_zero():
+    x = np.zeros((128, 128), np.float32)
+    x[3, :] = -0.0
+    q, s = O.quantize_weight_blockwise(_bf16(x))
+    assert s.tolist() == [[1.0]]
+    assert (q[3] == 0x80).all() and (np.delete(q, 3, axis=0) == 0).all()
+
+
+def test_quantizer_invariants():
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal((64, 1024)) * rng.choice([1e-3, 1, 40], (64, 1))).astype(np.float32)
+    xb = _bf16(x)
+    xf = _f32(xb)
+    q, s = O.quantize_act_per_token_group(xb)
+    dec = O.e4m3_decode(q)
+    for i in range(64):
+        for g in range(8):
+            cq = q[i, g * 128:(g + 1) * 128]
+            assert (cq == 0x7E).any() or (cq == 0xFE).any()  # the amax element hits 448
+            xs = xf[i, g * 128:(g + 1) * 128]
+            order = np.argsort(xs, kind="stable")
+            assert (np.diff(dec[i, g * 128:(g + 1) * 128][order]) >= 0).all()  # monotone
+            # rounding error at most half an E4M3 spacing (relative 2^-4) of x/S,
+            # or half the subnormal quantum 2^-10, plus binary32 division slack
+            t = xs.astype(np.float64) / s[i, g]
+            err = np.abs(dec[i, g * 128:(g + 1) * 128] - t)
+            bound = np.maximum(np.abs(t) * 2.0 ** -4, 2.0 ** -10) * (1 + 2.0 ** -20)
+            assert (err <= bound).all()
+
+
+def test_gather_commutes_with_per_token_quant():
+    rng = np.random.default_rng(6)
+    xb = _bf16(rng.standard_normal((50, 384)))
+    idx = rng.integers(0, 50, 120)
+    q1, s1 = O.quantize_act_per_token_group(xb)
+    q2, s2 = O.quantize_act_per_token_group(xb[idx])
+    assert (q1[idx] == q2).all() and (s1[idx] == s2).all()
+
+
+def test_kv_is_one_group_and_amax_matches_numpy():
+    rng = np.random.default_rng(7)
+    x = (rng.standard_normal((2, 64, 8, 128)) * np.exp(0.5 * rng.standard_normal((8, 128)))).astype(np.float32)
+    xb = _bf16(x)
+    q, scale, amax = O.kv_amax_quantize(xb)
+    assert amax == np.abs(_f32(xb)).max()
+    assert scale == np.float32(amax) / np.float32(448)
+    q2, s2 = _library_quantize(xb.reshape(1, -1), 1, xb.size)
+    assert (q.reshape(1, -1) == q2).all() and s2[0, 0] == scale
+    assert (O.quantize_with_scale(xb, scale) == q).all()
+
+
+# -------------------------------------------------------------------- GEMMs
+
+def _rand_q(rng, m, k, scale_range=(1e-3, 1e-1)):
+    xq = rng.integers(0, 256, (m, k), dtype=np.uint8)
+    xq[(xq & 0x7F) == 0x7F] = 0x7E  # no NaN codes
+    return xq
+
+
+def _dequant_numpy(q, s, br, bc):
+    """Dequantize with the library codec and numpy broadcasting."""
+    vals = torch.from_numpy(q).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    full = np.repeat(np.repeat(s.astype(np.float64), br, 0), bc, 1)[:q.shape[0], :q.shape[1]]
+    return vals * full
+
+
+@pytest.mark.parametrize("m,n,k", [(1, 16, 128), (3, 130, 256), (64, 256, 512), (17, 48, 384)])
+def test_gemm_matches_fp64_brute_force(m, n, k):
+    rng = np.random.default_rng(m * 1000 + n)
+    xq, wq = _rand_q(rng, m, k), _rand_q(rng, n, k)
+    xs = rng.uniform(1e-3, 1e-1, (m, k // 128)).astype(np.float32)
+    ws = rng.uniform(1e-4, 1e-2, (-(-n // 128), k // 128)).astype(np.float32)
+    y, absref = O.block_gemm(xq, xs, wq, ws)
+    a = _dequant_numpy(xq, xs, 1, 128)
+    b = _dequant_numpy(wq, ws, 128, 128)
+    yb = a @ b.T
+    ab = np.abs(a) @ np.abs(b).T
+    assert np.allclose(absref, ab, rtol=1e-12, atol=0)
+    assert (np.abs(y - yb) <= 1e-12 * ab + 1e-300).all()
+
+
+def test_gemm_integer_case_is_exact():
+    rng = np.random.default_rng(8)
+    ints = np.arange(-8, 9)
+    codes = O.e4m3_encode(ints.astype(np.float32))
+    xi = rng.integers(0, len(ints), (9, 256))
+    wi = rng.integers(0, len(ints), (20, 256))
+    y, _ = O.block_gemm(codes[xi], np.ones((9, 2), np.float32), codes[wi], np.ones((1, 2), np.float32))
+    exact = ints[xi].astype(np.int64) @ ints[wi].astype(np.int64).T
+    assert (y == exact).all()
+
+
+def test_gemm_single_slab_and_power_of_two_scaling():
+    rng = np.random.default_rng(9)
+    xq, wq = _rand_q(rng, 4, 128), _rand_q(rng, 8, 128)
+    xs = np.array([[0.5], [0.25], [3.0], [1.0]], np.float32)
+    ws = np.array([[0.125]], np.float32)
+    y, _ = O.block_gemm(xq, xs, wq, ws)
+    dx = torch.from_numpy(xq).view(torch.float8_e4m3fn).double().numpy()
+    dw = torch.from_numpy(wq).view(torch.float8_e4m3fn).double().numpy()
+    assert (y == (dx @ dw.T) * xs.astype(np.float64) * 0.125).all()
+    y2, _ = O.block_gemm(xq, xs, wq, ws * np.float32(8))
+    assert (y2 == y * 8).all()
+
+
+def test_gemm_sensitivity_to_plausible_mistakes():
+    """A transposed scale grid or a dropped slab must move the result by far
+    more than the tolerance the GPU is held to."""
+    rng = np.random.default_rng(10)
+    m, n, k = 8, 256, 384
+    xq, wq = _rand_q(rng, m, k), _rand_q(rng, n, k)
+    xs = rng.uniform(1e-3, 1e-1, (m, 3)).astype(np.float32)
+    ws = rng.uniform(1e-4, 1e-2, (2, 3)).astype(np.float32)
+    y, absref = O.block_gemm(xq, xs, wq, ws)
+    tol = 1e-3 * absref
+    ws_wrong = ws[::-1].copy()
+    yw, _ = O.block_gemm(xq, xs, wq, ws_wrong)
+    assert (np.abs(yw - y) > tol).mean() > 0.5
+    xs_drop = xs.copy()
+    xs_drop[:, 1] = 0
+    yd, _ = O.block_gemm(xq, xs_drop, wq, ws)
+    assert (np.abs(yd - y) > tol).mean() > 0.5
+
+
+def test_gemm_entries_and_f32_variant():
+    rng = np.random.default_rng(11)
+    m, n, k = 12, 160, 512
+    xq, wq = _rand_q(rng, m, k), _rand_q(rng, n, k)
+    xs = rng.uniform(1e-3, 1e-1, (m, 4)).astype(np.float32)
+    ws = rng.uniform(1e-4, 1e-2, (2, 4)).astype(np.float32)
+    y, absref = O.block_gemm(xq, xs, wq, ws)
+    ii = rng.integers(0, m, 50)
+    jj = rng.integers(0, n, 50)
+    ye, ae = O.block_gemm_entries(xq, xs, wq, ws, ii, jj)
+    assert (ye == y[ii, jj]).all() and (ae == absref[ii, jj]).all()
+    y32 = O.block_gemm_f32acc(xq, xs, wq, ws)
+    assert (np.abs(y32 - y) <= 1e-5 * absref).all()
+
+
+def test_grouped_gemm_reduces_to_dense():
+    rng = np.random.default_rng(12)
+    g, n, k, rows = 5, 144, 256, 40
+    xq = _rand_q(rng, rows, k)
+    xs = rng.uniform(1e-3, 1e-1, (rows, 2)).astype(np.float32)
+    wq = np.stack([_rand_q(rng, n, k) for _ in range(g)])
+    ws = rng.uniform(1e-4, 1e-2, (g, 2, 2)).astype(np.float32)
+    off = np.array([0, 7, 7, 30, 61, 90], np.int32)  # includes an empty group
+    row_idx = rng.integers(0, rows, 90).astype(np.int32)
+    y, a = O.grouped_gemm(xq, xs, row_idx, off, wq, ws)
+    for e in range(g):
+        r0, r1 = off[e], off[e + 1]
+        yd, ad = O.block_gemm(xq[row_idx[r0:r1]], xs[row_idx[r0:r1]], wq[e], ws[e])
+        assert (y[r0:r1] == yd).all() and (a[r0:r1] == ad).all()
+    # one group with the identity gather is the dense GEMM
+    y1, _ = O.grouped_gemm(xq, xs, None, np.array([0, rows], np.int32), wq[:1], ws[:1])
+    yd, _ = O.block_gemm(xq, xs, wq[0], ws[0])
+    assert (y1 == yd).all()
+
+
+def test_bf16_rounding_matches_library_on_binary32_values():
+    rng = np.random.default_rng(13)
+    x = (rng.standard_normal(200000) * rng.choice([1e-30, 1e-3, 1, 1e4], 200000)).astype(np.float32)
+    # include exact BF16 ties
+    ties = ((rng.integers(0, 1 << 16, 1000).astype(np.uint32) << 16) | 0x8000).view(np.float32)
+    x = np.concatenate([x, ties[np.isfinite(ties)]])
+    ours = O.bf16_from_f64(x.astype(np.float64))
+    lib = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert (ours == lib).all()
