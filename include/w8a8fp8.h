@@ -1,0 +1,212 @@
+/*
+ * w8a8fp8.h -- C ABI of the GB300 (sm_103a) FP8 W8A8 hot path.
+ *
+ * What the calls compute is fixed by these pages (title, then section/table):
+ *   [FP8-RL] "FP8-RL: A Practical and Stable Low-Precision Stack for LLM
+ *            Reinforcement Learning" (dcwnkz.com write-up), section 1 "dynamic
+ *            weight sync" (E4M3 over [-448, 448]; weights re-quantized in
+ *            128x128 blocks after every trainer update; activations quantized
+ *            dynamically) and section 4 "KV cache" (per-step scale
+ *            recalibration); the arXiv abstract on shd-paper.top, items (i)
+ *            and (ii).
+ *   [UFP8]   "Unified FP8: Moving Beyond Mixed Precision for Stable and
+ *            Accelerated MoE RL" (papercache.org notes), quick-read section:
+ *            S = max|X| / V_max and Q(x) = round(x / S); section "FP8 scale
+ *            choice": FP32 scales rather than E8M0.
+ *   [NeMo]   NeMo RL FP8 blog (nvidia.csdn.net), Table 1 (weights [128,128],
+ *            input activations [1,128], FP32 block scales) and Table 3
+ *            (per-tensor FP32 scales for QKV activations and the KV cache).
+ *
+ * Conventions for every call:
+ *   - Pointers are DEVICE pointers unless marked "host".  The library never
+ *     allocates, frees or retains memory: every buffer belongs to the caller
+ *     and must stay valid until the work queued on `stream` has finished.
+ *   - Matrices are contiguous and row-major.  BF16 data is passed as raw
+ *     16-bit words (uint16_t), E4M3 codes as bytes (uint8_t).
+ *   - Every call is asynchronous on `stream` (0 = the legacy default stream)
+ *     and never synchronizes the host.
+ *   - Arguments are validated on the host before anything is queued; a
+ *     failed check returns a nonzero status and queues nothing.  A launch
+ *     failure is reported as W8A8_ERR_CUDA (from cudaGetLastError).
+ *   - Non-finite inputs are outside the contract.
+ *   - Quantization: S = RN32(amax / 448) (S = 1 when amax = 0), and
+ *     q = E4M3(RN32(x / S)) with round-to-nearest-even and saturation to
+ *     +-448; signed zero keeps its sign.  Results are bit-exact with this
+ *     definition.
+ */
+#ifndef W8A8FP8_H
+#define W8A8FP8_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA runtime stream handle (same type as cudaStream_t). */
+typedef struct CUstream_st *w8a8_stream_t;
+
+typedef enum {
+    W8A8_OK = 0,
+    W8A8_ERR_NULL = 1,        /* a required pointer is NULL */
+    W8A8_ERR_SHAPE = 2,       /* a size is negative or breaks a stated rule */
+    W8A8_ERR_ALIGN = 3,       /* a pointer is not aligned as stated */
+    W8A8_ERR_UNSUPPORTED = 4, /* valid request this build does not serve */
+    W8A8_ERR_CUDA = 5         /* the CUDA runtime reported an error */
+} w8a8_status;
+
+/* Static, NUL-terminated description of a status code (host). */
+const char *w8a8_status_string(w8a8_status status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int w8a8_version(void);
+
+/* Text of the last CUDA runtime error seen by any call in this process
+ * (host, static storage; "" if none).  Diagnostic only. */
+const char *w8a8_last_cuda_error(void);
+
+/* Reads and clears the device-side error code the GEMM kernels set when a
+ * bounded wait inside them gives up (0 = none; nonzero identifies the wait).
+ * Such a kernel stops early and leaves its output incomplete.  Synchronous:
+ * blocks until the device has finished prior work on the legacy stream. */
+w8a8_status w8a8_consume_device_error(int *code);
+
+/* ------------------------------------------------------------------------
+ * E4M3 codec ([UFP8] "FP8 data formats", referring to the OCP FP8 spec;
+ * [FP8-RL] section 1 range +-448).
+ *
+ * e4m3_encode_f32: q[i] = E4M3(x[i]), round to nearest even, |x| > 448
+ *   saturates to +-448.  x: n floats; q: n bytes.
+ * e4m3_decode_f32: x[i] = exact value of code q[i] (0x7F/0xFF give NaN).
+ * Both: n >= 0; x and q 16-byte aligned.
+ * ---------------------------------------------------------------------- */
+w8a8_status e4m3_encode_f32(const float *x, int64_t n, uint8_t *q,
+                            w8a8_stream_t stream);
+w8a8_status e4m3_decode_f32(const uint8_t *q, int64_t n, float *x,
+                            w8a8_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * quantize_weight_blockwise -- [FP8-RL] section 1 (128x128 blocks, each with
+ * its own scale); [NeMo] Table 1 row "weights"; [UFP8] scale and
+ * quantization equations.
+ *
+ *   w_bf16  [n, k] BF16 weights.
+ *   wq      [n, k] E4M3 codes (out).
+ *   ws      [ceil(n/128), ceil(k/128)] FP32 block scales (out), row-major.
+ * Edge blocks that overhang the matrix use their in-bounds elements only.
+ * n, k >= 0.  w_bf16 and wq 16-byte aligned, ws 4-byte aligned.
+ * ---------------------------------------------------------------------- */
+w8a8_status quantize_weight_blockwise(const uint16_t *w_bf16, int64_t n,
+                                      int64_t k, uint8_t *wq, float *ws,
+                                      w8a8_stream_t stream);
+
+/* One matrix of a batched weight quantization (all pointers device). */
+typedef struct {
+    const uint16_t *w_bf16; /* [n, k] */
+    uint8_t *wq;            /* [n, k] */
+    float *ws;              /* [ceil(n/128), ceil(k/128)] */
+    int64_t n;
+    int64_t k;
+} w8a8_weight_desc;
+
+/* quantize_weight_blockwise over `count` matrices in as few launches as the
+ * kernel-parameter space allows (the whole-model weight sync of [FP8-RL]
+ * section 1 is one call).  descs is a HOST array, read before the call
+ * returns.  Each entry obeys the rules of quantize_weight_blockwise.
+ * count >= 0. */
+w8a8_status quantize_weight_blockwise_batched(const w8a8_weight_desc *descs,
+                                              int32_t count,
+                                              w8a8_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * quantize_act_per_token_group -- [NeMo] Table 1 row "input activations"
+ * ([1,128] groups, FP32 scales); [UFP8] quick-read section (per-token
+ * activation quantization) and its scale/quantization equations; [FP8-RL]
+ * section 1 (activations quantized dynamically at inference).
+ *
+ *   x_bf16  [m, k] BF16 activations.
+ *   xq      [m, k] E4M3 codes (out).
+ *   xs      [m, ceil(k/128)] FP32 group scales (out), row-major.
+ * The last group of a row may be shorter than 128.  m, k >= 0.  x_bf16 and
+ * xq 16-byte aligned, xs 4-byte aligned.
+ * ---------------------------------------------------------------------- */
+w8a8_status quantize_act_per_token_group(const uint16_t *x_bf16, int64_t m,
+                                         int64_t k, uint8_t *xq, float *xs,
+                                         w8a8_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * fp8_block_gemm -- the W8A8 linear of [FP8-RL] section 1 / arXiv abstract
+ * item (i) with the [NeMo] Table 1 granularities:
+ *
+ *   y[i,j] = BF16( sum_kb xs[i,kb] * ws[j/128,kb]
+ *                        * sum_{k in slab kb} dec(xq[i,k]) * dec(wq[j,k]) )
+ *
+ * with FP32 accumulation and the scales applied once per 128-wide K slab.
+ *   xq [m, k], xs [m, ceil(k/128)]     (from quantize_act_per_token_group)
+ *   wq [n, k], ws [ceil(n/128), ceil(k/128)] (from quantize_weight_blockwise)
+ *   y_bf16 [m, n] (out), round to nearest even.
+ * Rules: m, n >= 0; k >= 0 and k % 16 == 0; n % 8 == 0; xq, wq, y_bf16
+ * 16-byte aligned; xs, ws 4-byte aligned.  k == 0 writes zeros.
+ * Accuracy: |y - exact| <= 1e-3 * sum_k |a_ik b_jk| + half a BF16 ulp.
+ * ---------------------------------------------------------------------- */
+w8a8_status fp8_block_gemm(const uint8_t *xq, const float *xs,
+                           const uint8_t *wq, const float *ws,
+                           uint16_t *y_bf16, int64_t m, int64_t n, int64_t k,
+                           w8a8_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * fp8_grouped_gemm -- the MoE expert layers of [FP8-RL] section 1 (expert
+ * layers are quantized) and section 3 (30B-A3B MoE): fp8_block_gemm per
+ * expert over that expert's routed rows.
+ *
+ *   xq [rows_x, k], xs [rows_x, ceil(k/128)]  quantized activations.
+ *   row_idx [total_rows] int32 source row of each routed row, or NULL for
+ *           the identity (row r reads xq row r).
+ *   group_offsets [g+1] int32, non-decreasing, group_offsets[0] = 0 and
+ *           group_offsets[g] = total_rows: rows [off[e], off[e+1]) use
+ *           expert e.  (device)
+ *   total_rows   host copy of group_offsets[g].
+ *   wq [g, n, k], ws [g, ceil(n/128), ceil(k/128)] expert weights.
+ *   y_bf16 [total_rows, n] (out), in routed-row order.
+ * Rules as fp8_block_gemm, plus g >= 0 and total_rows >= 0.  Device data is
+ * range-checked in the kernel: a row_idx outside [0, rows_x) yields a zero
+ * output row, and offsets are clamped to [0, total_rows].
+ * ---------------------------------------------------------------------- */
+w8a8_status fp8_grouped_gemm(const uint8_t *xq, const float *xs,
+                             int64_t rows_x, const int32_t *row_idx,
+                             const int32_t *group_offsets, int32_t g,
+                             int64_t total_rows, const uint8_t *wq,
+                             const float *ws, uint16_t *y_bf16, int64_t n,
+                             int64_t k, w8a8_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * kv_amax_quantize -- the FP8 KV cache of [NeMo] "FP8 for KV cache and
+ * attention" with Table 3 (per-tensor FP32 scale for the stored KV cache)
+ * and the per-step recalibration of [FP8-RL] section 4 / arXiv abstract item
+ * (ii): amax over the whole tensor, S = amax / 448, every element coded with
+ * S.  Call once for K and once for V.
+ *
+ *   x_bf16 [numel] BF16 tensor (any shape, contiguous).
+ *   q      [numel] E4M3 codes (out; unused in AMAX_ONLY).
+ *   scale  1 float: out in AMAX_AND_QUANT and AMAX_ONLY, in for QUANT_ONLY.
+ *   amax   1 float: out in AMAX_AND_QUANT and AMAX_ONLY (may be NULL in
+ *          QUANT_ONLY).
+ *   mode   W8A8_KV_AMAX_AND_QUANT, W8A8_KV_AMAX_ONLY or W8A8_KV_QUANT_ONLY.
+ * numel >= 0 (numel == 0 gives amax 0 and scale 1).  x_bf16 and q 16-byte
+ * aligned; scale and amax 4-byte aligned.  In QUANT_ONLY a stale scale may
+ * push |x/S| past 448; those elements saturate.
+ * ---------------------------------------------------------------------- */
+enum {
+    W8A8_KV_AMAX_AND_QUANT = 0,
+    W8A8_KV_AMAX_ONLY = 1,
+    W8A8_KV_QUANT_ONLY = 2
+};
+w8a8_status kv_amax_quantize(const uint16_t *x_bf16, int64_t numel,
+                             uint8_t *q, float *scale, float *amax, int mode,
+                             w8a8_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W8A8FP8_H */

@@ -24,3 +24,15 @@ def oracle():
     import oracle as o
     o.lib()
     return o
+
+
+@pytest.fixture(scope="session")
+def W():
+    """The CUDA library's binding, built for sm_103a; a GPU must be present."""
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from w8a8_gemm_rl_gb300 import _build
+    _build.build()
+    import w8a8_gemm_rl_gb300 as w
+    w.lib()
+    return w

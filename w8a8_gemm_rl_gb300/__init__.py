@@ -1,0 +1,220 @@
+"""Python binding of the GB300 FP8 W8A8 library (libw8a8fp8.so).
+
+Argument marshalling only: each function checks the tensors it is given,
+allocates outputs with torch when the caller passes none, and calls the C
+entry point of the same name on the current CUDA stream.  Every step of the
+computation runs in the library's CUDA kernels; there is no other code path,
+and a missing library is an error.
+
+The C ABI and what each call computes are documented in include/w8a8fp8.h.
+"""
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "lib", "W8A8Error", "e4m3_encode_f32", "e4m3_decode_f32", "quantize_weight_blockwise",
+    "quantize_weight_blockwise_batched", "quantize_act_per_token_group", "fp8_block_gemm",
+    "fp8_grouped_gemm", "kv_amax_quantize", "w8a8_linear", "consume_device_error",
+    "KV_AMAX_AND_QUANT", "KV_AMAX_ONLY", "KV_QUANT_ONLY", "LIB_PATH",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libw8a8fp8.so")
+
+KV_AMAX_AND_QUANT, KV_AMAX_ONLY, KV_QUANT_ONLY = 0, 1, 2
+
+
+class W8A8Error(RuntimeError):
+    def __init__(self, name, status, msg, cuda_msg=""):
+        super().__init__(f"{name}: status {status} ({msg})" + (f": {cuda_msg}" if cuda_msg else ""))
+        self.status = status
+
+
+class WeightDesc(ctypes.Structure):
+    _fields_ = [("w_bf16", ctypes.c_void_p), ("wq", ctypes.c_void_p), ("ws", ctypes.c_void_p),
+                ("n", ctypes.c_int64), ("k", ctypes.c_int64)]
+
+
+_lib = None
+
+_P, _I64, _I32, _INT = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int
+_SIGNATURES = {
+    "w8a8_status_string": (ctypes.c_char_p, [_INT]),
+    "w8a8_version": (_INT, []),
+    "w8a8_last_cuda_error": (ctypes.c_char_p, []),
+    "w8a8_consume_device_error": (_INT, [_P]),
+    "e4m3_encode_f32": (_INT, [_P, _I64, _P, _P]),
+    "e4m3_decode_f32": (_INT, [_P, _I64, _P, _P]),
+    "quantize_weight_blockwise": (_INT, [_P, _I64, _I64, _P, _P, _P]),
+    "quantize_weight_blockwise_batched": (_INT, [_P, _I32, _P]),
+    "quantize_act_per_token_group": (_INT, [_P, _I64, _I64, _P, _P, _P]),
+    "fp8_block_gemm": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "fp8_grouped_gemm": (_INT, [_P, _P, _I64, _P, _P, _I32, _I64, _P, _P, _P, _I64, _I64, _P]),
+    "kv_amax_quantize": (_INT, [_P, _I64, _P, _P, _P, _INT, _P]),
+}
+
+
+def lib():
+    """The loaded C library (ctypes), with argument types declared."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with w8a8_gemm_rl_gb300._build.build() "
+                "(there is no fallback implementation)")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(name, status):
+    if status != 0:
+        L = lib()
+        raise W8A8Error(name, status, L.w8a8_status_string(status).decode(),
+                        L.w8a8_last_cuda_error().decode() if status == 5 else "")
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, dtype, name):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor")
+
+
+def _cdiv(a, b):
+    return (a + b - 1) // b
+
+
+# ------------------------------------------------------------------ codec
+
+def e4m3_encode_f32(x, out=None, stream=None):
+    _need(x, torch.float32, "x")
+    q = torch.empty(x.shape, dtype=torch.uint8, device=x.device) if out is None else out
+    _check("e4m3_encode_f32", lib().e4m3_encode_f32(_ptr(x), x.numel(), _ptr(q), _stream(stream)))
+    return q
+
+
+def e4m3_decode_f32(q, out=None, stream=None):
+    _need(q, torch.uint8, "q")
+    x = torch.empty(q.shape, dtype=torch.float32, device=q.device) if out is None else out
+    _check("e4m3_decode_f32", lib().e4m3_decode_f32(_ptr(q), q.numel(), _ptr(x), _stream(stream)))
+    return x
+
+
+# ------------------------------------------------------------- quantizers
+
+def quantize_weight_blockwise(w, wq=None, ws=None, stream=None):
+    """w BF16 [n, k] -> (wq uint8 [n, k], ws float32 [ceil(n/128), ceil(k/128)])."""
+    _need(w, torch.bfloat16, "w")
+    n, k = w.shape
+    wq = torch.empty((n, k), dtype=torch.uint8, device=w.device) if wq is None else wq
+    ws = torch.empty((_cdiv(n, 128), _cdiv(k, 128)), dtype=torch.float32, device=w.device) if ws is None else ws
+    _check("quantize_weight_blockwise",
+           lib().quantize_weight_blockwise(_ptr(w), n, k, _ptr(wq), _ptr(ws), _stream(stream)))
+    return wq, ws
+
+
+def quantize_weight_blockwise_batched(ws_in, outs=None, stream=None):
+    """Quantize a list of BF16 weight matrices in one call.  Returns a list of
+    (wq, ws) pairs (or fills `outs`, a list of such pairs)."""
+    if outs is None:
+        outs = []
+        for w in ws_in:
+            n, k = w.shape
+            outs.append((torch.empty((n, k), dtype=torch.uint8, device=w.device),
+                         torch.empty((_cdiv(n, 128), _cdiv(k, 128)), dtype=torch.float32, device=w.device)))
+    descs = (WeightDesc * len(ws_in))()
+    for i, (w, (q, s)) in enumerate(zip(ws_in, outs)):
+        _need(w, torch.bfloat16, "w")
+        descs[i] = WeightDesc(w.data_ptr(), q.data_ptr(), s.data_ptr(), w.shape[0], w.shape[1])
+    _check("quantize_weight_blockwise_batched",
+           lib().quantize_weight_blockwise_batched(ctypes.cast(descs, ctypes.c_void_p), len(ws_in),
+                                                   _stream(stream)))
+    return outs
+
+
+def quantize_act_per_token_group(x, xq=None, xs=None, stream=None):
+    """x BF16 [m, k] -> (xq uint8 [m, k], xs float32 [m, ceil(k/128)])."""
+    _need(x, torch.bfloat16, "x")
+    m, k = x.shape
+    xq = torch.empty((m, k), dtype=torch.uint8, device=x.device) if xq is None else xq
+    xs = torch.empty((m, _cdiv(k, 128)), dtype=torch.float32, device=x.device) if xs is None else xs
+    _check("quantize_act_per_token_group",
+           lib().quantize_act_per_token_group(_ptr(x), m, k, _ptr(xq), _ptr(xs), _stream(stream)))
+    return xq, xs
+
+
+# ------------------------------------------------------------------ GEMMs
+
+def fp8_block_gemm(xq, xs, wq, ws, y=None, stream=None):
+    """Y = X W^T with blockwise FP32 scales; returns BF16 [m, n]."""
+    _need(xq, torch.uint8, "xq")
+    _need(wq, torch.uint8, "wq")
+    m, k = xq.shape
+    n = wq.shape[0]
+    y = torch.empty((m, n), dtype=torch.bfloat16, device=xq.device) if y is None else y
+    _check("fp8_block_gemm", lib().fp8_block_gemm(_ptr(xq), _ptr(xs), _ptr(wq), _ptr(ws), _ptr(y),
+                                                  m, n, k, _stream(stream)))
+    return y
+
+
+def fp8_grouped_gemm(xq, xs, row_idx, group_offsets, total_rows, wq, ws, y=None, stream=None):
+    """Per-expert GEMM over routed rows.  wq [g, n, k], ws [g, ceil(n/128),
+    ceil(k/128)], group_offsets int32 [g+1] (device), row_idx int32 [total]
+    or None; total_rows is the host value of group_offsets[g]."""
+    _need(xq, torch.uint8, "xq")
+    _need(wq, torch.uint8, "wq")
+    g, n, k = wq.shape
+    y = torch.empty((total_rows, n), dtype=torch.bfloat16, device=xq.device) if y is None else y
+    _check("fp8_grouped_gemm",
+           lib().fp8_grouped_gemm(_ptr(xq), _ptr(xs), xq.shape[0], _ptr(row_idx), _ptr(group_offsets),
+                                  g, int(total_rows), _ptr(wq), _ptr(ws), _ptr(y), n, k,
+                                  _stream(stream)))
+    return y
+
+
+def w8a8_linear(x, wq, ws, stream=None):
+    """BF16 activations -> 1x128 quantization -> blockwise FP8 GEMM, on one stream."""
+    xq, xs = quantize_act_per_token_group(x, stream=stream)
+    return fp8_block_gemm(xq, xs, wq, ws, stream=stream)
+
+
+# --------------------------------------------------------------- KV cache
+
+def kv_amax_quantize(x, q=None, scale=None, amax=None, mode=KV_AMAX_AND_QUANT, stream=None):
+    """Per-tensor FP8 quantization with amax recalibration.  Returns
+    (q uint8 like x, scale float32 [1], amax float32 [1])."""
+    _need(x, torch.bfloat16, "x")
+    dev = x.device
+    if q is None and mode != KV_AMAX_ONLY:
+        q = torch.empty(x.shape, dtype=torch.uint8, device=dev)
+    scale = torch.empty(1, dtype=torch.float32, device=dev) if scale is None else scale
+    if amax is None and mode != KV_QUANT_ONLY:
+        amax = torch.empty(1, dtype=torch.float32, device=dev)
+    _check("kv_amax_quantize", lib().kv_amax_quantize(_ptr(x), x.numel(), _ptr(q), _ptr(scale),
+                                                      _ptr(amax), mode, _stream(stream)))
+    return q, scale, amax
+
+
+def consume_device_error():
+    """Reads and clears the error code a GEMM kernel records when one of its
+    bounded waits gives up (0 = none)."""
+    v = ctypes.c_int(0)
+    _check("w8a8_consume_device_error", lib().w8a8_consume_device_error(ctypes.byref(v)))
+    return v.value

@@ -1,0 +1,189 @@
+// api.cu -- the C ABI declared in include/w8a8fp8.h.  Host-side argument
+// checks happen here, before anything is queued; the kernels live in
+// quant.cu and gemm.cu.
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/w8a8fp8.h"
+#include "kernels.h"
+
+#define W8A8_API extern "C" __attribute__((visibility("default")))
+
+namespace w8a8 {
+cudaError_t consume_device_error(int* code);
+int grouped_gemm_max_groups();
+}  // namespace w8a8
+
+namespace {
+
+char g_last_cuda_error[256] = "";
+
+w8a8_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return W8A8_OK;
+  const char* s = cudaGetErrorString(e);
+  strncpy(g_last_cuda_error, s ? s : "unknown", sizeof(g_last_cuda_error) - 1);
+  g_last_cuda_error[sizeof(g_last_cuda_error) - 1] = '\0';
+  return W8A8_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+constexpr int64_t kMaxDim = (int64_t)1 << 31;  // TMA coordinates and tile math are 32-bit
+
+cudaStream_t cs(w8a8_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+W8A8_API const char* w8a8_status_string(w8a8_status status) {
+  switch (status) {
+    case W8A8_OK: return "ok";
+    case W8A8_ERR_NULL: return "a required pointer is NULL";
+    case W8A8_ERR_SHAPE: return "invalid size or shape";
+    case W8A8_ERR_ALIGN: return "pointer not aligned as required";
+    case W8A8_ERR_UNSUPPORTED: return "request not supported by this build";
+    case W8A8_ERR_CUDA: return "CUDA runtime error";
+  }
+  return "unknown status";
+}
+
+W8A8_API int w8a8_version(void) { return 100; }
+
+W8A8_API const char* w8a8_last_cuda_error(void) { return g_last_cuda_error; }
+
+// ------------------------------------------------------------- E4M3 codec
+
+W8A8_API w8a8_status e4m3_encode_f32(const float* x, int64_t n, uint8_t* q, w8a8_stream_t stream) {
+  if (n < 0) return W8A8_ERR_SHAPE;
+  if (n == 0) return W8A8_OK;
+  if (!x || !q) return W8A8_ERR_NULL;
+  if (!aligned(x, 16) || !aligned(q, 16)) return W8A8_ERR_ALIGN;
+  return from_cuda(w8a8::launch_e4m3_encode(x, n, q, cs(stream)));
+}
+
+W8A8_API w8a8_status e4m3_decode_f32(const uint8_t* q, int64_t n, float* x, w8a8_stream_t stream) {
+  if (n < 0) return W8A8_ERR_SHAPE;
+  if (n == 0) return W8A8_OK;
+  if (!x || !q) return W8A8_ERR_NULL;
+  if (!aligned(x, 16) || !aligned(q, 16)) return W8A8_ERR_ALIGN;
+  return from_cuda(w8a8::launch_e4m3_decode(q, n, x, cs(stream)));
+}
+
+// ------------------------------------------------------------- quantizers
+
+static w8a8_status check_quant_matrix(const uint16_t* x, int64_t rows, int64_t cols,
+                                      const uint8_t* q, const float* s) {
+  if (rows < 0 || cols < 0) return W8A8_ERR_SHAPE;
+  if (rows == 0 || cols == 0) return W8A8_OK;
+  if (!x || !q || !s) return W8A8_ERR_NULL;
+  if (!aligned(x, 16) || !aligned(q, 16) || !aligned(s, 4)) return W8A8_ERR_ALIGN;
+  return W8A8_OK;
+}
+
+W8A8_API w8a8_status quantize_weight_blockwise(const uint16_t* w_bf16, int64_t n, int64_t k,
+                                               uint8_t* wq, float* ws, w8a8_stream_t stream) {
+  w8a8_status st = check_quant_matrix(w_bf16, n, k, wq, ws);
+  if (st != W8A8_OK || n == 0 || k == 0) return st;
+  w8a8::WeightJob j{w_bf16, wq, ws, n, k};
+  return from_cuda(w8a8::launch_weight_quant(&j, 1, cs(stream)));
+}
+
+W8A8_API w8a8_status quantize_weight_blockwise_batched(const w8a8_weight_desc* descs,
+                                                       int32_t count, w8a8_stream_t stream) {
+  if (count < 0) return W8A8_ERR_SHAPE;
+  if (count == 0) return W8A8_OK;
+  if (!descs) return W8A8_ERR_NULL;
+  for (int32_t i = 0; i < count; ++i) {
+    w8a8_status st = check_quant_matrix(descs[i].w_bf16, descs[i].n, descs[i].k, descs[i].wq,
+                                        descs[i].ws);
+    if (st != W8A8_OK) return st;
+  }
+  // Jobs go to the launcher in groups of up to 256 (host stack bound).
+  constexpr int kChunk = 256;
+  w8a8::WeightJob jobs[kChunk];
+  int nj = 0;
+  for (int32_t i = 0; i < count; ++i) {
+    jobs[nj++] = w8a8::WeightJob{descs[i].w_bf16, descs[i].wq, descs[i].ws, descs[i].n, descs[i].k};
+    if (nj == kChunk || i == count - 1) {
+      w8a8_status st = from_cuda(w8a8::launch_weight_quant(jobs, nj, cs(stream)));
+      if (st != W8A8_OK) return st;
+      nj = 0;
+    }
+  }
+  return W8A8_OK;
+}
+
+W8A8_API w8a8_status quantize_act_per_token_group(const uint16_t* x_bf16, int64_t m, int64_t k,
+                                                  uint8_t* xq, float* xs, w8a8_stream_t stream) {
+  w8a8_status st = check_quant_matrix(x_bf16, m, k, xq, xs);
+  if (st != W8A8_OK || m == 0 || k == 0) return st;
+  return from_cuda(w8a8::launch_act_quant(x_bf16, m, k, xq, xs, cs(stream)));
+}
+
+// ------------------------------------------------------------------ GEMMs
+
+static w8a8_status check_gemm_common(const uint8_t* xq, const float* xs, const uint8_t* wq,
+                                     const float* ws, const uint16_t* y, int64_t n, int64_t k) {
+  if (n < 0 || k < 0 || n >= kMaxDim || k >= kMaxDim) return W8A8_ERR_SHAPE;
+  if (k % 16 != 0 || n % 8 != 0) return W8A8_ERR_SHAPE;
+  if (!y) return W8A8_ERR_NULL;
+  if (k > 0 && (!xq || !xs || !wq || !ws)) return W8A8_ERR_NULL;
+  if (!aligned(y, 16)) return W8A8_ERR_ALIGN;
+  if (k > 0 && (!aligned(xq, 16) || !aligned(wq, 16) || !aligned(xs, 4) || !aligned(ws, 4)))
+    return W8A8_ERR_ALIGN;
+  return W8A8_OK;
+}
+
+W8A8_API w8a8_status fp8_block_gemm(const uint8_t* xq, const float* xs, const uint8_t* wq,
+                                    const float* ws, uint16_t* y_bf16, int64_t m, int64_t n,
+                                    int64_t k, w8a8_stream_t stream) {
+  if (m < 0 || n < 0 || k < 0 || m >= kMaxDim) return W8A8_ERR_SHAPE;
+  if (m == 0 || n == 0) return (k % 16 == 0 && n % 8 == 0) ? W8A8_OK : W8A8_ERR_SHAPE;
+  w8a8_status st = check_gemm_common(xq, xs, wq, ws, y_bf16, n, k);
+  if (st != W8A8_OK) return st;
+  return from_cuda(w8a8::launch_block_gemm(xq, xs, wq, ws, y_bf16, m, n, k, cs(stream)));
+}
+
+W8A8_API w8a8_status fp8_grouped_gemm(const uint8_t* xq, const float* xs, int64_t rows_x,
+                                      const int32_t* row_idx, const int32_t* group_offsets,
+                                      int32_t g, int64_t total_rows, const uint8_t* wq,
+                                      const float* ws, uint16_t* y_bf16, int64_t n, int64_t k,
+                                      w8a8_stream_t stream) {
+  if (g < 0 || total_rows < 0 || rows_x < 0 || n < 0 || k < 0) return W8A8_ERR_SHAPE;
+  if (total_rows >= kMaxDim || rows_x >= kMaxDim) return W8A8_ERR_SHAPE;
+  if (g > w8a8::grouped_gemm_max_groups()) return W8A8_ERR_UNSUPPORTED;
+  if (total_rows == 0 || n == 0 || g == 0)
+    return (k % 16 == 0 && n % 8 == 0) ? W8A8_OK : W8A8_ERR_SHAPE;
+  if (!group_offsets) return W8A8_ERR_NULL;
+  if (!aligned(group_offsets, 4) || (row_idx && !aligned(row_idx, 4))) return W8A8_ERR_ALIGN;
+  if (!row_idx && total_rows > rows_x) return W8A8_ERR_SHAPE;  // identity gather reads row r
+  if ((int64_t)g * n >= kMaxDim) return W8A8_ERR_SHAPE;
+  w8a8_status st = check_gemm_common(xq, xs, wq, ws, y_bf16, n, k);
+  if (st != W8A8_OK) return st;
+  if (k > 0 && rows_x == 0) return W8A8_ERR_SHAPE;
+  return from_cuda(w8a8::launch_grouped_gemm(xq, xs, rows_x, row_idx, group_offsets, g,
+                                             total_rows, wq, ws, y_bf16, n, k, cs(stream)));
+}
+
+// --------------------------------------------------------------- KV cache
+
+W8A8_API w8a8_status kv_amax_quantize(const uint16_t* x_bf16, int64_t numel, uint8_t* q,
+                                      float* scale, float* amax, int mode, w8a8_stream_t stream) {
+  if (numel < 0) return W8A8_ERR_SHAPE;
+  if (mode != W8A8_KV_AMAX_AND_QUANT && mode != W8A8_KV_AMAX_ONLY && mode != W8A8_KV_QUANT_ONLY)
+    return W8A8_ERR_UNSUPPORTED;
+  if (!scale) return W8A8_ERR_NULL;
+  if (mode != W8A8_KV_QUANT_ONLY && !amax) return W8A8_ERR_NULL;
+  if (numel > 0 && !x_bf16) return W8A8_ERR_NULL;
+  if (numel > 0 && mode != W8A8_KV_AMAX_ONLY && !q) return W8A8_ERR_NULL;
+  if (!aligned(scale, 4) || (amax && !aligned(amax, 4))) return W8A8_ERR_ALIGN;
+  if (numel > 0 && !aligned(x_bf16, 16)) return W8A8_ERR_ALIGN;
+  if (numel > 0 && mode != W8A8_KV_AMAX_ONLY && !aligned(q, 16)) return W8A8_ERR_ALIGN;
+  return from_cuda(w8a8::launch_kv_amax_quantize(x_bf16, numel, q, scale, amax, mode, cs(stream)));
+}
+
+// ------------------------------------------------------------ diagnostics
+
+W8A8_API w8a8_status w8a8_consume_device_error(int* code) {
+  if (!code) return W8A8_ERR_NULL;
+  return from_cuda(w8a8::consume_device_error(code));
+}

@@ -1,0 +1,578 @@
+// gemm.cu -- blockwise-scaled FP8 (E4M3) GEMM and its grouped (MoE) variant
+// on the 5th-generation tensor cores of sm_103a.
+//
+// What is computed (NeMo RL FP8 blog, Table 1; "Unified FP8" notes, scale
+// choice: FP32 scales):
+//   Y[i,j] = BF16( sum_kb xs[i,kb] * ws[j/128,kb] * P[i,j,kb] ),
+//   P[i,j,kb] = sum_{k in 128-wide slab kb} dec(xq[i,k]) * dec(wq[j,k]),
+// FP32 accumulation.  The scales are FP32 and differ per (row, slab) and per
+// (128-column block, slab), so they cannot ride on the hardware's UE8M0
+// block-scaled MMA; instead every slab's partial P is produced on its own in
+// tensor memory and promoted into FP32 registers with its scale.
+//
+// Kernel structure (persistent, one CTA per SM, warp-specialized):
+//   warp 0      producer: TMA (or a cp.async row gather for routed MoE rows)
+//               of the A and B K-slabs into a 4-stage shared-memory ring;
+//   warp 1      allocates 512 TMEM columns; lane 0 issues 4 x
+//               tcgen05.mma.kind::f8f6f4 (128 x 256 x 32) per slab into one
+//               of two 256-column TMEM buffers, then commits to mbarriers;
+//   warps 2..9  promotion: tcgen05.ld of the slab partial, acc += P * s in
+//               FP32 registers (128 per thread), release the TMEM buffer,
+//               and after the last slab round to BF16 and store.
+// With two TMEM buffers the MMA of slab kb+1 overlaps the promotion of slab
+// kb.  Tiles are 128 x 256; tiles are visited in groups of 16 M-tiles so the
+// CTAs running at once share A and B tiles through L2.
+//
+// Every mbarrier wait is bounded (2 s of wall time).  A wait that gives up
+// records an error code in g_w8a8_gemm_error, tells the other roles to stop,
+// waits for its own copies / MMAs in flight, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace w8a8 {
+
+__device__ int g_w8a8_gemm_error = 0;
+
+namespace gemm {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 128;  // FP8 elements = bytes = one 128-byte swizzle row
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK;
+constexpr int B_BYTES = BN * BK;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int THREADS = 64 + 32 * NUM_EPI_WARPS;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int RASTER_M = 16;
+constexpr int GATHER_LAG = 2;  // cp.async groups kept in flight before signalling
+constexpr int MAX_GROUPS = 1024;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+constexpr uint32_t IDESC = ptx::idesc_e4m3_f32(BM, BN);
+
+// shared-memory map (offsets from a 1024-byte aligned base)
+constexpr int OFF_BARS = STAGES * STAGE_BYTES;
+constexpr int NUM_BARS = 2 * STAGES + 4 + 1;  // full, empty, tfull[2], tempty[2], done
+constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
+constexpr int OFF_GROUPS = (OFF_MISC + 16 + 15) / 16 * 16;
+constexpr int smem_bytes(int g) { return 1024 + OFF_GROUPS + 2 * 4 * (g + 1); }
+
+enum Mode { DENSE = 0, GROUPED = 1, GATHER = 2 };
+
+struct Params {
+  const uint8_t* xq;
+  const float* xs;
+  const float* ws;
+  uint16_t* y;
+  const int32_t* row_idx;
+  const int32_t* group_offsets;
+  int64_t m;       // dense: rows of X and Y; grouped: total routed rows
+  int64_t rows_x;  // rows of xq / xs
+  int32_t n, k, nkb, nnb;
+  int32_t g;
+  int32_t num_m_tiles;  // dense
+  int32_t num_n_tiles;
+};
+
+struct Tile {
+  int32_t e;
+  int32_t rows;  // valid rows (<= BM)
+  int64_t row0;  // first output row (routed order for grouped)
+  int32_t n0;
+};
+
+__device__ __forceinline__ void record_error(int code) { atomicCAS(&g_w8a8_gemm_error, 0, code); }
+__device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+__device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
+
+// Wait that also gives up early when another role has aborted.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         int code) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (ptx::globaltimer() - t0 > WAIT_LIMIT_NS) {
+      record_error(code);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+template <int kMode>
+__device__ __forceinline__ Tile decode_tile(const Params& p, int64_t t, const int32_t* s_prefix,
+                                            const int32_t* s_start) {
+  Tile T;
+  if (kMode == DENSE) {
+    const int64_t per_group = (int64_t)RASTER_M * p.num_n_tiles;
+    const int64_t grp = t / per_group;
+    const int32_t first_m = (int32_t)(grp * RASTER_M);
+    const int32_t gm = (int32_t)min64(RASTER_M, p.num_m_tiles - first_m);
+    const int32_t r = (int32_t)(t - grp * per_group);
+    const int32_t mt = first_m + r % gm;
+    const int32_t nt = r / gm;
+    T.e = 0;
+    T.row0 = (int64_t)mt * BM;
+    T.rows = (int32_t)min64(BM, p.m - T.row0);
+    T.n0 = nt * BN;
+  } else {
+    const int32_t mt_all = (int32_t)(t / p.num_n_tiles);
+    const int32_t nt = (int32_t)(t - (int64_t)mt_all * p.num_n_tiles);
+    int lo = 0, hi = p.g;  // s_prefix[lo] <= mt_all < s_prefix[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_prefix[mid] <= mt_all) lo = mid; else hi = mid;
+    }
+    const int32_t mt = mt_all - s_prefix[lo];
+    const int64_t gstart = s_start[lo];
+    const int64_t gend = s_start[lo + 1] > gstart ? s_start[lo + 1] : gstart;
+    T.e = lo;
+    T.row0 = gstart + (int64_t)mt * BM;
+    T.rows = (int32_t)min64(BM, gend - T.row0);
+    T.n0 = nt * BN;
+  }
+  return T;
+}
+
+template <int kMode>
+__global__ void __launch_bounds__(THREADS, 1)
+    fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                    const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_addr(smem);
+  const uint32_t bar0 = sbase + OFF_BARS;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+  int32_t* s_prefix = reinterpret_cast<int32_t*>(smem + OFF_GROUPS);
+  int32_t* s_start = s_prefix + (p.g + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(full_bar(s), kMode == GATHER ? 1 + 32 : 1);
+      ptx::mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(tfull_bar(b), 1);
+      ptx::mbar_init(tempty_bar(b), NUM_EPI_WARPS);
+    }
+    ptx::mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmap_b);
+    if (kMode != GATHER) ptx::prefetch_tmap(&tmap_a);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  int64_t num_tiles;
+  if (kMode == DENSE) {
+    num_tiles = (int64_t)p.num_m_tiles * p.num_n_tiles;
+  } else {
+    // per-group start row (clamped to [0, m]) and prefix sums of M-tiles
+    if (warp == 2) {
+      const int G = p.g;
+      const int per = (G + 31) / 32;
+      const int e0 = min(lane * per, G), e1 = min(e0 + per, G);
+      int32_t local = 0;
+      for (int e = e0; e < e1; ++e) {
+        int64_t a = p.group_offsets[e], b = p.group_offsets[e + 1];
+        a = min64(max64(a, 0), p.m);
+        b = min64(max64(b, a), p.m);
+        s_start[e] = (int32_t)a;
+        local += (int32_t)((b - a + BM - 1) / BM);
+      }
+      int32_t incl = local;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int32_t run = incl - local;
+      for (int e = e0; e < e1; ++e) {
+        s_prefix[e] = run;
+        int64_t a = s_start[e], b = p.group_offsets[e + 1];
+        b = min64(max64(b, a), p.m);
+        run += (int32_t)((b - a + BM - 1) / BM);
+      }
+      if (lane == 31) {
+        s_prefix[G] = incl;
+        int64_t last = p.group_offsets[G];
+        s_start[G] = (int32_t)min64(max64(last, 0), p.m);
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  if (kMode != DENSE) num_tiles = (int64_t)s_prefix[p.g] * p.num_n_tiles;
+
+  const int nkb = p.nkb;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t stage = 0, phase = 0;
+    int64_t issued = 0;
+    bool ok = true;
+    if (kMode != GATHER) {
+      if (lane == 0) {
+        for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+          const Tile T = decode_tile<kMode>(p, t, s_prefix, s_start);
+          const int brow = T.e * p.n + T.n0;
+          for (int kb = 0; kb < nkb; ++kb) {
+            if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, 1)) { ok = false; break; }
+            const uint32_t sa = sbase + stage * STAGE_BYTES;
+            ptx::mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
+            ptx::tma_load_2d(sa, &tmap_a, full_bar(stage), kb * BK, (int)T.row0);
+            ptx::tma_load_2d(sa + A_BYTES, &tmap_b, full_bar(stage), kb * BK, brow);
+            ++issued;
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          }
+        }
+      }
+    } else {
+      // routed rows: lane l copies rows l, l+32, l+64, l+96 of the A slab with
+      // 16-byte cp.async into the 128-byte-swizzled layout the MMA expects;
+      // lane 0 also brings the B slab by TMA.
+      int64_t pending_from = 0;  // first issued stage not yet signalled
+      uint32_t sig_stage = 0;
+      for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        const Tile T = decode_tile<kMode>(p, t, s_prefix, s_start);
+        const int brow = T.e * p.n + T.n0;
+        const uint8_t* src[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = lane + 32 * j;
+          src[j] = nullptr;
+          if (r < T.rows) {
+            const int64_t s = p.row_idx[T.row0 + r];
+            if (s >= 0 && s < p.rows_x) src[j] = p.xq + s * (int64_t)p.k;
+          }
+        }
+        for (int kb = 0; kb < nkb; ++kb) {
+          uint32_t okw = 1;
+          if (lane == 0) okw = wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, 2) ? 1u : 0u;
+          okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+          if (!okw) { ok = false; break; }
+          const uint32_t sa = sbase + stage * STAGE_BYTES;
+          if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(full_bar(stage), B_BYTES);
+            ptx::tma_load_2d(sa + A_BYTES, &tmap_b, full_bar(stage), kb * BK, brow);
+          }
+          const int kofs = kb * BK;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int r = lane + 32 * j;
+            const uint32_t rbase = sa + r * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const int kc = kofs + c * 16;
+              const bool in = src[j] != nullptr && kc < p.k;
+              ptx::cp_async_16(rbase + ((c ^ (r & 7)) << 4), in ? src[j] + kc : p.xq,
+                               in ? 16u : 0u);
+            }
+          }
+          ptx::cp_async_commit();
+          ++issued;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (issued - pending_from > GATHER_LAG) {
+            ptx::cp_async_wait_group<GATHER_LAG>();
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(full_bar(sig_stage));
+            ++pending_from;
+            if (++sig_stage == STAGES) sig_stage = 0;
+          }
+        }
+      }
+      ptx::cp_async_wait_group<0>();
+      ptx::fence_proxy_async_smem();
+      while (pending_from < issued) {
+        ptx::mbar_arrive(full_bar(sig_stage));
+        ++pending_from;
+        if (++sig_stage == STAGES) sig_stage = 0;
+      }
+    }
+    // Before leaving, make sure no copy is still landing in shared memory:
+    // wait (bounded) for the last phase of each stage this warp filled.
+    if (lane == 0 && issued > 0) {
+      const int64_t first = issued > STAGES ? issued - STAGES : 0;
+      for (int64_t i = first; i < issued; ++i) {
+        const uint32_t s = (uint32_t)(i % STAGES);
+        const uint32_t par = (uint32_t)((i / STAGES) & 1);
+        const uint64_t t0 = ptx::globaltimer();
+        while (!ptx::mbar_try_wait(full_bar(s), par)) {
+          if (ptx::globaltimer() - t0 > WAIT_LIMIT_NS) { record_error(3); break; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, tb = 0, tphase = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait_bar(tempty_bar(tb), tphase ^ 1u, abort_flag, 4)) { ok = false; break; }
+          if (!wait_bar(full_bar(stage), phase, abort_flag, 5)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const uint32_t sa = sbase + stage * STAGE_BYTES;
+          const uint64_t adesc = ptx::smem_desc_kmajor_sw128(sa);
+          const uint64_t bdesc = ptx::smem_desc_kmajor_sw128(sa + A_BYTES);
+          const uint32_t dcol = tmem_base + tb * BN;
+#pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk)  // K = 32 bytes per MMA: +2 in the >>4 field
+            ptx::mma_f8f6f4(dcol, adesc + 2u * kk, bdesc + 2u * kk, IDESC, kk > 0 ? 1u : 0u);
+          ptx::mma_commit(empty_bar(stage));
+          ptx::mma_commit(tfull_bar(tb));
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (++tb == 2) { tb = 0; tphase ^= 1u; }
+        }
+      }
+      // all MMAs issued by this thread have finished once done_bar fires
+      ptx::mma_commit(done_bar);
+      const uint64_t t0 = ptx::globaltimer();
+      while (!ptx::mbar_try_wait(done_bar, 0)) {
+        if (ptx::globaltimer() - t0 > WAIT_LIMIT_NS) { record_error(6); break; }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ promotion
+    const int ew = warp - 2;
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int half = ew >> 2;      // which 128 of the 256 tile columns
+    const int lrow = quarter * 32 + lane;
+    uint32_t tb = 0, tphase = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      const Tile T = decode_tile<kMode>(p, t, s_prefix, s_start);
+      const bool row_ok = lrow < T.rows;
+      const int64_t yrow = T.row0 + lrow;
+      int64_t src = yrow;
+      bool src_ok = row_ok;
+      if (kMode == GATHER && row_ok) {
+        src = p.row_idx[yrow];
+        src_ok = src >= 0 && src < p.rows_x;
+      }
+      const int nb = (T.n0 >> 7) + half;
+      const bool nb_ok = nb < p.nnb;
+      const float* xsr = p.xs + (src_ok ? src : 0) * (int64_t)nkb;
+      const float* wsr = p.ws + ((int64_t)T.e * p.nnb + (nb_ok ? nb : 0)) * nkb;
+      float a0 = src_ok ? xsr[0] : 0.0f;
+      float w0 = nb_ok ? wsr[0] : 0.0f;
+      float a1 = (src_ok && nkb > 1) ? xsr[1] : 0.0f;
+      float w1 = (nb_ok && nkb > 1) ? wsr[1] : 0.0f;
+      float acc[128];
+#pragma unroll
+      for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const float s = a0 * w0;
+        a0 = a1;
+        w0 = w1;
+        a1 = (src_ok && kb + 2 < nkb) ? xsr[kb + 2] : 0.0f;
+        w1 = (nb_ok && kb + 2 < nkb) ? wsr[kb + 2] : 0.0f;
+        uint32_t okw = 1;
+        if (lane == 0) okw = wait_bar(tfull_bar(tb), tphase, abort_flag, 7) ? 1u : 0u;
+        okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+        if (!okw) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + tb * BN + half * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          ptx::tmem_ld_32x32b_x32(tcol + c * 32, r);
+          ptx::tmem_wait_ld();
+          if (c == 3) {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(tempty_bar(tb));
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) acc[c * 32 + j] = fmaf(__uint_as_float(r[j]), s, acc[c * 32 + j]);
+        }
+        if (++tb == 2) { tb = 0; tphase ^= 1u; }
+      }
+      if (!ok) break;
+      if (row_ok) {
+        uint16_t* yr = p.y + yrow * (int64_t)p.n;
+        const int c0 = T.n0 + half * 128;
+#pragma unroll
+        for (int v = 0; v < 16; ++v) {
+          const int col = c0 + v * 8;
+          if (col < p.n) {
+            uint4 o;
+            o.x = ptx::pack_bf16x2(acc[v * 8 + 0], acc[v * 8 + 1]);
+            o.y = ptx::pack_bf16x2(acc[v * 8 + 2], acc[v * 8 + 3]);
+            o.z = ptx::pack_bf16x2(acc[v * 8 + 4], acc[v * 8 + 5]);
+            o.w = ptx::pack_bf16x2(acc[v * 8 + 6], acc[v * 8 + 7]);
+            *reinterpret_cast<uint4*>(yr + col) = o;
+          }
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace gemm
+
+// ---------------------------------------------------------------- host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// Row-major [rows, cols] bytes, box [box_rows, 128 bytes], 128-byte swizzle.
+static bool make_tmap_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                         uint32_t box_rows) {
+  auto fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int kMode>
+static cudaError_t prepare_kernel(int smem) {
+  // Raise the dynamic shared-memory limit once per device and size class.
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || smem > configured[dev]) {
+    e = cudaFuncSetAttribute(gemm::fp8_gemm_kernel<kMode>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev] = smem;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_block_gemm(const uint8_t* xq, const float* xs, const uint8_t* wq,
+                              const float* ws, uint16_t* y, int64_t m, int64_t n, int64_t k,
+                              cudaStream_t st) {
+  using namespace gemm;
+  if (m == 0 || n == 0) return cudaSuccess;
+  if (k == 0) return cudaMemsetAsync(y, 0, (size_t)(m * n * 2), st);
+  CUtensorMap ta, tb;
+  if (!make_tmap_u8(&ta, xq, (uint64_t)m, (uint64_t)k, BM)) return cudaErrorInvalidValue;
+  if (!make_tmap_u8(&tb, wq, (uint64_t)n, (uint64_t)k, BN)) return cudaErrorInvalidValue;
+  Params p{};
+  p.xq = xq; p.xs = xs; p.ws = ws; p.y = y;
+  p.row_idx = nullptr; p.group_offsets = nullptr;
+  p.m = m; p.rows_x = m;
+  p.n = (int32_t)n; p.k = (int32_t)k;
+  p.nkb = (int32_t)((k + 127) / 128);
+  p.nnb = (int32_t)((n + 127) / 128);
+  p.g = 1;
+  p.num_m_tiles = (int32_t)((m + BM - 1) / BM);
+  p.num_n_tiles = (int32_t)((n + BN - 1) / BN);
+  const int64_t tiles = (int64_t)p.num_m_tiles * p.num_n_tiles;
+  const int smem = smem_bytes(1);
+  cudaError_t e = prepare_kernel<DENSE>(smem);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)std::min<int64_t>(tiles, sm_count());
+  fp8_gemm_kernel<DENSE><<<grid, THREADS, smem, st>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_grouped_gemm(const uint8_t* xq, const float* xs, int64_t rows_x,
+                                const int32_t* row_idx, const int32_t* group_offsets, int32_t g,
+                                int64_t total_rows, const uint8_t* wq, const float* ws,
+                                uint16_t* y, int64_t n, int64_t k, cudaStream_t st) {
+  using namespace gemm;
+  if (total_rows == 0 || n == 0 || g == 0) return cudaSuccess;
+  if (k == 0) return cudaMemsetAsync(y, 0, (size_t)(total_rows * n * 2), st);
+  CUtensorMap ta, tb;
+  const bool gather = row_idx != nullptr;
+  // The A map is only used for the identity gather (rows of a group are
+  // contiguous); with a gather it is still encoded (over xq) but never read.
+  if (!make_tmap_u8(&ta, xq, (uint64_t)std::max<int64_t>(rows_x, 1), (uint64_t)k, BM))
+    return cudaErrorInvalidValue;
+  if (!make_tmap_u8(&tb, wq, (uint64_t)g * (uint64_t)n, (uint64_t)k, BN))
+    return cudaErrorInvalidValue;
+  Params p{};
+  p.xq = xq; p.xs = xs; p.ws = ws; p.y = y;
+  p.row_idx = row_idx; p.group_offsets = group_offsets;
+  p.m = total_rows; p.rows_x = rows_x;
+  p.n = (int32_t)n; p.k = (int32_t)k;
+  p.nkb = (int32_t)((k + 127) / 128);
+  p.nnb = (int32_t)((n + 127) / 128);
+  p.g = g;
+  p.num_m_tiles = 0;
+  p.num_n_tiles = (int32_t)((n + BN - 1) / BN);
+  const int64_t max_tiles = ((total_rows + BM - 1) / BM + g) * (int64_t)p.num_n_tiles;
+  const int smem = smem_bytes(g);
+  const unsigned grid = (unsigned)std::min<int64_t>(max_tiles, sm_count());
+  cudaError_t e;
+  if (gather) {
+    e = prepare_kernel<GATHER>(smem);
+    if (e != cudaSuccess) return e;
+    fp8_gemm_kernel<GATHER><<<grid, THREADS, smem, st>>>(ta, tb, p);
+  } else {
+    e = prepare_kernel<GROUPED>(smem);
+    if (e != cudaSuccess) return e;
+    fp8_gemm_kernel<GROUPED><<<grid, THREADS, smem, st>>>(ta, tb, p);
+  }
+  return cudaGetLastError();
+}
+
+int grouped_gemm_max_groups() { return gemm::MAX_GROUPS; }
+
+cudaError_t consume_device_error(int* code) {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_w8a8_gemm_error, sizeof(int));
+  if (e != cudaSuccess) return e;
+  if (v != 0) {
+    int z = 0;
+    e = cudaMemcpyToSymbol(g_w8a8_gemm_error, &z, sizeof(int));
+  }
+  *code = v;
+  return e;
+}
+
+}  // namespace w8a8

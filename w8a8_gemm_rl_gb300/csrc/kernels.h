@@ -1,0 +1,41 @@
+// kernels.h -- internal launchers behind the C ABI.  Each returns the CUDA
+// error of its launch(es); argument checking is done by the callers in
+// api.cu before any of these run.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace w8a8 {
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+cudaError_t launch_e4m3_encode(const float* x, int64_t n, uint8_t* q, cudaStream_t st);
+cudaError_t launch_e4m3_decode(const uint8_t* q, int64_t n, float* x, cudaStream_t st);
+
+cudaError_t launch_act_quant(const uint16_t* x, int64_t m, int64_t k, uint8_t* q, float* s,
+                             cudaStream_t st);
+
+struct WeightJob {
+  const uint16_t* w;
+  uint8_t* wq;
+  float* ws;
+  int64_t n, k;
+};
+cudaError_t launch_weight_quant(const WeightJob* jobs, int count, cudaStream_t st);
+
+// Per-tensor KV quantization; mode as in the public header.
+cudaError_t launch_kv_amax_quantize(const uint16_t* x, int64_t n, uint8_t* q, float* scale,
+                                    float* amax, int mode, cudaStream_t st);
+
+cudaError_t launch_block_gemm(const uint8_t* xq, const float* xs, const uint8_t* wq,
+                              const float* ws, uint16_t* y, int64_t m, int64_t n, int64_t k,
+                              cudaStream_t st);
+
+cudaError_t launch_grouped_gemm(const uint8_t* xq, const float* xs, int64_t rows_x,
+                                const int32_t* row_idx, const int32_t* group_offsets, int32_t g,
+                                int64_t total_rows, const uint8_t* wq, const float* ws,
+                                uint16_t* y, int64_t n, int64_t k, cudaStream_t st);
+
+}  // namespace w8a8

@@ -1,0 +1,452 @@
+// quant.cu -- the HBM-bound kernels of the path: E4M3 codec, 1x128
+// per-token activation quantizer, 128x128 blockwise weight quantizer and the
+// per-tensor KV-cache quantizer.
+//
+// Every quantizer computes, per group G ("Unified FP8" notes, scale and
+// quantization equations; NeMo RL FP8 Table 1 and Table 3 granularities):
+//   amax = max_{x in G} |x|,  S = RN32(amax / 448) (1 if amax = 0),
+//   q = E4M3(RN32(x / S))     round to nearest even, saturating at 448,
+// bit-exactly (see common.cuh for the coding of x / S).
+//
+// Design for GB300: 16-byte coalesced BF16 loads with the non-coherent,
+// no-L1-allocate hint; a group of 128 BF16 values is 256 contiguous bytes
+// handled by 16 lanes, its amax reduced with 4 butterfly shuffles; several
+// groups in flight per thread so each SM keeps tens of KB of loads
+// outstanding; codes leave as 8-byte stores.  Grids are multiples of the SM
+// count.
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace w8a8 {
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+__host__ __device__ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Grid for a grid-stride kernel: enough CTAs to cover `work` items of
+// `per_cta` each, capped at `waves` CTAs per SM.
+static inline unsigned grid_for(int64_t work, int64_t per_cta, int waves) {
+  int64_t want = cdiv(std::max<int64_t>(work, 1), per_cta);
+  int64_t cap = (int64_t)sm_count() * waves;
+  return (unsigned)std::max<int64_t>(1, std::min(want, cap));
+}
+
+// =====================================================================
+// E4M3 codec
+// =====================================================================
+
+__global__ void __launch_bounds__(256) e4m3_encode_kernel(const float* __restrict__ x, int64_t n,
+                                                          uint8_t* __restrict__ q) {
+  const int64_t nv = n / 8;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (int64_t i = tid; i < nv; i += stride) {
+    const uint4 a = ld_stream_v4(x + i * 8);
+    const uint4 b = ld_stream_v4(x + i * 8 + 4);
+    uint2 c;
+    c.x = cvt_e4m3x2(__uint_as_float(a.x), __uint_as_float(a.y)) |
+          (cvt_e4m3x2(__uint_as_float(a.z), __uint_as_float(a.w)) << 16);
+    c.y = cvt_e4m3x2(__uint_as_float(b.x), __uint_as_float(b.y)) |
+          (cvt_e4m3x2(__uint_as_float(b.z), __uint_as_float(b.w)) << 16);
+    st_stream_v2(q + i * 8, c);
+  }
+  for (int64_t i = nv * 8 + tid; i < n; i += stride)
+    q[i] = (uint8_t)(cvt_e4m3x2(x[i], 0.0f) & 0xFFu);
+}
+
+__global__ void __launch_bounds__(256) e4m3_decode_kernel(const uint8_t* __restrict__ q, int64_t n,
+                                                          float* __restrict__ x) {
+  const int64_t nv = n / 16;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (int64_t i = tid; i < nv; i += stride) {
+    const uint4 c = ld_stream_v4(q + i * 16);
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 lo = e4m3x2_to_float2((uint16_t)(w[j] & 0xFFFFu));
+      const float2 hi = e4m3x2_to_float2((uint16_t)(w[j] >> 16));
+      uint4 o = make_uint4(__float_as_uint(lo.x), __float_as_uint(lo.y), __float_as_uint(hi.x),
+                           __float_as_uint(hi.y));
+      st_stream_v4(x + i * 16 + j * 4, o);
+    }
+  }
+  for (int64_t i = nv * 16 + tid; i < n; i += stride) x[i] = e4m3x2_to_float2(q[i]).x;
+}
+
+cudaError_t launch_e4m3_encode(const float* x, int64_t n, uint8_t* q, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  e4m3_encode_kernel<<<grid_for(n, 256 * 8, 8), 256, 0, st>>>(x, n, q);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_e4m3_decode(const uint8_t* q, int64_t n, float* x, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  e4m3_decode_kernel<<<grid_for(n, 256 * 16, 8), 256, 0, st>>>(q, n, x);
+  return cudaGetLastError();
+}
+
+// =====================================================================
+// Generic block quantizer (any block shape, any row length): one CTA per
+// block, scalar loads, two passes.  Serves rows whose length is not a
+// multiple of 8 BF16 values, where 16-byte row segments do not exist.
+// =====================================================================
+
+__global__ void __launch_bounds__(256) block_quant_generic_kernel(const uint16_t* __restrict__ x,
+                                                                  int64_t rows, int64_t cols,
+                                                                  int64_t br, int64_t bc,
+                                                                  uint8_t* __restrict__ q,
+                                                                  float* __restrict__ s) {
+  __shared__ float red[8];
+  const int64_t nbc = cdiv(cols, bc);
+  const int64_t blk = blockIdx.x;
+  const int64_t bi = blk / nbc, bj = blk - bi * nbc;
+  const int64_t r0 = bi * br, r1 = min(r0 + br, rows);
+  const int64_t c0 = bj * bc, c1 = min(c0 + bc, cols);
+  const int64_t w = c1 - c0, cnt = (r1 - r0) * w;
+  float a = 0.0f;
+  for (int64_t t = threadIdx.x; t < cnt; t += blockDim.x) {
+    const int64_t r = r0 + t / w, c = c0 + t % w;
+    a = fmaxf(a, fabsf(bf16_lo(x[r * cols + c])));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+  __syncthreads();
+  a = red[0];
+  for (int i = 1; i < (int)(blockDim.x >> 5); ++i) a = fmaxf(a, red[i]);
+  const float S = scale_from_amax(a);
+  const QuantScale qs = make_quant_scale(S);
+  for (int64_t t = threadIdx.x; t < cnt; t += blockDim.x) {
+    const int64_t r = r0 + t / w, c = c0 + t % w;
+    q[r * cols + c] = (uint8_t)(quant_pair(bf16_lo(x[r * cols + c]), 0.0f, qs) & 0xFFu);
+  }
+  if (threadIdx.x == 0) s[blk] = S;
+}
+
+static cudaError_t launch_generic(const uint16_t* x, int64_t rows, int64_t cols, int64_t br,
+                                  int64_t bc, uint8_t* q, float* s, cudaStream_t st) {
+  const int64_t nb = cdiv(rows, br) * cdiv(cols, bc);
+  if (nb == 0) return cudaSuccess;
+  if (nb > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  block_quant_generic_kernel<<<(unsigned)nb, 256, 0, st>>>(x, rows, cols, br, bc, q, s);
+  return cudaGetLastError();
+}
+
+// =====================================================================
+// 1x128 per-token activation quantizer (row length a multiple of 8)
+// =====================================================================
+// A warp quantizes 2 groups per unit (lanes 0-15 and 16-31, 8 BF16 values
+// per lane) and U units per iteration, loads first, so 4 KB per warp are in
+// flight.  Consecutive warps take consecutive groups: the access stream is
+// contiguous.
+
+template <typename IdxT>
+__global__ void __launch_bounds__(256) act_quant_kernel(const uint16_t* __restrict__ x, IdxT m,
+                                                        IdxT k, uint8_t* __restrict__ q,
+                                                        float* __restrict__ s) {
+  constexpr int U = 4;
+  const IdxT gpr = (k + 127) / 128;
+  const IdxT G = m * gpr;
+  const int lane = threadIdx.x & 31;
+  const int half = lane >> 4, l16 = lane & 15;
+  const IdxT warp = (IdxT)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const IdxT nwarps = (IdxT)gridDim.x * (blockDim.x >> 5);
+  for (IdxT base = warp * (2 * U); base < G; base += nwarps * (2 * U)) {
+    uint4 v[U];
+    IdxT off[U];
+    bool ok[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const IdxT g = base + 2 * u + half;
+      const IdxT row = g / gpr;
+      const IdxT col = (g - row * gpr) * 128 + l16 * 8;
+      ok[u] = (g < G) && (col < k);
+      off[u] = row * k + col;
+      v[u] = ok[u] ? ld_stream_v4(x + off[u]) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float a = absmax_bf16x2(v[u].x, 0.0f);
+      a = absmax_bf16x2(v[u].y, a);
+      a = absmax_bf16x2(v[u].z, a);
+      a = absmax_bf16x2(v[u].w, a);
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+      const float S = scale_from_amax(a);
+      const QuantScale qs = make_quant_scale(S);
+      if (ok[u]) {
+        uint2 c;
+        c.x = quant_bf16x4(v[u].x, v[u].y, qs);
+        c.y = quant_bf16x4(v[u].z, v[u].w, qs);
+        st_stream_v2(q + off[u], c);
+      }
+      const IdxT g = base + 2 * u + half;
+      if (l16 == 0 && g < G) s[g] = S;
+    }
+  }
+}
+
+cudaError_t launch_act_quant(const uint16_t* x, int64_t m, int64_t k, uint8_t* q, float* s,
+                             cudaStream_t st) {
+  if (m == 0 || k == 0) return cudaSuccess;
+  if (k % 8 != 0) return launch_generic(x, m, k, 1, 128, q, s, st);
+  const int64_t G = m * cdiv(k, 128);
+  const unsigned grid = grid_for(G, 8 * 8, 16);  // 8 warps x 8 groups per CTA iteration
+  if (m * k < (int64_t)0x7FFFFFFF)
+    act_quant_kernel<uint32_t><<<grid, 256, 0, st>>>(x, (uint32_t)m, (uint32_t)k, q, s);
+  else
+    act_quant_kernel<int64_t><<<grid, 256, 0, st>>>(x, m, k, q, s);
+  return cudaGetLastError();
+}
+
+// =====================================================================
+// 128x128 blockwise weight quantizer (row length a multiple of 8)
+// =====================================================================
+// One CTA of 256 threads per block: thread t covers columns (t%16)*8..+8 of
+// rows t/16 + 16p, p = 0..7 -- 64 values, all loaded before any use (32 KB
+// per CTA in flight).  Block amax: butterfly over the warp, then 8 partials
+// through shared memory.  A batch of matrices is one launch: the CTA finds
+// its matrix by binary search over the block prefix sums held in the
+// kernel's parameter space.
+
+template <int kMax>
+struct WeightBatch {
+  const uint16_t* w[kMax];
+  uint8_t* wq[kMax];
+  float* ws[kMax];
+  int64_t n[kMax];
+  int64_t k[kMax];
+  int64_t first[kMax + 1];  // first block index of each matrix; first[count] = total
+  int count;
+};
+
+template <int kMax>
+__global__ void __launch_bounds__(256) weight_quant_kernel(const __grid_constant__ WeightBatch<kMax> b) {
+  __shared__ float red[8];
+  const int64_t blk = blockIdx.x;
+  int lo = 0;
+  if (kMax > 1) {
+    int hi = b.count;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (b.first[mid] <= blk) lo = mid; else hi = mid;
+    }
+  }
+  const uint16_t* __restrict__ w = b.w[lo];
+  uint8_t* __restrict__ wq = b.wq[lo];
+  const int64_t n = b.n[lo], k = b.k[lo];
+  const int64_t local = blk - b.first[lo];
+  const int64_t nbk = (k + 127) >> 7;
+  const int64_t bi = local / nbk, bj = local - bi * nbk;
+  const int t = threadIdx.x;
+  const int64_t col = bj * 128 + (t & 15) * 8;
+  const int64_t row0 = bi * 128 + (t >> 4);
+  const bool col_ok = col < k;
+  uint4 v[8];
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    const int64_t row = row0 + 16 * p;
+    v[p] = (col_ok && row < n) ? ld_stream_v4(w + row * k + col) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  float a = 0.0f;
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    a = absmax_bf16x2(v[p].x, a);
+    a = absmax_bf16x2(v[p].y, a);
+    a = absmax_bf16x2(v[p].z, a);
+    a = absmax_bf16x2(v[p].w, a);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+  if ((t & 31) == 0) red[t >> 5] = a;
+  __syncthreads();
+  a = fmaxf(fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])),
+            fmaxf(fmaxf(red[4], red[5]), fmaxf(red[6], red[7])));
+  const float S = scale_from_amax(a);
+  const QuantScale qs = make_quant_scale(S);
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    const int64_t row = row0 + 16 * p;
+    if (col_ok && row < n) {
+      uint2 c;
+      c.x = quant_bf16x4(v[p].x, v[p].y, qs);
+      c.y = quant_bf16x4(v[p].z, v[p].w, qs);
+      st_stream_v2(wq + row * k + col, c);
+    }
+  }
+  if (t == 0) b.ws[lo][bi * nbk + bj] = S;
+}
+
+template <int kMax>
+static cudaError_t launch_weight_batch(const WeightJob* jobs, int count, cudaStream_t st) {
+  WeightBatch<kMax> b;
+  int64_t total = 0;
+  b.count = count;
+  for (int i = 0; i < count; ++i) {
+    b.w[i] = jobs[i].w;
+    b.wq[i] = jobs[i].wq;
+    b.ws[i] = jobs[i].ws;
+    b.n[i] = jobs[i].n;
+    b.k[i] = jobs[i].k;
+    b.first[i] = total;
+    total += cdiv(jobs[i].n, 128) * cdiv(jobs[i].k, 128);
+  }
+  for (int i = count; i <= kMax; ++i) b.first[i] = total;
+  for (int i = count; i < kMax; ++i) {
+    b.w[i] = nullptr; b.wq[i] = nullptr; b.ws[i] = nullptr; b.n[i] = 0; b.k[i] = 0;
+  }
+  if (total == 0) return cudaSuccess;
+  if (total > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  weight_quant_kernel<kMax><<<(unsigned)total, 256, 0, st>>>(b);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_weight_quant(const WeightJob* jobs, int count, cudaStream_t st) {
+  constexpr int kBatch = 192;  // ~10 KB of kernel parameters
+  WeightJob fast[kBatch];
+  int nf = 0;
+  for (int i = 0; i < count; ++i) {
+    const WeightJob& j = jobs[i];
+    if (j.n == 0 || j.k == 0) continue;
+    if (j.k % 8 != 0) {
+      cudaError_t e = launch_generic(j.w, j.n, j.k, 128, 128, j.wq, j.ws, st);
+      if (e != cudaSuccess) return e;
+      continue;
+    }
+    fast[nf++] = j;
+    if (nf == kBatch) {
+      cudaError_t e = launch_weight_batch<kBatch>(fast, nf, st);
+      if (e != cudaSuccess) return e;
+      nf = 0;
+    }
+  }
+  if (nf == 1) return launch_weight_batch<1>(fast, 1, st);
+  if (nf > 1) return launch_weight_batch<kBatch>(fast, nf, st);
+  return cudaSuccess;
+}
+
+// =====================================================================
+// Per-tensor KV-cache quantizer: pass 1 amax, pass 2 code
+// =====================================================================
+// Pass 1 folds |x| into one float per CTA and combines CTAs with atomicMax
+// on the float's bit pattern (non-negative floats order like their bits), so
+// the result does not depend on the order.  Pass 2 reads the amax, forms S
+// and codes every element; it walks the tensor backwards so that the last
+// tens of MB pass 1 read are still in L2 when pass 2 starts.  The stream
+// orders the passes: no grid-wide wait inside a kernel.
+
+__global__ void __launch_bounds__(256) kv_amax_kernel(const uint16_t* __restrict__ x, int64_t n,
+                                                      unsigned int* __restrict__ amax_bits) {
+  __shared__ float red[8];
+  constexpr int U = 4;
+  const int64_t nv = n / 8;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  float a = 0.0f;
+  int64_t i = tid;
+  for (; i + (U - 1) * stride < nv; i += U * stride) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) v[u] = ld_stream_v4(x + (i + u * stride) * 8);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      a = absmax_bf16x2(v[u].x, a);
+      a = absmax_bf16x2(v[u].y, a);
+      a = absmax_bf16x2(v[u].z, a);
+      a = absmax_bf16x2(v[u].w, a);
+    }
+  }
+  for (; i < nv; i += stride) {
+    const uint4 v = ld_stream_v4(x + i * 8);
+    a = absmax_bf16x2(v.x, a);
+    a = absmax_bf16x2(v.y, a);
+    a = absmax_bf16x2(v.z, a);
+    a = absmax_bf16x2(v.w, a);
+  }
+  for (int64_t j = nv * 8 + tid; j < n; j += stride) a = fmaxf(a, fabsf(bf16_lo(x[j])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) a = fmaxf(a, red[w]);
+    atomicMax(amax_bits, __float_as_uint(a));
+  }
+}
+
+__global__ void __launch_bounds__(256) kv_quant_kernel(const uint16_t* __restrict__ x, int64_t n,
+                                                       uint8_t* __restrict__ q,
+                                                       float* __restrict__ scale,
+                                                       const float* __restrict__ amax,
+                                                       int mode) {
+  float S;
+  if (mode == 2) {
+    S = *scale;
+  } else {
+    S = scale_from_amax(*amax);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *scale = S;
+    if (mode == 1) return;
+  }
+  const QuantScale qs = make_quant_scale(S);
+  constexpr int U = 4;
+  const int64_t nv = n / 8;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  // tail first (it is at the end, which pass 1 read last)
+  for (int64_t j = nv * 8 + tid; j < n; j += stride)
+    q[j] = (uint8_t)(quant_pair(bf16_lo(x[j]), 0.0f, qs) & 0xFFu);
+  int64_t i = tid;
+  for (; i + (U - 1) * stride < nv; i += U * stride) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) v[u] = ld_stream_v4(x + (nv - 1 - (i + u * stride)) * 8);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      uint2 c;
+      c.x = quant_bf16x4(v[u].x, v[u].y, qs);
+      c.y = quant_bf16x4(v[u].z, v[u].w, qs);
+      st_stream_v2(q + (nv - 1 - (i + u * stride)) * 8, c);
+    }
+  }
+  for (; i < nv; i += stride) {
+    const uint4 v = ld_stream_v4(x + (nv - 1 - i) * 8);
+    uint2 c;
+    c.x = quant_bf16x4(v.x, v.y, qs);
+    c.y = quant_bf16x4(v.z, v.w, qs);
+    st_stream_v2(q + (nv - 1 - i) * 8, c);
+  }
+}
+
+cudaError_t launch_kv_amax_quantize(const uint16_t* x, int64_t n, uint8_t* q, float* scale,
+                                    float* amax, int mode, cudaStream_t st) {
+  if (mode != 2) {
+    cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), st);
+    if (e != cudaSuccess) return e;
+    if (n > 0) {
+      kv_amax_kernel<<<grid_for(n, 256 * 8 * 4, 8), 256, 0, st>>>(
+          x, n, reinterpret_cast<unsigned int*>(amax));
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
+  }
+  const unsigned grid = (mode == 1) ? 1u : grid_for(n, 256 * 8 * 4, 8);
+  if (mode == 2 && n == 0) return cudaSuccess;
+  kv_quant_kernel<<<grid, 256, 0, st>>>(x, n, q, scale, amax, mode);
+  return cudaGetLastError();
+}
+
+}  // namespace w8a8
