@@ -68,7 +68,7 @@ def test_act_quant_every_bf16_value_against_several_scales(W):
     pats = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
     f = (pats.astype(np.uint32) << 16).view(np.float32)
     pats = pats[np.isfinite(f)]
-    for amax in [448.0, 1.0, 3.0, 0.0173, 1e-30, 3e38, 5.5e3]:
+    for amax in [448.0, 1.0, 3.0, 0.0173, 1e-30, 3e38, 5.5e3, 1e-39, 2e-41]:
         keep = np.abs((pats.astype(np.uint32) << 16).view(np.float32)) <= amax
         vals = pats[keep]
         per = 127

@@ -61,7 +61,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
             and all(os.path.getmtime(OUT) >= os.path.getmtime(o) for o in objs)):
         return OUT
     tmp = OUT + f".tmp{os.getpid()}"
-    cmd = [NVCC, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
+    cmd = [NVCC, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static", "-Xlinker", "--no-undefined"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

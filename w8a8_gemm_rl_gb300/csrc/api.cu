@@ -11,6 +11,7 @@
 
 namespace w8a8 {
 cudaError_t consume_device_error(int* code);
+cudaError_t consume_quant_error(int* code);
 int grouped_gemm_max_groups();
 }  // namespace w8a8
 
@@ -185,5 +186,10 @@ W8A8_API w8a8_status kv_amax_quantize(const uint16_t* x_bf16, int64_t numel, uin
 
 W8A8_API w8a8_status w8a8_consume_device_error(int* code) {
   if (!code) return W8A8_ERR_NULL;
-  return from_cuda(w8a8::consume_device_error(code));
+  int g = 0, q = 0;
+  w8a8_status st = from_cuda(w8a8::consume_device_error(&g));
+  if (st != W8A8_OK) return st;
+  st = from_cuda(w8a8::consume_quant_error(&q));
+  *code = g != 0 ? g : q;
+  return st;
 }

@@ -44,52 +44,87 @@ __device__ __forceinline__ float scale_from_amax(float amax) {
   return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
 }
 
-// ---- E4M3(RN32(x / S)) for two elements ----
-// The quotient is needed only as far as its E4M3 code.  t = RN32(x * r) with
-// r = RN32(1/S) lies within 2.5 binary32 ulps of RN32(x / S) (two relative
-// rounding errors of 2^-24 plus half an ulp).  Coding is monotone, so when
-// t - 8 ulps and t + 8 ulps get the same code, every value between them --
-// RN32(x / S) included -- gets that code too.  Otherwise (t within 8 ulps of
-// an E4M3 rounding midpoint: about 1 element in 60000) the element is
-// recomputed with the correctly rounded division.  Magnitudes step by bit
-// patterns; a pattern that runs past the binary32 range becomes NaN, whose
-// code differs, so such elements also take the exact path.
+// ---- E4M3(RN32(x / S)), exactly, without a division per element ----
+// Let q = x / S (exact real), r = RN32(1/S), r_dn = RN32(r (1 - 2^-21)) and
+// r_up = RN32(r (1 + 2^-21)).  Each of r, r_dn/r_up and the products
+// t_dn = RN32(x r_dn), t_up = RN32(x r_up) adds one relative error of at
+// most 2^-24, so for binary32-normal q
+//     t_dn <= q (1 - 5 * 2^-24) < RN32(q) < q (1 + 5 * 2^-24) <= t_up
+// (mirrored for q < 0): the two products bracket RN32(x / S).  E4M3 coding
+// with round-to-nearest and saturation is monotone, so when t_dn and t_up
+// get the same code, RN32(x / S) gets that code too.  (When q is a
+// binary32 subnormal every candidate codes to a zero of the right sign.)
+// When the codes differ -- the bracket straddles an E4M3 rounding midpoint,
+// about 1 element in 60000 for normal-range values -- that element is
+// recomputed with the correctly rounded division.  If r_up overflows, every
+// element of the group takes the division.
 struct QuantScale {
   float s;     // S
-  float r;     // RN32(1 / S)
-  bool exact;  // 1/S overflows: use the division for every element
+  float r_dn;  // RN32(RN32(1/S) * (1 - 2^-21))
+  float r_up;  // RN32(RN32(1/S) * (1 + 2^-21))
+  bool exact;  // bracket unavailable: use the division for every element
 };
 
 __device__ __forceinline__ QuantScale make_quant_scale(float s) {
   QuantScale q;
   q.s = s;
-  q.r = __frcp_rn(s);
-  q.exact = !(q.r <= 3.0e38f);
+  const float r = __frcp_rn(s);
+  q.r_dn = __fmul_rn(r, 1.0f - 0x1p-21f);
+  q.r_up = __fmul_rn(r, 1.0f + 0x1p-21f);
+  q.exact = !(q.r_up <= 3.0e38f);
   return q;
 }
 
-__device__ __forceinline__ uint32_t quant_pair(float x0, float x1, const QuantScale& qs) {
-  if (qs.exact) return cvt_e4m3x2(__fdiv_rn(x0, qs.s), __fdiv_rn(x1, qs.s));
-  const float t0 = __fmul_rn(x0, qs.r), t1 = __fmul_rn(x1, qs.r);
-  uint32_t c = cvt_e4m3x2(t0, t1);
-  const uint32_t a0 = __float_as_uint(t0) & 0x7FFFFFFFu;
-  const uint32_t a1 = __float_as_uint(t1) & 0x7FFFFFFFu;
-  const uint32_t clo = cvt_e4m3x2(__uint_as_float(a0 > 8u ? a0 - 8u : 0u),
-                                  __uint_as_float(a1 > 8u ? a1 - 8u : 0u));
-  const uint32_t chi = cvt_e4m3x2(__uint_as_float(a0 + 8u), __uint_as_float(a1 + 8u));
-  const uint32_t diff = clo ^ chi;
-  if (__builtin_expect(diff != 0u, 0)) {
-    if (diff & 0x00FFu) c = (c & 0xFF00u) | (cvt_e4m3x2(__fdiv_rn(x0, qs.s), 0.0f) & 0x00FFu);
-    if (diff & 0xFF00u) c = (c & 0x00FFu) | (cvt_e4m3x2(0.0f, __fdiv_rn(x1, qs.s)) & 0xFF00u);
+__device__ __forceinline__ uint32_t code_exact(float x, float s) {
+  return cvt_e4m3x2(__fdiv_rn(x, s), 0.0f) & 0xFFu;
+}
+
+// Four codes (byte i = code of x_i) from four binary32 values.
+__device__ __forceinline__ uint32_t quant_f32x4(float x0, float x1, float x2, float x3,
+                                                const QuantScale& qs) {
+  if (qs.exact)
+    return code_exact(x0, qs.s) | (code_exact(x1, qs.s) << 8) | (code_exact(x2, qs.s) << 16) |
+           (code_exact(x3, qs.s) << 24);
+  const float2 rd = make_float2(qs.r_dn, qs.r_dn), ru = make_float2(qs.r_up, qs.r_up);
+  const float2 d01 = __fmul2_rn(make_float2(x0, x1), rd), u01 = __fmul2_rn(make_float2(x0, x1), ru);
+  const float2 d23 = __fmul2_rn(make_float2(x2, x3), rd), u23 = __fmul2_rn(make_float2(x2, x3), ru);
+  // p_i = (code(t_dn_i), code(t_up_i)) in bytes 0 and 1
+  const uint32_t p0 = cvt_e4m3x2(d01.x, u01.x), p1 = cvt_e4m3x2(d01.y, u01.y);
+  const uint32_t p2 = cvt_e4m3x2(d23.x, u23.x), p3 = cvt_e4m3x2(d23.y, u23.y);
+  const uint32_t a = __byte_perm(p0, p1, 0x5140);  // dn0 dn1 up0 up1
+  const uint32_t b = __byte_perm(p2, p3, 0x5140);  // dn2 dn3 up2 up3
+  uint32_t dn = __byte_perm(a, b, 0x5410);
+  const uint32_t up = __byte_perm(a, b, 0x7632);
+  if (__builtin_expect(dn != up, 0)) {
+    const uint32_t diff = dn ^ up;
+    if (diff & 0x000000FFu) dn = (dn & 0xFFFFFF00u) | code_exact(x0, qs.s);
+    if (diff & 0x0000FF00u) dn = (dn & 0xFFFF00FFu) | (code_exact(x1, qs.s) << 8);
+    if (diff & 0x00FF0000u) dn = (dn & 0xFF00FFFFu) | (code_exact(x2, qs.s) << 16);
+    if (diff & 0xFF000000u) dn = (dn & 0x00FFFFFFu) | (code_exact(x3, qs.s) << 24);
   }
-  return c;
+  return dn;
 }
 
 // Four codes from two BF16x2 words, packed little-endian into 32 bits.
 __device__ __forceinline__ uint32_t quant_bf16x4(uint32_t w0, uint32_t w1, const QuantScale& qs) {
-  const uint32_t c0 = quant_pair(bf16_lo(w0), bf16_hi(w0), qs);
-  const uint32_t c1 = quant_pair(bf16_lo(w1), bf16_hi(w1), qs);
-  return c0 | (c1 << 16);
+  return quant_f32x4(bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1), qs);
+}
+
+// One code (the scalar path of ragged rows and tails).
+__device__ __forceinline__ uint32_t quant_one(float x, const QuantScale& qs) {
+  return quant_f32x4(x, 0.0f, 0.0f, 0.0f, qs) & 0xFFu;
+}
+
+// Running max of |x| over the BF16 halves of a word, kept as a BF16x2 whose
+// two halves are reduced at the end (max is exact in any precision).
+__device__ __forceinline__ uint32_t absmax_bf16x2_packed(uint32_t m, uint32_t w) {
+  uint32_t r;
+  const uint32_t a = w & 0x7FFF7FFFu;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(a));
+  return r;
+}
+__device__ __forceinline__ float absmax_finish(uint32_t m) {
+  return fmaxf(bf16_lo(m), bf16_hi(m));
 }
 
 // ---- cache-hinted vector access for data touched once ----

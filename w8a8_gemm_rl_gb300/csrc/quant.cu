@@ -18,8 +18,23 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace w8a8 {
+
+// Set (first error wins) when a bounded wait in a quantization kernel gives up.
+__device__ int g_w8a8_quant_error = 0;
+
+cudaError_t consume_quant_error(int* code) {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_w8a8_quant_error, sizeof(int));
+  if (e == cudaSuccess && v != 0) {
+    const int z = 0;
+    e = cudaMemcpyToSymbol(g_w8a8_quant_error, &z, sizeof(int));
+  }
+  *code = v;
+  return e;
+}
 
 int sm_count() {
   static int cached[64] = {0};
@@ -132,7 +147,7 @@ __global__ void __launch_bounds__(256) block_quant_generic_kernel(const uint16_t
   const QuantScale qs = make_quant_scale(S);
   for (int64_t t = threadIdx.x; t < cnt; t += blockDim.x) {
     const int64_t r = r0 + t / w, c = c0 + t % w;
-    q[r * cols + c] = (uint8_t)(quant_pair(bf16_lo(x[r * cols + c]), 0.0f, qs) & 0xFFu);
+    q[r * cols + c] = (uint8_t)quant_one(bf16_lo(x[r * cols + c]), qs);
   }
   if (threadIdx.x == 0) s[blk] = S;
 }
@@ -216,12 +231,18 @@ cudaError_t launch_act_quant(const uint16_t* x, int64_t m, int64_t k, uint8_t* q
 // =====================================================================
 // 128x128 blockwise weight quantizer (row length a multiple of 8)
 // =====================================================================
-// One CTA of 256 threads per block: thread t covers columns (t%16)*8..+8 of
-// rows t/16 + 16p, p = 0..7 -- 64 values, all loaded before any use (32 KB
-// per CTA in flight).  Block amax: butterfly over the warp, then 8 partials
-// through shared memory.  A batch of matrices is one launch: the CTA finds
-// its matrix by binary search over the block prefix sums held in the
-// kernel's parameter space.
+// Persistent CTAs (2 per SM), each a producer warp plus 8 consumer warps,
+// over a 3-stage shared-memory ring of 32 KB blocks:
+//   producer  one bulk async copy per block row (up to 256 contiguous bytes)
+//             completing on the stage's mbarrier, up to 3 blocks ahead;
+//   consumers 16-byte conflict-free shared loads (lanes 0-15 one row, 16-31
+//             the next), release the stage, block amax (butterfly + 8
+//             partials through shared memory + a named barrier), S, then
+//             the codes straight to global memory as 8-byte stores.
+// A batch of matrices is one launch; a CTA finds the matrix of a block by
+// binary search over the block prefix sums held in the kernel parameters.
+// All waits are bounded; a wait that gives up records an error and the CTA
+// stops after draining its copies.
 
 template <int kMax>
 struct WeightBatch {
@@ -234,10 +255,22 @@ struct WeightBatch {
   int count;
 };
 
+constexpr int WQ_STAGES = 3;
+constexpr int WQ_CONSUMER_WARPS = 8;
+constexpr int WQ_THREADS = 32 * (WQ_CONSUMER_WARPS + 1);
+constexpr int WQ_STAGE_BYTES = 128 * 256;
+constexpr int WQ_SMEM = WQ_STAGES * WQ_STAGE_BYTES + 2 * WQ_STAGES * 8 + 2 * 8 * 4 + 16;
+constexpr uint64_t WQ_WAIT_NS = 2000000000ull;
+
+struct BlockRef {
+  int mat;
+  int64_t bi, bj, nbk;
+  int rows;  // valid rows in the block
+  int cols;  // valid columns (multiple of 8)
+};
+
 template <int kMax>
-__global__ void __launch_bounds__(256) weight_quant_kernel(const __grid_constant__ WeightBatch<kMax> b) {
-  __shared__ float red[8];
-  const int64_t blk = blockIdx.x;
+__device__ __forceinline__ BlockRef locate_block(const WeightBatch<kMax>& b, int64_t blk) {
   int lo = 0;
   if (kMax > 1) {
     int hi = b.count;
@@ -246,49 +279,134 @@ __global__ void __launch_bounds__(256) weight_quant_kernel(const __grid_constant
       if (b.first[mid] <= blk) lo = mid; else hi = mid;
     }
   }
-  const uint16_t* __restrict__ w = b.w[lo];
-  uint8_t* __restrict__ wq = b.wq[lo];
+  BlockRef r;
+  r.mat = lo;
   const int64_t n = b.n[lo], k = b.k[lo];
+  r.nbk = (k + 127) >> 7;
   const int64_t local = blk - b.first[lo];
-  const int64_t nbk = (k + 127) >> 7;
-  const int64_t bi = local / nbk, bj = local - bi * nbk;
-  const int t = threadIdx.x;
-  const int64_t col = bj * 128 + (t & 15) * 8;
-  const int64_t row0 = bi * 128 + (t >> 4);
-  const bool col_ok = col < k;
-  uint4 v[8];
-#pragma unroll
-  for (int p = 0; p < 8; ++p) {
-    const int64_t row = row0 + 16 * p;
-    v[p] = (col_ok && row < n) ? ld_stream_v4(w + row * k + col) : make_uint4(0u, 0u, 0u, 0u);
-  }
-  float a = 0.0f;
-#pragma unroll
-  for (int p = 0; p < 8; ++p) {
-    a = absmax_bf16x2(v[p].x, a);
-    a = absmax_bf16x2(v[p].y, a);
-    a = absmax_bf16x2(v[p].z, a);
-    a = absmax_bf16x2(v[p].w, a);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
-  if ((t & 31) == 0) red[t >> 5] = a;
-  __syncthreads();
-  a = fmaxf(fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])),
-            fmaxf(fmaxf(red[4], red[5]), fmaxf(red[6], red[7])));
-  const float S = scale_from_amax(a);
-  const QuantScale qs = make_quant_scale(S);
-#pragma unroll
-  for (int p = 0; p < 8; ++p) {
-    const int64_t row = row0 + 16 * p;
-    if (col_ok && row < n) {
-      uint2 c;
-      c.x = quant_bf16x4(v[p].x, v[p].y, qs);
-      c.y = quant_bf16x4(v[p].z, v[p].w, qs);
-      st_stream_v2(wq + row * k + col, c);
+  r.bi = local / r.nbk;
+  r.bj = local - r.bi * r.nbk;
+  r.rows = (int)min((int64_t)128, n - r.bi * 128);
+  r.cols = (int)min((int64_t)128, k - r.bj * 128);
+  return r;
+}
+
+template <int kMax>
+__global__ void __launch_bounds__(WQ_THREADS, 2)
+    weight_quant_kernel(const __grid_constant__ WeightBatch<kMax> b) {
+  extern __shared__ __align__(1024) uint8_t wq_smem[];
+  const uint32_t sbase = ptx::smem_addr(wq_smem);
+  const uint32_t bar0 = sbase + WQ_STAGES * WQ_STAGE_BYTES;
+  float* red = reinterpret_cast<float*>(wq_smem + WQ_STAGES * WQ_STAGE_BYTES + 2 * WQ_STAGES * 8);
+  volatile int* abort_flag =
+      reinterpret_cast<volatile int*>(wq_smem + WQ_STAGES * WQ_STAGE_BYTES + 2 * WQ_STAGES * 8 + 64);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (WQ_STAGES + s); };
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < WQ_STAGES; ++s) {
+      ptx::mbar_init(full_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), WQ_CONSUMER_WARPS);
     }
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
   }
-  if (t == 0) b.ws[lo][bi * nbk + bj] = S;
+  __syncthreads();
+  const int64_t total = b.first[b.count];
+
+  if (warp == WQ_CONSUMER_WARPS) {
+    // ------------------------------------------------------------ producer
+    int64_t issued = 0;
+    for (int64_t blk = blockIdx.x; blk < total; blk += gridDim.x, ++issued) {
+      const int s = (int)(issued % WQ_STAGES);
+      const uint32_t par = (uint32_t)((issued / WQ_STAGES) & 1);
+      uint32_t ok = 1;
+      if (lane == 0) {
+        ok = ptx::mbar_wait(empty_bar(s), par ^ 1u, WQ_WAIT_NS) ? 1u : 0u;
+        if (!ok) { atomicCAS(&g_w8a8_quant_error, 0, 11); *abort_flag = 1; }
+      }
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok || *abort_flag) break;
+      const BlockRef r = locate_block(b, blk);
+      const uint32_t row_bytes = (uint32_t)r.cols * 2u;
+      if (lane == 0) ptx::mbar_arrive_expect_tx(full_bar(s), row_bytes * (uint32_t)r.rows);
+      __syncwarp();
+      const uint16_t* src = b.w[r.mat] + (r.bi * 128) * b.k[r.mat] + r.bj * 128;
+      const uint32_t dst = sbase + s * WQ_STAGE_BYTES;
+      for (int row = lane; row < r.rows; row += 32)
+        ptx::bulk_load(dst + row * 256, src + row * b.k[r.mat], row_bytes, full_bar(s));
+    }
+    // drain: no copy may still be landing when the CTA exits
+    if (lane == 0) {
+      const int64_t first = issued > WQ_STAGES ? issued - WQ_STAGES : 0;
+      for (int64_t i = first; i < issued; ++i)
+        if (!ptx::mbar_wait(full_bar((int)(i % WQ_STAGES)), (uint32_t)((i / WQ_STAGES) & 1), WQ_WAIT_NS))
+          atomicCAS(&g_w8a8_quant_error, 0, 12);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int t = threadIdx.x;  // 0..255
+  const int ch = t & 15;      // 16-byte chunk within a 256-byte row
+  int64_t it = 0;
+  for (int64_t blk = blockIdx.x; blk < total; blk += gridDim.x, ++it) {
+    const int s = (int)(it % WQ_STAGES);
+    const uint32_t par = (uint32_t)((it / WQ_STAGES) & 1);
+    uint32_t ok = 1;
+    if (lane == 0) ok = ptx::mbar_wait(full_bar(s), par, WQ_WAIT_NS) ? 1u : 0u;
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    if (!ok && lane == 0) atomicCAS(&g_w8a8_quant_error, 0, 13);
+    const BlockRef r = locate_block(b, blk);
+    const uint32_t stage = sbase + s * WQ_STAGE_BYTES;
+    const bool col_ok = ch * 8 < r.cols;
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int row = (t >> 4) + 16 * j;
+      v[j] = (col_ok && row < r.rows) ? ptx::lds128(stage + row * 256 + ch * 16)
+                                      : make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(empty_bar(s));
+    uint32_t m = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      m = absmax_bf16x2_packed(m, v[j].x);
+      m = absmax_bf16x2_packed(m, v[j].y);
+      m = absmax_bf16x2_packed(m, v[j].z);
+      m = absmax_bf16x2_packed(m, v[j].w);
+    }
+    float a = absmax_finish(m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+    // Partials (and each warp's wait outcome) meet at one named barrier; the
+    // decision to stop is taken from the same shared values by every
+    // consumer, so all leave together and none waits on a barrier alone.
+    float* rb = red + (it & 1) * 8;
+    if (lane == 0) rb[warp] = ok ? a : -1.0f;
+    ptx::named_bar_sync(1, 32 * WQ_CONSUMER_WARPS);
+    if (fminf(fminf(fminf(rb[0], rb[1]), fminf(rb[2], rb[3])),
+              fminf(fminf(rb[4], rb[5]), fminf(rb[6], rb[7]))) < 0.0f)
+      break;
+    a = fmaxf(fmaxf(fmaxf(rb[0], rb[1]), fmaxf(rb[2], rb[3])),
+              fmaxf(fmaxf(rb[4], rb[5]), fmaxf(rb[6], rb[7])));
+    const float S = scale_from_amax(a);
+    const QuantScale qs = make_quant_scale(S);
+    const int64_t k = b.k[r.mat];
+    uint8_t* dstq = b.wq[r.mat] + (r.bi * 128) * k + r.bj * 128 + ch * 8;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int row = (t >> 4) + 16 * j;
+      if (col_ok && row < r.rows) {
+        uint2 c;
+        c.x = quant_bf16x4(v[j].x, v[j].y, qs);
+        c.y = quant_bf16x4(v[j].z, v[j].w, qs);
+        st_stream_v2(dstq + row * k, c);
+      }
+    }
+    if (t == 0) b.ws[r.mat][r.bi * r.nbk + r.bj] = S;
+  }
 }
 
 template <int kMax>
@@ -310,8 +428,18 @@ static cudaError_t launch_weight_batch(const WeightJob* jobs, int count, cudaStr
     b.w[i] = nullptr; b.wq[i] = nullptr; b.ws[i] = nullptr; b.n[i] = 0; b.k[i] = 0;
   }
   if (total == 0) return cudaSuccess;
-  if (total > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-  weight_quant_kernel<kMax><<<(unsigned)total, 256, 0, st>>>(b);
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    e = cudaFuncSetAttribute(weight_quant_kernel<kMax>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             WQ_SMEM);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev] = 1;
+  }
+  const unsigned grid = (unsigned)std::min<int64_t>(total, 2 * (int64_t)sm_count());
+  weight_quant_kernel<kMax><<<grid, WQ_THREADS, WQ_SMEM, st>>>(b);
   return cudaGetLastError();
 }
 
@@ -408,7 +536,7 @@ __global__ void __launch_bounds__(256) kv_quant_kernel(const uint16_t* __restric
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   // tail first (it is at the end, which pass 1 read last)
   for (int64_t j = nv * 8 + tid; j < n; j += stride)
-    q[j] = (uint8_t)(quant_pair(bf16_lo(x[j]), 0.0f, qs) & 0xFFu);
+    q[j] = (uint8_t)quant_one(bf16_lo(x[j]), qs);
   int64_t i = tid;
   for (; i + (U - 1) * stride < nv; i += U * stride) {
     uint4 v[U];
