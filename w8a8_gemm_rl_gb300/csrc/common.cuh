@@ -79,12 +79,22 @@ __device__ __forceinline__ uint32_t code_exact(float x, float s) {
   return cvt_e4m3x2(__fdiv_rn(x, s), 0.0f) & 0xFFu;
 }
 
+// The rare path, kept out of line so the hot loops stay small in the
+// instruction cache: recompute with the division the bytes of `codes` whose
+// bits are set in `diff`.
+__device__ __noinline__ uint32_t fix_codes_exact(uint32_t codes, uint32_t diff, float x0, float x1,
+                                                 float x2, float x3, float s) {
+  if (diff & 0x000000FFu) codes = (codes & 0xFFFFFF00u) | code_exact(x0, s);
+  if (diff & 0x0000FF00u) codes = (codes & 0xFFFF00FFu) | (code_exact(x1, s) << 8);
+  if (diff & 0x00FF0000u) codes = (codes & 0xFF00FFFFu) | (code_exact(x2, s) << 16);
+  if (diff & 0xFF000000u) codes = (codes & 0x00FFFFFFu) | (code_exact(x3, s) << 24);
+  return codes;
+}
+
 // Four codes (byte i = code of x_i) from four binary32 values.
 __device__ __forceinline__ uint32_t quant_f32x4(float x0, float x1, float x2, float x3,
                                                 const QuantScale& qs) {
-  if (qs.exact)
-    return code_exact(x0, qs.s) | (code_exact(x1, qs.s) << 8) | (code_exact(x2, qs.s) << 16) |
-           (code_exact(x3, qs.s) << 24);
+  if (qs.exact) return fix_codes_exact(0u, 0xFFFFFFFFu, x0, x1, x2, x3, qs.s);
   const float2 rd = make_float2(qs.r_dn, qs.r_dn), ru = make_float2(qs.r_up, qs.r_up);
   const float2 d01 = __fmul2_rn(make_float2(x0, x1), rd), u01 = __fmul2_rn(make_float2(x0, x1), ru);
   const float2 d23 = __fmul2_rn(make_float2(x2, x3), rd), u23 = __fmul2_rn(make_float2(x2, x3), ru);
@@ -93,15 +103,9 @@ __device__ __forceinline__ uint32_t quant_f32x4(float x0, float x1, float x2, fl
   const uint32_t p2 = cvt_e4m3x2(d23.x, u23.x), p3 = cvt_e4m3x2(d23.y, u23.y);
   const uint32_t a = __byte_perm(p0, p1, 0x5140);  // dn0 dn1 up0 up1
   const uint32_t b = __byte_perm(p2, p3, 0x5140);  // dn2 dn3 up2 up3
-  uint32_t dn = __byte_perm(a, b, 0x5410);
+  const uint32_t dn = __byte_perm(a, b, 0x5410);
   const uint32_t up = __byte_perm(a, b, 0x7632);
-  if (__builtin_expect(dn != up, 0)) {
-    const uint32_t diff = dn ^ up;
-    if (diff & 0x000000FFu) dn = (dn & 0xFFFFFF00u) | code_exact(x0, qs.s);
-    if (diff & 0x0000FF00u) dn = (dn & 0xFFFF00FFu) | (code_exact(x1, qs.s) << 8);
-    if (diff & 0x00FF0000u) dn = (dn & 0xFF00FFFFu) | (code_exact(x2, qs.s) << 16);
-    if (diff & 0xFF000000u) dn = (dn & 0x00FFFFFFu) | (code_exact(x3, qs.s) << 24);
-  }
+  if (__builtin_expect(dn != up, 0)) return fix_codes_exact(dn, dn ^ up, x0, x1, x2, x3, qs.s);
   return dn;
 }
 

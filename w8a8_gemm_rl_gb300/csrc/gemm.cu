@@ -16,7 +16,9 @@
 //   warp 1      allocates 512 TMEM columns; lane 0 issues 4 x
 //               tcgen05.mma.kind::f8f6f4 (128 x 256 x 32) per slab into one
 //               of two 256-column TMEM buffers, then commits to mbarriers;
-//   warps 2..9  promotion: tcgen05.ld of the slab partial, acc += P * s in
+//   warps 2, 3  idle (they complete warpgroup 0, whose registers are handed
+//               to the promotion warpgroups with setmaxnreg);
+//   warps 4..11 promotion: tcgen05.ld of the slab partial, acc += P * s in
 //               FP32 registers (128 per thread), release the TMEM buffer,
 //               and after the last slab round to BF16 and store.
 // With two TMEM buffers the MMA of slab kb+1 overlaps the promotion of slab
@@ -26,14 +28,11 @@
 // Every mbarrier wait is bounded (2 s of wall time).  A wait that gives up
 // records an error code in g_w8a8_gemm_error, tells the other roles to stop,
 // waits for its own copies / MMAs in flight, frees TMEM and returns.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include <algorithm>
-#include <mutex>
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "tmap.h"
 
 namespace w8a8 {
 
@@ -49,7 +48,13 @@ constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_EPI_WARPS = 8;
-constexpr int THREADS = 64 + 32 * NUM_EPI_WARPS;
+constexpr int EPI_WARP0 = 4;  // warpgroup 0: producer, MMA, two idle warps
+constexpr int THREADS = 32 * EPI_WARP0 + 32 * NUM_EPI_WARPS;
+// Registers: launched at 168 per thread (384 threads = 64512); warpgroup 0
+// drops to 72 and the two promotion warpgroups rise to 216:
+// 128 * 72 + 256 * 216 = 64512.
+constexpr int REGS_LAUNCH = 168, REGS_CTRL = 72, REGS_EPI = 216;
+static_assert(128 * REGS_CTRL + 256 * REGS_EPI <= THREADS * REGS_LAUNCH, "register split");
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int RASTER_M = 16;
 constexpr int GATHER_LAG = 2;  // cp.async groups kept in flight before signalling
@@ -233,6 +238,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int nkb = p.nkb;
 
+  if (warp < EPI_WARP0) {
+  // warpgroup 0 hands registers to the promotion warpgroups (one setmaxnreg
+  // for the whole warpgroup)
+  ptx::reg_dealloc<REGS_CTRL>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     uint32_t stage = 0, phase = 0;
@@ -359,35 +368,55 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (ptx::globaltimer() - t0 > WAIT_LIMIT_NS) { record_error(6); break; }
       }
     }
+  }
   } else {
     // ------------------------------------------------------------ promotion
-    const int ew = warp - 2;
+    ptx::reg_alloc<REGS_EPI>();
+    // Thread (quarter, lane) owns tile row quarter*32+lane; warps 4-7 take
+    // columns 0-127 of the tile, warps 8-11 columns 128-255 (one weight-scale
+    // block each).  Per slab: s = xs[row,kb] * ws[nb,kb] (loads issued two
+    // slabs ahead), then the partial comes out of TMEM 16 columns at a time
+    // -- the next load in flight while the current one is folded in with
+    // packed FMAs -- and the TMEM buffer is handed back as soon as the last
+    // load has landed.
+    const int ew = warp - EPI_WARP0;
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int half = ew >> 2;      // which 128 of the 256 tile columns
     const int lrow = quarter * 32 + lane;
     uint32_t tb = 0, tphase = 0;
     bool ok = true;
-    for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-      const Tile T = decode_tile<kMode>(p, t, s_prefix, s_start);
-      const bool row_ok = lrow < T.rows;
-      const int64_t yrow = T.row0 + lrow;
+
+    // per-tile state, filled for the next tile before the current one is stored
+    Tile T;
+    bool row_ok = false, src_ok = false, nb_ok = false;
+    int64_t yrow = 0;
+    const float* xsr = p.xs;
+    const float* wsr = p.ws;
+    float a0 = 0.f, w0 = 0.f, a1 = 0.f, w1 = 0.f;
+    auto setup_tile = [&](int64_t t) {
+      T = decode_tile<kMode>(p, t, s_prefix, s_start);
+      row_ok = lrow < T.rows;
+      yrow = T.row0 + lrow;
       int64_t src = yrow;
-      bool src_ok = row_ok;
+      src_ok = row_ok;
       if (kMode == GATHER && row_ok) {
         src = p.row_idx[yrow];
         src_ok = src >= 0 && src < p.rows_x;
       }
       const int nb = (T.n0 >> 7) + half;
-      const bool nb_ok = nb < p.nnb;
-      const float* xsr = p.xs + (src_ok ? src : 0) * (int64_t)nkb;
-      const float* wsr = p.ws + ((int64_t)T.e * p.nnb + (nb_ok ? nb : 0)) * nkb;
-      float a0 = src_ok ? xsr[0] : 0.0f;
-      float w0 = nb_ok ? wsr[0] : 0.0f;
-      float a1 = (src_ok && nkb > 1) ? xsr[1] : 0.0f;
-      float w1 = (nb_ok && nkb > 1) ? wsr[1] : 0.0f;
-      float acc[128];
+      nb_ok = nb < p.nnb;
+      xsr = p.xs + (src_ok ? src : 0) * (int64_t)nkb;
+      wsr = p.ws + ((int64_t)T.e * p.nnb + (nb_ok ? nb : 0)) * nkb;
+      a0 = src_ok ? xsr[0] : 0.0f;
+      w0 = nb_ok ? wsr[0] : 0.0f;
+      a1 = (src_ok && nkb > 1) ? xsr[1] : 0.0f;
+      w1 = (nb_ok && nkb > 1) ? wsr[1] : 0.0f;
+    };
+    if ((int64_t)blockIdx.x < num_tiles) setup_tile(blockIdx.x);
+    for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      float2 acc[64];
 #pragma unroll
-      for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+      for (int j = 0; j < 64; ++j) acc[j] = make_float2(0.0f, 0.0f);
       for (int kb = 0; kb < nkb; ++kb) {
         const float s = a0 * w0;
         a0 = a1;
@@ -400,40 +429,53 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!okw) { ok = false; break; }
         ptx::tc_fence_after();
         const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + tb * BN + half * 128;
+        const float2 s2 = make_float2(s, s);
+        uint32_t ra[16], rb[16];
+        ptx::tmem_ld_32x32b_x16(tcol, ra);
+        ptx::tmem_wait_ld_dep(ra);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          ptx::tmem_ld_32x32b_x32(tcol + c * 32, r);
-          ptx::tmem_wait_ld();
-          if (c == 3) {
+        for (int c = 0; c < 8; ++c) {
+          uint32_t(&cur)[16] = (c & 1) ? rb : ra;
+          uint32_t(&nxt)[16] = (c & 1) ? ra : rb;
+          if (c < 7) ptx::tmem_ld_32x32b_x16(tcol + (c + 1) * 16, nxt);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            acc[c * 8 + j] = __ffma2_rn(
+                make_float2(__uint_as_float(cur[2 * j]), __uint_as_float(cur[2 * j + 1])), s2,
+                acc[c * 8 + j]);
+          if (c < 7) ptx::tmem_wait_ld_dep(nxt);
+          if (c == 6) {
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(tempty_bar(tb));
           }
-#pragma unroll
-          for (int j = 0; j < 32; ++j) acc[c * 32 + j] = fmaf(__uint_as_float(r[j]), s, acc[c * 32 + j]);
         }
         if (++tb == 2) { tb = 0; tphase ^= 1u; }
       }
       if (!ok) break;
-      if (row_ok) {
-        uint16_t* yr = p.y + yrow * (int64_t)p.n;
-        const int c0 = T.n0 + half * 128;
+      // start the next tile's scale loads before the stores of this one
+      const bool cur_row_ok = row_ok;
+      const int64_t cur_yrow = yrow;
+      const int c0 = T.n0 + half * 128;
+      if (t + gridDim.x < num_tiles) setup_tile(t + gridDim.x);
+      if (cur_row_ok) {
+        uint16_t* yr = p.y + cur_yrow * (int64_t)p.n;
 #pragma unroll
         for (int v = 0; v < 16; ++v) {
           const int col = c0 + v * 8;
           if (col < p.n) {
             uint4 o;
-            o.x = ptx::pack_bf16x2(acc[v * 8 + 0], acc[v * 8 + 1]);
-            o.y = ptx::pack_bf16x2(acc[v * 8 + 2], acc[v * 8 + 3]);
-            o.z = ptx::pack_bf16x2(acc[v * 8 + 4], acc[v * 8 + 5]);
-            o.w = ptx::pack_bf16x2(acc[v * 8 + 6], acc[v * 8 + 7]);
+            o.x = ptx::pack_bf16x2(acc[v * 4 + 0].x, acc[v * 4 + 0].y);
+            o.y = ptx::pack_bf16x2(acc[v * 4 + 1].x, acc[v * 4 + 1].y);
+            o.z = ptx::pack_bf16x2(acc[v * 4 + 2].x, acc[v * 4 + 2].y);
+            o.w = ptx::pack_bf16x2(acc[v * 4 + 3].x, acc[v * 4 + 3].y);
             *reinterpret_cast<uint4*>(yr + col) = o;
           }
         }
       }
     }
   }
+
 
   ptx::tc_fence_before();
   __syncthreads();
@@ -447,33 +489,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 // ---------------------------------------------------------------- host side
 
-static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
-
 // Row-major [rows, cols] bytes, box [box_rows, 128 bytes], 128-byte swizzle.
 static bool make_tmap_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                          uint32_t box_rows) {
-  auto fn = get_encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols};
-  cuuint32_t box[2] = {128, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return make_tmap_2d(map, base, 1, rows, cols, box_rows, 128, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 template <int kMode>

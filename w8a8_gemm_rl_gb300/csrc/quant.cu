@@ -19,6 +19,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
+#include "tmap.h"
 
 namespace w8a8 {
 
@@ -215,11 +216,70 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const uint16_t* __restri
   }
 }
 
+// Rows that are whole multiples of 128: group g is the 256 bytes at g * 128
+// elements and its scale is s[g], so no row/column arithmetic is needed.
+// Four lanes share a group (32 values each, four 16-byte loads), which
+// spreads the per-group work -- two butterfly steps, S and the reciprocal --
+// over 32 values per lane; a warp covers 8 consecutive groups (2 KB) per
+// unit and U units are loaded before any is used.
+template <int U>
+__global__ void __launch_bounds__(256) act_quant_k128_kernel(const uint16_t* __restrict__ x,
+                                                             int64_t G, uint8_t* __restrict__ q,
+                                                             float* __restrict__ s) {
+  const int lane = threadIdx.x & 31;
+  const int sub = lane & 3, gi = lane >> 2;
+  const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t base = warp * (8 * U); base < G; base += nwarps * (8 * U)) {
+    uint4 v[U][4];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t g = base + 8 * u + gi;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        v[u][j] = g < G ? ld_stream_v4(x + g * 128 + (sub + 4 * j) * 8) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t g = base + 8 * u + gi;
+      uint32_t m2 = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        m2 = absmax_bf16x2_packed(m2, v[u][j].x);
+        m2 = absmax_bf16x2_packed(m2, v[u][j].y);
+        m2 = absmax_bf16x2_packed(m2, v[u][j].z);
+        m2 = absmax_bf16x2_packed(m2, v[u][j].w);
+      }
+      float a = absmax_finish(m2);
+      a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+      a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+      const float S = scale_from_amax(a);
+      const QuantScale qs = make_quant_scale(S);
+      if (g < G) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint2 c;
+          c.x = quant_bf16x4(v[u][j].x, v[u][j].y, qs);
+          c.y = quant_bf16x4(v[u][j].z, v[u][j].w, qs);
+          st_stream_v2(q + g * 128 + (sub + 4 * j) * 8, c);
+        }
+        if (sub == 0) s[g] = S;
+      }
+    }
+  }
+}
+
 cudaError_t launch_act_quant(const uint16_t* x, int64_t m, int64_t k, uint8_t* q, float* s,
                              cudaStream_t st) {
   if (m == 0 || k == 0) return cudaSuccess;
   if (k % 8 != 0) return launch_generic(x, m, k, 1, 128, q, s, st);
   const int64_t G = m * cdiv(k, 128);
+  if (k % 128 == 0) {
+    constexpr int U = 2;
+    const unsigned grid = grid_for(G, 8 * 8 * U, 8);  // 8 warps x 8 groups x U per CTA pass
+    act_quant_k128_kernel<U><<<grid, 256, 0, st>>>(x, G, q, s);
+    return cudaGetLastError();
+  }
   const unsigned grid = grid_for(G, 8 * 8, 16);  // 8 warps x 8 groups per CTA iteration
   if (m * k < (int64_t)0x7FFFFFFF)
     act_quant_kernel<uint32_t><<<grid, 256, 0, st>>>(x, (uint32_t)m, (uint32_t)k, q, s);
@@ -233,8 +293,9 @@ cudaError_t launch_act_quant(const uint16_t* x, int64_t m, int64_t k, uint8_t* q
 // =====================================================================
 // Persistent CTAs (2 per SM), each a producer warp plus 8 consumer warps,
 // over a 3-stage shared-memory ring of 32 KB blocks:
-//   producer  one bulk async copy per block row (up to 256 contiguous bytes)
-//             completing on the stage's mbarrier, up to 3 blocks ahead;
+//   producer  one 2-D TMA tensor load per block (128 rows x 256 bytes; rows
+//             and columns past the matrix edge arrive as zeros), completing
+//             on the stage's mbarrier, up to 3 blocks ahead;
 //   consumers 16-byte conflict-free shared loads (lanes 0-15 one row, 16-31
 //             the next), release the stage, block amax (butterfly + 8
 //             partials through shared memory + a named barrier), S, then
@@ -246,6 +307,7 @@ cudaError_t launch_act_quant(const uint16_t* x, int64_t m, int64_t k, uint8_t* q
 
 template <int kMax>
 struct WeightBatch {
+  CUtensorMap tmap[kMax];  // [n, k] BF16, box 128 x 128, zero fill outside
   const uint16_t* w[kMax];
   uint8_t* wq[kMax];
   float* ws[kMax];
@@ -328,13 +390,11 @@ __global__ void __launch_bounds__(WQ_THREADS, 2)
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok || *abort_flag) break;
       const BlockRef r = locate_block(b, blk);
-      const uint32_t row_bytes = (uint32_t)r.cols * 2u;
-      if (lane == 0) ptx::mbar_arrive_expect_tx(full_bar(s), row_bytes * (uint32_t)r.rows);
-      __syncwarp();
-      const uint16_t* src = b.w[r.mat] + (r.bi * 128) * b.k[r.mat] + r.bj * 128;
-      const uint32_t dst = sbase + s * WQ_STAGE_BYTES;
-      for (int row = lane; row < r.rows; row += 32)
-        ptx::bulk_load(dst + row * 256, src + row * b.k[r.mat], row_bytes, full_bar(s));
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(full_bar(s), WQ_STAGE_BYTES);
+        ptx::tma_load_2d(sbase + s * WQ_STAGE_BYTES, &b.tmap[r.mat], full_bar(s), (int)(r.bj * 128),
+                         (int)(r.bi * 128));
+      }
     }
     // drain: no copy may still be landing when the CTA exits
     if (lane == 0) {
@@ -362,11 +422,7 @@ __global__ void __launch_bounds__(WQ_THREADS, 2)
     const bool col_ok = ch * 8 < r.cols;
     uint4 v[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int row = (t >> 4) + 16 * j;
-      v[j] = (col_ok && row < r.rows) ? ptx::lds128(stage + row * 256 + ch * 16)
-                                      : make_uint4(0u, 0u, 0u, 0u);
-    }
+    for (int j = 0; j < 8; ++j) v[j] = ptx::lds128(stage + ((t >> 4) + 16 * j) * 256 + ch * 16);
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(empty_bar(s));
     uint32_t m = 0;
@@ -415,6 +471,9 @@ static cudaError_t launch_weight_batch(const WeightJob* jobs, int count, cudaStr
   int64_t total = 0;
   b.count = count;
   for (int i = 0; i < count; ++i) {
+    if (!make_tmap_2d(&b.tmap[i], jobs[i].w, 2, (uint64_t)jobs[i].n, (uint64_t)jobs[i].k, 128, 128,
+                      CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
     b.w[i] = jobs[i].w;
     b.wq[i] = jobs[i].wq;
     b.ws[i] = jobs[i].ws;
@@ -444,7 +503,7 @@ static cudaError_t launch_weight_batch(const WeightJob* jobs, int count, cudaStr
 }
 
 cudaError_t launch_weight_quant(const WeightJob* jobs, int count, cudaStream_t st) {
-  constexpr int kBatch = 192;  // ~10 KB of kernel parameters
+  constexpr int kBatch = 128;  // ~22 KB of kernel parameters (tensor maps included)
   WeightJob fast[kBatch];
   int nf = 0;
   for (int i = 0; i < count; ++i) {
