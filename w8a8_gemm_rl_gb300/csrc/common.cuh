@@ -91,20 +91,24 @@ __device__ __noinline__ uint32_t fix_codes_exact(uint32_t codes, uint32_t diff, 
   return codes;
 }
 
-// Four codes (byte i = code of x_i) from four binary32 values.
+// Four codes (byte i = code of x_i) from four binary32 values.  The two
+// products per value (packed FP32x2 multiplies), the four conversions and the
+// byte packing are one PTX block: t_dn codes come out as one 32-bit word and
+// t_up codes as another, compared with a single test.
 __device__ __forceinline__ uint32_t quant_f32x4(float x0, float x1, float x2, float x3,
                                                 const QuantScale& qs) {
   if (qs.exact) return fix_codes_exact(0u, 0xFFFFFFFFu, x0, x1, x2, x3, qs.s);
-  const float2 rd = make_float2(qs.r_dn, qs.r_dn), ru = make_float2(qs.r_up, qs.r_up);
-  const float2 d01 = __fmul2_rn(make_float2(x0, x1), rd), u01 = __fmul2_rn(make_float2(x0, x1), ru);
-  const float2 d23 = __fmul2_rn(make_float2(x2, x3), rd), u23 = __fmul2_rn(make_float2(x2, x3), ru);
-  // p_i = (code(t_dn_i), code(t_up_i)) in bytes 0 and 1
-  const uint32_t p0 = cvt_e4m3x2(d01.x, u01.x), p1 = cvt_e4m3x2(d01.y, u01.y);
-  const uint32_t p2 = cvt_e4m3x2(d23.x, u23.x), p3 = cvt_e4m3x2(d23.y, u23.y);
-  const uint32_t a = __byte_perm(p0, p1, 0x5140);  // dn0 dn1 up0 up1
-  const uint32_t b = __byte_perm(p2, p3, 0x5140);  // dn2 dn3 up2 up3
-  const uint32_t dn = __byte_perm(a, b, 0x5410);
-  const uint32_t up = __byte_perm(a, b, 0x7632);
+  uint32_t dn, up;
+  asm("{\n\t.reg .b16 l0, l1, h0, h1;\n\t.reg .b64 a01, a23, rd, ru, d01, d23, u01, u23;\n\t"
+      ".reg .f32 d0, d1, d2, d3, u0, u1, u2, u3;\n\t"
+      "mov.b64 a01, {%2, %3};\n\tmov.b64 a23, {%4, %5};\n\tmov.b64 rd, {%6, %6};\n\tmov.b64 ru, {%7, %7};\n\t"
+      "mul.rn.f32x2 d01, a01, rd;\n\tmul.rn.f32x2 d23, a23, rd;\n\tmul.rn.f32x2 u01, a01, ru;\n\tmul.rn.f32x2 u23, a23, ru;\n\t"
+      "mov.b64 {d0, d1}, d01;\n\tmov.b64 {d2, d3}, d23;\n\tmov.b64 {u0, u1}, u01;\n\tmov.b64 {u2, u3}, u23;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 l0, d1, d0;\n\tcvt.rn.satfinite.e4m3x2.f32 l1, d3, d2;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 h0, u1, u0;\n\tcvt.rn.satfinite.e4m3x2.f32 h1, u3, u2;\n\t"
+      "mov.b32 %0, {l0, l1};\n\tmov.b32 %1, {h0, h1};\n\t}"
+      : "=r"(dn), "=r"(up)
+      : "f"(x0), "f"(x1), "f"(x2), "f"(x3), "f"(qs.r_dn), "f"(qs.r_up));
   if (__builtin_expect(dn != up, 0)) return fix_codes_exact(dn, dn ^ up, x0, x1, x2, x3, qs.s);
   return dn;
 }
@@ -112,6 +116,46 @@ __device__ __forceinline__ uint32_t quant_f32x4(float x0, float x1, float x2, fl
 // Four codes from two BF16x2 words, packed little-endian into 32 bits.
 __device__ __forceinline__ uint32_t quant_bf16x4(uint32_t w0, uint32_t w1, const QuantScale& qs) {
   return quant_f32x4(bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1), qs);
+}
+
+// The bracketed coding of four values without the fallback branch: returns
+// the t_dn codes and sets `diff` to the bytes whose t_up code differs.
+__device__ __forceinline__ uint32_t quant_f32x4_fast(float x0, float x1, float x2, float x3,
+                                                     const QuantScale& qs, uint32_t& diff) {
+  uint32_t dn, up;
+  asm("{\n\t.reg .b16 l0, l1, h0, h1;\n\t.reg .b64 a01, a23, rd, ru, d01, d23, u01, u23;\n\t"
+      ".reg .f32 d0, d1, d2, d3, u0, u1, u2, u3;\n\t"
+      "mov.b64 a01, {%2, %3};\n\tmov.b64 a23, {%4, %5};\n\tmov.b64 rd, {%6, %6};\n\tmov.b64 ru, {%7, %7};\n\t"
+      "mul.rn.f32x2 d01, a01, rd;\n\tmul.rn.f32x2 d23, a23, rd;\n\tmul.rn.f32x2 u01, a01, ru;\n\tmul.rn.f32x2 u23, a23, ru;\n\t"
+      "mov.b64 {d0, d1}, d01;\n\tmov.b64 {d2, d3}, d23;\n\tmov.b64 {u0, u1}, u01;\n\tmov.b64 {u2, u3}, u23;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 l0, d1, d0;\n\tcvt.rn.satfinite.e4m3x2.f32 l1, d3, d2;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 h0, u1, u0;\n\tcvt.rn.satfinite.e4m3x2.f32 h1, u3, u2;\n\t"
+      "mov.b32 %0, {l0, l1};\n\tmov.b32 %1, {h0, h1};\n\t}"
+      : "=r"(dn), "=r"(up)
+      : "f"(x0), "f"(x1), "f"(x2), "f"(x3), "f"(qs.r_dn), "f"(qs.r_up));
+  diff = dn ^ up;
+  return dn;
+}
+
+// Eight codes from one 16-byte word of eight BF16 values, with a single
+// (rarely taken) branch to the exact fallback.
+__device__ __forceinline__ uint2 quant_bf16x8(const uint4& v, const QuantScale& qs) {
+  const float x0 = bf16_lo(v.x), x1 = bf16_hi(v.x), x2 = bf16_lo(v.y), x3 = bf16_hi(v.y);
+  const float x4 = bf16_lo(v.z), x5 = bf16_hi(v.z), x6 = bf16_lo(v.w), x7 = bf16_hi(v.w);
+  uint2 c;
+  if (qs.exact) {
+    c.x = fix_codes_exact(0u, 0xFFFFFFFFu, x0, x1, x2, x3, qs.s);
+    c.y = fix_codes_exact(0u, 0xFFFFFFFFu, x4, x5, x6, x7, qs.s);
+    return c;
+  }
+  uint32_t d0, d1;
+  c.x = quant_f32x4_fast(x0, x1, x2, x3, qs, d0);
+  c.y = quant_f32x4_fast(x4, x5, x6, x7, qs, d1);
+  if (__builtin_expect((d0 | d1) != 0u, 0)) {
+    if (d0) c.x = fix_codes_exact(c.x, d0, x0, x1, x2, x3, qs.s);
+    if (d1) c.y = fix_codes_exact(c.y, d1, x4, x5, x6, x7, qs.s);
+  }
+  return c;
 }
 
 // One code (the scalar path of ragged rows and tails).
@@ -129,6 +173,25 @@ __device__ __forceinline__ uint32_t absmax_bf16x2_packed(uint32_t m, uint32_t w)
 }
 __device__ __forceinline__ float absmax_finish(uint32_t m) {
   return fmaxf(bf16_lo(m), bf16_hi(m));
+}
+
+// max |x| over N x 8 BF16 values as four independent max chains.  The
+// running values keep max(|m|, |w|) as magnitude (max.xorsign.abs: the sign
+// bit is a by-product and is cleared once at the end).
+template <int N>
+__device__ __forceinline__ float absmax_bf16x8_tree(const uint4 (&v)[N]) {
+  uint32_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m0) : "r"(v[i].x));
+    asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m1) : "r"(v[i].y));
+    asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(v[i].z));
+    asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m3) : "r"(v[i].w));
+  }
+  asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m0) : "r"(m1));
+  asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(m3));
+  asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m0) : "r"(m2));
+  return absmax_finish(m0 & 0x7FFF7FFFu);
 }
 
 // ---- cache-hinted vector access for data touched once ----

@@ -242,15 +242,7 @@ __global__ void __launch_bounds__(256) act_quant_k128_kernel(const uint16_t* __r
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t g = base + 8 * u + gi;
-      uint32_t m2 = 0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        m2 = absmax_bf16x2_packed(m2, v[u][j].x);
-        m2 = absmax_bf16x2_packed(m2, v[u][j].y);
-        m2 = absmax_bf16x2_packed(m2, v[u][j].z);
-        m2 = absmax_bf16x2_packed(m2, v[u][j].w);
-      }
-      float a = absmax_finish(m2);
+      float a = absmax_bf16x8_tree<4>(v[u]);
       a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
       a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
       const float S = scale_from_amax(a);
@@ -344,10 +336,13 @@ __device__ __forceinline__ BlockRef locate_block(const WeightBatch<kMax>& b, int
   BlockRef r;
   r.mat = lo;
   const int64_t n = b.n[lo], k = b.k[lo];
-  r.nbk = (k + 127) >> 7;
-  const int64_t local = blk - b.first[lo];
-  r.bi = local / r.nbk;
-  r.bj = local - r.bi * r.nbk;
+  // block counts of one matrix fit in 32 bits (rows and columns are < 2^31)
+  const uint32_t nbk = (uint32_t)((k + 127) >> 7);
+  const uint32_t local = (uint32_t)(blk - b.first[lo]);
+  const uint32_t bi = local / nbk;
+  r.nbk = nbk;
+  r.bi = bi;
+  r.bj = local - bi * nbk;
   r.rows = (int)min((int64_t)128, n - r.bi * 128);
   r.cols = (int)min((int64_t)128, k - r.bj * 128);
   return r;
@@ -425,15 +420,7 @@ __global__ void __launch_bounds__(WQ_THREADS, 2)
     for (int j = 0; j < 8; ++j) v[j] = ptx::lds128(stage + ((t >> 4) + 16 * j) * 256 + ch * 16);
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(empty_bar(s));
-    uint32_t m = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      m = absmax_bf16x2_packed(m, v[j].x);
-      m = absmax_bf16x2_packed(m, v[j].y);
-      m = absmax_bf16x2_packed(m, v[j].z);
-      m = absmax_bf16x2_packed(m, v[j].w);
-    }
-    float a = absmax_finish(m);
+    float a = absmax_bf16x8_tree<8>(v);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
     // Partials (and each warp's wait outcome) meet at one named barrier; the
