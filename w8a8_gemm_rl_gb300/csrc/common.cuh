@@ -45,33 +45,41 @@ __device__ __forceinline__ float scale_from_amax(float amax) {
 }
 
 // ---- E4M3(RN32(x / S)), exactly, without a division per element ----
-// Let q = x / S (exact real), r = RN32(1/S), r_dn = RN32(r (1 - 2^-21)) and
-// r_up = RN32(r (1 + 2^-21)).  Each of r, r_dn/r_up and the products
-// t_dn = RN32(x r_dn), t_up = RN32(x r_up) adds one relative error of at
-// most 2^-24, so for binary32-normal q
-//     t_dn <= q (1 - 5 * 2^-24) < RN32(q) < q (1 + 5 * 2^-24) <= t_up
-// (mirrored for q < 0): the two products bracket RN32(x / S).  E4M3 coding
-// with round-to-nearest and saturation is monotone, so when t_dn and t_up
-// get the same code, RN32(x / S) gets that code too.  (When q is a
-// binary32 subnormal every candidate codes to a zero of the right sign.)
-// When the codes differ -- the bracket straddles an E4M3 rounding midpoint,
-// about 1 element in 60000 for normal-range values -- that element is
-// recomputed with the correctly rounded division.  If r_up overflows, every
-// element of the group takes the division.
+// The binary32 quotient RN32(x / S) is formed with Markstein's correction
+// step (P. Markstein, "Computation of elementary functions on the IBM
+// RISC System/6000 processor", IBM J. Res. Develop. 34(1), 1990; see also
+// Muller et al., "Handbook of Floating-Point Arithmetic", the section on
+// division with a fused multiply-add): with r = RN32(1/S) and
+// t = RN32(x r), the residual e = x - t S is exact when computed by one
+// fused multiply-add, and q = RN32(t + e r) is the correctly rounded
+// quotient as long as nothing overflows or underflows.  The hardware
+// conversion of q then gives the E4M3 code.  Two values share each packed
+// FP32x2 operation, so a pair costs three arithmetic instructions and one
+// conversion, with no branch.  Scales outside [2^-100, 2^100], and scales
+// given by a caller rather than derived from the data, take the correctly
+// rounded division instead.  A GPU self-test compares this coding with the
+// division on every (BF16 x, BF16 amax) pair the quantizers can see.
 struct QuantScale {
-  float s;     // S
-  float r_dn;  // RN32(RN32(1/S) * (1 - 2^-21))
-  float r_up;  // RN32(RN32(1/S) * (1 + 2^-21))
-  bool exact;  // bracket unavailable: use the division for every element
+  float s;      // S
+  float r;      // RN32(1 / S)
+  bool exact;   // use the division for every element
 };
 
 __device__ __forceinline__ QuantScale make_quant_scale(float s) {
   QuantScale q;
   q.s = s;
-  const float r = __frcp_rn(s);
-  q.r_dn = __fmul_rn(r, 1.0f - 0x1p-21f);
-  q.r_up = __fmul_rn(r, 1.0f + 0x1p-21f);
-  q.exact = !(q.r_up <= 3.0e38f);
+  q.r = __frcp_rn(s);
+  q.exact = !(s >= 0x1p-100f && s <= 0x1p100f);
+  return q;
+}
+
+// For a scale that does not come from the data's own amax (x / S may then
+// overflow binary32): every element takes the division.
+__device__ __forceinline__ QuantScale make_quant_scale_division(float s) {
+  QuantScale q;
+  q.s = s;
+  q.r = 0.0f;
+  q.exact = true;
   return q;
 }
 
@@ -79,83 +87,52 @@ __device__ __forceinline__ uint32_t code_exact(float x, float s) {
   return cvt_e4m3x2(__fdiv_rn(x, s), 0.0f) & 0xFFu;
 }
 
-// The rare path, kept out of line so the hot loops stay small in the
-// instruction cache: recompute with the division the bytes of `codes` whose
-// bits are set in `diff`.
-__device__ __noinline__ uint32_t fix_codes_exact(uint32_t codes, uint32_t diff, float x0, float x1,
-                                                 float x2, float x3, float s) {
-  if (diff & 0x000000FFu) codes = (codes & 0xFFFFFF00u) | code_exact(x0, s);
-  if (diff & 0x0000FF00u) codes = (codes & 0xFFFF00FFu) | (code_exact(x1, s) << 8);
-  if (diff & 0x00FF0000u) codes = (codes & 0xFF00FFFFu) | (code_exact(x2, s) << 16);
-  if (diff & 0xFF000000u) codes = (codes & 0x00FFFFFFu) | (code_exact(x3, s) << 24);
-  return codes;
+// Four codes by the correctly rounded division (out of line: the path of
+// unusual scales only).
+__device__ __noinline__ uint32_t codes_by_division(float x0, float x1, float x2, float x3,
+                                                   float s) {
+  return code_exact(x0, s) | (code_exact(x1, s) << 8) | (code_exact(x2, s) << 16) |
+         (code_exact(x3, s) << 24);
 }
 
-// Four codes (byte i = code of x_i) from four binary32 values.  The two
-// products per value (packed FP32x2 multiplies), the four conversions and the
-// byte packing are one PTX block: t_dn codes come out as one 32-bit word and
-// t_up codes as another, compared with a single test.
+// Four codes (byte i = code of x_i) from four binary32 values, except for
+// the sign of zero: an input of -0 yields +0 here (the residual of a zero
+// quotient is +0), so the callers below OR the inputs' sign bits into the
+// codes -- RN32(x / S) always has the sign of x, so that is exact.
+__device__ __forceinline__ uint32_t quant_f32x4_unsigned_zero(float x0, float x1, float x2,
+                                                              float x3, const QuantScale& qs) {
+  if (qs.exact) return codes_by_division(x0, x1, x2, x3, qs.s);
+  uint32_t c;
+  asm("{\n\t.reg .b16 l0, l1;\n\t.reg .b64 a01, a23, rr, ns, t01, t23, e01, e23, q01, q23;\n\t"
+      ".reg .f32 q0, q1, q2, q3;\n\t"
+      "mov.b64 a01, {%1, %2};\n\tmov.b64 a23, {%3, %4};\n\t"
+      "mov.b64 rr, {%5, %5};\n\tmov.b64 ns, {%6, %6};\n\t"
+      "mul.rn.f32x2 t01, a01, rr;\n\tmul.rn.f32x2 t23, a23, rr;\n\t"
+      "fma.rn.f32x2 e01, t01, ns, a01;\n\tfma.rn.f32x2 e23, t23, ns, a23;\n\t"
+      "fma.rn.f32x2 q01, e01, rr, t01;\n\tfma.rn.f32x2 q23, e23, rr, t23;\n\t"
+      "mov.b64 {q0, q1}, q01;\n\tmov.b64 {q2, q3}, q23;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 l0, q1, q0;\n\tcvt.rn.satfinite.e4m3x2.f32 l1, q3, q2;\n\t"
+      "mov.b32 %0, {l0, l1};\n\t}"
+      : "=r"(c)
+      : "f"(x0), "f"(x1), "f"(x2), "f"(x3), "f"(qs.r), "f"(-qs.s));
+  return c;
+}
+
+// Four codes (byte i = code of x_i) from four binary32 values.
 __device__ __forceinline__ uint32_t quant_f32x4(float x0, float x1, float x2, float x3,
                                                 const QuantScale& qs) {
-  if (qs.exact) return fix_codes_exact(0u, 0xFFFFFFFFu, x0, x1, x2, x3, qs.s);
-  uint32_t dn, up;
-  asm("{\n\t.reg .b16 l0, l1, h0, h1;\n\t.reg .b64 a01, a23, rd, ru, d01, d23, u01, u23;\n\t"
-      ".reg .f32 d0, d1, d2, d3, u0, u1, u2, u3;\n\t"
-      "mov.b64 a01, {%2, %3};\n\tmov.b64 a23, {%4, %5};\n\tmov.b64 rd, {%6, %6};\n\tmov.b64 ru, {%7, %7};\n\t"
-      "mul.rn.f32x2 d01, a01, rd;\n\tmul.rn.f32x2 d23, a23, rd;\n\tmul.rn.f32x2 u01, a01, ru;\n\tmul.rn.f32x2 u23, a23, ru;\n\t"
-      "mov.b64 {d0, d1}, d01;\n\tmov.b64 {d2, d3}, d23;\n\tmov.b64 {u0, u1}, u01;\n\tmov.b64 {u2, u3}, u23;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f32 l0, d1, d0;\n\tcvt.rn.satfinite.e4m3x2.f32 l1, d3, d2;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f32 h0, u1, u0;\n\tcvt.rn.satfinite.e4m3x2.f32 h1, u3, u2;\n\t"
-      "mov.b32 %0, {l0, l1};\n\tmov.b32 %1, {h0, h1};\n\t}"
-      : "=r"(dn), "=r"(up)
-      : "f"(x0), "f"(x1), "f"(x2), "f"(x3), "f"(qs.r_dn), "f"(qs.r_up));
-  if (__builtin_expect(dn != up, 0)) return fix_codes_exact(dn, dn ^ up, x0, x1, x2, x3, qs.s);
-  return dn;
+  const uint32_t c = quant_f32x4_unsigned_zero(x0, x1, x2, x3, qs);
+  const uint32_t s01 = __byte_perm(__float_as_uint(x0), __float_as_uint(x1), 0x0073);
+  const uint32_t s23 = __byte_perm(__float_as_uint(x2), __float_as_uint(x3), 0x0073);
+  return c | (__byte_perm(s01, s23, 0x5410) & 0x80808080u);
 }
 
-// Four codes from two BF16x2 words, packed little-endian into 32 bits.
+// Four codes from two BF16x2 words, packed little-endian into 32 bits (the
+// sign bits come straight from the words: bytes 1 and 3 of each).
 __device__ __forceinline__ uint32_t quant_bf16x4(uint32_t w0, uint32_t w1, const QuantScale& qs) {
-  return quant_f32x4(bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1), qs);
-}
-
-// The bracketed coding of four values without the fallback branch: returns
-// the t_dn codes and sets `diff` to the bytes whose t_up code differs.
-__device__ __forceinline__ uint32_t quant_f32x4_fast(float x0, float x1, float x2, float x3,
-                                                     const QuantScale& qs, uint32_t& diff) {
-  uint32_t dn, up;
-  asm("{\n\t.reg .b16 l0, l1, h0, h1;\n\t.reg .b64 a01, a23, rd, ru, d01, d23, u01, u23;\n\t"
-      ".reg .f32 d0, d1, d2, d3, u0, u1, u2, u3;\n\t"
-      "mov.b64 a01, {%2, %3};\n\tmov.b64 a23, {%4, %5};\n\tmov.b64 rd, {%6, %6};\n\tmov.b64 ru, {%7, %7};\n\t"
-      "mul.rn.f32x2 d01, a01, rd;\n\tmul.rn.f32x2 d23, a23, rd;\n\tmul.rn.f32x2 u01, a01, ru;\n\tmul.rn.f32x2 u23, a23, ru;\n\t"
-      "mov.b64 {d0, d1}, d01;\n\tmov.b64 {d2, d3}, d23;\n\tmov.b64 {u0, u1}, u01;\n\tmov.b64 {u2, u3}, u23;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f32 l0, d1, d0;\n\tcvt.rn.satfinite.e4m3x2.f32 l1, d3, d2;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f32 h0, u1, u0;\n\tcvt.rn.satfinite.e4m3x2.f32 h1, u3, u2;\n\t"
-      "mov.b32 %0, {l0, l1};\n\tmov.b32 %1, {h0, h1};\n\t}"
-      : "=r"(dn), "=r"(up)
-      : "f"(x0), "f"(x1), "f"(x2), "f"(x3), "f"(qs.r_dn), "f"(qs.r_up));
-  diff = dn ^ up;
-  return dn;
-}
-
-// Eight codes from one 16-byte word of eight BF16 values, with a single
-// (rarely taken) branch to the exact fallback.
-__device__ __forceinline__ uint2 quant_bf16x8(const uint4& v, const QuantScale& qs) {
-  const float x0 = bf16_lo(v.x), x1 = bf16_hi(v.x), x2 = bf16_lo(v.y), x3 = bf16_hi(v.y);
-  const float x4 = bf16_lo(v.z), x5 = bf16_hi(v.z), x6 = bf16_lo(v.w), x7 = bf16_hi(v.w);
-  uint2 c;
-  if (qs.exact) {
-    c.x = fix_codes_exact(0u, 0xFFFFFFFFu, x0, x1, x2, x3, qs.s);
-    c.y = fix_codes_exact(0u, 0xFFFFFFFFu, x4, x5, x6, x7, qs.s);
-    return c;
-  }
-  uint32_t d0, d1;
-  c.x = quant_f32x4_fast(x0, x1, x2, x3, qs, d0);
-  c.y = quant_f32x4_fast(x4, x5, x6, x7, qs, d1);
-  if (__builtin_expect((d0 | d1) != 0u, 0)) {
-    if (d0) c.x = fix_codes_exact(c.x, d0, x0, x1, x2, x3, qs.s);
-    if (d1) c.y = fix_codes_exact(c.y, d1, x4, x5, x6, x7, qs.s);
-  }
-  return c;
+  const uint32_t c =
+      quant_f32x4_unsigned_zero(bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1), qs);
+  return c | (__byte_perm(w0, w1, 0x7531) & 0x80808080u);
 }
 
 // One code (the scalar path of ragged rows and tails).

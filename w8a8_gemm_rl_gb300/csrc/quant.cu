@@ -575,7 +575,8 @@ __global__ void __launch_bounds__(256) kv_quant_kernel(const uint16_t* __restric
     if (blockIdx.x == 0 && threadIdx.x == 0) *scale = S;
     if (mode == 1) return;
   }
-  const QuantScale qs = make_quant_scale(S);
+  // a scale handed in by the caller may make x / S overflow: code by division
+  const QuantScale qs = mode == 2 ? make_quant_scale_division(S) : make_quant_scale(S);
   constexpr int U = 4;
   const int64_t nv = n / 8;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
