@@ -237,7 +237,7 @@ class Workload:
         return outs
 
 
-LAUNCHES_PER_STEP = 2 + 4 * 2 + 4 + 2 * 2  # weight batches (128 + 16 matrices), 4 x (act quant + GEMM), MoE 4, KV 2 x 2
+LAUNCHES_PER_STEP = 1 + 4 * 2 + 4 + 2 * 2  # weight batch (144 matrices), 4 x (act quant + GEMM), MoE 4, KV 2 x 2
 
 
 def run_step(W, wl, events=None):

@@ -490,7 +490,7 @@ static cudaError_t launch_weight_batch(const WeightJob* jobs, int count, cudaStr
 }
 
 cudaError_t launch_weight_quant(const WeightJob* jobs, int count, cudaStream_t st) {
-  constexpr int kBatch = 128;  // ~22 KB of kernel parameters (tensor maps included)
+  constexpr int kBatch = 160;  // ~28 KB of kernel parameters (tensor maps included)
   WeightJob fast[kBatch];
   int nf = 0;
   for (int i = 0; i < count; ++i) {
