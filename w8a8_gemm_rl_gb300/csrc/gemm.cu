@@ -11,13 +11,14 @@
 // tensor memory and promoted into FP32 registers with its scale.
 //
 // Kernel structure (persistent, one CTA per SM, warp-specialized):
-//   warp 0      producer: TMA (or a cp.async row gather for routed MoE rows)
-//               of the A and B K-slabs into a 4-stage shared-memory ring;
+//   warp 0      producer: TMA of the A and B K-slabs into a 4-stage
+//               shared-memory ring (for routed MoE rows, B only);
 //   warp 1      allocates 512 TMEM columns; lane 0 issues 4 x
 //               tcgen05.mma.kind::f8f6f4 (128 x 256 x 32) per slab into one
 //               of two 256-column TMEM buffers, then commits to mbarriers;
-//   warps 2, 3  idle (they complete warpgroup 0, whose registers are handed
-//               to the promotion warpgroups with setmaxnreg);
+//   warps 2, 3  routed MoE rows: gather the A rows with cp.async, 64 rows
+//               each; otherwise idle (they complete warpgroup 0, whose
+//               registers are handed to the promotion warpgroups);
 //   warps 4..11 promotion: tcgen05.ld of the slab partial, acc += P * s in
 //               FP32 registers (128 per thread), release the TMEM buffer,
 //               and after the last slab round to BF16 and store.
@@ -48,7 +49,7 @@ constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_EPI_WARPS = 8;
-constexpr int EPI_WARP0 = 4;  // warpgroup 0: producer, MMA, two idle warps
+constexpr int EPI_WARP0 = 4;  // warpgroup 0: producer, MMA, two gather warps
 constexpr int THREADS = 32 * EPI_WARP0 + 32 * NUM_EPI_WARPS;
 // Registers: launched at 168 per thread (384 threads = 64512); warpgroup 0
 // drops to 72 and the two promotion warpgroups rise to 216:
@@ -57,7 +58,6 @@ constexpr int REGS_LAUNCH = 168, REGS_CTRL = 72, REGS_EPI = 216;
 static_assert(128 * REGS_CTRL + 256 * REGS_EPI <= THREADS * REGS_LAUNCH, "register split");
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int RASTER_M = 16;
-constexpr int GATHER_LAG = 2;  // cp.async groups kept in flight before signalling
 constexpr int MAX_GROUPS = 1024;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr uint32_t IDESC = ptx::idesc_e4m3_f32(BM, BN);
@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      ptx::mbar_init(full_bar(s), kMode == GATHER ? 1 + 32 : 1);
+      ptx::mbar_init(full_bar(s), kMode == GATHER ? 1 + 64 : 1);
       ptx::mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -247,82 +247,23 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t stage = 0, phase = 0;
     int64_t issued = 0;
     bool ok = true;
-    if (kMode != GATHER) {
-      if (lane == 0) {
-        for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-          const Tile T = decode_tile<kMode>(p, t, s_prefix, s_start);
-          const int brow = T.e * p.n + T.n0;
-          for (int kb = 0; kb < nkb; ++kb) {
-            if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, 1)) { ok = false; break; }
-            const uint32_t sa = sbase + stage * STAGE_BYTES;
-            ptx::mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
-            ptx::tma_load_2d(sa, &tmap_a, full_bar(stage), kb * BK, (int)T.row0);
-            ptx::tma_load_2d(sa + A_BYTES, &tmap_b, full_bar(stage), kb * BK, brow);
-            ++issued;
-            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-          }
-        }
-      }
-    } else {
-      // routed rows: lane l copies rows l, l+32, l+64, l+96 of the A slab with
-      // 16-byte cp.async into the 128-byte-swizzled layout the MMA expects;
-      // lane 0 also brings the B slab by TMA.
-      int64_t pending_from = 0;  // first issued stage not yet signalled
-      uint32_t sig_stage = 0;
+    if (lane == 0) {
       for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
         const Tile T = decode_tile<kMode>(p, t, s_prefix, s_start);
         const int brow = T.e * p.n + T.n0;
-        const uint8_t* src[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int r = lane + 32 * j;
-          src[j] = nullptr;
-          if (r < T.rows) {
-            const int64_t s = p.row_idx[T.row0 + r];
-            if (s >= 0 && s < p.rows_x) src[j] = p.xq + s * (int64_t)p.k;
-          }
-        }
         for (int kb = 0; kb < nkb; ++kb) {
-          uint32_t okw = 1;
-          if (lane == 0) okw = wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, 2) ? 1u : 0u;
-          okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
-          if (!okw) { ok = false; break; }
+          if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, 1)) { ok = false; break; }
           const uint32_t sa = sbase + stage * STAGE_BYTES;
-          if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(full_bar(stage), B_BYTES);
-            ptx::tma_load_2d(sa + A_BYTES, &tmap_b, full_bar(stage), kb * BK, brow);
+          if (kMode != GATHER) {
+            ptx::mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
+            ptx::tma_load_2d(sa, &tmap_a, full_bar(stage), kb * BK, (int)T.row0);
+          } else {
+            ptx::mbar_arrive_expect_tx(full_bar(stage), B_BYTES);  // A: warps 2, 3
           }
-          const int kofs = kb * BK;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int r = lane + 32 * j;
-            const uint32_t rbase = sa + r * 128;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const int kc = kofs + c * 16;
-              const bool in = src[j] != nullptr && kc < p.k;
-              ptx::cp_async_16(rbase + ((c ^ (r & 7)) << 4), in ? src[j] + kc : p.xq,
-                               in ? 16u : 0u);
-            }
-          }
-          ptx::cp_async_commit();
+          ptx::tma_load_2d(sa + A_BYTES, &tmap_b, full_bar(stage), kb * BK, brow);
           ++issued;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-          if (issued - pending_from > GATHER_LAG) {
-            ptx::cp_async_wait_group<GATHER_LAG>();
-            ptx::fence_proxy_async_smem();
-            ptx::mbar_arrive(full_bar(sig_stage));
-            ++pending_from;
-            if (++sig_stage == STAGES) sig_stage = 0;
-          }
         }
-      }
-      ptx::cp_async_wait_group<0>();
-      ptx::fence_proxy_async_smem();
-      while (pending_from < issued) {
-        ptx::mbar_arrive(full_bar(sig_stage));
-        ++pending_from;
-        if (++sig_stage == STAGES) sig_stage = 0;
       }
     }
     // Before leaving, make sure no copy is still landing in shared memory:
@@ -338,6 +279,56 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     }
+  } else if (kMode == GATHER && warp >= 2) {
+    // ------------------------------------------------- routed-row A gather
+    // Warp 2 + w copies tile rows 64w .. 64w+63 of each A slab with 16-byte
+    // cp.async into the 128-byte-swizzled layout the MMA expects: lane l
+    // takes chunk l % 8 of rows 64w + 4j + l / 8 (j = 0..15), so every
+    // warp-wide copy moves four whole 128-byte rows.  A row past the group's
+    // end, or whose index lies outside [0, rows_x), is zero-filled.  Each
+    // lane's copies of a stage arrive on the stage's full barrier once they
+    // have landed (cp.async.mbarrier.arrive), so the warp never waits for
+    // its own copies and keeps up to STAGES slabs in flight.
+    const int w = warp - 2;
+    const int q = lane >> 3, c = lane & 7;
+    // swizzled offset of (row 64w + 4j + q, chunk c): (row & 7) = 4 (j & 1) + q
+    const uint32_t dofs_even = (uint32_t)((64 * w + q) * 128 + ((c ^ q) << 4));
+    const uint32_t dofs_odd = (uint32_t)((64 * w + q) * 128 + ((c ^ (q | 4)) << 4));
+    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      const Tile T = decode_tile<kMode>(p, t, s_prefix, s_start);
+      int32_t src_row[16];
+      uint32_t valid = 0;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int r = 64 * w + 4 * j + q;
+        int64_t sr = -1;
+        if (r < T.rows) sr = p.row_idx[T.row0 + r];
+        const bool v = sr >= 0 && sr < p.rows_x;
+        src_row[j] = v ? (int32_t)sr : 0;
+        valid |= (v ? 1u : 0u) << j;
+      }
+      for (int kb = 0; kb < nkb; ++kb) {
+        uint32_t okw = 1;
+        if (lane == 0) okw = wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, 2) ? 1u : 0u;
+        okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+        if (!okw) { ok = false; break; }
+        const uint32_t sa = sbase + stage * STAGE_BYTES;
+        const int kc = kb * BK + c * 16;
+        const uint32_t vk = kc < p.k ? valid : 0u;
+        const uint8_t* xk = p.xq + kc;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const bool in = (vk >> j) & 1u;
+          ptx::cp_async_16(sa + 512u * j + ((j & 1) ? dofs_odd : dofs_even),
+                           in ? xk + (int64_t)src_row[j] * p.k : p.xq, in ? 16u : 0u);
+        }
+        ptx::cp_async_arrive_noinc(full_bar(stage));
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    ptx::cp_async_wait_all();
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issue
     if (lane == 0) {
@@ -347,6 +338,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int kb = 0; kb < nkb; ++kb) {
           if (!wait_bar(tempty_bar(tb), tphase ^ 1u, abort_flag, 4)) { ok = false; break; }
           if (!wait_bar(full_bar(stage), phase, abort_flag, 5)) { ok = false; break; }
+          // gathered A rows were written by cp.async (generic proxy); the
+          // MMA reads them through the async proxy
+          if (kMode == GATHER) ptx::fence_proxy_async_smem();
           ptx::tc_fence_after();
           const uint32_t sa = sbase + stage * STAGE_BYTES;
           const uint64_t adesc = ptx::smem_desc_kmajor_sw128(sa);

@@ -103,15 +103,17 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint3
                "r"(src_bytes)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
+// Arrive on an mbarrier once every cp.async this thread issued so far has
+// landed; the barrier's expected count includes this arrival (.noinc).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
-// Make this thread's generic-proxy shared-memory writes visible to the async
-// proxy (the tensor cores read operands through it).
+// Proxy fence: shared-memory writes of the generic proxy that this thread has
+// made or observed (through an mbarrier) are ordered before its later
+// async-proxy accesses (the tensor cores read operands through that proxy).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
