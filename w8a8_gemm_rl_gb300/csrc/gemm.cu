@@ -12,13 +12,14 @@
 //
 // Kernel structure (persistent, one CTA per SM, warp-specialized):
 //   warp 0      producer: TMA of the A and B K-slabs into a 4-stage
-//               shared-memory ring (for routed MoE rows, B only);
+//               shared-memory ring (for routed MoE rows, B by TMA and A rows
+//               0-63 by a cp.async gather);
 //   warp 1      allocates 512 TMEM columns; lane 0 issues 4 x
 //               tcgen05.mma.kind::f8f6f4 (128 x 256 x 32) per slab into one
 //               of two 256-column TMEM buffers, then commits to mbarriers;
-//   warps 2, 3  routed MoE rows: gather the A rows with cp.async, 64 rows
-//               each; otherwise idle (they complete warpgroup 0, whose
-//               registers are handed to the promotion warpgroups);
+//   warp 2      waits for each slab's MMAs and releases the promotion warps
+//               through a named barrier per TMEM buffer;
+//   warp 3      routed MoE rows: gathers A rows 64-127; otherwise idle;
 //   warps 4..11 promotion: tcgen05.ld of the slab partial, acc += P * s in
 //               FP32 registers (128 per thread), release the TMEM buffer,
 //               and after the last slab round to BF16 and store.
@@ -49,7 +50,7 @@ constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_EPI_WARPS = 8;
-constexpr int EPI_WARP0 = 4;  // warpgroup 0: producer, MMA, two gather warps
+constexpr int EPI_WARP0 = 4;  // warpgroup 0: producer, MMA, hand-off, gather
 constexpr int THREADS = 32 * EPI_WARP0 + 32 * NUM_EPI_WARPS;
 // Registers: launched at 168 per thread (384 threads = 64512); warpgroup 0
 // drops to 72 and the two promotion warpgroups rise to 216:
@@ -60,6 +61,11 @@ constexpr int TMEM_COLS = 2 * BN;
 constexpr int RASTER_M = 16;
 constexpr int MAX_GROUPS = 1024;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+constexpr uint64_t ABORT_DRAIN_LIMIT_NS = 10000000000ull;
+// named barriers 1 and 2 (0 is __syncthreads): warp 2 hands the slab in
+// TMEM buffer b to the promotion warps on barrier BAR_SLAB + b
+constexpr uint32_t BAR_SLAB = 1;
+constexpr uint32_t BAR_SLAB_THREADS = 32 * (1 + NUM_EPI_WARPS);
 constexpr uint32_t IDESC = ptx::idesc_e4m3_f32(BM, BN);
 
 // shared-memory map (offsets from a 1024-byte aligned base)
@@ -242,33 +248,85 @@ __global__ void __launch_bounds__(THREADS, 1)
   // warpgroup 0 hands registers to the promotion warpgroups (one setmaxnreg
   // for the whole warpgroup)
   ptx::reg_dealloc<REGS_CTRL>();
-  if (warp == 0) {
+  if (warp == 0 || (kMode == GATHER && warp == 3)) {
     // ------------------------------------------------------------ producer
     uint32_t stage = 0, phase = 0;
-    int64_t issued = 0;
+    int64_t issued = 0;  // stages whose B slab (and A slab) lane 0 of warp 0 loaded by TMA
     bool ok = true;
-    if (lane == 0) {
+    if (kMode != GATHER) {
+      if (lane == 0) {
+        for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+          const Tile T = decode_tile<kMode>(p, t, s_prefix, s_start);
+          const int brow = T.e * p.n + T.n0;
+          for (int kb = 0; kb < nkb; ++kb) {
+            if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, 1)) { ok = false; break; }
+            const uint32_t sa = sbase + stage * STAGE_BYTES;
+            ptx::mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
+            ptx::tma_load_2d(sa, &tmap_a, full_bar(stage), kb * BK, (int)T.row0);
+            ptx::tma_load_2d(sa + A_BYTES, &tmap_b, full_bar(stage), kb * BK, brow);
+            ++issued;
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          }
+        }
+      }
+    } else {
+      // Routed rows: warps 0 and 3 copy tile rows 0-63 and 64-127 of each A
+      // slab with 16-byte cp.async into the 128-byte-swizzled layout the MMA
+      // expects; lane 0 of warp 0 also brings the B slab by TMA.  Lane l
+      // takes chunk l % 8 of rows 64w + 4j + l / 8 (j = 0..15), so every
+      // warp-wide copy moves four whole 128-byte rows.  A row past the
+      // group's end, or whose index lies outside [0, rows_x), is zero-filled.
+      // Each lane's copies of a stage arrive on the stage's full barrier once
+      // they have landed (cp.async.mbarrier.arrive), so the warps never wait
+      // for their own copies and keep up to STAGES slabs in flight.
+      const int w = warp == 0 ? 0 : 1;
+      const int q = lane >> 3, c = lane & 7;
+      // swizzled offset of (row 64w + 4j + q, chunk c): (row & 7) = 4 (j & 1) + q
+      const uint32_t dofs_even = (uint32_t)((64 * w + q) * 128 + ((c ^ q) << 4));
+      const uint32_t dofs_odd = (uint32_t)((64 * w + q) * 128 + ((c ^ (q | 4)) << 4));
       for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
         const Tile T = decode_tile<kMode>(p, t, s_prefix, s_start);
         const int brow = T.e * p.n + T.n0;
+        int32_t src_row[16];
+        uint32_t valid = 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int r = 64 * w + 4 * j + q;
+          int64_t sr = -1;
+          if (r < T.rows) sr = p.row_idx[T.row0 + r];
+          const bool v = sr >= 0 && sr < p.rows_x;
+          src_row[j] = v ? (int32_t)sr : 0;
+          valid |= (v ? 1u : 0u) << j;
+        }
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, 1)) { ok = false; break; }
+          uint32_t okw = 1;
+          if (lane == 0) okw = wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, 2) ? 1u : 0u;
+          okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+          if (!okw) { ok = false; break; }
           const uint32_t sa = sbase + stage * STAGE_BYTES;
-          if (kMode != GATHER) {
-            ptx::mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
-            ptx::tma_load_2d(sa, &tmap_a, full_bar(stage), kb * BK, (int)T.row0);
-          } else {
-            ptx::mbar_arrive_expect_tx(full_bar(stage), B_BYTES);  // A: warps 2, 3
+          if (warp == 0 && lane == 0) {
+            ptx::mbar_arrive_expect_tx(full_bar(stage), B_BYTES);
+            ptx::tma_load_2d(sa + A_BYTES, &tmap_b, full_bar(stage), kb * BK, brow);
+            ++issued;
           }
-          ptx::tma_load_2d(sa + A_BYTES, &tmap_b, full_bar(stage), kb * BK, brow);
-          ++issued;
+          const int kc = kb * BK + c * 16;
+          const uint32_t vk = kc < p.k ? valid : 0u;
+          const uint8_t* xk = p.xq + kc;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const bool in = (vk >> j) & 1u;
+            ptx::cp_async_16(sa + 512u * j + ((j & 1) ? dofs_odd : dofs_even),
+                             in ? xk + (int64_t)src_row[j] * p.k : p.xq, in ? 16u : 0u);
+          }
+          ptx::cp_async_arrive_noinc(full_bar(stage));
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
+      ptx::cp_async_wait_all();
     }
-    // Before leaving, make sure no copy is still landing in shared memory:
-    // wait (bounded) for the last phase of each stage this warp filled.
-    if (lane == 0 && issued > 0) {
+    // Before leaving, make sure no TMA copy is still landing in shared
+    // memory: wait (bounded) for the last phase of each stage filled.
+    if (warp == 0 && lane == 0 && issued > 0) {
       const int64_t first = issued > STAGES ? issued - STAGES : 0;
       for (int64_t i = first; i < issued; ++i) {
         const uint32_t s = (uint32_t)(i % STAGES);
@@ -279,56 +337,39 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     }
-  } else if (kMode == GATHER && warp >= 2) {
-    // ------------------------------------------------- routed-row A gather
-    // Warp 2 + w copies tile rows 64w .. 64w+63 of each A slab with 16-byte
-    // cp.async into the 128-byte-swizzled layout the MMA expects: lane l
-    // takes chunk l % 8 of rows 64w + 4j + l / 8 (j = 0..15), so every
-    // warp-wide copy moves four whole 128-byte rows.  A row past the group's
-    // end, or whose index lies outside [0, rows_x), is zero-filled.  Each
-    // lane's copies of a stage arrive on the stage's full barrier once they
-    // have landed (cp.async.mbarrier.arrive), so the warp never waits for
-    // its own copies and keeps up to STAGES slabs in flight.
-    const int w = warp - 2;
-    const int q = lane >> 3, c = lane & 7;
-    // swizzled offset of (row 64w + 4j + q, chunk c): (row & 7) = 4 (j & 1) + q
-    const uint32_t dofs_even = (uint32_t)((64 * w + q) * 128 + ((c ^ q) << 4));
-    const uint32_t dofs_odd = (uint32_t)((64 * w + q) * 128 + ((c ^ (q | 4)) << 4));
-    uint32_t stage = 0, phase = 0;
+  } else if (warp == 2) {
+    // ------------------------------------------------------ slab hand-off
+    // Lane 0 waits for each slab's MMAs to finish; then the warp releases the
+    // eight promotion warps through the named barrier of the slab's TMEM
+    // buffer.  A hardware barrier wakes all eight at once; waiting on the
+    // MMA's mbarrier (or polling a shared-memory word) themselves, they woke
+    // hundreds of cycles apart, and the slowest one gates the next MMA into
+    // that buffer.
+    //
+    // Why the promotion warps can never be left waiting: this warp arrives
+    // exactly once per slab of the CTA's tile sequence, and the promotion
+    // warps wait exactly once per slab, on barrier 1 + buffer.  An arrival
+    // for slab j on buffer b's barrier must not come before all eight warps
+    // have passed that barrier for slab j-2, or the two generations would
+    // mix.  Normally this holds because slab j's MMA was issued only after
+    // the eight warps released buffer b (tempty) after slab j-2.  After an
+    // abort (no more MMAs to wait for) the warp waits for that release
+    // itself, which the promotion warps always make: they wait on nothing
+    // but these barriers.
+    uint32_t tb = 0, tphase = 0;
     bool ok = true;
-    for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-      const Tile T = decode_tile<kMode>(p, t, s_prefix, s_start);
-      int32_t src_row[16];
-      uint32_t valid = 0;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int r = 64 * w + 4 * j + q;
-        int64_t sr = -1;
-        if (r < T.rows) sr = p.row_idx[T.row0 + r];
-        const bool v = sr >= 0 && sr < p.rows_x;
-        src_row[j] = v ? (int32_t)sr : 0;
-        valid |= (v ? 1u : 0u) << j;
-      }
+    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
       for (int kb = 0; kb < nkb; ++kb) {
-        uint32_t okw = 1;
-        if (lane == 0) okw = wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, 2) ? 1u : 0u;
-        okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
-        if (!okw) { ok = false; break; }
-        const uint32_t sa = sbase + stage * STAGE_BYTES;
-        const int kc = kb * BK + c * 16;
-        const uint32_t vk = kc < p.k ? valid : 0u;
-        const uint8_t* xk = p.xq + kc;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const bool in = (vk >> j) & 1u;
-          ptx::cp_async_16(sa + 512u * j + ((j & 1) ? dofs_odd : dofs_even),
-                           in ? xk + (int64_t)src_row[j] * p.k : p.xq, in ? 16u : 0u);
+        if (lane == 0) {
+          if (ok) ok = wait_bar(tfull_bar(tb), tphase, abort_flag, 7);
+          if (!ok && !ptx::mbar_wait(tempty_bar(tb), tphase ^ 1u, ABORT_DRAIN_LIMIT_NS))
+            record_error(8);
         }
-        ptx::cp_async_arrive_noinc(full_bar(stage));
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        __syncwarp();
+        ptx::named_bar_arrive(BAR_SLAB + tb, BAR_SLAB_THREADS);
+        if (++tb == 2) { tb = 0; tphase ^= 1u; }
       }
     }
-    ptx::cp_async_wait_all();
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issue
     if (lane == 0) {
@@ -377,8 +418,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int half = ew >> 2;      // which 128 of the 256 tile columns
     const int lrow = quarter * 32 + lane;
-    uint32_t tb = 0, tphase = 0;
-    bool ok = true;
+    uint32_t tb = 0;
 
     // per-tile state, filled for the next tile before the current one is stored
     Tile T;
@@ -407,7 +447,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       w1 = (nb_ok && nkb > 1) ? wsr[1] : 0.0f;
     };
     if ((int64_t)blockIdx.x < num_tiles) setup_tile(blockIdx.x);
-    for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
       float2 acc[64];
 #pragma unroll
       for (int j = 0; j < 64; ++j) acc[j] = make_float2(0.0f, 0.0f);
@@ -417,10 +457,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         w0 = w1;
         a1 = (src_ok && kb + 2 < nkb) ? xsr[kb + 2] : 0.0f;
         w1 = (nb_ok && kb + 2 < nkb) ? wsr[kb + 2] : 0.0f;
-        uint32_t okw = 1;
-        if (lane == 0) okw = wait_bar(tfull_bar(tb), tphase, abort_flag, 7) ? 1u : 0u;
-        okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
-        if (!okw) { ok = false; break; }
+        ptx::named_bar_sync(BAR_SLAB + tb, BAR_SLAB_THREADS);  // slab kb is in TMEM buffer tb
         ptx::tc_fence_after();
         const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + tb * BN + half * 128;
         const float2 s2 = make_float2(s, s);
@@ -444,9 +481,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (lane == 0) ptx::mbar_arrive(tempty_bar(tb));
           }
         }
-        if (++tb == 2) { tb = 0; tphase ^= 1u; }
+        tb ^= 1u;
       }
-      if (!ok) break;
       // start the next tile's scale loads before the stores of this one
       const bool cur_row_ok = row_ok;
       const int64_t cur_yrow = yrow;
