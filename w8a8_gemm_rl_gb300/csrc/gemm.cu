@@ -72,10 +72,18 @@ constexpr uint32_t IDESC = ptx::idesc_e4m3_f32(BM, BN);
 constexpr int OFF_BARS = STAGES * STAGE_BYTES;
 constexpr int NUM_BARS = 2 * STAGES + 4 + 1;  // full, empty, tfull[2], tempty[2], done
 constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
-constexpr int OFF_GROUPS = (OFF_MISC + 16 + 15) / 16 * 16;
-constexpr int smem_bytes(int g) { return 1024 + OFF_GROUPS + 2 * 4 * (g + 1); }
-
 enum Mode { DENSE = 0, GROUPED = 1, GATHER = 2 };
+// Output staging: each promotion warp turns its 32 rows x 128 columns into
+// row-contiguous global stores through a private area of 32 rows x
+// store_cols BF16 columns, in 128 / store_cols passes (narrower for the
+// grouped modes, whose group tables also need room).
+__host__ __device__ constexpr int store_cols(int mode) { return mode == DENSE ? 64 : 32; }
+constexpr int OFF_STAGE = (OFF_MISC + 16 + 15) / 16 * 16;
+__host__ __device__ constexpr int stage_bytes(int mode) { return NUM_EPI_WARPS * 32 * store_cols(mode) * 2; }
+__host__ __device__ constexpr int off_groups(int mode) { return OFF_STAGE + stage_bytes(mode); }
+__host__ __device__ constexpr int smem_bytes(int mode, int g) { return 1024 + off_groups(mode) + 2 * 4 * (g + 1); }
+static_assert(smem_bytes(DENSE, 1) <= 232448, "shared memory");
+static_assert(smem_bytes(GATHER, MAX_GROUPS) <= 232448, "shared memory");
 
 struct Params {
   const uint8_t* xq;
@@ -172,7 +180,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
-  int32_t* s_prefix = reinterpret_cast<int32_t*>(smem + OFF_GROUPS);
+  int32_t* s_prefix = reinterpret_cast<int32_t*>(smem + off_groups(kMode));
   int32_t* s_start = s_prefix + (p.g + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -484,24 +492,44 @@ __global__ void __launch_bounds__(THREADS, 1)
         tb ^= 1u;
       }
       // start the next tile's scale loads before the stores of this one
-      const bool cur_row_ok = row_ok;
-      const int64_t cur_yrow = yrow;
+      const int64_t cur_row0 = T.row0;
+      const int cur_rows = T.rows;
       const int c0 = T.n0 + half * 128;
       if (t + gridDim.x < num_tiles) setup_tile(t + gridDim.x);
-      if (cur_row_ok) {
-        uint16_t* yr = p.y + cur_yrow * (int64_t)p.n;
+      // BF16 out through the warp's staging area: lane = row writes its
+      // chunks of 8 columns (chunk ch at position ch ^ swz(row), which keeps
+      // the shared-memory accesses conflict-free), then each copy instruction
+      // moves whole row segments of SC columns to global memory.
+      constexpr int SC = store_cols(kMode);
+      constexpr int CPR = SC / 8;                    // 16-byte chunks per staged row
+      constexpr int RPI = 32 / CPR;                  // rows per warp-wide copy
+      constexpr int SWZ_SHIFT = CPR == 8 ? 0 : 1;
+      const uint32_t stg = sbase + OFF_STAGE + (uint32_t)(ew * 32 * SC * 2);
 #pragma unroll
-        for (int v = 0; v < 16; ++v) {
-          const int col = c0 + v * 8;
-          if (col < p.n) {
-            uint4 o;
-            o.x = ptx::pack_bf16x2(acc[v * 4 + 0].x, acc[v * 4 + 0].y);
-            o.y = ptx::pack_bf16x2(acc[v * 4 + 1].x, acc[v * 4 + 1].y);
-            o.z = ptx::pack_bf16x2(acc[v * 4 + 2].x, acc[v * 4 + 2].y);
-            o.w = ptx::pack_bf16x2(acc[v * 4 + 3].x, acc[v * 4 + 3].y);
-            *reinterpret_cast<uint4*>(yr + col) = o;
-          }
+      for (int pass = 0; pass < 128 / SC; ++pass) {
+#pragma unroll
+        for (int ch = 0; ch < CPR; ++ch) {
+          const int v = pass * CPR + ch;
+          const uint32_t pos = (uint32_t)(ch ^ ((lane >> SWZ_SHIFT) & (CPR - 1)));
+          ptx::sts128(stg + (uint32_t)(lane * SC * 2) + pos * 16u,
+                      ptx::pack_bf16x2(acc[v * 4 + 0].x, acc[v * 4 + 0].y),
+                      ptx::pack_bf16x2(acc[v * 4 + 1].x, acc[v * 4 + 1].y),
+                      ptx::pack_bf16x2(acc[v * 4 + 2].x, acc[v * 4 + 2].y),
+                      ptx::pack_bf16x2(acc[v * 4 + 3].x, acc[v * 4 + 3].y));
         }
+        __syncwarp();
+#pragma unroll
+        for (int it = 0; it < 32 / RPI; ++it) {
+          const int r = it * RPI + lane / CPR;
+          const int ch = lane % CPR;
+          const uint32_t pos = (uint32_t)(ch ^ ((r >> SWZ_SHIFT) & (CPR - 1)));
+          const uint4 o = ptx::lds128(stg + (uint32_t)(r * SC * 2) + pos * 16u);
+          const int trow = quarter * 32 + r;
+          const int col = c0 + pass * SC + ch * 8;
+          if (trow < cur_rows && col < p.n)
+            *reinterpret_cast<uint4*>(p.y + (cur_row0 + trow) * (int64_t)p.n + col) = o;
+        }
+        __syncwarp();
       }
     }
   }
@@ -561,7 +589,7 @@ cudaError_t launch_block_gemm(const uint8_t* xq, const float* xs, const uint8_t*
   p.num_m_tiles = (int32_t)((m + BM - 1) / BM);
   p.num_n_tiles = (int32_t)((n + BN - 1) / BN);
   const int64_t tiles = (int64_t)p.num_m_tiles * p.num_n_tiles;
-  const int smem = smem_bytes(1);
+  const int smem = smem_bytes(DENSE, 1);
   cudaError_t e = prepare_kernel<DENSE>(smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)std::min<int64_t>(tiles, sm_count());
@@ -595,7 +623,7 @@ cudaError_t launch_grouped_gemm(const uint8_t* xq, const float* xs, int64_t rows
   p.num_m_tiles = 0;
   p.num_n_tiles = (int32_t)((n + BN - 1) / BN);
   const int64_t max_tiles = ((total_rows + BM - 1) / BM + g) * (int64_t)p.num_n_tiles;
-  const int smem = smem_bytes(g);
+  const int smem = smem_bytes(gather ? GATHER : GROUPED, g);
   const unsigned grid = (unsigned)std::min<int64_t>(max_tiles, sm_count());
   cudaError_t e;
   if (gather) {
