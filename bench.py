@@ -126,7 +126,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -297,6 +297,40 @@ def max_over_ranks(v, world):
     return float(t.item())
 
 
+# DRAM bytes (read + written) of one launch of the batched weight quantizer
+# (144 matrices), from an ncu capture of the same kernel on one Qwen3-8B
+# layer's 4 matrices scaled by the 36 layers (traffic grows with the
+# elements), keyed by a hash of the kernel's sources: any change to them
+# makes the figure stale, and it is then reported as null.
+WEIGHT_QUANT_SOURCES = ("quant.cu", "common.cuh", "ptx.cuh", "tmap.h")
+WEIGHT_QUANT_TRAFFIC = {}
+
+
+def weight_quant_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in WEIGHT_QUANT_SOURCES:
+        with open(os.path.join(ROOT, "w8a8_gemm_rl_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def weight_quant_traffic(args):
+    if args.traffic is not None:
+        return args.traffic
+    return WEIGHT_QUANT_TRAFFIC.get(weight_quant_source_hash())
+
+
+def job_value(ms_total_local, steps, roof_step_s, world):
+    """Whole-job result of a timed region: the slowest rank's wall time
+    (max over ranks) and `value` = 100 * (roofline time of the work all
+    ranks did) / that wall time.  Every rank gets the same numbers."""
+    ms_total = max_over_ranks(ms_total_local, world)
+    ms_step = ms_total / steps
+    value = 100.0 * world * roof_step_s / (ms_step * 1e-3)
+    return ms_total, ms_step, value
+
+
 def cpu_baseline_oracle(budget_s=12.0):
     """The CPU oracle, as it stands, on a bounded sample of the same step's
     phases; returns the same metric (roofline % of one GB300) and details."""
@@ -396,8 +430,7 @@ def bench_ours(args):
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
-    ms_total = start.elapsed_time(end)
-    ms_total = max_over_ranks(ms_total, world)
+    ms_total_local = start.elapsed_time(end)
     phase_ms = {name: 0.0 for name in PHASE_ORDER}
     for s in range(args.steps):
         for i, name in enumerate(PHASE_ORDER):
@@ -406,8 +439,7 @@ def bench_ours(args):
 
     model = {name: (f, b) for name, f, b in work_model()}
     roof_step = sum(t_roof(f, b, peaks) for f, b in model.values())
-    ms_step = ms_total / args.steps
-    value = 100.0 * world * roof_step / (ms_step * 1e-3)
+    ms_total, ms_step, value = job_value(ms_total_local, args.steps, roof_step, world)
     phases = {}
     for name in PHASE_ORDER:
         f, b = model[name]
@@ -428,7 +460,7 @@ def bench_ours(args):
     roofline = {"kernel": "weight_quant_kernel (batched, 1 launch = 144 matrices)", "bound": "hbm",
                 "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
-                "traffic": args.traffic}
+                "traffic": weight_quant_traffic(args)}
     gemm_roof = {"kernel": "fp8_gemm_kernel<DENSE> (4 launches, M=8192)", "bound": "tensor",
                  "achieved": round(model["gemm_linears"][0] / (phase_ms["gemm_linears"] * 1e-3) / 1e12, 1),
                  "peak": round(FP8_OVER_BF16 * peaks["bf16_tflops_sustained"], 1), "unit": "TFLOP/s",
@@ -527,7 +559,7 @@ def bench_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")

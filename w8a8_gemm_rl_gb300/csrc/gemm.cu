@@ -73,12 +73,13 @@ constexpr int OFF_BARS = STAGES * STAGE_BYTES;
 constexpr int NUM_BARS = 2 * STAGES + 4 + 1;  // full, empty, tfull[2], tempty[2], done
 constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
 enum Mode { DENSE = 0, GROUPED = 1, GATHER = 2 };
-// Output staging: each promotion warp turns its 32 rows x 128 columns into
-// row-contiguous global stores through a private area of 32 rows x
-// store_cols BF16 columns, in 128 / store_cols passes (narrower for the
-// grouped modes, whose group tables also need room).
+// Output staging: each promotion warp writes its 32 rows x 128 columns, in
+// 128 / store_cols passes, into a private area of 32 rows x store_cols BF16
+// columns laid out as the TMA's 128-byte (dense) or 64-byte (grouped)
+// swizzle, and one lane stores the box to global memory by TMA (narrower
+// for the grouped modes, whose group tables also need room).
 __host__ __device__ constexpr int store_cols(int mode) { return mode == DENSE ? 64 : 32; }
-constexpr int OFF_STAGE = (OFF_MISC + 16 + 15) / 16 * 16;
+constexpr int OFF_STAGE = (OFF_MISC + 16 + 1023) / 1024 * 1024;  // swizzle atoms: 1024-byte aligned
 __host__ __device__ constexpr int stage_bytes(int mode) { return NUM_EPI_WARPS * 32 * store_cols(mode) * 2; }
 __host__ __device__ constexpr int off_groups(int mode) { return OFF_STAGE + stage_bytes(mode); }
 __host__ __device__ constexpr int smem_bytes(int mode, int g) { return 1024 + off_groups(mode) + 2 * 4 * (g + 1); }
@@ -167,7 +168,8 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, int64_t t, const in
 template <int kMode>
 __global__ void __launch_bounds__(THREADS, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                    const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ Params p) {
+                    const __grid_constant__ CUtensorMap tmap_b,
+                    const __grid_constant__ CUtensorMap tmap_y, const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -202,6 +204,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&tmap_b);
     if (kMode != GATHER) ptx::prefetch_tmap(&tmap_a);
+    ptx::prefetch_tmap(&tmap_y);
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_addr(tmem_slot), TMEM_COLS);
@@ -455,7 +458,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       w1 = (nb_ok && nkb > 1) ? wsr[1] : 0.0f;
     };
     if ((int64_t)blockIdx.x < num_tiles) setup_tile(blockIdx.x);
+    constexpr int SC = store_cols(kMode);
+    constexpr int CPR = SC / 8;  // 16-byte chunks per staged row
+    constexpr int RPI = 32 / CPR;  // rows per warp-wide copy (partial-tile path)
+    constexpr int SWZ_SHIFT = CPR == 8 ? 0 : 1;  // 128-byte / 64-byte swizzle
+    const uint32_t stg = sbase + OFF_STAGE + (uint32_t)(ew * 32 * SC * 2);
     for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      const int64_t cur_row0 = T.row0;
+      const int cur_rows = T.rows;
+      const int c0 = T.n0 + half * 128;
       float2 acc[64];
 #pragma unroll
       for (int j = 0; j < 64; ++j) acc[j] = make_float2(0.0f, 0.0f);
@@ -465,6 +476,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         w0 = w1;
         a1 = (src_ok && kb + 2 < nkb) ? xsr[kb + 2] : 0.0f;
         w1 = (nb_ok && kb + 2 < nkb) ? wsr[kb + 2] : 0.0f;
+        // the next tile's decode and first scale loads overlap the last slab
         ptx::named_bar_sync(BAR_SLAB + tb, BAR_SLAB_THREADS);  // slab kb is in TMEM buffer tb
         ptx::tc_fence_after();
         const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + tb * BN + half * 128;
@@ -491,22 +503,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         tb ^= 1u;
       }
-      // start the next tile's scale loads before the stores of this one
-      const int64_t cur_row0 = T.row0;
-      const int cur_rows = T.rows;
-      const int c0 = T.n0 + half * 128;
+      // BF16 out.  Lane = row writes its chunks of 8 columns into the staging
+      // area (chunk ch at position ch ^ swizzle(row): conflict-free, and the
+      // layout the TMA store expects).  A warp whose 32 rows all lie in the
+      // tile stores the box by TMA; the rows of a partial tile (the last one
+      // of a group, or past M) go out by plain row-segment copies instead,
+      // so that no row beyond the tile is written.
+      const bool full_rows = quarter * 32 + 32 <= cur_rows;
+      // the next tile's decode and first scale loads overlap the stores
+      // (started inside the last slab instead, they slowed it down)
       if (t + gridDim.x < num_tiles) setup_tile(t + gridDim.x);
-      // BF16 out through the warp's staging area: lane = row writes its
-      // chunks of 8 columns (chunk ch at position ch ^ swz(row), which keeps
-      // the shared-memory accesses conflict-free), then each copy instruction
-      // moves whole row segments of SC columns to global memory.
-      constexpr int SC = store_cols(kMode);
-      constexpr int CPR = SC / 8;                    // 16-byte chunks per staged row
-      constexpr int RPI = 32 / CPR;                  // rows per warp-wide copy
-      constexpr int SWZ_SHIFT = CPR == 8 ? 0 : 1;
-      const uint32_t stg = sbase + OFF_STAGE + (uint32_t)(ew * 32 * SC * 2);
 #pragma unroll
       for (int pass = 0; pass < 128 / SC; ++pass) {
+        // the previous TMA store from this area must have read it
+        if (lane == 0) ptx::bulk_wait_read_all();
+        __syncwarp();
 #pragma unroll
         for (int ch = 0; ch < CPR; ++ch) {
           const int v = pass * CPR + ch;
@@ -517,21 +528,33 @@ __global__ void __launch_bounds__(THREADS, 1)
                       ptx::pack_bf16x2(acc[v * 4 + 2].x, acc[v * 4 + 2].y),
                       ptx::pack_bf16x2(acc[v * 4 + 3].x, acc[v * 4 + 3].y));
         }
-        __syncwarp();
+        const int col0 = c0 + pass * SC;
+        if (full_rows) {
+          ptx::fence_proxy_async_smem();  // staging writes -> TMA (async proxy)
+          __syncwarp();
+          if (lane == 0 && col0 < p.n) {
+            ptx::tma_store_2d(&tmap_y, stg, col0, (int)(cur_row0 + quarter * 32));
+            ptx::bulk_commit();
+          }
+        } else {
+          __syncwarp();
 #pragma unroll
-        for (int it = 0; it < 32 / RPI; ++it) {
-          const int r = it * RPI + lane / CPR;
-          const int ch = lane % CPR;
-          const uint32_t pos = (uint32_t)(ch ^ ((r >> SWZ_SHIFT) & (CPR - 1)));
-          const uint4 o = ptx::lds128(stg + (uint32_t)(r * SC * 2) + pos * 16u);
-          const int trow = quarter * 32 + r;
-          const int col = c0 + pass * SC + ch * 8;
-          if (trow < cur_rows && col < p.n)
-            *reinterpret_cast<uint4*>(p.y + (cur_row0 + trow) * (int64_t)p.n + col) = o;
+          for (int it = 0; it < 32 / RPI; ++it) {
+            const int r = it * RPI + lane / CPR;
+            const int ch = lane % CPR;
+            const uint32_t pos = (uint32_t)(ch ^ ((r >> SWZ_SHIFT) & (CPR - 1)));
+            const uint4 o = ptx::lds128(stg + (uint32_t)(r * SC * 2) + pos * 16u);
+            const int trow = quarter * 32 + r;
+            const int col = col0 + ch * 8;
+            if (trow < cur_rows && col < p.n)
+              *reinterpret_cast<uint4*>(p.y + (cur_row0 + trow) * (int64_t)p.n + col) = o;
+          }
+          __syncwarp();
         }
-        __syncwarp();
       }
     }
+    // every TMA store of this warp has completed before the CTA retires
+    if (lane == 0) ptx::bulk_wait_all();
   }
 
 
@@ -578,6 +601,10 @@ cudaError_t launch_block_gemm(const uint8_t* xq, const float* xs, const uint8_t*
   CUtensorMap ta, tb;
   if (!make_tmap_u8(&ta, xq, (uint64_t)m, (uint64_t)k, BM)) return cudaErrorInvalidValue;
   if (!make_tmap_u8(&tb, wq, (uint64_t)n, (uint64_t)k, BN)) return cudaErrorInvalidValue;
+  CUtensorMap ty;
+  if (!make_tmap_2d(&ty, y, 2, (uint64_t)m, (uint64_t)n, 32, store_cols(DENSE),
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
   Params p{};
   p.xq = xq; p.xs = xs; p.ws = ws; p.y = y;
   p.row_idx = nullptr; p.group_offsets = nullptr;
@@ -593,7 +620,7 @@ cudaError_t launch_block_gemm(const uint8_t* xq, const float* xs, const uint8_t*
   cudaError_t e = prepare_kernel<DENSE>(smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)std::min<int64_t>(tiles, sm_count());
-  fp8_gemm_kernel<DENSE><<<grid, THREADS, smem, st>>>(ta, tb, p);
+  fp8_gemm_kernel<DENSE><<<grid, THREADS, smem, st>>>(ta, tb, ty, p);
   return cudaGetLastError();
 }
 
@@ -612,6 +639,10 @@ cudaError_t launch_grouped_gemm(const uint8_t* xq, const float* xs, int64_t rows
     return cudaErrorInvalidValue;
   if (!make_tmap_u8(&tb, wq, (uint64_t)g * (uint64_t)n, (uint64_t)k, BN))
     return cudaErrorInvalidValue;
+  CUtensorMap ty;
+  if (!make_tmap_2d(&ty, y, 2, (uint64_t)total_rows, (uint64_t)n, 32, store_cols(GROUPED),
+                    CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
   Params p{};
   p.xq = xq; p.xs = xs; p.ws = ws; p.y = y;
   p.row_idx = row_idx; p.group_offsets = group_offsets;
@@ -629,11 +660,11 @@ cudaError_t launch_grouped_gemm(const uint8_t* xq, const float* xs, int64_t rows
   if (gather) {
     e = prepare_kernel<GATHER>(smem);
     if (e != cudaSuccess) return e;
-    fp8_gemm_kernel<GATHER><<<grid, THREADS, smem, st>>>(ta, tb, p);
+    fp8_gemm_kernel<GATHER><<<grid, THREADS, smem, st>>>(ta, tb, ty, p);
   } else {
     e = prepare_kernel<GROUPED>(smem);
     if (e != cudaSuccess) return e;
-    fp8_gemm_kernel<GROUPED><<<grid, THREADS, smem, st>>>(ta, tb, p);
+    fp8_gemm_kernel<GROUPED><<<grid, THREADS, smem, st>>>(ta, tb, ty, p);
   }
   return cudaGetLastError();
 }
