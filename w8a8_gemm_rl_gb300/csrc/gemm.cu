@@ -74,13 +74,17 @@ constexpr int NUM_BARS = 2 * STAGES + 4 + 1;  // full, empty, tfull[2], tempty[2
 constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
 enum Mode { DENSE = 0, GROUPED = 1, GATHER = 2 };
 // Output staging: each promotion warp writes its 32 rows x 128 columns, in
-// 128 / store_cols passes, into a private area of 32 rows x store_cols BF16
-// columns laid out as the TMA's 128-byte (dense) or 64-byte (grouped)
-// swizzle, and one lane stores the box to global memory by TMA (narrower
-// for the grouped modes, whose group tables also need room).
-__host__ __device__ constexpr int store_cols(int mode) { return mode == DENSE ? 64 : 32; }
+// 128 / store_cols passes, into one of two private buffers of 32 rows x
+// store_cols BF16 columns laid out as the TMA's 64-byte (dense) or 32-byte
+// (grouped) swizzle, and one lane stores the box to global memory by TMA
+// while the next pass fills the other buffer (narrower for the grouped
+// modes, whose group tables also need room).
+constexpr int STAGE_BUFS = 2;
+__host__ __device__ constexpr int store_cols(int mode) { return mode == DENSE ? 32 : 16; }
 constexpr int OFF_STAGE = (OFF_MISC + 16 + 1023) / 1024 * 1024;  // swizzle atoms: 1024-byte aligned
-__host__ __device__ constexpr int stage_bytes(int mode) { return NUM_EPI_WARPS * 32 * store_cols(mode) * 2; }
+__host__ __device__ constexpr int stage_bytes(int mode) {
+  return NUM_EPI_WARPS * STAGE_BUFS * 32 * store_cols(mode) * 2;
+}
 __host__ __device__ constexpr int off_groups(int mode) { return OFF_STAGE + stage_bytes(mode); }
 __host__ __device__ constexpr int smem_bytes(int mode, int g) { return 1024 + off_groups(mode) + 2 * 4 * (g + 1); }
 static_assert(smem_bytes(DENSE, 1) <= 232448, "shared memory");
@@ -134,21 +138,24 @@ template <int kMode>
 __device__ __forceinline__ Tile decode_tile(const Params& p, int64_t t, const int32_t* s_prefix,
                                             const int32_t* s_start) {
   Tile T;
+  // tile indices fit in 32 bits (the launchers check), and 32-bit division
+  // is several times cheaper than 64-bit on the tile-boundary critical path
+  const uint32_t tt = (uint32_t)t;
   if (kMode == DENSE) {
-    const int64_t per_group = (int64_t)RASTER_M * p.num_n_tiles;
-    const int64_t grp = t / per_group;
+    const uint32_t per_group = (uint32_t)RASTER_M * (uint32_t)p.num_n_tiles;
+    const uint32_t grp = tt / per_group;
     const int32_t first_m = (int32_t)(grp * RASTER_M);
-    const int32_t gm = (int32_t)min64(RASTER_M, p.num_m_tiles - first_m);
-    const int32_t r = (int32_t)(t - grp * per_group);
-    const int32_t mt = first_m + r % gm;
-    const int32_t nt = r / gm;
+    const uint32_t gm = (uint32_t)min(RASTER_M, p.num_m_tiles - first_m);
+    const uint32_t r = tt - grp * per_group;
+    const int32_t mt = first_m + (int32_t)(r % gm);
+    const int32_t nt = (int32_t)(r / gm);
     T.e = 0;
     T.row0 = (int64_t)mt * BM;
     T.rows = (int32_t)min64(BM, p.m - T.row0);
     T.n0 = nt * BN;
   } else {
-    const int32_t mt_all = (int32_t)(t / p.num_n_tiles);
-    const int32_t nt = (int32_t)(t - (int64_t)mt_all * p.num_n_tiles);
+    const int32_t mt_all = (int32_t)(tt / (uint32_t)p.num_n_tiles);
+    const int32_t nt = (int32_t)(tt - (uint32_t)mt_all * (uint32_t)p.num_n_tiles);
     int lo = 0, hi = p.g;  // s_prefix[lo] <= mt_all < s_prefix[hi]
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -450,19 +457,26 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       const int nb = (T.n0 >> 7) + half;
       nb_ok = nb < p.nnb;
+      // A row or B column outside the operands reads zeros (TMA fill or the
+      // gather's zero fill), so its partial is 0 whatever the scale: such a
+      // row takes row 0's scales (a valid address) and the loads need no
+      // condition -- a select on a load result would wait for the load here
       xsr = p.xs + (src_ok ? src : 0) * (int64_t)nkb;
       wsr = p.ws + ((int64_t)T.e * p.nnb + (nb_ok ? nb : 0)) * nkb;
-      a0 = src_ok ? xsr[0] : 0.0f;
-      w0 = nb_ok ? wsr[0] : 0.0f;
-      a1 = (src_ok && nkb > 1) ? xsr[1] : 0.0f;
-      w1 = (nb_ok && nkb > 1) ? wsr[1] : 0.0f;
+      a0 = xsr[0];
+      w0 = wsr[0];
+      if (nkb > 1) {
+        a1 = xsr[1];
+        w1 = wsr[1];
+      }
     };
     if ((int64_t)blockIdx.x < num_tiles) setup_tile(blockIdx.x);
     constexpr int SC = store_cols(kMode);
     constexpr int CPR = SC / 8;  // 16-byte chunks per staged row
     constexpr int RPI = 32 / CPR;  // rows per warp-wide copy (partial-tile path)
-    constexpr int SWZ_SHIFT = CPR == 8 ? 0 : 1;  // 128-byte / 64-byte swizzle
-    const uint32_t stg = sbase + OFF_STAGE + (uint32_t)(ew * 32 * SC * 2);
+    constexpr int SWZ_SHIFT = CPR == 8 ? 0 : (CPR == 4 ? 1 : 2);  // 128/64/32-byte swizzle
+    constexpr uint32_t BUF_BYTES = 32 * SC * 2;
+    const uint32_t stg0 = sbase + OFF_STAGE + (uint32_t)ew * STAGE_BUFS * BUF_BYTES;
     for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
       const int64_t cur_row0 = T.row0;
       const int cur_rows = T.rows;
@@ -474,8 +488,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         const float s = a0 * w0;
         a0 = a1;
         w0 = w1;
-        a1 = (src_ok && kb + 2 < nkb) ? xsr[kb + 2] : 0.0f;
-        w1 = (nb_ok && kb + 2 < nkb) ? wsr[kb + 2] : 0.0f;
+        if (kb + 2 < nkb) {
+          a1 = xsr[kb + 2];
+          w1 = wsr[kb + 2];
+        }
         // the next tile's decode and first scale loads overlap the last slab
         ptx::named_bar_sync(BAR_SLAB + tb, BAR_SLAB_THREADS);  // slab kb is in TMEM buffer tb
         ptx::tc_fence_after();
@@ -515,8 +531,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (t + gridDim.x < num_tiles) setup_tile(t + gridDim.x);
 #pragma unroll
       for (int pass = 0; pass < 128 / SC; ++pass) {
-        // the previous TMA store from this area must have read it
-        if (lane == 0) ptx::bulk_wait_read_all();
+        const uint32_t stg = stg0 + (uint32_t)(pass % STAGE_BUFS) * BUF_BYTES;
+        // the TMA store issued from this buffer two passes ago must have read
+        // it (the store from the other buffer may still be reading)
+        if (lane == 0) ptx::bulk_wait_read_1();
         __syncwarp();
 #pragma unroll
         for (int ch = 0; ch < CPR; ++ch) {
@@ -603,7 +621,7 @@ cudaError_t launch_block_gemm(const uint8_t* xq, const float* xs, const uint8_t*
   if (!make_tmap_u8(&tb, wq, (uint64_t)n, (uint64_t)k, BN)) return cudaErrorInvalidValue;
   CUtensorMap ty;
   if (!make_tmap_2d(&ty, y, 2, (uint64_t)m, (uint64_t)n, 32, store_cols(DENSE),
-                    CU_TENSOR_MAP_SWIZZLE_128B))
+                    CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   Params p{};
   p.xq = xq; p.xs = xs; p.ws = ws; p.y = y;
@@ -616,6 +634,7 @@ cudaError_t launch_block_gemm(const uint8_t* xq, const float* xs, const uint8_t*
   p.num_m_tiles = (int32_t)((m + BM - 1) / BM);
   p.num_n_tiles = (int32_t)((n + BN - 1) / BN);
   const int64_t tiles = (int64_t)p.num_m_tiles * p.num_n_tiles;
+  if (tiles > INT32_MAX) return cudaErrorNotSupported;  // 2^31 tiles of output cannot exist
   const int smem = smem_bytes(DENSE, 1);
   cudaError_t e = prepare_kernel<DENSE>(smem);
   if (e != cudaSuccess) return e;
@@ -641,7 +660,7 @@ cudaError_t launch_grouped_gemm(const uint8_t* xq, const float* xs, int64_t rows
     return cudaErrorInvalidValue;
   CUtensorMap ty;
   if (!make_tmap_2d(&ty, y, 2, (uint64_t)total_rows, (uint64_t)n, 32, store_cols(GROUPED),
-                    CU_TENSOR_MAP_SWIZZLE_64B))
+                    CU_TENSOR_MAP_SWIZZLE_32B))
     return cudaErrorInvalidValue;
   Params p{};
   p.xq = xq; p.xs = xs; p.ws = ws; p.y = y;
@@ -654,6 +673,7 @@ cudaError_t launch_grouped_gemm(const uint8_t* xq, const float* xs, int64_t rows
   p.num_m_tiles = 0;
   p.num_n_tiles = (int32_t)((n + BN - 1) / BN);
   const int64_t max_tiles = ((total_rows + BM - 1) / BM + g) * (int64_t)p.num_n_tiles;
+  if (max_tiles > INT32_MAX) return cudaErrorNotSupported;
   const int smem = smem_bytes(gather ? GATHER : GROUPED, g);
   const unsigned grid = (unsigned)std::min<int64_t>(max_tiles, sm_count());
   cudaError_t e;
