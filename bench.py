@@ -303,7 +303,10 @@ def max_over_ranks(v, world):
 # elements), keyed by a hash of the kernel's sources: any change to them
 # makes the figure stale, and it is then reported as null.
 WEIGHT_QUANT_SOURCES = ("quant.cu", "common.cuh", "ptx.cuh", "tmap.h")
-WEIGHT_QUANT_TRAFFIC = {}
+WEIGHT_QUANT_TRAFFIC = {
+    # profiles/weight_quant_batched_qwen3_8b_layer.md: 36 x (385.9 + 151.8) MB
+    "02b5f8fe3603a596": 36 * (385921536 + 151804928),
+}
 
 
 def weight_quant_source_hash():
