@@ -135,6 +135,28 @@ w8a8_status quantize_act_per_token_group(const uint16_t *x_bf16, int64_t m,
                                          w8a8_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * quantize_act_per_token_group_gather -- the activation quantizer above
+ * applied to the routed rows of an MoE layer ([FP8-RL] section 1 expert
+ * layers, [NeMo] Table 1 [1,128] groups): output row r is the per-token
+ * group quantization of x row row_idx[r].  Quantization works per row, so
+ * this equals quantizing x and then gathering its rows; the routed, expert-
+ * sorted copy lets fp8_grouped_gemm read contiguous rows (row_idx = NULL).
+ *
+ *   x_bf16   [rows_x, k] BF16 activations (may be NULL when rows_x == 0).
+ *   row_idx  [total_rows] int32 source row of each routed row; an index
+ *            outside [0, rows_x) gives a zero row (codes 0, scales 1).
+ *   xq       [total_rows, k] E4M3 codes (out).
+ *   xs       [total_rows, ceil(k/128)] FP32 group scales (out), row-major.
+ * Rules: rows_x, k, total_rows >= 0; k % 8 == 0 (else W8A8_ERR_UNSUPPORTED);
+ * x_bf16 and xq 16-byte aligned; xs and row_idx 4-byte aligned.
+ * ---------------------------------------------------------------------- */
+w8a8_status quantize_act_per_token_group_gather(const uint16_t *x_bf16,
+                                                int64_t rows_x, int64_t k,
+                                                const int32_t *row_idx,
+                                                int64_t total_rows, uint8_t *xq,
+                                                float *xs, w8a8_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * fp8_block_gemm -- the W8A8 linear of [FP8-RL] section 1 / arXiv abstract
  * item (i) with the [NeMo] Table 1 granularities:
  *

@@ -134,6 +134,20 @@ def quantize_act_per_token_group(x_bits):
     return quantize_blocks(x_bits, 1, 128)
 
 
+def quantize_act_per_token_group_gather(x_bits, row_idx):
+    """Routed rows (FP8-RL page, section 1: the expert layers' inputs): row r
+    of the result is the 1x128 group quantization of x row row_idx[r]; an
+    index outside [0, rows_x) stands for an all-zero row.  Gather first
+    (numpy indexing), then the block quantizer."""
+    x = _c(x_bits, np.uint16)
+    ri = np.asarray(row_idx, dtype=np.int64).reshape(-1)
+    rows_x, k = x.shape
+    g = np.zeros((ri.size, k), np.uint16)
+    ok = (ri >= 0) & (ri < rows_x)
+    g[ok] = x[ri[ok]]
+    return quantize_blocks(g, 1, 128)
+
+
 def amax_bf16(x_bits):
     x = _c(x_bits, np.uint16).reshape(-1)
     return lib().oracle_amax_bf16(_p(x), x.size)

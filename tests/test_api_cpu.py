@@ -76,6 +76,22 @@ def test_quantizer_argument_checks(L):
     assert b(ctypes.cast(descs, ctypes.c_void_p), 2, None) == NULL
 
 
+def test_gather_quantizer_argument_checks(L):
+    g = L.quantize_act_per_token_group_gather
+    assert g(A, -1, 128, A, 5, A, A, None) == SHAPE
+    assert g(A, 10, -2, A, 5, A, A, None) == SHAPE
+    assert g(A, 10, 128, A, -5, A, A, None) == SHAPE
+    assert g(None, 10, 128, None, 0, None, None, None) == OK  # nothing routed
+    assert g(A, 10, 0, A, 5, A, A, None) == OK  # empty rows
+    assert g(A, 10, 128, None, 5, A, A, None) == NULL
+    assert g(None, 10, 128, A, 5, A, A, None) == NULL
+    assert g(A, 10, 128, A, 5, None, A, None) == NULL
+    assert g(A + 2, 10, 128, A, 5, A, A, None) == ALIGN
+    assert g(A, 10, 128, A + 2, 5, A, A, None) == ALIGN
+    assert g(A, 10, 128, A, 5, A + 8, A, None) == ALIGN
+    assert g(A, 10, 100, A, 5, A, A, None) == UNSUP  # k % 8
+
+
 def test_gemm_argument_checks(L):
     g = L.fp8_block_gemm
     assert g(A, A, A, A, A, 128, 256, 100, None) == SHAPE  # k % 16

@@ -239,6 +239,25 @@ def test_gather_commutes_with_per_token_quant():
     assert (q1[idx] == q2).all() and (s1[idx] == s2).all()
 
 
+def test_routed_row_quant_is_quant_then_gather_with_zero_rows():
+    """The routed-row quantizer of the oracle: valid indices give the rows of
+    the plain per-token quantization (quantization works per row), duplicated
+    indices identical rows, and an index outside [0, rows_x) the quantization
+    of an all-zero row: codes 0x00, scale 1 (the all-zero group's reading)."""
+    rng = np.random.default_rng(16)
+    xb = _bf16(rng.standard_normal((40, 384)) * 3.0)
+    idx = np.concatenate([rng.integers(0, 40, 90), [-1, 40, 7, 7, 2 ** 31 - 1, -(2 ** 31)]])
+    q, s = O.quantize_act_per_token_group_gather(xb, idx)
+    qd, sd = O.quantize_act_per_token_group(xb)
+    ok = (idx >= 0) & (idx < 40)
+    assert (q[ok] == qd[idx[ok]]).all() and (s[ok] == sd[idx[ok]]).all()
+    assert (q[~ok] == 0).all() and (s[~ok] == 1.0).all()
+    assert (q[-4] == q[-3]).all()
+    # and not the identity: a shifted index set changes the rows
+    q2, _ = O.quantize_act_per_token_group_gather(xb, (idx[ok] + 1) % 40)
+    assert (q2 != q[ok]).any()
+
+
 def test_kv_is_one_group_and_amax_matches_numpy():
     rng = np.random.default_rng(7)
     x = (rng.standard_normal((2, 64, 8, 128)) * np.exp(0.5 * rng.standard_normal((8, 128)))).astype(np.float32)

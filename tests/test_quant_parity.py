@@ -46,6 +46,38 @@ def test_e4m3_decode_all_codes(W):
 
 # --------------------------------------------------------- act quantizer
 
+GATHER_CASES = [  # rows_x, k, total routed rows
+    (300, 2048, 1000), (50, 768, 400), (37, 200, 123), (64, 1024, 64), (10, 8, 33),
+    (0, 256, 17), (5, 128, 0), (4096, 2048, 32768)]
+
+
+@pytest.mark.parametrize("rows_x,k,total", GATHER_CASES)
+def test_act_quant_gather_bit_exact(W, rows_x, k, total):
+    """Routed-row quantizer: every row and scale equals the oracle's, including
+    duplicated rows and indices outside [0, rows_x) (zero rows)."""
+    x = synth.activations(max(rows_x, 1), k, seed=rows_x * 31 + k, device="cpu")[:rows_x]
+    g = torch.Generator().manual_seed(rows_x + 7 * total)
+    idx = torch.randint(-3, rows_x + 3, (total,), generator=g, dtype=torch.int64)
+    if total >= 4:
+        idx[:4] = torch.tensor([-(2 ** 31), 2 ** 31 - 1, 0, max(rows_x - 1, 0)])
+    idx = idx.to(torch.int32)
+    xq, xs = W.quantize_act_per_token_group_gather(x.cuda(), idx.cuda())
+    q_ref, s_ref = O.quantize_act_per_token_group_gather(synth.bf16_bits(x), idx.numpy())
+    assert (u8(xq) == q_ref).all()
+    assert (f32(xs).view(np.uint32) == s_ref.view(np.uint32)).all()
+
+
+def test_act_quant_gather_of_moe_routing_equals_quant_then_gather(W):
+    """On the Qwen3-30B-A3B routing: quantizing the routed rows directly gives
+    the gathered rows of the plain per-token quantization."""
+    r = synth.moe_routing(4096, 128, 8, seed=60)
+    x = synth.activations(4096, 2048, seed=61, device="cuda")
+    xq, xs = W.quantize_act_per_token_group(x)
+    gq, gs = W.quantize_act_per_token_group_gather(x, r.row_idx.cuda())
+    ri = r.row_idx.cuda().long()
+    assert torch.equal(gq, xq[ri]) and torch.equal(gs.view(torch.int32), xs[ri].view(torch.int32))
+
+
 ACT_SHAPES = [(1, 128), (3, 256), (7, 200), (5, 300), (128, 512), (33, 4096), (2, 8), (9, 1000),
               (0, 128), (4, 0), (1, 12288), (300, 768)]
 

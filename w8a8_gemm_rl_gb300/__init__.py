@@ -15,7 +15,8 @@ import torch
 
 __all__ = [
     "lib", "W8A8Error", "e4m3_encode_f32", "e4m3_decode_f32", "quantize_weight_blockwise",
-    "quantize_weight_blockwise_batched", "quantize_act_per_token_group", "fp8_block_gemm",
+    "quantize_weight_blockwise_batched", "quantize_act_per_token_group",
+    "quantize_act_per_token_group_gather", "fp8_block_gemm",
     "fp8_grouped_gemm", "kv_amax_quantize", "w8a8_linear", "consume_device_error",
     "KV_AMAX_AND_QUANT", "KV_AMAX_ONLY", "KV_QUANT_ONLY", "LIB_PATH",
 ]
@@ -49,6 +50,7 @@ _SIGNATURES = {
     "quantize_weight_blockwise": (_INT, [_P, _I64, _I64, _P, _P, _P]),
     "quantize_weight_blockwise_batched": (_INT, [_P, _I32, _P]),
     "quantize_act_per_token_group": (_INT, [_P, _I64, _I64, _P, _P, _P]),
+    "quantize_act_per_token_group_gather": (_INT, [_P, _I64, _I64, _P, _I64, _P, _P, _P]),
     "fp8_block_gemm": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "fp8_grouped_gemm": (_INT, [_P, _P, _I64, _P, _P, _I32, _I64, _P, _P, _P, _I64, _I64, _P]),
     "kv_amax_quantize": (_INT, [_P, _I64, _P, _P, _P, _INT, _P]),
@@ -157,6 +159,21 @@ def quantize_act_per_token_group(x, xq=None, xs=None, stream=None):
     xs = torch.empty((m, _cdiv(k, 128)), dtype=torch.float32, device=x.device) if xs is None else xs
     _check("quantize_act_per_token_group",
            lib().quantize_act_per_token_group(_ptr(x), m, k, _ptr(xq), _ptr(xs), _stream(stream)))
+    return xq, xs
+
+
+def quantize_act_per_token_group_gather(x, row_idx, xq=None, xs=None, stream=None):
+    """x BF16 [rows_x, k], row_idx int32 [total] -> (xq uint8 [total, k],
+    xs float32 [total, ceil(k/128)]): row r quantizes x[row_idx[r]]."""
+    _need(x, torch.bfloat16, "x")
+    _need(row_idx, torch.int32, "row_idx")
+    rows_x, k = x.shape
+    total = row_idx.shape[0]
+    xq = torch.empty((total, k), dtype=torch.uint8, device=x.device) if xq is None else xq
+    xs = torch.empty((total, _cdiv(k, 128)), dtype=torch.float32, device=x.device) if xs is None else xs
+    _check("quantize_act_per_token_group_gather",
+           lib().quantize_act_per_token_group_gather(_ptr(x), rows_x, k, _ptr(row_idx), total,
+                                                     _ptr(xq), _ptr(xs), _stream(stream)))
     return xq, xs
 
 

@@ -120,6 +120,20 @@ W8A8_API w8a8_status quantize_act_per_token_group(const uint16_t* x_bf16, int64_
   return from_cuda(w8a8::launch_act_quant(x_bf16, m, k, xq, xs, cs(stream)));
 }
 
+W8A8_API w8a8_status quantize_act_per_token_group_gather(const uint16_t* x_bf16, int64_t rows_x,
+                                                         int64_t k, const int32_t* row_idx,
+                                                         int64_t total_rows, uint8_t* xq, float* xs,
+                                                         w8a8_stream_t stream) {
+  if (rows_x < 0 || k < 0 || total_rows < 0) return W8A8_ERR_SHAPE;
+  if (total_rows == 0 || k == 0) return W8A8_OK;
+  if (!row_idx || !xq || !xs || (rows_x > 0 && !x_bf16)) return W8A8_ERR_NULL;
+  if (!aligned(x_bf16, 16) || !aligned(xq, 16) || !aligned(xs, 4) || !aligned(row_idx, 4))
+    return W8A8_ERR_ALIGN;
+  if (k % 8 != 0) return W8A8_ERR_UNSUPPORTED;
+  return from_cuda(w8a8::launch_act_quant_gather(x_bf16, rows_x, k, row_idx, total_rows, xq, xs,
+                                                 cs(stream)));
+}
+
 // ------------------------------------------------------------------ GEMMs
 
 static w8a8_status check_gemm_common(const uint8_t* xq, const float* xs, const uint8_t* wq,

@@ -17,6 +17,11 @@ cudaError_t launch_e4m3_decode(const uint8_t* q, int64_t n, float* x, cudaStream
 cudaError_t launch_act_quant(const uint16_t* x, int64_t m, int64_t k, uint8_t* q, float* s,
                              cudaStream_t st);
 
+// Output row r quantizes x row row_idx[r] (zeros when outside [0, rows_x)).
+cudaError_t launch_act_quant_gather(const uint16_t* x, int64_t rows_x, int64_t k,
+                                    const int32_t* row_idx, int64_t total_rows, uint8_t* q,
+                                    float* s, cudaStream_t st);
+
 struct WeightJob {
   const uint16_t* w;
   uint8_t* wq;

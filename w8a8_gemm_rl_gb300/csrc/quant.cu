@@ -170,10 +170,14 @@ static cudaError_t launch_generic(const uint16_t* x, int64_t rows, int64_t cols,
 // flight.  Consecutive warps take consecutive groups: the access stream is
 // contiguous.
 
+// With row_idx, output row r quantizes x row row_idx[r] (a zero row when the
+// index is outside [0, rows_x)); without it, row r quantizes row r.
 template <typename IdxT>
 __global__ void __launch_bounds__(256) act_quant_kernel(const uint16_t* __restrict__ x, IdxT m,
                                                         IdxT k, uint8_t* __restrict__ q,
-                                                        float* __restrict__ s) {
+                                                        float* __restrict__ s,
+                                                        const int32_t* __restrict__ row_idx,
+                                                        IdxT rows_x) {
   constexpr int U = 4;
   const IdxT gpr = (k + 127) / 128;
   const IdxT G = m * gpr;
@@ -192,7 +196,14 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const uint16_t* __restri
       const IdxT col = (g - row * gpr) * 128 + l16 * 8;
       ok[u] = (g < G) && (col < k);
       off[u] = row * k + col;
-      v[u] = ok[u] ? ld_stream_v4(x + off[u]) : make_uint4(0u, 0u, 0u, 0u);
+      bool rd = ok[u];
+      IdxT src = row;
+      if (row_idx != nullptr && rd) {
+        const int64_t r = row_idx[row];
+        rd = r >= 0 && r < (int64_t)rows_x;
+        src = rd ? (IdxT)r : 0;
+      }
+      v[u] = rd ? ld_stream_v4(x + src * k + col) : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -261,6 +272,57 @@ __global__ void __launch_bounds__(256) act_quant_k128_kernel(const uint16_t* __r
   }
 }
 
+// The same over routed rows, rows a multiple of 128: output group g (row
+// g / gpr, group g % gpr) reads the group of x row row_idx[g / gpr], or zeros
+// when that index is outside [0, rows_x).  Group counts fit in 32 bits.
+template <int U>
+__global__ void __launch_bounds__(256) act_quant_gather_k128_kernel(
+    const uint16_t* __restrict__ x, int64_t rows_x, const int32_t* __restrict__ row_idx,
+    uint32_t gpr, uint32_t G, uint8_t* __restrict__ q, float* __restrict__ s) {
+  const int lane = threadIdx.x & 31;
+  const int sub = lane & 3, gi = lane >> 2;
+  const uint32_t warp = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const uint32_t nwarps = gridDim.x * (blockDim.x >> 5);
+  for (uint32_t base = warp * (8 * U); base < G; base += nwarps * (8 * U)) {
+    const uint16_t* src[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t g = base + 8 * u + gi;
+      src[u] = nullptr;
+      if (g < G) {
+        const uint32_t r = g / gpr;
+        const int64_t sr = row_idx[r];
+        if (sr >= 0 && sr < rows_x) src[u] = x + ((uint64_t)sr * gpr + (g - r * gpr)) * 128;
+      }
+    }
+    uint4 v[U][4];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        v[u][j] = src[u] ? ld_stream_v4(src[u] + (sub + 4 * j) * 8) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t g = base + 8 * u + gi;
+      float a = absmax_bf16x8_tree<4>(v[u]);
+      a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+      a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+      const float S = scale_from_amax(a);
+      const QuantScale qs = make_quant_scale(S);
+      if (g < G) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint2 c;
+          c.x = quant_bf16x4(v[u][j].x, v[u][j].y, qs);
+          c.y = quant_bf16x4(v[u][j].z, v[u][j].w, qs);
+          st_stream_v2(q + (uint64_t)g * 128 + (sub + 4 * j) * 8, c);
+        }
+        if (sub == 0) s[g] = S;
+      }
+    }
+  }
+}
+
 cudaError_t launch_act_quant(const uint16_t* x, int64_t m, int64_t k, uint8_t* q, float* s,
                              cudaStream_t st) {
   if (m == 0 || k == 0) return cudaSuccess;
@@ -274,9 +336,28 @@ cudaError_t launch_act_quant(const uint16_t* x, int64_t m, int64_t k, uint8_t* q
   }
   const unsigned grid = grid_for(G, 8 * 8, 16);  // 8 warps x 8 groups per CTA iteration
   if (m * k < (int64_t)0x7FFFFFFF)
-    act_quant_kernel<uint32_t><<<grid, 256, 0, st>>>(x, (uint32_t)m, (uint32_t)k, q, s);
+    act_quant_kernel<uint32_t><<<grid, 256, 0, st>>>(x, (uint32_t)m, (uint32_t)k, q, s, nullptr,
+                                                     (uint32_t)m);
   else
-    act_quant_kernel<int64_t><<<grid, 256, 0, st>>>(x, m, k, q, s);
+    act_quant_kernel<int64_t><<<grid, 256, 0, st>>>(x, m, k, q, s, nullptr, m);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_act_quant_gather(const uint16_t* x, int64_t rows_x, int64_t k,
+                                    const int32_t* row_idx, int64_t total_rows, uint8_t* q,
+                                    float* s, cudaStream_t st) {
+  if (total_rows == 0 || k == 0) return cudaSuccess;
+  if (k % 8 != 0) return cudaErrorNotSupported;
+  const int64_t G = total_rows * cdiv(k, 128);
+  if (k % 128 == 0 && G < (int64_t)0x7FFFFFFF) {
+    constexpr int U = 2;
+    const unsigned grid = grid_for(G, 8 * 8 * U, 8);
+    act_quant_gather_k128_kernel<U><<<grid, 256, 0, st>>>(x, rows_x, row_idx, (uint32_t)(k / 128),
+                                                          (uint32_t)G, q, s);
+    return cudaGetLastError();
+  }
+  const unsigned grid = grid_for(G, 8 * 8, 16);
+  act_quant_kernel<int64_t><<<grid, 256, 0, st>>>(x, total_rows, k, q, s, row_idx, rows_x);
   return cudaGetLastError();
 }
 
