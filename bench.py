@@ -475,6 +475,7 @@ def bench_ours(args):
                  "peak_note": "measured bf16 sustained x 2 (nominal fp8/bf16)"}
     gemm_roof["frac"] = round(gemm_roof["achieved"] / gemm_roof["peak"], 4)
 
+    next_rows = measure_next_rows(W, wl, peaks)
     e2e = None
     if not args.no_e2e:
         e2e = measure_e2e(W, wl, args, roof_step, world)
@@ -493,13 +494,57 @@ def bench_ours(args):
         "gemm_tflops": round(g_flops / (g_ms * 1e-3) / 1e12 * world, 1),
         "phases": phases, "roofline": roofline, "gemm_roofline": gemm_roof,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": LAUNCHES_PER_STEP * args.steps,
-        "clocks": clk, "peaks": peaks,
+        "clocks": clk, "peaks": peaks, "next_rows": next_rows,
     }
     if rank == 0:
         print(json.dumps(out))
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def measure_next_rows(W, wl, peaks, reps=3):
+    """Rows past the hot path, each on its own kernel roofline (HBM): the
+    dequantizer (fake quant) over every weight matrix of the model from its
+    128x128-block codes, and the quantization-error report over the same
+    matrices (128x128 report blocks).  One launch per matrix, inputs (20 GB)
+    far larger than L2; CUDA events around each sweep of all 144 matrices."""
+    out = {}
+    big = max(w.numel() for w in wl.w)
+    y = torch.empty(big, dtype=torch.bfloat16, device=wl.w[0].device)
+    stats = torch.empty(cdiv(big, 128 * 128) * 3 + 64, dtype=torch.float64, device=y.device)
+    elems = sum(w.numel() for w in wl.w)
+    blocks = sum(cdiv(w.shape[0], 128) * cdiv(w.shape[1], 128) for w in wl.w)
+
+    def sweep(kind):
+        for w, (q, sc) in zip(wl.w, wl.wout):
+            n, k = w.shape
+            if kind == "dequant":
+                W.dequantize_blockwise(q, sc, 128, 128, y[: n * k].view(n, k))
+            else:
+                W.quant_error_report(w, q, sc, (128, 128), (128, 128),
+                                     stats[: cdiv(n, 128) * cdiv(k, 128) * 3].view(cdiv(n, 128), cdiv(k, 128), 3))
+
+    W.quantize_weight_blockwise_batched(wl.w, wl.wout)
+    for kind, nbytes in (("dequant", 3 * elems + 4 * blocks),
+                         ("quant_error_report", 3 * elems + 4 * blocks + 24 * blocks)):
+        sweep(kind)
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(reps):
+            sweep(kind)
+        t1.record()
+        torch.cuda.synchronize()
+        sec = t0.elapsed_time(t1) * 1e-3 / reps
+        name = "dequantize_blockwise" if kind == "dequant" else "quant_error_report"
+        out[name] = {"workload": "all 144 Qwen3-8B weight matrices, 128x128 blocks, 1 launch each",
+                     "ms": round(sec * 1e3, 3), "gbs": round(nbytes / sec / 1e9, 1),
+                     "pct_roofline": round(100 * nbytes / sec / 1e9 / peaks["hbm_gbs"], 2),
+                     "bytes_per_sweep": nbytes}
+    assert W.consume_device_error() == 0
+    return out
 
 
 def measure_e2e(W, wl, args, roof_step, world):

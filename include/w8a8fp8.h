@@ -157,6 +157,55 @@ w8a8_status quantize_act_per_token_group_gather(const uint16_t *x_bf16,
                                                 float *xs, w8a8_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * dequantize_blockwise -- the inverse of the quantizers, "fake quant" in
+ * the [UFP8] notes' error analysis (quantize-dequantize against the real
+ * FP8 path):
+ *
+ *   y[r,c] = BF16_RN( RN32( dec(q[r,c]) * s[r/block_rows, c/block_cols] ) )
+ *
+ *   q       [rows, cols] E4M3 codes.
+ *   s       [ceil(rows/block_rows), ceil(cols/block_cols)] FP32 scales,
+ *           row-major: 128 x 128 for weights, 1 x 128 for activations,
+ *           rows x cols (one scale) for a per-tensor KV cache.
+ *   y_bf16  [rows, cols] BF16 (out).
+ * Rules: rows, cols >= 0; block sizes > 0; q and y_bf16 16-byte aligned, s
+ * 4-byte aligned.
+ * ---------------------------------------------------------------------- */
+w8a8_status dequantize_blockwise(const uint8_t *q, const float *s, int64_t rows,
+                                 int64_t cols, int64_t block_rows,
+                                 int64_t block_cols, uint16_t *y_bf16,
+                                 w8a8_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * quant_error_report -- the quantization error the [UFP8] notes attribute
+ * the train/rollout mismatch to, measured per report block: with
+ * x_hat = RN32(dec(q) * s) as above,
+ *
+ *   stats[b] = { max |x - x_hat|,  sum (x - x_hat)^2,  sum x^2 }   (FP64)
+ *
+ * over report block b of report_block_rows x report_block_cols elements
+ * (row-major block index, ragged edge blocks hold the in-bounds elements).
+ * The quantization blocks (scale_block_rows x scale_block_cols) and the
+ * report blocks are independent: a per-tensor KV scale can be reported per
+ * row, for instance.  SQNR of any union of blocks is
+ * 10 log10(sum x^2 / sum e^2).
+ *   stats [ceil(rows/rbr), ceil(cols/rbc), 3] doubles (out).
+ * Accuracy: the maximum is exact for pairs the quantizers produce (x_hat
+ * within a factor 2 of x); the sums are within 1e-5 relative of FP64
+ * (binary32 squares summed over 8 elements), for |x| and |e| in
+ * [2^-63, 2^63].
+ * Rules: as dequantize_blockwise, x_bf16 16-byte aligned, stats 8-byte
+ * aligned; a report block holds at most 2^20 elements, else
+ * W8A8_ERR_UNSUPPORTED.
+ * ---------------------------------------------------------------------- */
+w8a8_status quant_error_report(const uint16_t *x_bf16, const uint8_t *q,
+                               const float *s, int64_t rows, int64_t cols,
+                               int64_t scale_block_rows, int64_t scale_block_cols,
+                               int64_t report_block_rows,
+                               int64_t report_block_cols, double *stats,
+                               w8a8_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * fp8_block_gemm -- the W8A8 linear of [FP8-RL] section 1 / arXiv abstract
  * item (i) with the [NeMo] Table 1 granularities:
  *

@@ -44,6 +44,9 @@ def lib():
             "oracle_block_gemm_entries": (ctypes.c_int, [P, P, P, P, i64, P, P, i64, P, P]),
             "oracle_block_gemm_f32acc": (ctypes.c_int, [P, P, P, P, i64, i64, i64, P]),
             "oracle_grouped_gemm": (ctypes.c_int, [P, P, i64, P, P, i32, P, P, i64, i64, P, P]),
+            "oracle_dequant_value": (ctypes.c_float, [u8, ctypes.c_float]),
+            "oracle_dequantize_blocks": (ctypes.c_int, [P, P, i64, i64, i64, i64, P]),
+            "oracle_quant_error": (ctypes.c_int, [P, P, P, i64, i64, i64, i64, i64, i64, P]),
             "oracle_bf16_from_f64": (u16, [ctypes.c_double]),
             "oracle_bf16_from_f64_array": (None, [P, i64, P]),
         }
@@ -146,6 +149,31 @@ def quantize_act_per_token_group_gather(x_bits, row_idx):
     ok = (ri >= 0) & (ri < rows_x)
     g[ok] = x[ri[ok]]
     return quantize_blocks(g, 1, 128)
+
+
+def dequantize_blocks(q, s, br, bc):
+    """Fake quant ([UFP8] quantize-dequantize experiments): BF16 bits of
+    dec(q) * S (one binary32 multiply, then BF16 round to nearest even)."""
+    q = _c(q, np.uint8)
+    s = _c(s, np.float32)
+    rows, cols = q.shape
+    y = np.empty((rows, cols), np.uint16)
+    assert lib().oracle_dequantize_blocks(_p(q), _p(s), rows, cols, br, bc, _p(y)) == 0
+    return y
+
+
+def quant_error(x_bits, q, s, sbr, sbc, rbr, rbc):
+    """Per report block (rbr x rbc): [max |x - x_hat|, sum (x - x_hat)^2,
+    sum x^2] in FP64, x_hat = dec(q) * S in binary32; shape
+    [ceil(rows/rbr), ceil(cols/rbc), 3]."""
+    x = _c(x_bits, np.uint16)
+    q = _c(q, np.uint8)
+    s = _c(s, np.float32)
+    rows, cols = x.shape
+    st = np.empty((cdiv(rows, rbr), cdiv(cols, rbc), 3), np.float64)
+    assert lib().oracle_quant_error(_p(x), _p(q), _p(s), rows, cols, sbr, sbc, rbr, rbc,
+                                    _p(st)) == 0
+    return st
 
 
 def amax_bf16(x_bits):

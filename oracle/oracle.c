@@ -396,6 +396,68 @@ ORACLE_EXPORT int oracle_grouped_gemm(const uint8_t *xq, const float *xs,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Dequantization (fake quant) and the quantization-error report             */
+/* ------------------------------------------------------------------------ */
+
+/* The inverse the pages pair with Q in their error analysis ([UFP8] "fake
+ * quant" vs "real quant" experiments): x_hat = dec(q) * S as one binary32
+ * multiply.  dec(q) is exact in binary32. */
+ORACLE_EXPORT float oracle_dequant_value(uint8_t q, float s) {
+    float d = (float)oracle_e4m3_decode(q);
+    return d * s;
+}
+
+uint16_t oracle_bf16_from_f64(double y);
+
+/* Dequantize a block-scaled matrix to BF16: y = BF16_RN(x_hat), scale of
+ * element (r, c) at s[(r / br) * ceil(cols / bc) + c / bc]. */
+ORACLE_EXPORT int oracle_dequantize_blocks(const uint8_t *q, const float *s, int64_t rows,
+                                           int64_t cols, int64_t br, int64_t bc,
+                                           uint16_t *y) {
+    int64_t r, c, nbc;
+    if (rows < 0 || cols < 0 || br <= 0 || bc <= 0) return -1;
+    nbc = (cols + bc - 1) / bc;
+    for (r = 0; r < rows; ++r)
+        for (c = 0; c < cols; ++c)
+            y[r * cols + c] = oracle_bf16_from_f64(
+                (double)oracle_dequant_value(q[r * cols + c], s[(r / br) * nbc + c / bc]));
+    return 0;
+}
+
+/* Quantization-error report over report blocks of rbr x rbc elements (the
+ * quantization blocks, sbr x sbc, are given separately): per report block,
+ * stats[3*b + 0] = max |x - x_hat|, stats[3*b + 1] = sum (x - x_hat)^2,
+ * stats[3*b + 2] = sum x^2, all in FP64, elements taken in row-major order
+ * inside the block; x_hat is the binary32 dequantized value. */
+ORACLE_EXPORT int oracle_quant_error(const uint16_t *x, const uint8_t *q, const float *s,
+                                     int64_t rows, int64_t cols, int64_t sbr, int64_t sbc,
+                                     int64_t rbr, int64_t rbc, double *stats) {
+    int64_t nsbc, nrbr, nrbc, br, bc, r, c;
+    if (rows < 0 || cols < 0 || sbr <= 0 || sbc <= 0 || rbr <= 0 || rbc <= 0) return -1;
+    nsbc = (cols + sbc - 1) / sbc;
+    nrbr = (rows + rbr - 1) / rbr;
+    nrbc = (cols + rbc - 1) / rbc;
+    for (br = 0; br < nrbr; ++br)
+        for (bc = 0; bc < nrbc; ++bc) {
+            double mx = 0.0, se = 0.0, sx = 0.0;
+            for (r = br * rbr; r < rows && r < (br + 1) * rbr; ++r)
+                for (c = bc * rbc; c < cols && c < (bc + 1) * rbc; ++c) {
+                    double xv = (double)oracle_bf16_to_f32(x[r * cols + c]);
+                    double xh = (double)oracle_dequant_value(q[r * cols + c],
+                                                             s[(r / sbr) * nsbc + c / sbc]);
+                    double e = xv - xh;
+                    if (fabs(e) > mx) mx = fabs(e);
+                    se += e * e;
+                    sx += xv * xv;
+                }
+            stats[3 * (br * nrbc + bc) + 0] = mx;
+            stats[3 * (br * nrbc + bc) + 1] = se;
+            stats[3 * (br * nrbc + bc) + 2] = sx;
+        }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Output rounding                                                            */
 /* ------------------------------------------------------------------------ */
 

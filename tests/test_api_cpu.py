@@ -92,6 +92,24 @@ def test_gather_quantizer_argument_checks(L):
     assert g(A, 10, 100, A, 5, A, A, None) == UNSUP  # k % 8
 
 
+def test_dequant_and_report_argument_checks(L):
+    d = L.dequantize_blockwise
+    assert d(A, A, -1, 128, 1, 128, A, None) == SHAPE
+    assert d(A, A, 4, 128, 0, 128, A, None) == SHAPE
+    assert d(None, None, 0, 128, 1, 128, None, None) == OK
+    assert d(None, A, 4, 128, 1, 128, A, None) == NULL
+    assert d(A, A, 4, 128, 1, 128, A + 2, None) == ALIGN
+    assert d(A + 8, A, 4, 128, 1, 128, A, None) == ALIGN
+    r = L.quant_error_report
+    assert r(A, A, A, 4, 128, 1, 0, 1, 128, A, None) == SHAPE
+    assert r(A, A, A, 4, 128, 1, 128, -1, 128, A, None) == SHAPE
+    assert r(A, A, A, 4, 128, 1, 128, 1, 128, None, None) == NULL
+    assert r(A, A, A, 4, 128, 1, 128, 1, 128, A + 4, None) == ALIGN
+    assert r(A + 2, A, A, 4, 128, 1, 128, 1, 128, A, None) == ALIGN
+    assert r(A, A, A, 4, 1 << 21, 1, 128, 1, 1 << 21, A, None) == UNSUP
+    assert r(None, None, None, 0, 128, 1, 128, 1, 128, None, None) == OK
+
+
 def test_gemm_argument_checks(L):
     g = L.fp8_block_gemm
     assert g(A, A, A, A, A, 128, 256, 100, None) == SHAPE  # k % 16

@@ -258,6 +258,98 @@ def test_routed_row_quant_is_quant_then_gather_with_zero_rows():
     assert (q2 != q[ok]).any()
 
 
+# ------------------------------------------------- dequantization (fake quant)
+
+def _bf16_val(bits):
+    return (np.asarray(bits, np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def test_dequant_with_unit_scale_is_the_format_decode():
+    """With S = 1 the dequantized BF16 value is the code's E4M3 value itself
+    (every E4M3 value has at most 4 significant bits, so BF16 holds it):
+    the landmarks of the format come back, and every non-NaN code decodes to
+    the pinned decoder's value, signs included."""
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8).reshape(1, -1)
+    y = _bf16_val(O.dequantize_blocks(codes, np.ones((1, 1), np.float32), 1, codes.shape[1]))[0]
+    want = O.e4m3_decode(codes[0])
+    assert (y == want).all() and (np.signbit(y) == np.signbit(want)).all()
+    d = dict(zip(codes[0].tolist(), y.tolist()))
+    assert d[0x7E] == 448.0 and d[0xFE] == -448.0 and d[0x01] == 2.0 ** -9 and d[0x38] == 1.0
+
+
+def test_dequant_scales_by_powers_of_two_exactly():
+    codes = np.arange(0, 0x7F, dtype=np.uint8).reshape(1, -1)
+    base = _bf16_val(O.dequantize_blocks(codes, np.ones((1, 1), np.float32), 1, 127))
+    for j in (-20, -3, 1, 7, 30):
+        y = _bf16_val(O.dequantize_blocks(codes, np.full((1, 1), 2.0 ** j, np.float32), 1, 127))
+        assert (y == base * 2.0 ** j).all()
+
+
+def test_dequant_rounds_the_binary32_product_to_bf16():
+    """Hand-worked double rounding (the reading: one binary32 multiply, then
+    BF16 round-to-nearest-even).  For d = 1.125 (code 0x39) pick the binary32
+    S whose exact product d*S lies just above 1 + 2^-8 (the midpoint between
+    the BF16 neighbours 1 and 1 + 2^-7) but rounds to that midpoint in
+    binary32; the tie then goes to the even BF16 value 1.0.  Rounding the
+    exact product once would give 1 + 2^-7 instead."""
+    d = 1.125
+    found = None
+    s = np.float32((1 + 2.0 ** -8) / d)
+    for _ in range(64):
+        exact = d * float(s)
+        if exact > 1 + 2.0 ** -8 and float(np.float32(d) * s) == 1 + 2.0 ** -8:
+            found = s
+            break
+        s = np.nextafter(s, np.float32(2.0))
+    assert found is not None
+    y = _bf16_val(O.dequantize_blocks(np.array([[0x39]], np.uint8), np.array([[found]], np.float32), 1, 1))
+    assert y[0, 0] == 1.0
+
+
+def test_dequant_of_quant_is_within_half_a_code_step():
+    """Round trip: |BF16(dec(q) S) - x| <= (half an E4M3 spacing of x/S, or
+    half the subnormal quantum) * S + half a BF16 ulp, on weights and on
+    activations with outliers; a transposed or shifted scale grid fails it."""
+    rng = np.random.default_rng(21)
+    for (r, c, br, bc) in [(256, 384, 128, 128), (37, 300, 1, 128)]:
+        xb = _bf16(rng.standard_normal((r, c)) * np.where(rng.random((r, c)) < 0.01, 50, 1))
+        q, s = O.quantize_blocks(xb, br, bc)
+        y = _bf16_val(O.dequantize_blocks(q, s, br, bc))
+        x = _bf16_val(xb)
+        S = np.repeat(np.repeat(s, br, 0), bc, 1)[:r, :c].astype(np.float64)
+        t = np.abs(x) / S
+        step = np.maximum(2.0 ** (np.floor(np.log2(np.maximum(t, 2.0 ** -6))) - 3), 2.0 ** -9)
+        bound = 0.5 * step * S * (1 + 2.0 ** -20) + 2.0 ** -8 * np.abs(y)
+        assert (np.abs(y - x) <= bound).all()
+        if br == 128 and s.shape[0] > 1 and s.shape[1] > 1:
+            yt = _bf16_val(O.dequantize_blocks(q, np.ascontiguousarray(s[::-1]), br, bc))
+            assert not (np.abs(yt - x) <= bound).all()
+
+
+def test_quant_error_hand_block_and_library_sums():
+    """A hand-worked block: amax 448 gives S = 1; 1.0625 lies halfway
+    between the E4M3 values 1.0 and 1.125 and goes to 1.0, so e = 1/16:
+    max 0.0625, sum e^2 = 2^-8, sum x^2 = 1 + 1.12890625 + 200704 + 9.
+    Then random blocks: the sums equal numpy's float64 sums, and reporting
+    over 1x128 or 128x128 blocks gives the same totals."""
+    xb = _bf16(np.array([[1.0, 1.0625, 448.0, 3.0]]))
+    q, s = O.quantize_blocks(xb, 1, 4)
+    assert s[0, 0] == 1.0
+    st = O.quant_error(xb, q, s, 1, 4, 1, 4)[0, 0]
+    assert st[0] == 0.0625 and st[1] == 2.0 ** -8 and st[2] == 1 + 1.12890625 + 200704 + 9
+    rng = np.random.default_rng(22)
+    xb = _bf16(rng.standard_normal((256, 384)))
+    q, s = O.quantize_blocks(xb, 128, 128)
+    a = O.quant_error(xb, q, s, 128, 128, 128, 128)
+    b = O.quant_error(xb, q, s, 128, 128, 1, 128)
+    x = _bf16_val(xb)
+    y32 = (O.e4m3_decode(q) * np.repeat(np.repeat(s, 128, 0), 128, 1).astype(np.float64))
+    assert np.isclose(a[..., 2].sum(), np.sum(x * x), rtol=1e-12, atol=0)
+    assert np.isclose(a[..., 1].sum(), b[..., 1].sum(), rtol=1e-12, atol=0)
+    assert a[..., 0].max() == b[..., 0].max()
+    assert a[..., 0].max() <= np.abs(x - y32).max() * (1 + 2.0 ** -20)
+
+
 def test_kv_is_one_group_and_amax_matches_numpy():
     rng = np.random.default_rng(7)
     x = (rng.standard_normal((2, 64, 8, 128)) * np.exp(0.5 * rng.standard_normal((8, 128)))).astype(np.float32)

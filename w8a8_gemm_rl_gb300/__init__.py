@@ -16,7 +16,8 @@ import torch
 __all__ = [
     "lib", "W8A8Error", "e4m3_encode_f32", "e4m3_decode_f32", "quantize_weight_blockwise",
     "quantize_weight_blockwise_batched", "quantize_act_per_token_group",
-    "quantize_act_per_token_group_gather", "fp8_block_gemm",
+    "quantize_act_per_token_group_gather", "dequantize_blockwise", "quant_error_report",
+    "sqnr_db", "fp8_block_gemm",
     "fp8_grouped_gemm", "kv_amax_quantize", "w8a8_linear", "consume_device_error",
     "KV_AMAX_AND_QUANT", "KV_AMAX_ONLY", "KV_QUANT_ONLY", "LIB_PATH",
 ]
@@ -51,6 +52,8 @@ _SIGNATURES = {
     "quantize_weight_blockwise_batched": (_INT, [_P, _I32, _P]),
     "quantize_act_per_token_group": (_INT, [_P, _I64, _I64, _P, _P, _P]),
     "quantize_act_per_token_group_gather": (_INT, [_P, _I64, _I64, _P, _I64, _P, _P, _P]),
+    "dequantize_blockwise": (_INT, [_P, _P, _I64, _I64, _I64, _I64, _P, _P]),
+    "quant_error_report": (_INT, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, _P]),
     "fp8_block_gemm": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "fp8_grouped_gemm": (_INT, [_P, _P, _I64, _P, _P, _I32, _I64, _P, _P, _P, _I64, _I64, _P]),
     "kv_amax_quantize": (_INT, [_P, _I64, _P, _P, _P, _INT, _P]),
@@ -175,6 +178,40 @@ def quantize_act_per_token_group_gather(x, row_idx, xq=None, xs=None, stream=Non
            lib().quantize_act_per_token_group_gather(_ptr(x), rows_x, k, _ptr(row_idx), total,
                                                      _ptr(xq), _ptr(xs), _stream(stream)))
     return xq, xs
+
+
+def dequantize_blockwise(q, s, block_rows, block_cols, y=None, stream=None):
+    """q uint8 [rows, cols], s float32 scale grid -> BF16 [rows, cols] of dec(q) * S."""
+    _need(q, torch.uint8, "q")
+    rows, cols = q.shape
+    y = torch.empty((rows, cols), dtype=torch.bfloat16, device=q.device) if y is None else y
+    _check("dequantize_blockwise",
+           lib().dequantize_blockwise(_ptr(q), _ptr(s), rows, cols, block_rows, block_cols,
+                                      _ptr(y), _stream(stream)))
+    return y
+
+
+def quant_error_report(x, q, s, scale_block, report_block, stats=None, stream=None):
+    """Per report block: float64 [..., 3] = (max |x - x_hat|, sum e^2, sum x^2)."""
+    _need(x, torch.bfloat16, "x")
+    _need(q, torch.uint8, "q")
+    rows, cols = x.shape
+    rbr, rbc = report_block
+    if stats is None:
+        stats = torch.empty((_cdiv(rows, rbr), _cdiv(cols, rbc), 3), dtype=torch.float64,
+                            device=x.device)
+    _check("quant_error_report",
+           lib().quant_error_report(_ptr(x), _ptr(q), _ptr(s), rows, cols, scale_block[0],
+                                    scale_block[1], rbr, rbc, _ptr(stats), _stream(stream)))
+    return stats
+
+
+def sqnr_db(stats):
+    """10 log10(sum x^2 / sum e^2) over all blocks of a report."""
+    import math
+    se = float(stats[..., 1].sum())
+    sx = float(stats[..., 2].sum())
+    return math.inf if se == 0.0 else 10.0 * math.log10(sx / se)
 
 
 # ------------------------------------------------------------------ GEMMs

@@ -134,6 +134,40 @@ W8A8_API w8a8_status quantize_act_per_token_group_gather(const uint16_t* x_bf16,
                                                  cs(stream)));
 }
 
+// ----------------------------------------------- dequantization and report
+
+W8A8_API w8a8_status dequantize_blockwise(const uint8_t* q, const float* s, int64_t rows,
+                                          int64_t cols, int64_t block_rows, int64_t block_cols,
+                                          uint16_t* y_bf16, w8a8_stream_t stream) {
+  if (rows < 0 || cols < 0 || block_rows <= 0 || block_cols <= 0) return W8A8_ERR_SHAPE;
+  if (rows == 0 || cols == 0) return W8A8_OK;
+  if (!q || !s || !y_bf16) return W8A8_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(y_bf16, 16) || !aligned(s, 4)) return W8A8_ERR_ALIGN;
+  return from_cuda(w8a8::launch_dequant(q, s, rows, cols, block_rows, block_cols, y_bf16,
+                                        cs(stream)));
+}
+
+W8A8_API w8a8_status quant_error_report(const uint16_t* x_bf16, const uint8_t* q, const float* s,
+                                        int64_t rows, int64_t cols, int64_t scale_block_rows,
+                                        int64_t scale_block_cols, int64_t report_block_rows,
+                                        int64_t report_block_cols, double* stats,
+                                        w8a8_stream_t stream) {
+  if (rows < 0 || cols < 0 || scale_block_rows <= 0 || scale_block_cols <= 0 ||
+      report_block_rows <= 0 || report_block_cols <= 0)
+    return W8A8_ERR_SHAPE;
+  if (rows == 0 || cols == 0) return W8A8_OK;
+  if (!x_bf16 || !q || !s || !stats) return W8A8_ERR_NULL;
+  if (!aligned(x_bf16, 16) || !aligned(q, 16) || !aligned(s, 4) || !aligned(stats, 8))
+    return W8A8_ERR_ALIGN;
+  // one warp walks a report block: keep blocks to at most 2^20 elements
+  if (report_block_rows > (1 << 20) || report_block_cols > (1 << 20) ||
+      report_block_rows * report_block_cols > (1 << 20))
+    return W8A8_ERR_UNSUPPORTED;
+  return from_cuda(w8a8::launch_quant_error(x_bf16, q, s, rows, cols, scale_block_rows,
+                                            scale_block_cols, report_block_rows,
+                                            report_block_cols, stats, cs(stream)));
+}
+
 // ------------------------------------------------------------------ GEMMs
 
 static w8a8_status check_gemm_common(const uint8_t* xq, const float* xs, const uint8_t* wq,

@@ -89,7 +89,7 @@ __device__ __forceinline__ uint32_t code_exact(float x, float s) {
 
 // Four codes by the correctly rounded division (out of line: the path of
 // unusual scales only).
-__device__ __noinline__ uint32_t codes_by_division(float x0, float x1, float x2, float x3,
+static __device__ __noinline__ uint32_t codes_by_division(float x0, float x1, float x2, float x3,
                                                    float s) {
   return code_exact(x0, s) | (code_exact(x1, s) << 8) | (code_exact(x2, s) << 16) |
          (code_exact(x3, s) << 24);

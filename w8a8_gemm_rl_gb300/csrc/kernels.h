@@ -34,6 +34,14 @@ cudaError_t launch_weight_quant(const WeightJob* jobs, int count, cudaStream_t s
 cudaError_t launch_kv_amax_quantize(const uint16_t* x, int64_t n, uint8_t* q, float* scale,
                                     float* amax, int mode, cudaStream_t st);
 
+// dequant.cu: y = BF16(dec(q) * S) over br x bc scale blocks, and the
+// per-report-block error statistics [max |x - x_hat|, sum e^2, sum x^2].
+cudaError_t launch_dequant(const uint8_t* q, const float* s, int64_t rows, int64_t cols,
+                           int64_t br, int64_t bc, uint16_t* y, cudaStream_t st);
+cudaError_t launch_quant_error(const uint16_t* x, const uint8_t* q, const float* s, int64_t rows,
+                               int64_t cols, int64_t sbr, int64_t sbc, int64_t rbr, int64_t rbc,
+                               double* stats, cudaStream_t st);
+
 cudaError_t launch_block_gemm(const uint8_t* xq, const float* xs, const uint8_t* wq,
                               const float* ws, uint16_t* y, int64_t m, int64_t n, int64_t k,
                               cudaStream_t st);
