@@ -373,8 +373,8 @@ cudaError_t launch_act_quant_gather(const uint16_t* x, int64_t rows_x, int64_t k
 //             the next), release the stage, block amax (butterfly + 8
 //             partials through shared memory + a named barrier), S, then
 //             the codes straight to global memory as 8-byte stores.
-// A batch of matrices is one launch; a CTA finds the matrix of a block by
-// binary search over the block prefix sums held in the kernel parameters.
+// A batch of matrices is one launch; a CTA finds the matrix of a block from
+// the block prefix sums held in the kernel parameters.
 // All waits are bounded; a wait that gives up records an error and the CTA
 // stops after draining its copies.
 
@@ -404,16 +404,19 @@ struct BlockRef {
   int cols;  // valid columns (multiple of 8)
 };
 
+// The matrix holding block blk.  A CTA visits its blocks in increasing
+// order, so the previous answer (hint) is advanced instead of searched for:
+// usually no step at all (matrices hold >= 1024 blocks, a CTA strides ~300).
 template <int kMax>
-__device__ __forceinline__ BlockRef locate_block(const WeightBatch<kMax>& b, int64_t blk) {
-  int lo = 0;
-  if (kMax > 1) {
-    int hi = b.count;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (b.first[mid] <= blk) lo = mid; else hi = mid;
-    }
-  }
+__device__ __forceinline__ int find_matrix(const WeightBatch<kMax>& b, int64_t blk, int hint) {
+  int lo = hint;
+  if (kMax > 1)
+    while (b.first[lo + 1] <= blk) ++lo;
+  return lo;
+}
+
+template <int kMax>
+__device__ __forceinline__ BlockRef locate_block(const WeightBatch<kMax>& b, int64_t blk, int lo) {
   BlockRef r;
   r.mat = lo;
   const int64_t n = b.n[lo], k = b.k[lo];
@@ -455,6 +458,7 @@ __global__ void __launch_bounds__(WQ_THREADS, 2)
   if (warp == WQ_CONSUMER_WARPS) {
     // ------------------------------------------------------------ producer
     int64_t issued = 0;
+    int mat = 0;
     for (int64_t blk = blockIdx.x; blk < total; blk += gridDim.x, ++issued) {
       const int s = (int)(issued % WQ_STAGES);
       const uint32_t par = (uint32_t)((issued / WQ_STAGES) & 1);
@@ -465,7 +469,8 @@ __global__ void __launch_bounds__(WQ_THREADS, 2)
       }
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok || *abort_flag) break;
-      const BlockRef r = locate_block(b, blk);
+      mat = find_matrix(b, blk, mat);
+      const BlockRef r = locate_block(b, blk, mat);
       if (lane == 0) {
         ptx::mbar_arrive_expect_tx(full_bar(s), WQ_STAGE_BYTES);
         ptx::tma_load_2d(sbase + s * WQ_STAGE_BYTES, &b.tmap[r.mat], full_bar(s), (int)(r.bj * 128),
@@ -486,14 +491,17 @@ __global__ void __launch_bounds__(WQ_THREADS, 2)
   const int t = threadIdx.x;  // 0..255
   const int ch = t & 15;      // 16-byte chunk within a 256-byte row
   int64_t it = 0;
+  int mat = 0;
   for (int64_t blk = blockIdx.x; blk < total; blk += gridDim.x, ++it) {
+    // the block's place does not depend on its data: find it before waiting
+    mat = find_matrix(b, blk, mat);
+    const BlockRef r = locate_block(b, blk, mat);
     const int s = (int)(it % WQ_STAGES);
     const uint32_t par = (uint32_t)((it / WQ_STAGES) & 1);
     uint32_t ok = 1;
     if (lane == 0) ok = ptx::mbar_wait(full_bar(s), par, WQ_WAIT_NS) ? 1u : 0u;
     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
     if (!ok && lane == 0) atomicCAS(&g_w8a8_quant_error, 0, 13);
-    const BlockRef r = locate_block(b, blk);
     const uint32_t stage = sbase + s * WQ_STAGE_BYTES;
     const bool col_ok = ch * 8 < r.cols;
     uint4 v[8];
