@@ -507,9 +507,10 @@ def bench_ours(args):
 
 def measure_next_rows(W, wl, peaks, reps=3):
     """Rows past the hot path, each on its own kernel roofline (HBM): the
-    dequantizer (fake quant) over every weight matrix of the model from its
-    128x128-block codes, and the quantization-error report over the same
-    matrices (128x128 report blocks).  One launch per matrix, inputs (20 GB)
+    power-of-two-scale weight quantizer, the dequantizer (fake quant) over
+    every weight matrix of the model from its 128x128-block codes, and the
+    quantization-error report over the same matrices (128x128 report
+    blocks).  One launch per matrix, inputs (20 GB)
     far larger than L2; CUDA events around each sweep of all 144 matrices."""
     out = {}
     big = max(w.numel() for w in wl.w)
@@ -527,6 +528,24 @@ def measure_next_rows(W, wl, peaks, reps=3):
                 W.quant_error_report(w, q, sc, (128, 128), (128, 128),
                                      stats[: cdiv(n, 128) * cdiv(k, 128) * 3].view(cdiv(n, 128), cdiv(k, 128), 3))
 
+    # power-of-two scales: the same weight sync as the step, one batched launch
+    def pow2_sweep():
+        W.quantize_weight_blockwise_batched(wl.w, wl.wout, pow2=True)
+    pow2_sweep()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(reps):
+        pow2_sweep()
+    t1.record()
+    torch.cuda.synchronize()
+    sec = t0.elapsed_time(t1) * 1e-3 / reps
+    nb = 3 * elems + 4 * blocks
+    out["quantize_weight_blockwise_batched_pow2"] = {
+        "workload": "all 144 Qwen3-8B weight matrices, 128x128 blocks, 1 batched launch",
+        "ms": round(sec * 1e3, 3), "gbs": round(nb / sec / 1e9, 1),
+        "pct_roofline": round(100 * nb / sec / 1e9 / peaks["hbm_gbs"], 2), "bytes_per_sweep": nb}
     W.quantize_weight_blockwise_batched(wl.w, wl.wout)
     for kind, nbytes in (("dequant", 3 * elems + 4 * blocks),
                          ("quant_error_report", 3 * elems + 4 * blocks + 24 * blocks)):

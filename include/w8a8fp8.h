@@ -135,6 +135,30 @@ w8a8_status quantize_act_per_token_group(const uint16_t *x_bf16, int64_t m,
                                          w8a8_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * quantize_weight_blockwise_pow2, quantize_act_per_token_group_pow2 -- the
+ * same quantizers with power-of-two scales, the "Power-of-2 Scaling Factor"
+ * recipe option of the [NeMo] blog (section on recipe variants; [UFP8]
+ * "FP8 scale choice" weighs it against FP32 scales):
+ *
+ *   S = the smallest 2^e with 448 * 2^e >= amax   (S = 1 when amax == 0)
+ *   q = E4M3_RNE(x / S)                           (x / S is exact)
+ *
+ * so no code saturates and every scale is a UE8M0-representable power of
+ * two.  Arguments, layouts and rules as the FP32-scale versions (the
+ * batched one as quantize_weight_blockwise_batched); the GEMMs take these
+ * scales unchanged.
+ * ---------------------------------------------------------------------- */
+w8a8_status quantize_weight_blockwise_pow2(const uint16_t *w_bf16, int64_t n,
+                                           int64_t k, uint8_t *wq, float *ws,
+                                           w8a8_stream_t stream);
+w8a8_status quantize_act_per_token_group_pow2(const uint16_t *x_bf16, int64_t m,
+                                              int64_t k, uint8_t *xq, float *xs,
+                                              w8a8_stream_t stream);
+w8a8_status quantize_weight_blockwise_batched_pow2(const w8a8_weight_desc *descs,
+                                                   int32_t count,
+                                                   w8a8_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * quantize_act_per_token_group_gather -- the activation quantizer above
  * applied to the routed rows of an MoE layer ([FP8-RL] section 1 expert
  * layers, [NeMo] Table 1 [1,128] groups): output row r is the per-token

@@ -38,6 +38,8 @@ def lib():
             "oracle_scale_from_amax": (ctypes.c_float, [ctypes.c_float]),
             "oracle_quantize_value": (u8, [ctypes.c_float, ctypes.c_float]),
             "oracle_quantize_blocks": (ctypes.c_int, [P, i64, i64, i64, i64, P, P]),
+            "oracle_quantize_blocks_mode": (ctypes.c_int, [P, i64, i64, i64, i64, ctypes.c_int, P, P]),
+            "oracle_scale_pow2_from_amax": (ctypes.c_float, [ctypes.c_float]),
             "oracle_amax_bf16": (ctypes.c_float, [P, i64]),
             "oracle_quantize_with_scale": (None, [P, i64, ctypes.c_float, P]),
             "oracle_block_gemm": (ctypes.c_int, [P, P, P, P, i64, i64, i64, P, P]),
@@ -115,14 +117,19 @@ def scale_from_amax(amax):
     return lib().oracle_scale_from_amax(float(amax))
 
 
-def quantize_blocks(x_bf16_bits, br, bc):
+def scale_pow2_from_amax(amax):
+    return lib().oracle_scale_pow2_from_amax(float(amax))
+
+
+def quantize_blocks(x_bf16_bits, br, bc, pow2=False):
     """x_bf16_bits: uint16 [rows, cols].  Returns (q uint8 [rows, cols],
-    s float32 [ceil(rows/br), ceil(cols/bc)])."""
+    s float32 [ceil(rows/br), ceil(cols/bc)]).  pow2: power-of-two scales
+    (NeMo blog, recipe variants), S = the smallest 2^e with 448 S >= amax."""
     x = _c(x_bf16_bits, np.uint16)
     rows, cols = x.shape
     q = np.empty((rows, cols), np.uint8)
     s = np.empty((cdiv(rows, br), cdiv(cols, bc)), np.float32)
-    rc = lib().oracle_quantize_blocks(_p(x), rows, cols, br, bc, _p(q), _p(s))
+    rc = lib().oracle_quantize_blocks_mode(_p(x), rows, cols, br, bc, 1 if pow2 else 0, _p(q), _p(s))
     assert rc == 0
     return q, s
 

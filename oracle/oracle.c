@@ -213,6 +213,18 @@ ORACLE_EXPORT float oracle_scale_from_amax(float amax) {
 
 /* Q(x) = round(x / S): binary32 division, then E4M3 rounding with
  * saturation. */
+/* Power-of-two scale ([NeMo] blog, recipe variants: "power-of-2 scaling
+ * factor"): the smallest power of two S with 448 * S >= amax, found by
+ * walking the exponent with exact comparisons (448 * 2^e is exact in
+ * binary32 over the whole range used); S = 1 for an all-zero group. */
+ORACLE_EXPORT float oracle_scale_pow2_from_amax(float amax) {
+    int e = 0;
+    if (amax == 0.0f) return 1.0f;
+    while (448.0f * ldexpf(1.0f, e) < amax) ++e;
+    while (448.0f * ldexpf(1.0f, e - 1) >= amax) --e;
+    return ldexpf(1.0f, e);
+}
+
 ORACLE_EXPORT uint8_t oracle_quantize_value(float x, float s) {
     float t = x / s;
     return oracle_e4m3_encode(t);
@@ -228,9 +240,10 @@ ORACLE_EXPORT uint8_t oracle_quantize_value(float x, float s) {
  *   activations:  br = 1,  bc = 128    ([NeMo] Table 1; [UFP8] per-token)
  *   KV cache:     rows = 1, br = 1, bc = cols = numel  ([NeMo] Table 3)
  */
-ORACLE_EXPORT int oracle_quantize_blocks(const uint16_t *x, int64_t rows,
-                                         int64_t cols, int64_t br, int64_t bc,
-                                         uint8_t *q, float *s) {
+/* pow2 != 0: power-of-two scales (oracle_scale_pow2_from_amax). */
+ORACLE_EXPORT int oracle_quantize_blocks_mode(const uint16_t *x, int64_t rows,
+                                              int64_t cols, int64_t br, int64_t bc,
+                                              int pow2, uint8_t *q, float *s) {
     int64_t nbr, nbc, bi, bj, r, c;
     if (rows < 0 || cols < 0 || br <= 0 || bc <= 0) return -1;
     nbr = (rows + br - 1) / br;
@@ -245,7 +258,7 @@ ORACLE_EXPORT int oracle_quantize_blocks(const uint16_t *x, int64_t rows,
                     float a = fabsf(oracle_bf16_to_f32(x[r * cols + c]));
                     if (a > amax) amax = a;
                 }
-            scale = oracle_scale_from_amax(amax);
+            scale = pow2 ? oracle_scale_pow2_from_amax(amax) : oracle_scale_from_amax(amax);
             s[bi * nbc + bj] = scale;
             for (r = r0; r < r1; ++r)
                 for (c = c0; c < c1; ++c)
@@ -254,6 +267,12 @@ ORACLE_EXPORT int oracle_quantize_blocks(const uint16_t *x, int64_t rows,
         }
     }
     return 0;
+}
+
+ORACLE_EXPORT int oracle_quantize_blocks(const uint16_t *x, int64_t rows,
+                                         int64_t cols, int64_t br, int64_t bc,
+                                         uint8_t *q, float *s) {
+    return oracle_quantize_blocks_mode(x, rows, cols, br, bc, 0, q, s);
 }
 
 /* max |x| over a BF16 array (the per-tensor KV amax). */

@@ -110,6 +110,14 @@ def test_dequant_and_report_argument_checks(L):
     assert r(None, None, None, 0, 128, 1, 128, 1, 128, None, None) == OK
 
 
+def test_pow2_quantizer_argument_checks(L):
+    for f in (L.quantize_weight_blockwise_pow2, L.quantize_act_per_token_group_pow2):
+        assert f(None, 4, 128, A, A, None) == NULL
+        assert f(A, -1, 128, A, A, None) == SHAPE
+        assert f(A + 2, 4, 128, A, A, None) == ALIGN
+        assert f(None, 0, 128, None, None, None) == OK
+
+
 def test_gemm_argument_checks(L):
     g = L.fp8_block_gemm
     assert g(A, A, A, A, A, 128, 256, 100, None) == SHAPE  # k % 16

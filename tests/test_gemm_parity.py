@@ -79,6 +79,23 @@ def test_single_w8a8_linear_config(W):
     assert (bits16(y2) == bits16(y)).all()
 
 
+def test_linear_with_power_of_two_scales(W):
+    """The GEMM takes power-of-two scales as they come: both operands
+    quantized on the GPU with pow2 scales (bit-exact with the oracle's), then
+    the GEMM within the tolerance of the oracle's exact product."""
+    x = synth.activations(200, 1024, seed=8)
+    w = synth.weights(384, 1024, seed=9)
+    xq, xs = W.quantize_act_per_token_group(x.cuda(), pow2=True)
+    wq, ws = W.quantize_weight_blockwise(w.cuda(), pow2=True)
+    y = W.fp8_block_gemm(xq, xs, wq, ws)
+    torch.cuda.synchronize()
+    xq_r, xs_r = O.quantize_blocks(synth.bf16_bits(x), 1, 128, pow2=True)
+    wq_r, ws_r = O.quantize_blocks(synth.bf16_bits(w), 128, 128, pow2=True)
+    assert (xq.cpu().numpy() == xq_r).all() and (wq.cpu().numpy() == wq_r).all()
+    y_ref, absref = O.block_gemm(xq_r, xs_r, wq_r, ws_r)
+    assert_gemm_close(bits16(y), y_ref, absref, "pow2 linear")
+
+
 def test_scale_power_of_two_is_exact(W):
     m, n, k = 96, 512, 1024
     xq, wq = _codes((m, k), 3), _codes((n, k), 4)

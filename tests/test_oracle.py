@@ -258,6 +258,44 @@ def test_routed_row_quant_is_quant_then_gather_with_zero_rows():
     assert (q2 != q[ok]).any()
 
 
+# ------------------------------------------------------ power-of-two scales
+
+def test_pow2_scale_hand_values_and_definition():
+    """S is the smallest power of two with 448 S >= amax: hand values at the
+    boundaries (448 -> 1, 448 + 1 ulp -> 2, 224 -> 1/2, 1 -> 2^-8 since
+    448 * 2^-9 = 0.875 < 1), the zero group, the extremes of BF16, and on a
+    sweep: a power of two (frexp mantissa 1/2), 448 S >= amax, 448 S/2 < amax."""
+    f32 = np.float32
+    assert O.scale_pow2_from_amax(0.0) == 1.0
+    assert O.scale_pow2_from_amax(448.0) == 1.0
+    assert O.scale_pow2_from_amax(float(np.nextafter(f32(448), f32(1e9)))) == 2.0
+    assert O.scale_pow2_from_amax(224.0) == 0.5 and O.scale_pow2_from_amax(1.0) == 2.0 ** -8
+    assert O.scale_pow2_from_amax(2.0 ** -133) == 2.0 ** -141  # smallest BF16 subnormal
+    assert O.scale_pow2_from_amax(float(_bf16_val(np.array([0x7F7F]))[0])) == 2.0 ** 120
+    rng = np.random.default_rng(23)
+    for a in np.exp(rng.uniform(-80, 80, 2000)).astype(np.float32):
+        sc = O.scale_pow2_from_amax(float(a))
+        m, _ = np.frexp(sc)
+        assert m == 0.5 and 448.0 * sc >= a and 448.0 * sc / 2 < a
+
+
+def test_pow2_quant_is_one_rounding_of_an_exact_quotient():
+    """With S a power of two, x / S is exact, so a code is torch's E4M3
+    rounding of x * 2^-e; no code saturates: amax / S lies in (224, 448], so
+    the largest code magnitude in a non-zero group lies in [224, 448]
+    (224 itself when amax / S rounds down to it, the grid step there being 32)."""
+    rng = np.random.default_rng(24)
+    xb = _bf16(rng.standard_normal((64, 384)) * np.where(rng.random((64, 384)) < 0.01, 50, 1))
+    q, s = O.quantize_blocks(xb, 1, 128, pow2=True)
+    x = _bf16_val(xb).astype(np.float32)
+    S = np.repeat(s, 128, 1)
+    t = torch.from_numpy((x / S).astype(np.float32))
+    want = t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert (q == want).all()
+    mag = np.abs(O.e4m3_decode(q)).reshape(64, 3, 128).max(-1)
+    assert ((mag >= 224) & (mag <= 448)).all()
+
+
 # ------------------------------------------------- dequantization (fake quant)
 
 def _bf16_val(bits):

@@ -253,3 +253,47 @@ def test_kv_full_size_sampled(W):
         assert (got == O.quantize_with_scale(xb[idx], s_ref)).all()
         del x, q
     torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------- power-of-two scales
+
+@pytest.mark.parametrize("m,k", [(1, 128), (7, 200), (128, 512), (33, 4096), (9, 1000), (2, 12)])
+def test_act_quant_pow2_bit_exact(W, m, k):
+    x = synth.activations(m, k, seed=m * 31 + k + 5, device="cpu")
+    xq, xs = W.quantize_act_per_token_group(x.cuda(), pow2=True)
+    q_ref, s_ref = O.quantize_blocks(synth.bf16_bits(x), 1, 128, pow2=True)
+    assert (u8(xq) == q_ref).all()
+    assert (f32(xs).view(np.uint32) == s_ref.view(np.uint32)).all()
+
+
+@pytest.mark.parametrize("n,k", [(256, 512), (300, 200), (129, 1000), (6144, 4096), (5, 12)])
+def test_weight_quant_pow2_bit_exact(W, n, k):
+    w = synth.weights(n, k, seed=n + k, device="cpu")
+    wq, ws = W.quantize_weight_blockwise(w.cuda(), pow2=True)
+    q_ref, s_ref = O.quantize_blocks(synth.bf16_bits(w), 128, 128, pow2=True)
+    assert (u8(wq) == q_ref).all()
+    assert (f32(ws).view(np.uint32) == s_ref.view(np.uint32)).all()
+
+
+def test_pow2_scales_extreme_magnitudes(W):
+    """Groups spanning the BF16 range: subnormal groups (S down to 2^-141),
+    all-zero groups (S = 1) and groups near the BF16 maximum (S = 2^120)."""
+    bits = np.zeros((4, 256), np.uint16)
+    bits[0] = 0x0001                      # smallest BF16 subnormal everywhere
+    bits[1, :128] = 0x7F7F                # BF16 max
+    bits[1, 128:] = 0x8000                # -0 group
+    bits[2] = np.arange(256, dtype=np.uint16) | 0x0100
+    bits[3, ::2] = 0x3F80                 # 1.0 and zeros
+    x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+    xq, xs = W.quantize_act_per_token_group(x, pow2=True)
+    q_ref, s_ref = O.quantize_blocks(bits, 1, 128, pow2=True)
+    assert (u8(xq) == q_ref).all()
+    assert (f32(xs).view(np.uint32) == s_ref.view(np.uint32)).all()
+
+
+def test_weight_quant_batched_pow2_matches_single(W):
+    ws_ = [synth.weights(n, k, seed=40 + n, device="cuda") for n, k in [(256, 512), (300, 200), (128, 4096)]]
+    outs = W.quantize_weight_blockwise_batched(ws_, pow2=True)
+    for w, (q, s) in zip(ws_, outs):
+        q1, s1 = W.quantize_weight_blockwise(w, pow2=True)
+        assert torch.equal(q, q1) and torch.equal(s.view(torch.int32), s1.view(torch.int32))

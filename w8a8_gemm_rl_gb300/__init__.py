@@ -50,7 +50,10 @@ _SIGNATURES = {
     "e4m3_decode_f32": (_INT, [_P, _I64, _P, _P]),
     "quantize_weight_blockwise": (_INT, [_P, _I64, _I64, _P, _P, _P]),
     "quantize_weight_blockwise_batched": (_INT, [_P, _I32, _P]),
+    "quantize_weight_blockwise_batched_pow2": (_INT, [_P, _I32, _P]),
     "quantize_act_per_token_group": (_INT, [_P, _I64, _I64, _P, _P, _P]),
+    "quantize_weight_blockwise_pow2": (_INT, [_P, _I64, _I64, _P, _P, _P]),
+    "quantize_act_per_token_group_pow2": (_INT, [_P, _I64, _I64, _P, _P, _P]),
     "quantize_act_per_token_group_gather": (_INT, [_P, _I64, _I64, _P, _I64, _P, _P, _P]),
     "dequantize_blockwise": (_INT, [_P, _P, _I64, _I64, _I64, _I64, _P, _P]),
     "quant_error_report": (_INT, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, _P]),
@@ -124,20 +127,22 @@ def e4m3_decode_f32(q, out=None, stream=None):
 
 # ------------------------------------------------------------- quantizers
 
-def quantize_weight_blockwise(w, wq=None, ws=None, stream=None):
-    """w BF16 [n, k] -> (wq uint8 [n, k], ws float32 [ceil(n/128), ceil(k/128)])."""
+def quantize_weight_blockwise(w, wq=None, ws=None, stream=None, pow2=False):
+    """w BF16 [n, k] -> (wq uint8 [n, k], ws float32 [ceil(n/128), ceil(k/128)]);
+    pow2: power-of-two scales (quantize_weight_blockwise_pow2)."""
     _need(w, torch.bfloat16, "w")
     n, k = w.shape
     wq = torch.empty((n, k), dtype=torch.uint8, device=w.device) if wq is None else wq
     ws = torch.empty((_cdiv(n, 128), _cdiv(k, 128)), dtype=torch.float32, device=w.device) if ws is None else ws
-    _check("quantize_weight_blockwise",
-           lib().quantize_weight_blockwise(_ptr(w), n, k, _ptr(wq), _ptr(ws), _stream(stream)))
+    name = "quantize_weight_blockwise_pow2" if pow2 else "quantize_weight_blockwise"
+    _check(name, getattr(lib(), name)(_ptr(w), n, k, _ptr(wq), _ptr(ws), _stream(stream)))
     return wq, ws
 
 
-def quantize_weight_blockwise_batched(ws_in, outs=None, stream=None):
+def quantize_weight_blockwise_batched(ws_in, outs=None, stream=None, pow2=False):
     """Quantize a list of BF16 weight matrices in one call.  Returns a list of
-    (wq, ws) pairs (or fills `outs`, a list of such pairs)."""
+    (wq, ws) pairs (or fills `outs`, a list of such pairs).  pow2:
+    power-of-two scales."""
     if outs is None:
         outs = []
         for w in ws_in:
@@ -148,20 +153,20 @@ def quantize_weight_blockwise_batched(ws_in, outs=None, stream=None):
     for i, (w, (q, s)) in enumerate(zip(ws_in, outs)):
         _need(w, torch.bfloat16, "w")
         descs[i] = WeightDesc(w.data_ptr(), q.data_ptr(), s.data_ptr(), w.shape[0], w.shape[1])
-    _check("quantize_weight_blockwise_batched",
-           lib().quantize_weight_blockwise_batched(ctypes.cast(descs, ctypes.c_void_p), len(ws_in),
-                                                   _stream(stream)))
+    name = "quantize_weight_blockwise_batched_pow2" if pow2 else "quantize_weight_blockwise_batched"
+    _check(name, getattr(lib(), name)(ctypes.cast(descs, ctypes.c_void_p), len(ws_in), _stream(stream)))
     return outs
 
 
-def quantize_act_per_token_group(x, xq=None, xs=None, stream=None):
-    """x BF16 [m, k] -> (xq uint8 [m, k], xs float32 [m, ceil(k/128)])."""
+def quantize_act_per_token_group(x, xq=None, xs=None, stream=None, pow2=False):
+    """x BF16 [m, k] -> (xq uint8 [m, k], xs float32 [m, ceil(k/128)]);
+    pow2: power-of-two scales (quantize_act_per_token_group_pow2)."""
     _need(x, torch.bfloat16, "x")
     m, k = x.shape
     xq = torch.empty((m, k), dtype=torch.uint8, device=x.device) if xq is None else xq
     xs = torch.empty((m, _cdiv(k, 128)), dtype=torch.float32, device=x.device) if xs is None else xs
-    _check("quantize_act_per_token_group",
-           lib().quantize_act_per_token_group(_ptr(x), m, k, _ptr(xq), _ptr(xs), _stream(stream)))
+    name = "quantize_act_per_token_group_pow2" if pow2 else "quantize_act_per_token_group"
+    _check(name, getattr(lib(), name)(_ptr(x), m, k, _ptr(xq), _ptr(xs), _stream(stream)))
     return xq, xs
 
 

@@ -88,8 +88,8 @@ W8A8_API w8a8_status quantize_weight_blockwise(const uint16_t* w_bf16, int64_t n
   return from_cuda(w8a8::launch_weight_quant(&j, 1, cs(stream)));
 }
 
-W8A8_API w8a8_status quantize_weight_blockwise_batched(const w8a8_weight_desc* descs,
-                                                       int32_t count, w8a8_stream_t stream) {
+static w8a8_status weight_batch(const w8a8_weight_desc* descs, int32_t count, bool pow2,
+                                w8a8_stream_t stream) {
   if (count < 0) return W8A8_ERR_SHAPE;
   if (count == 0) return W8A8_OK;
   if (!descs) return W8A8_ERR_NULL;
@@ -105,12 +105,38 @@ W8A8_API w8a8_status quantize_weight_blockwise_batched(const w8a8_weight_desc* d
   for (int32_t i = 0; i < count; ++i) {
     jobs[nj++] = w8a8::WeightJob{descs[i].w_bf16, descs[i].wq, descs[i].ws, descs[i].n, descs[i].k};
     if (nj == kChunk || i == count - 1) {
-      w8a8_status st = from_cuda(w8a8::launch_weight_quant(jobs, nj, cs(stream)));
+      w8a8_status st = from_cuda(w8a8::launch_weight_quant(jobs, nj, cs(stream), pow2));
       if (st != W8A8_OK) return st;
       nj = 0;
     }
   }
   return W8A8_OK;
+}
+
+W8A8_API w8a8_status quantize_weight_blockwise_batched(const w8a8_weight_desc* descs,
+                                                       int32_t count, w8a8_stream_t stream) {
+  return weight_batch(descs, count, false, stream);
+}
+
+W8A8_API w8a8_status quantize_weight_blockwise_batched_pow2(const w8a8_weight_desc* descs,
+                                                            int32_t count, w8a8_stream_t stream) {
+  return weight_batch(descs, count, true, stream);
+}
+
+W8A8_API w8a8_status quantize_weight_blockwise_pow2(const uint16_t* w_bf16, int64_t n, int64_t k,
+                                                    uint8_t* wq, float* ws, w8a8_stream_t stream) {
+  w8a8_status st = check_quant_matrix(w_bf16, n, k, wq, ws);
+  if (st != W8A8_OK || n == 0 || k == 0) return st;
+  w8a8::WeightJob j{w_bf16, wq, ws, n, k};
+  return from_cuda(w8a8::launch_weight_quant(&j, 1, cs(stream), true));
+}
+
+W8A8_API w8a8_status quantize_act_per_token_group_pow2(const uint16_t* x_bf16, int64_t m,
+                                                       int64_t k, uint8_t* xq, float* xs,
+                                                       w8a8_stream_t stream) {
+  w8a8_status st = check_quant_matrix(x_bf16, m, k, xq, xs);
+  if (st != W8A8_OK || m == 0 || k == 0) return st;
+  return from_cuda(w8a8::launch_act_quant(x_bf16, m, k, xq, xs, cs(stream), true));
 }
 
 W8A8_API w8a8_status quantize_act_per_token_group(const uint16_t* x_bf16, int64_t m, int64_t k,

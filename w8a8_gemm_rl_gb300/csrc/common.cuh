@@ -44,6 +44,23 @@ __device__ __forceinline__ float scale_from_amax(float amax) {
   return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
 }
 
+// ---- power-of-two scale: the smallest S = 2^e with 448 S >= amax ----
+// (the pages' "power-of-2 scaling factor" option, NeMo RL FP8 blog, section
+// on recipe variants).  With amax = f 2^p, f in [0.5, 1), and 448 = 0.875 2^9:
+// e = p - 9, plus one when f > 0.875.  x / S is then exact, so a code is the
+// single rounding E4M3(x / S); S = 1 for an all-zero group.
+__device__ __forceinline__ float scale_pow2_from_amax(float amax) {
+  if (amax == 0.0f) return 1.0f;
+  int p;
+  const float f = frexpf(amax, &p);
+  return ldexpf(1.0f, p - 9 + (f > 0.875f ? 1 : 0));
+}
+
+template <bool kPow2>
+__device__ __forceinline__ float group_scale(float amax) {
+  return kPow2 ? scale_pow2_from_amax(amax) : scale_from_amax(amax);
+}
+
 // ---- E4M3(RN32(x / S)), exactly, without a division per element ----
 // The binary32 quotient RN32(x / S) is formed with Markstein's correction
 // step (P. Markstein, "Computation of elementary functions on the IBM

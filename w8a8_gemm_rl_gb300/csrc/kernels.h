@@ -14,8 +14,9 @@ int sm_count();
 cudaError_t launch_e4m3_encode(const float* x, int64_t n, uint8_t* q, cudaStream_t st);
 cudaError_t launch_e4m3_decode(const uint8_t* q, int64_t n, float* x, cudaStream_t st);
 
+// pow2: power-of-two scales (the smallest 2^e with 448 * 2^e >= amax).
 cudaError_t launch_act_quant(const uint16_t* x, int64_t m, int64_t k, uint8_t* q, float* s,
-                             cudaStream_t st);
+                             cudaStream_t st, bool pow2 = false);
 
 // Output row r quantizes x row row_idx[r] (zeros when outside [0, rows_x)).
 cudaError_t launch_act_quant_gather(const uint16_t* x, int64_t rows_x, int64_t k,
@@ -28,7 +29,8 @@ struct WeightJob {
   float* ws;
   int64_t n, k;
 };
-cudaError_t launch_weight_quant(const WeightJob* jobs, int count, cudaStream_t st);
+cudaError_t launch_weight_quant(const WeightJob* jobs, int count, cudaStream_t st,
+                                bool pow2 = false);
 
 // Per-tensor KV quantization; mode as in the public header.
 cudaError_t launch_kv_amax_quantize(const uint16_t* x, int64_t n, uint8_t* q, float* scale,

@@ -121,6 +121,7 @@ cudaError_t launch_e4m3_decode(const uint8_t* q, int64_t n, float* x, cudaStream
 // multiple of 8 BF16 values, where 16-byte row segments do not exist.
 // =====================================================================
 
+template <bool kPow2>
 __global__ void __launch_bounds__(256) block_quant_generic_kernel(const uint16_t* __restrict__ x,
                                                                   int64_t rows, int64_t cols,
                                                                   int64_t br, int64_t bc,
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(256) block_quant_generic_kernel(const uint16_t
   __syncthreads();
   a = red[0];
   for (int i = 1; i < (int)(blockDim.x >> 5); ++i) a = fmaxf(a, red[i]);
-  const float S = scale_from_amax(a);
+  const float S = group_scale<kPow2>(a);
   const QuantScale qs = make_quant_scale(S);
   for (int64_t t = threadIdx.x; t < cnt; t += blockDim.x) {
     const int64_t r = r0 + t / w, c = c0 + t % w;
@@ -154,11 +155,15 @@ __global__ void __launch_bounds__(256) block_quant_generic_kernel(const uint16_t
 }
 
 static cudaError_t launch_generic(const uint16_t* x, int64_t rows, int64_t cols, int64_t br,
-                                  int64_t bc, uint8_t* q, float* s, cudaStream_t st) {
+                                  int64_t bc, uint8_t* q, float* s, cudaStream_t st,
+                                  bool pow2 = false) {
   const int64_t nb = cdiv(rows, br) * cdiv(cols, bc);
   if (nb == 0) return cudaSuccess;
   if (nb > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-  block_quant_generic_kernel<<<(unsigned)nb, 256, 0, st>>>(x, rows, cols, br, bc, q, s);
+  if (pow2)
+    block_quant_generic_kernel<true><<<(unsigned)nb, 256, 0, st>>>(x, rows, cols, br, bc, q, s);
+  else
+    block_quant_generic_kernel<false><<<(unsigned)nb, 256, 0, st>>>(x, rows, cols, br, bc, q, s);
   return cudaGetLastError();
 }
 
@@ -172,7 +177,7 @@ static cudaError_t launch_generic(const uint16_t* x, int64_t rows, int64_t cols,
 
 // With row_idx, output row r quantizes x row row_idx[r] (a zero row when the
 // index is outside [0, rows_x)); without it, row r quantizes row r.
-template <typename IdxT>
+template <typename IdxT, bool kPow2>
 __global__ void __launch_bounds__(256) act_quant_kernel(const uint16_t* __restrict__ x, IdxT m,
                                                         IdxT k, uint8_t* __restrict__ q,
                                                         float* __restrict__ s,
@@ -213,7 +218,7 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const uint16_t* __restri
       a = absmax_bf16x2(v[u].w, a);
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
-      const float S = scale_from_amax(a);
+      const float S = group_scale<kPow2>(a);
       const QuantScale qs = make_quant_scale(S);
       if (ok[u]) {
         uint2 c;
@@ -233,7 +238,7 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const uint16_t* __restri
 // spreads the per-group work -- two butterfly steps, S and the reciprocal --
 // over 32 values per lane; a warp covers 8 consecutive groups (2 KB) per
 // unit and U units are loaded before any is used.
-template <int U>
+template <int U, bool kPow2>
 __global__ void __launch_bounds__(256) act_quant_k128_kernel(const uint16_t* __restrict__ x,
                                                              int64_t G, uint8_t* __restrict__ q,
                                                              float* __restrict__ s) {
@@ -256,7 +261,7 @@ __global__ void __launch_bounds__(256) act_quant_k128_kernel(const uint16_t* __r
       float a = absmax_bf16x8_tree<4>(v[u]);
       a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
       a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
-      const float S = scale_from_amax(a);
+      const float S = group_scale<kPow2>(a);
       const QuantScale qs = make_quant_scale(S);
       if (g < G) {
 #pragma unroll
@@ -323,24 +328,31 @@ __global__ void __launch_bounds__(256) act_quant_gather_k128_kernel(
   }
 }
 
-cudaError_t launch_act_quant(const uint16_t* x, int64_t m, int64_t k, uint8_t* q, float* s,
-                             cudaStream_t st) {
+template <bool kPow2>
+static cudaError_t launch_act_quant_t(const uint16_t* x, int64_t m, int64_t k, uint8_t* q,
+                                      float* s, cudaStream_t st) {
   if (m == 0 || k == 0) return cudaSuccess;
-  if (k % 8 != 0) return launch_generic(x, m, k, 1, 128, q, s, st);
+  if (k % 8 != 0) return launch_generic(x, m, k, 1, 128, q, s, st, kPow2);
   const int64_t G = m * cdiv(k, 128);
   if (k % 128 == 0) {
     constexpr int U = 2;
     const unsigned grid = grid_for(G, 8 * 8 * U, 8);  // 8 warps x 8 groups x U per CTA pass
-    act_quant_k128_kernel<U><<<grid, 256, 0, st>>>(x, G, q, s);
+    act_quant_k128_kernel<U, kPow2><<<grid, 256, 0, st>>>(x, G, q, s);
     return cudaGetLastError();
   }
   const unsigned grid = grid_for(G, 8 * 8, 16);  // 8 warps x 8 groups per CTA iteration
   if (m * k < (int64_t)0x7FFFFFFF)
-    act_quant_kernel<uint32_t><<<grid, 256, 0, st>>>(x, (uint32_t)m, (uint32_t)k, q, s, nullptr,
-                                                     (uint32_t)m);
+    act_quant_kernel<uint32_t, kPow2><<<grid, 256, 0, st>>>(x, (uint32_t)m, (uint32_t)k, q, s,
+                                                            nullptr, (uint32_t)m);
   else
-    act_quant_kernel<int64_t><<<grid, 256, 0, st>>>(x, m, k, q, s, nullptr, m);
+    act_quant_kernel<int64_t, kPow2><<<grid, 256, 0, st>>>(x, m, k, q, s, nullptr, m);
   return cudaGetLastError();
+}
+
+cudaError_t launch_act_quant(const uint16_t* x, int64_t m, int64_t k, uint8_t* q, float* s,
+                             cudaStream_t st, bool pow2) {
+  return pow2 ? launch_act_quant_t<true>(x, m, k, q, s, st)
+              : launch_act_quant_t<false>(x, m, k, q, s, st);
 }
 
 cudaError_t launch_act_quant_gather(const uint16_t* x, int64_t rows_x, int64_t k,
@@ -357,7 +369,7 @@ cudaError_t launch_act_quant_gather(const uint16_t* x, int64_t rows_x, int64_t k
     return cudaGetLastError();
   }
   const unsigned grid = grid_for(G, 8 * 8, 16);
-  act_quant_kernel<int64_t><<<grid, 256, 0, st>>>(x, total_rows, k, q, s, row_idx, rows_x);
+  act_quant_kernel<int64_t, false><<<grid, 256, 0, st>>>(x, total_rows, k, q, s, row_idx, rows_x);
   return cudaGetLastError();
 }
 
@@ -432,7 +444,7 @@ __device__ __forceinline__ BlockRef locate_block(const WeightBatch<kMax>& b, int
   return r;
 }
 
-template <int kMax>
+template <int kMax, bool kPow2>
 __global__ void __launch_bounds__(WQ_THREADS, 2)
     weight_quant_kernel(const __grid_constant__ WeightBatch<kMax> b) {
   extern __shared__ __align__(1024) uint8_t wq_smem[];
@@ -523,7 +535,7 @@ __global__ void __launch_bounds__(WQ_THREADS, 2)
       break;
     a = fmaxf(fmaxf(fmaxf(rb[0], rb[1]), fmaxf(rb[2], rb[3])),
               fmaxf(fmaxf(rb[4], rb[5]), fmaxf(rb[6], rb[7])));
-    const float S = scale_from_amax(a);
+    const float S = group_scale<kPow2>(a);
     const QuantScale qs = make_quant_scale(S);
     const int64_t k = b.k[r.mat];
     uint8_t* dstq = b.wq[r.mat] + (r.bi * 128) * k + r.bj * 128 + ch * 8;
@@ -541,7 +553,7 @@ __global__ void __launch_bounds__(WQ_THREADS, 2)
   }
 }
 
-template <int kMax>
+template <int kMax, bool kPow2>
 static cudaError_t launch_weight_batch(const WeightJob* jobs, int count, cudaStream_t st) {
   WeightBatch<kMax> b;
   int64_t total = 0;
@@ -568,17 +580,19 @@ static cudaError_t launch_weight_batch(const WeightJob* jobs, int count, cudaStr
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(weight_quant_kernel<kMax>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(weight_quant_kernel<kMax, kPow2>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              WQ_SMEM);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = 1;
   }
   const unsigned grid = (unsigned)std::min<int64_t>(total, 2 * (int64_t)sm_count());
-  weight_quant_kernel<kMax><<<grid, WQ_THREADS, WQ_SMEM, st>>>(b);
+  weight_quant_kernel<kMax, kPow2><<<grid, WQ_THREADS, WQ_SMEM, st>>>(b);
   return cudaGetLastError();
 }
 
-cudaError_t launch_weight_quant(const WeightJob* jobs, int count, cudaStream_t st) {
+template <bool kPow2>
+static cudaError_t launch_weight_quant_t(const WeightJob* jobs, int count, cudaStream_t st) {
   constexpr int kBatch = 160;  // ~28 KB of kernel parameters (tensor maps included)
   WeightJob fast[kBatch];
   int nf = 0;
@@ -586,20 +600,25 @@ cudaError_t launch_weight_quant(const WeightJob* jobs, int count, cudaStream_t s
     const WeightJob& j = jobs[i];
     if (j.n == 0 || j.k == 0) continue;
     if (j.k % 8 != 0) {
-      cudaError_t e = launch_generic(j.w, j.n, j.k, 128, 128, j.wq, j.ws, st);
+      cudaError_t e = launch_generic(j.w, j.n, j.k, 128, 128, j.wq, j.ws, st, kPow2);
       if (e != cudaSuccess) return e;
       continue;
     }
     fast[nf++] = j;
     if (nf == kBatch) {
-      cudaError_t e = launch_weight_batch<kBatch>(fast, nf, st);
+      cudaError_t e = launch_weight_batch<kBatch, kPow2>(fast, nf, st);
       if (e != cudaSuccess) return e;
       nf = 0;
     }
   }
-  if (nf == 1) return launch_weight_batch<1>(fast, 1, st);
-  if (nf > 1) return launch_weight_batch<kBatch>(fast, nf, st);
+  if (nf == 1) return launch_weight_batch<1, kPow2>(fast, 1, st);
+  if (nf > 1) return launch_weight_batch<kBatch, kPow2>(fast, nf, st);
   return cudaSuccess;
+}
+
+cudaError_t launch_weight_quant(const WeightJob* jobs, int count, cudaStream_t st, bool pow2) {
+  return pow2 ? launch_weight_quant_t<true>(jobs, count, st)
+              : launch_weight_quant_t<false>(jobs, count, st);
 }
 
 // =====================================================================
