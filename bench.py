@@ -546,6 +546,30 @@ def measure_next_rows(W, wl, peaks, reps=3):
         "workload": "all 144 Qwen3-8B weight matrices, 128x128 blocks, 1 batched launch",
         "ms": round(sec * 1e3, 3), "gbs": round(nb / sec / 1e9, 1),
         "pct_roofline": round(100 * nb / sec / 1e9 / peaks["hbm_gbs"], 2), "bytes_per_sweep": nb}
+    # decode attention: one query token per sequence (32 query heads) over
+    # the step's FP8 KV cache [32, 8192, 8, 128], every token attended
+    kq, vq = wl.kv_q
+    B, S, Hkv, D = kq.shape
+    g = torch.Generator(device=kq.device)
+    g.manual_seed(90)
+    qa = torch.randint(0, 126, (B, 4 * Hkv, D), dtype=torch.uint8, device=kq.device, generator=g)
+    qsc = torch.full((1,), 0.01, dtype=torch.float32, device=kq.device)
+    lens = torch.full((B,), S, dtype=torch.int32, device=kq.device)
+    att = W.fp8_decode_attention(qa, qsc, kq, wl.kv_s[0], vq, wl.kv_s[1], lens)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(10):
+        W.fp8_decode_attention(qa, qsc, kq, wl.kv_s[0], vq, wl.kv_s[1], lens, out=att)
+    t1.record()
+    torch.cuda.synchronize()
+    sec = t0.elapsed_time(t1) * 1e-3 / 10
+    nb = 2 * kq.numel() + qa.numel() + 2 * att.numel() + 4 * B
+    out["fp8_decode_attention"] = {
+        "workload": "32 sequences x 8192 tokens, 32 query heads over 8 KV heads, head dim 128",
+        "us": round(sec * 1e6, 1), "gbs": round(nb / sec / 1e9, 1),
+        "pct_roofline": round(100 * nb / sec / 1e9 / peaks["hbm_gbs"], 2), "bytes_per_call": nb}
     W.quantize_weight_blockwise_batched(wl.w, wl.wout)
     for kind, nbytes in (("dequant", 3 * elems + 4 * blocks),
                          ("quant_error_report", 3 * elems + 4 * blocks + 24 * blocks)):

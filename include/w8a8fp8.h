@@ -230,6 +230,37 @@ w8a8_status quant_error_report(const uint16_t *x_bf16, const uint8_t *q,
                                w8a8_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * fp8_decode_attention -- attention of one new query token per sequence
+ * over the FP8 KV cache, with the per-tensor FP32 scales of [NeMo] Table 3
+ * (QKV activations and the stored KV cache) and [FP8-RL] section 4:
+ *
+ *   score_t = softmax_scale * sq * sk * sum_d dec(q[b,h,d]) dec(k[b,t,kh,d])
+ *   out[b,h,d] = BF16( sv * sum_{t < len_b} softmax_t(score) dec(v[b,t,kh,d]) )
+ *
+ * with kh = h / (num_q_heads / num_kv_heads) (grouped-query heads).
+ *   q        [batch, num_q_heads, head_dim] E4M3; q_scale one FP32 (device).
+ *   k_cache, v_cache [batch, max_seq, num_kv_heads, head_dim] E4M3, as
+ *            written by kv_amax_quantize; k_scale, v_scale one FP32 each.
+ *   seq_lens [batch] int32 (device), each in [0, max_seq]; an empty
+ *            sequence gives zeros.
+ *   out_bf16 [batch, num_q_heads, head_dim] (out).
+ * Accuracy: binary32 arithmetic with an online softmax; |out - exact| <=
+ * 1e-3 * sv * sum_t p_t |dec(v_t,d)| + half a BF16 ulp.
+ * Rules: head_dim == 128 and num_q_heads / num_kv_heads in {1, 2} or a
+ * multiple of 4 (else W8A8_ERR_UNSUPPORTED); q and the caches 16-byte
+ * aligned, the rest 4-byte aligned.  Each (sequence, KV head) slice of the
+ * cache is read once per 4 query heads.
+ * ---------------------------------------------------------------------- */
+w8a8_status fp8_decode_attention(const uint8_t *q, const float *q_scale,
+                                 const uint8_t *k_cache, const float *k_scale,
+                                 const uint8_t *v_cache, const float *v_scale,
+                                 const int32_t *seq_lens, int64_t batch,
+                                 int64_t max_seq, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t head_dim,
+                                 float softmax_scale, uint16_t *out_bf16,
+                                 w8a8_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * fp8_block_gemm -- the W8A8 linear of [FP8-RL] section 1 / arXiv abstract
  * item (i) with the [NeMo] Table 1 granularities:
  *

@@ -49,6 +49,9 @@ def lib():
             "oracle_dequant_value": (ctypes.c_float, [u8, ctypes.c_float]),
             "oracle_dequantize_blocks": (ctypes.c_int, [P, P, i64, i64, i64, i64, P]),
             "oracle_quant_error": (ctypes.c_int, [P, P, P, i64, i64, i64, i64, i64, i64, P]),
+            "oracle_decode_attention": (ctypes.c_int, [P, ctypes.c_float, P, ctypes.c_float, P,
+                                                        ctypes.c_float, P, i64, i64, i64, i64, i64,
+                                                        ctypes.c_double, P, P]),
             "oracle_bf16_from_f64": (u16, [ctypes.c_double]),
             "oracle_bf16_from_f64_array": (None, [P, i64, P]),
         }
@@ -258,6 +261,23 @@ def grouped_gemm(xq, xs, row_idx, group_offsets, wq, ws):
                                    _p(wq), _p(ws), n, k, _p(y), _p(a))
     assert rc == 0
     return y, a
+
+
+def decode_attention(q, sq, k, sk, v, sv, lens, softmax_scale):
+    """FP8 decode attention (NeMo blog Table 3, per-tensor Q/K/V scales):
+    q [B, Hq, D], k and v [B, S, Hkv, D] E4M3 codes, lens [B].  Returns
+    (out, absout) float64 [B, Hq, D]: the exact-math output and the bound
+    sv * sum_t p_t |dec(v_t)| used for its tolerance."""
+    q, k, v = _c(q, np.uint8), _c(k, np.uint8), _c(v, np.uint8)
+    lens = _c(lens, np.int32)
+    B, Hq, D = q.shape
+    S, Hkv = k.shape[1], k.shape[2]
+    out = np.empty((B, Hq, D), np.float64)
+    ab = np.empty((B, Hq, D), np.float64)
+    rc = lib().oracle_decode_attention(_p(q), float(sq), _p(k), float(sk), _p(v), float(sv), _p(lens),
+                                       B, S, Hq, Hkv, D, float(softmax_scale), _p(out), _p(ab))
+    assert rc == 0
+    return out, ab
 
 
 def bf16_from_f64(y):

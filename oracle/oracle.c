@@ -477,6 +477,69 @@ ORACLE_EXPORT int oracle_quant_error(const uint16_t *x, const uint8_t *q, const 
 }
 
 /* ------------------------------------------------------------------------ */
+/* Decode attention over the FP8 KV cache                                    */
+/* ------------------------------------------------------------------------ */
+
+/* [NeMo] Table 3 and the FP8 KV-cache section: Q, K and V carry one FP32
+ * scale each (per tensor); [FP8-RL] section 4: attention reads the FP8 KV
+ * cache.  One query token per sequence b and query head h, grouped-query
+ * attention (query head h reads KV head h / (hq / hkv)):
+ *   score_t = softmax_scale * sq * sk * sum_d dec(q[b,h,d]) dec(k[b,t,kh,d])
+ *   p_t     = exp(score_t - max) / sum_u exp(score_u - max),   t < len_b
+ *   out_d   = sv * sum_t p_t dec(v[b,t,kh,d])
+ * all in FP64; absout_d = sv * sum_t p_t |dec(v)| bounds the rounding.  An
+ * empty sequence gives out = 0. */
+ORACLE_EXPORT int oracle_decode_attention(const uint8_t *q, float sq, const uint8_t *k, float sk,
+                                          const uint8_t *v, float sv, const int32_t *lens,
+                                          int64_t batch, int64_t smax, int64_t hq, int64_t hkv,
+                                          int64_t d, double softmax_scale, double *out,
+                                          double *absout) {
+    int64_t b, h, t, i;
+    double dec[256];
+    if (batch < 0 || smax < 0 || hq <= 0 || hkv <= 0 || d <= 0 || hq % hkv) return -1;
+    for (i = 0; i < 256; ++i) dec[i] = oracle_e4m3_decode((uint8_t)i); /* the codec above, tabulated */
+    for (b = 0; b < batch; ++b) {
+        int64_t len = lens[b];
+        if (len < 0 || len > smax) return -2;
+        for (h = 0; h < hq; ++h) {
+            int64_t kh = h / (hq / hkv);
+            const uint8_t *qv = q + (b * hq + h) * d;
+            double *o = out + (b * hq + h) * d;
+            double *ao = absout + (b * hq + h) * d;
+            double mx = -HUGE_VAL, den = 0.0;
+            for (i = 0; i < d; ++i) o[i] = ao[i] = 0.0;
+            if (len == 0) continue;
+            for (t = 0; t < len; ++t) {
+                const uint8_t *kv = k + ((b * smax + t) * hkv + kh) * d;
+                double sc = 0.0;
+                for (i = 0; i < d; ++i) sc += dec[qv[i]] * dec[kv[i]];
+                sc *= softmax_scale * (double)sq * (double)sk;
+                if (sc > mx) mx = sc;
+            }
+            for (t = 0; t < len; ++t) {
+                const uint8_t *kv = k + ((b * smax + t) * hkv + kh) * d;
+                const uint8_t *vv = v + ((b * smax + t) * hkv + kh) * d;
+                double sc = 0.0, pt;
+                for (i = 0; i < d; ++i) sc += dec[qv[i]] * dec[kv[i]];
+                sc *= softmax_scale * (double)sq * (double)sk;
+                pt = exp(sc - mx);
+                den += pt;
+                for (i = 0; i < d; ++i) {
+                    double x = dec[vv[i]];
+                    o[i] += pt * x;
+                    ao[i] += pt * fabs(x);
+                }
+            }
+            for (i = 0; i < d; ++i) {
+                o[i] = o[i] / den * (double)sv;
+                ao[i] = ao[i] / den * fabs((double)sv);
+            }
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Output rounding                                                            */
 /* ------------------------------------------------------------------------ */
 

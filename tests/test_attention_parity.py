@@ -1,0 +1,92 @@
+"""GPU parity of the FP8 decode attention against the oracle's FP64
+attention: every output within 1e-3 * sv * sum_t p_t |dec(v_t)| plus half a
+BF16 ulp (the documented accuracy), and within a much tighter 2^-14 of the
+same sum, which binary32 accumulation reaches."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from parity_util import bf16_to_f64, bits16, ulp_bf16
+from w8a8_gemm_rl_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _codes(shape, g):
+    c = torch.randint(0, 256, shape, generator=g, dtype=torch.int32)
+    c[(c & 0x7F) == 0x7F] = 0x7E
+    return c.to(torch.uint8)
+
+
+def _check(out, ref, ab, rel):
+    got = bf16_to_f64(bits16(out)).reshape(ref.shape)
+    err = np.abs(got - ref)
+    bound = rel * ab + 0.5 * ulp_bf16(ref)
+    bad = err > bound
+    assert not bad.any(), (int(bad.sum()), float((err - bound).max()))
+
+
+CASES = [  # batch, max_seq, q heads, kv heads, lengths
+    (2, 300, 8, 2, [300, 123]), (3, 64, 4, 4, [1, 64, 0]), (2, 40, 4, 2, [40, 17]),
+    (1, 1000, 32, 8, [997]), (2, 96, 16, 2, [96, 95]), (4, 7, 8, 8, [7, 1, 2, 3])]
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv,lens", CASES)
+def test_decode_attention_matches_oracle(W, B, S, Hq, Hkv, lens):
+    g = torch.Generator().manual_seed(B * 1000 + S)
+    q, k, v = _codes((B, Hq, 128), g), _codes((B, S, Hkv, 128), g), _codes((B, S, Hkv, 128), g)
+    scales = torch.tensor([0.02, 0.03, 0.5], dtype=torch.float32)
+    ln = torch.tensor(lens, dtype=torch.int32)
+    dev = lambda t: t.cuda()
+    out = W.fp8_decode_attention(dev(q), dev(scales[0:1]), dev(k), dev(scales[1:2]), dev(v),
+                                 dev(scales[2:3]), dev(ln))
+    torch.cuda.synchronize()
+    ref, ab = O.decode_attention(q.numpy(), scales[0].item(), k.numpy(), scales[1].item(), v.numpy(),
+                                 scales[2].item(), ln.numpy(), 1 / math.sqrt(128))
+    _check(out, ref, ab, 1e-3)
+    _check(out, ref, ab, 2.0 ** -14)
+    for b, L in enumerate(lens):
+        if L == 0:
+            assert (bits16(out[b]) == 0).all()
+
+
+def test_decode_attention_over_the_quantized_kv_cache(W):
+    """The KV-cache layout of the recalibration step: K and V quantized by
+    kv_amax_quantize ([4, 512, 8, 128], gains per channel), a query
+    quantized per tensor, ragged lengths; 32 query heads over 8 KV heads."""
+    kc = synth.kv_cache(seed=11, shape=(4, 512, 8, 128), device="cuda")
+    vc = synth.kv_cache(seed=12, shape=(4, 512, 8, 128), device="cuda")
+    qx = synth.kv_cache(seed=13, shape=(4, 32, 1, 128), device="cuda").reshape(4, 32, 128)
+    kq, ks, _ = W.kv_amax_quantize(kc)
+    vq, vs, _ = W.kv_amax_quantize(vc)
+    qq, qs, _ = W.kv_amax_quantize(qx)
+    ln = torch.tensor([512, 300, 1, 77], dtype=torch.int32, device="cuda")
+    out = W.fp8_decode_attention(qq, qs, kq, ks, vq, vs, ln)
+    torch.cuda.synchronize()
+    ref, ab = O.decode_attention(qq.cpu().numpy(), qs.item(), kq.cpu().numpy(), ks.item(),
+                                 vq.cpu().numpy(), vs.item(), ln.cpu().numpy(), 1 / math.sqrt(128))
+    _check(out, ref, ab, 2.0 ** -14)
+
+
+def test_decode_attention_full_cache_sampled(W):
+    """The KV configuration itself ([32, 8192, 8, 128], 32 query heads):
+    every output of two sequences (one full, one of 4097 tokens) against the
+    oracle."""
+    g = torch.Generator().manual_seed(7)
+    B, S = 32, 8192
+    k = _codes((B, S, 8, 128), g).cuda()
+    v = _codes((B, S, 8, 128), g).cuda()
+    q = _codes((B, 32, 128), g).cuda()
+    sc = torch.tensor([0.01, 0.01, 0.25], dtype=torch.float32, device="cuda")
+    ln = torch.full((B,), S, dtype=torch.int32, device="cuda")
+    ln[5] = 4097
+    out = W.fp8_decode_attention(q, sc[0:1], k, sc[1:2], v, sc[2:3], ln)
+    torch.cuda.synchronize()
+    for b in (5, 31):
+        ref, ab = O.decode_attention(q[b:b + 1].cpu().numpy(), 0.01, k[b:b + 1].cpu().numpy(), 0.01,
+                                     v[b:b + 1].cpu().numpy(), 0.25, ln[b:b + 1].cpu().numpy(),
+                                     1 / math.sqrt(128))
+        _check(out[b:b + 1], ref, ab, 2.0 ** -14)

@@ -258,6 +258,65 @@ def test_routed_row_quant_is_quant_then_gather_with_zero_rows():
     assert (q2 != q[ok]).any()
 
 
+# ------------------------------------------------- decode attention (FP8 KV)
+
+def _attn_inputs(rng, B, S, Hq, Hkv, D=128):
+    def codes(shape):
+        c = rng.integers(0, 256, shape).astype(np.uint8)
+        c[(c & 0x7F) == 0x7F] = 0x7E
+        return c
+    return codes((B, Hq, D)), codes((B, S, Hkv, D)), codes((B, S, Hkv, D))
+
+
+def test_attention_closed_forms():
+    """One token: the output is that token's dequantized V.  A zero query:
+    uniform weights, so the output is the mean of the dequantized V rows.
+    No tokens: zeros.  Each query head reads KV head h / (Hq / Hkv)."""
+    rng = np.random.default_rng(30)
+    q, k, v = _attn_inputs(rng, 3, 20, 8, 2)
+    sv = 0.375
+    lens = np.array([1, 20, 0], np.int32)
+    out, _ = O.decode_attention(q, 0.01, k, 0.02, v, sv, lens, 1 / np.sqrt(128))
+    for h in range(8):
+        assert np.array_equal(out[0, h], sv * O.e4m3_decode(v[0, 0, h // 4]))
+    assert (out[2] == 0).all()
+    qz = np.zeros_like(q)
+    outz, _ = O.decode_attention(qz, 1.0, k, 1.0, v, sv, lens, 1.0)
+    for h in range(8):
+        want = sv * O.e4m3_decode(v[1, :20, h // 4]).mean(axis=0)
+        assert np.allclose(outz[1, h], want, rtol=1e-14, atol=1e-300)
+    # GQA: KV heads holding distinct constants show which one each query head read
+    vc = np.zeros_like(v)
+    vc[:, :, 0, :] = 0x38  # 1.0
+    vc[:, :, 1, :] = 0x40  # 2.0
+    outc, _ = O.decode_attention(q, 0.01, k, 0.02, vc, 1.0, lens, 1 / np.sqrt(128))
+    assert (outc[1, :4] == 1.0).all() and (outc[1, 4:] == 2.0).all()
+
+
+def test_attention_matches_library_softmax():
+    """Against torch: float64 softmax and einsum over the dequantized
+    tensors (library routines, written independently of the oracle)."""
+    rng = np.random.default_rng(31)
+    B, S, Hq, Hkv = 2, 37, 8, 2
+    q, k, v = _attn_inputs(rng, B, S, Hq, Hkv)
+    # the scales are binary32 values (as the library stores them)
+    sq, sk, sv = (float(np.float32(t)) for t in (0.02, 0.05, 0.5))
+    sc = 1 / np.sqrt(128)
+    lens = np.array([37, 23], np.int32)
+    out, ab = O.decode_attention(q, sq, k, sk, v, sv, lens, sc)
+    dq = torch.from_numpy(O.e4m3_decode(q)) * sq
+    dk = torch.from_numpy(O.e4m3_decode(k)) * sk
+    dv = torch.from_numpy(O.e4m3_decode(v)) * sv
+    for b in range(B):
+        L = int(lens[b])
+        kk = dk[b, :L].repeat_interleave(Hq // Hkv, dim=1)  # [L, Hq, D]
+        vv = dv[b, :L].repeat_interleave(Hq // Hkv, dim=1)
+        p = torch.softmax(torch.einsum("hd,thd->ht", dq[b], kk) * sc, dim=-1)
+        want = torch.einsum("ht,thd->hd", p, vv).numpy()
+        assert np.allclose(out[b], want, rtol=1e-12, atol=1e-12 * np.abs(want).max())
+        assert (ab[b] >= np.abs(out[b]) * (1 - 1e-12)).all()
+
+
 # ------------------------------------------------------ power-of-two scales
 
 def test_pow2_scale_hand_values_and_definition():

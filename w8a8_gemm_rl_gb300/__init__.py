@@ -9,6 +9,7 @@ and a missing library is an error.
 The C ABI and what each call computes are documented in include/w8a8fp8.h.
 """
 import ctypes
+import math
 import os
 
 import torch
@@ -17,7 +18,7 @@ __all__ = [
     "lib", "W8A8Error", "e4m3_encode_f32", "e4m3_decode_f32", "quantize_weight_blockwise",
     "quantize_weight_blockwise_batched", "quantize_act_per_token_group",
     "quantize_act_per_token_group_gather", "dequantize_blockwise", "quant_error_report",
-    "sqnr_db", "fp8_block_gemm",
+    "sqnr_db", "fp8_decode_attention", "fp8_block_gemm",
     "fp8_grouped_gemm", "kv_amax_quantize", "w8a8_linear", "consume_device_error",
     "KV_AMAX_AND_QUANT", "KV_AMAX_ONLY", "KV_QUANT_ONLY", "LIB_PATH",
 ]
@@ -57,6 +58,8 @@ _SIGNATURES = {
     "quantize_act_per_token_group_gather": (_INT, [_P, _I64, _I64, _P, _I64, _P, _P, _P]),
     "dequantize_blockwise": (_INT, [_P, _P, _I64, _I64, _I64, _I64, _P, _P]),
     "quant_error_report": (_INT, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, _P]),
+    "fp8_decode_attention": (_INT, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _I32,
+                                    ctypes.c_float, _P, _P]),
     "fp8_block_gemm": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "fp8_grouped_gemm": (_INT, [_P, _P, _I64, _P, _P, _I32, _I64, _P, _P, _P, _I64, _I64, _P]),
     "kv_amax_quantize": (_INT, [_P, _I64, _P, _P, _P, _INT, _P]),
@@ -217,6 +220,25 @@ def sqnr_db(stats):
     se = float(stats[..., 1].sum())
     sx = float(stats[..., 2].sum())
     return math.inf if se == 0.0 else 10.0 * math.log10(sx / se)
+
+
+def fp8_decode_attention(q, q_scale, k_cache, k_scale, v_cache, v_scale, seq_lens,
+                         softmax_scale=None, out=None, stream=None):
+    """q uint8 [B, Hq, 128]; k_cache, v_cache uint8 [B, S, Hkv, 128]; scales
+    float32 [1] (device); seq_lens int32 [B] -> BF16 [B, Hq, 128]."""
+    _need(q, torch.uint8, "q")
+    _need(k_cache, torch.uint8, "k_cache")
+    _need(v_cache, torch.uint8, "v_cache")
+    _need(seq_lens, torch.int32, "seq_lens")
+    B, Hq, D = q.shape
+    S, Hkv = k_cache.shape[1], k_cache.shape[2]
+    sc = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device) if out is None else out
+    _check("fp8_decode_attention",
+           lib().fp8_decode_attention(_ptr(q), _ptr(q_scale), _ptr(k_cache), _ptr(k_scale),
+                                      _ptr(v_cache), _ptr(v_scale), _ptr(seq_lens), B, S, Hq, Hkv,
+                                      D, sc, _ptr(out), _stream(stream)))
+    return out
 
 
 # ------------------------------------------------------------------ GEMMs

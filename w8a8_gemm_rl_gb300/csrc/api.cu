@@ -194,6 +194,34 @@ W8A8_API w8a8_status quant_error_report(const uint16_t* x_bf16, const uint8_t* q
                                             report_block_cols, stats, cs(stream)));
 }
 
+// --------------------------------------------------------------- attention
+
+W8A8_API w8a8_status fp8_decode_attention(const uint8_t* q, const float* q_scale,
+                                          const uint8_t* k_cache, const float* k_scale,
+                                          const uint8_t* v_cache, const float* v_scale,
+                                          const int32_t* seq_lens, int64_t batch,
+                                          int64_t max_seq, int32_t num_q_heads,
+                                          int32_t num_kv_heads, int32_t head_dim,
+                                          float softmax_scale, uint16_t* out_bf16,
+                                          w8a8_stream_t stream) {
+  if (batch < 0 || max_seq < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+    return W8A8_ERR_SHAPE;
+  if (num_q_heads % num_kv_heads != 0) return W8A8_ERR_SHAPE;
+  const int32_t g = num_q_heads / num_kv_heads;
+  if (head_dim != 128 || !(g == 1 || g == 2 || g % 4 == 0)) return W8A8_ERR_UNSUPPORTED;
+  if (max_seq >= kMaxDim || batch >= kMaxDim) return W8A8_ERR_SHAPE;
+  if (batch == 0) return W8A8_OK;
+  if (!q || !q_scale || !k_cache || !k_scale || !v_cache || !v_scale || !seq_lens || !out_bf16)
+    return W8A8_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out_bf16, 4) ||
+      !aligned(seq_lens, 4) || !aligned(q_scale, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4))
+    return W8A8_ERR_ALIGN;
+  return from_cuda(w8a8::launch_decode_attention(q, q_scale, k_cache, k_scale, v_cache, v_scale,
+                                                 seq_lens, batch, max_seq, num_q_heads,
+                                                 num_kv_heads, softmax_scale, out_bf16,
+                                                 cs(stream)));
+}
+
 // ------------------------------------------------------------------ GEMMs
 
 static w8a8_status check_gemm_common(const uint8_t* xq, const float* xs, const uint8_t* wq,

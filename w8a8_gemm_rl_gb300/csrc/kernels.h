@@ -44,6 +44,13 @@ cudaError_t launch_quant_error(const uint16_t* x, const uint8_t* q, const float*
                                int64_t cols, int64_t sbr, int64_t sbc, int64_t rbr, int64_t rbc,
                                double* stats, cudaStream_t st);
 
+// attention.cu: decode attention over the FP8 KV cache (head dim 128).
+cudaError_t launch_decode_attention(const uint8_t* q, const float* sq, const uint8_t* k,
+                                    const float* sk, const uint8_t* v, const float* sv,
+                                    const int32_t* lens, int64_t batch, int64_t smax, int hq,
+                                    int hkv, float softmax_scale, uint16_t* out,
+                                    cudaStream_t st);
+
 cudaError_t launch_block_gemm(const uint8_t* xq, const float* xs, const uint8_t* wq,
                               const float* ws, uint16_t* y, int64_t m, int64_t n, int64_t k,
                               cudaStream_t st);
