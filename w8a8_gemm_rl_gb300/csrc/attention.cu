@@ -28,6 +28,7 @@ namespace {
 constexpr int AT_D = 128;
 constexpr int AT_WARPS = 4;
 constexpr int AT_THREADS = 32 * AT_WARPS;
+constexpr int AT_U = 4;  // tokens per lane group in flight
 
 // 16 codes (one 16-byte vector) -> 16 binary32 values, exactly.
 __device__ __forceinline__ void decode16(const uint4& c, float (&f)[16]) {
@@ -110,44 +111,53 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
   const uint8_t* vbase = v + ((b * smax) * hkv + kh) * AT_D + 16 * l8;
   // Every lane runs the same number of iterations (the warp-wide shuffles
   // below need all 32 lanes); a lane group whose token is past the end
-  // loads nothing and skips the update.
-  for (int tb = t0; tb < t1; tb += 4) {
-    const int t = tb + grp;
-    const bool tok = t < t1;
-    const uint4 kc = tok ? ld_stream_v4(kbase + t * tstride) : make_uint4(0u, 0u, 0u, 0u);
-    const uint4 vc = tok ? ld_stream_v4(vbase + t * tstride) : make_uint4(0u, 0u, 0u, 0u);
-    float kf[16], vf[16];
-    decode16(kc, kf);
-    float s[GH];
+  // loads nothing and skips the update.  AT_U tokens per lane group are
+  // loaded before any is used, so that enough bytes are in flight.
+  for (int tb = t0; tb < t1; tb += 4 * AT_U) {
+    uint4 kc[AT_U], vc[AT_U];
 #pragma unroll
-    for (int h = 0; h < GH; ++h) {
-      float a = 0.0f, c = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 16; i += 2) {
-        a = __fmaf_rn(qf[h][i], kf[i], a);
-        c = __fmaf_rn(qf[h][i + 1], kf[i + 1], c);
-      }
-      s[h] = a + c;
+    for (int u = 0; u < AT_U; ++u) {
+      const int t = tb + grp + 4 * u;
+      const bool tok = t < t1;
+      kc[u] = tok ? ld_stream_v4(kbase + t * tstride) : make_uint4(0u, 0u, 0u, 0u);
+      vc[u] = tok ? ld_stream_v4(vbase + t * tstride) : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
-    for (int o = 1; o < 8; o <<= 1)
+    for (int u = 0; u < AT_U; ++u) {
+      const bool tok = tb + grp + 4 * u < t1;
+      float kf[16], vf[16];
+      decode16(kc[u], kf);
+      float s[GH];
 #pragma unroll
-      for (int h = 0; h < GH; ++h) s[h] += __shfl_xor_sync(0xFFFFFFFFu, s[h], o);
-    decode16(vc, vf);
+      for (int h = 0; h < GH; ++h) {
+        float a = 0.0f, c = 0.0f;
 #pragma unroll
-    for (int h = 0; h < GH; ++h) {
-      if (!tok) continue;
-      if (s[h] > m[h]) {  // a new running maximum: rescale what was summed so far
-        const float cr = exp2f(m[h] - s[h]);
-        l[h] *= cr;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) acc[h][i] *= cr;
-        m[h] = s[h];
+        for (int i = 0; i < 16; i += 2) {
+          a = __fmaf_rn(qf[h][i], kf[i], a);
+          c = __fmaf_rn(qf[h][i + 1], kf[i + 1], c);
+        }
+        s[h] = a + c;
       }
-      const float p = exp2f(s[h] - m[h]);
-      l[h] += p;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) acc[h][i] = __fmaf_rn(p, vf[i], acc[h][i]);
+      for (int o = 1; o < 8; o <<= 1)
+#pragma unroll
+        for (int h = 0; h < GH; ++h) s[h] += __shfl_xor_sync(0xFFFFFFFFu, s[h], o);
+      decode16(vc[u], vf);
+#pragma unroll
+      for (int h = 0; h < GH; ++h) {
+        if (!tok) continue;
+        if (s[h] > m[h]) {  // a new running maximum: rescale what was summed so far
+          const float cr = exp2f(m[h] - s[h]);
+          l[h] *= cr;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) acc[h][i] *= cr;
+          m[h] = s[h];
+        }
+        const float p = exp2f(s[h] - m[h]);
+        l[h] += p;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[h][i] = __fmaf_rn(p, vf[i], acc[h][i]);
+      }
     }
   }
 
