@@ -65,10 +65,13 @@ int w8a8_version(void);
  * (host, static storage; "" if none).  Diagnostic only. */
 const char *w8a8_last_cuda_error(void);
 
-/* Reads and clears the device-side error code the GEMM kernels set when a
- * bounded wait inside them gives up (0 = none; nonzero identifies the wait).
- * Such a kernel stops early and leaves its output incomplete.  Synchronous:
- * blocks until the device has finished prior work on the legacy stream. */
+/* Reads and clears the device-side error code that a kernel sets when a
+ * bounded wait inside it gives up (0 = none; nonzero identifies the wait:
+ * below 11 the GEMMs, 11..13 the weight quantizer, 21..22 the decode
+ * attention).  When several are set, the GEMMs' code is reported first,
+ * then the quantizer's, and all are cleared.  Such a kernel stops early
+ * and leaves its output incomplete.  Synchronous: blocks until the device
+ * has finished prior work on the legacy stream. */
 w8a8_status w8a8_consume_device_error(int *code);
 
 /* ------------------------------------------------------------------------
@@ -247,9 +250,11 @@ w8a8_status quant_error_report(const uint16_t *x_bf16, const uint8_t *q,
  * Accuracy: binary32 arithmetic with an online softmax; |out - exact| <=
  * 1e-3 * sv * sum_t p_t |dec(v_t,d)| + half a BF16 ulp.
  * Rules: head_dim == 128 and num_q_heads / num_kv_heads in {1, 2} or a
- * multiple of 4 (else W8A8_ERR_UNSUPPORTED); q and the caches 16-byte
- * aligned, the rest 4-byte aligned.  Each (sequence, KV head) slice of the
- * cache is read once per 4 query heads.
+ * multiple of 4 (else W8A8_ERR_UNSUPPORTED); batch * max_seq below
+ * 2^31 - 16 (TMA row coordinates; else W8A8_ERR_UNSUPPORTED); q and the
+ * caches 16-byte aligned, the rest 4-byte aligned.  Each (sequence, KV
+ * head) slice of the cache is read once per 4 query heads, through TMA
+ * tile loads of 16 tokens.
  * ---------------------------------------------------------------------- */
 w8a8_status fp8_decode_attention(const uint8_t *q, const float *q_scale,
                                  const uint8_t *k_cache, const float *k_scale,

@@ -12,6 +12,7 @@
 namespace w8a8 {
 cudaError_t consume_device_error(int* code);
 cudaError_t consume_quant_error(int* code);
+cudaError_t consume_attention_error(int* code);
 int grouped_gemm_max_groups();
 }  // namespace w8a8
 
@@ -211,6 +212,7 @@ W8A8_API w8a8_status fp8_decode_attention(const uint8_t* q, const float* q_scale
   if (head_dim != 128 || !(g == 1 || g == 2 || g % 4 == 0)) return W8A8_ERR_UNSUPPORTED;
   if (max_seq >= kMaxDim || batch >= kMaxDim) return W8A8_ERR_SHAPE;
   if (batch == 0) return W8A8_OK;
+  if (batch * max_seq > kMaxDim - 1 - 16) return W8A8_ERR_UNSUPPORTED;
   if (!q || !q_scale || !k_cache || !k_scale || !v_cache || !v_scale || !seq_lens || !out_bf16)
     return W8A8_ERR_NULL;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out_bf16, 4) ||
@@ -288,10 +290,12 @@ W8A8_API w8a8_status kv_amax_quantize(const uint16_t* x_bf16, int64_t numel, uin
 
 W8A8_API w8a8_status w8a8_consume_device_error(int* code) {
   if (!code) return W8A8_ERR_NULL;
-  int g = 0, q = 0;
+  int g = 0, q = 0, a = 0;
   w8a8_status st = from_cuda(w8a8::consume_device_error(&g));
   if (st != W8A8_OK) return st;
   st = from_cuda(w8a8::consume_quant_error(&q));
-  *code = g != 0 ? g : q;
+  if (st != W8A8_OK) return st;
+  st = from_cuda(w8a8::consume_attention_error(&a));
+  *code = g != 0 ? g : (q != 0 ? q : a);
   return st;
 }
