@@ -61,6 +61,7 @@ constexpr int AT_TILE = AT_CHUNK * AT_D;           // bytes of K (or of V) per c
 constexpr int AT_STAGE = 2 * AT_TILE;              // K tile, then V tile
 constexpr int AT_RING = AT_STAGES * AT_STAGE;      // per warp
 constexpr int AT_BAR_OFF = AT_WARPS * AT_RING;     // mbarriers after the rings
+constexpr int AT_SPLIT = 4;                        // CTAs (one cluster) per slice
 constexpr int AT_DYN_SMEM = AT_BAR_OFF + AT_WARPS * AT_STAGES * 8;
 constexpr uint64_t AT_WAIT_LIMIT_NS = 2000000000ull;
 static_assert(AT_TILE % 128 == 0 && AT_STAGE % 128 == 0, "TMA destinations stay 128-byte aligned");
@@ -81,6 +82,21 @@ __device__ __forceinline__ uint16_t bf16_rn(float x) {
   return r;
 }
 
+// Thread-block cluster helpers: a full cluster barrier (release / acquire,
+// so shared-memory writes before it are visible to every CTA after it) and
+// a load from the shared memory of another CTA of the cluster.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+__device__ __forceinline__ float ld_cluster_f32(const float* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(ptx::smem_addr(p)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r) : "memory");
+  return v;
+}
+
 // Factors that bring two online-softmax states (running maxima m, m2 in
 // log2 units; -inf for an empty state) to their common maximum.
 __device__ __forceinline__ float2 merge_factors(float m, float m2, float& mt) {
@@ -91,7 +107,7 @@ __device__ __forceinline__ float2 merge_factors(float m, float m2, float& mt) {
 }  // namespace
 
 template <int GH>
-__global__ void __launch_bounds__(AT_THREADS, 2)
+__global__ void __cluster_dims__(AT_SPLIT, 1, 1) __launch_bounds__(AT_THREADS, 2)
     decode_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v,
                             const uint8_t* __restrict__ q, const float* __restrict__ sq_p,
@@ -101,18 +117,26 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
   extern __shared__ __align__(1024) uint8_t at_smem[];
   __shared__ float s_acc[AT_WARPS][GH][AT_D];
   __shared__ float s_ml[AT_WARPS][GH][2];
+  __shared__ float s_ca[GH][AT_D];  // this CTA's merged state, read by the cluster
+  __shared__ float s_cm[GH][2];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = lane >> 3, l8 = lane & 7;
-  const int hg = blockIdx.x % hgroups;
-  const int64_t bk = blockIdx.x / hgroups;
+  const int rank = blockIdx.x % AT_SPLIT;  // rank in the cluster (clusters run along x)
+  const int unit = blockIdx.x / AT_SPLIT;
+  const int hg = unit % hgroups;
+  const int64_t bk = unit / hgroups;
   const int kh = (int)(bk % hkv);
   const int64_t b = bk / hkv;
   const int h0 = kh * (hq / hkv) + hg * GH;  // first query head of this CTA
   // lengths are device data the host cannot check: clamp to [0, smax]
   const int len = (int)min((int64_t)max(lens[b], 0), smax);
 
-  const int per = (len + AT_WARPS - 1) / AT_WARPS;
-  const int t0 = min(len, warp * per), t1 = min(len, t0 + per);
+  // the cluster's CTAs split the tokens into AT_SPLIT contiguous parts,
+  // and each CTA's warps split its part into AT_WARPS
+  const int pc = (len + AT_SPLIT - 1) / AT_SPLIT;
+  const int c_lo = min(len, rank * pc), c_hi = min(len, c_lo + pc);
+  const int per = (c_hi - c_lo + AT_WARPS - 1) / AT_WARPS;
+  const int t0 = min(c_hi, c_lo + warp * per), t1 = min(c_hi, t0 + per);
   const int nch = (t1 - t0 + AT_CHUNK - 1) / AT_CHUNK;
   const uint32_t ring = ptx::smem_addr(at_smem) + warp * AT_RING;
   const uint32_t bar0 = ptx::smem_addr(at_smem) + AT_BAR_OFF + warp * AT_STAGES * 8;
@@ -274,8 +298,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
     }
   }
   __syncthreads();
-  // merge the warps in a fixed order; thread d writes dim d of every head
-  const float sv = sv_p[0];
+  // merge the warps in a fixed order: thread d holds dim d of every head
   const int d = threadIdx.x;
 #pragma unroll
   for (int h = 0; h < GH; ++h) {
@@ -288,9 +311,29 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
       aa = aa * f.x + s_acc[w][h][d] * f.y;
       mm = mt;
     }
+    s_ca[h][d] = aa;
+    if (d == 0) {
+      s_cm[h][0] = mm;
+      s_cm[h][1] = ll;
+    }
+  }
+  // then the cluster's CTAs in rank order: CTA r finishes heads r, r + AT_SPLIT, ...
+  cluster_sync_all();
+  const float sv = sv_p[0];
+  for (int h = rank; h < GH; h += AT_SPLIT) {
+    float mm = -INFINITY, ll = 0.0f, aa = 0.0f;
+#pragma unroll
+    for (int r = 0; r < AT_SPLIT; ++r) {
+      float mt;
+      const float2 f = merge_factors(mm, ld_cluster_f32(&s_cm[h][0], r), mt);
+      ll = ll * f.x + ld_cluster_f32(&s_cm[h][1], r) * f.y;
+      aa = aa * f.x + ld_cluster_f32(&s_ca[h][d], r) * f.y;
+      mm = mt;
+    }
     const float y = ll > 0.0f ? aa / ll * sv : 0.0f;
     out[((b * hq) + h0 + h) * AT_D + d] = bf16_rn(y);
   }
+  cluster_sync_all();  // no CTA leaves while another may still read its shared memory
 }
 
 template <int GH>
@@ -323,7 +366,7 @@ cudaError_t launch_decode_attention(const uint8_t* q, const float* sq, const uin
   const int g = hq / hkv;
   const int gh = g >= 4 ? 4 : g;
   const int hgroups = g / gh;
-  const int64_t grid = batch * hkv * hgroups;
+  const int64_t grid = batch * hkv * hgroups * AT_SPLIT;
   // TMA row coordinates are 32-bit: the last chunk may start AT_CHUNK rows
   // before batch * smax and run past it (those rows read as zero)
   if (grid > 0x7FFFFFFFLL || batch * smax > 0x7FFFFFFFLL - AT_CHUNK) return cudaErrorInvalidValue;
