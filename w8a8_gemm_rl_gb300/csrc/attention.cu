@@ -6,22 +6,31 @@
 //   out_d   = sv * sum_{t < len_b} softmax(score)_t * dec(v[b,t,kh,d])
 //
 // one query token per sequence, grouped-query heads (query head h reads KV
-// head h / (hq / hkv)), head dim 128.  Each CTA reads one (sequence, KV
-// head) slice of K and V exactly once for up to 4 query heads, so the
-// kernel streams the cache: it is HBM-bound, and runs on the CUDA cores.
+// head h / (hq / hkv)), head dim 128.  A cluster of AT_SPLIT CTAs reads one
+// (sequence, KV head) slice of K and V exactly once for up to 8 query
+// heads, so the kernel streams the cache and is HBM-bound.
 //
-// Layout inside a CTA (4 warps): warp w takes a contiguous quarter of the
-// tokens and streams it through its own ring of shared-memory stages, each
-// filled by two TMA tile loads (16 tokens of K, 16 of V: the 128-byte rows
-// of one KV head sit hkv * 128 bytes apart in the cache, a 2-D box of
-// 16 rows x 128 bytes).  Lane 0 keeps AT_STAGES - 1 chunks in flight while
-// the warp computes on the oldest.  In a warp, lane group g (lanes
-// 8g..8g+7) takes every 4th token of a chunk and lane l8 = lane % 8 holds
-// dims 16 l8 .. 16 l8 + 15.  Scores are in log2 units (log2 e and every
-// scale folded into the query), kept by an online softmax per lane group;
-// the groups, then the warps, are merged at the end.  Binary32 arithmetic
-// throughout; dot products and the value update use packed two-lane FMAs
-// (even and odd dims in the two halves).
+// Each CTA takes a contiguous part of the slice's tokens and each of its 4
+// warps a contiguous quarter of that, streamed through the warp's own ring
+// of shared-memory stages: two TMA tile loads per chunk of 16 tokens (the
+// 128-byte rows of one KV head sit hkv * 128 bytes apart in the cache, a
+// 2-D box of 16 rows x 128 bytes, stored with the 128-byte swizzle so that
+// the 8-row matrix loads below hit distinct banks).  Lane 0 keeps
+// AT_STAGES - 1 chunks in flight while the warp computes on the oldest.
+//
+// Both contractions of a chunk run on the tensor cores (mma.sync
+// m16n8k16, f16 operands, f32 accumulation), with the query heads as the
+// rows (8 of the 16 rows used):
+//   S[h, t] = sum_d q[h, d] k[t, d]: K fragments come from the raw E4M3
+//     tile by ldmatrix and are widened to f16 (exact: every E4M3 value is
+//     an f16 value), the products are exact;
+//   O[h, d] += P[h, t] v[t, d]: the accumulator of S is already laid out as
+//     the A operand P, V fragments come from ldmatrix.trans on the raw tile
+//     plus a byte permute, and P = 2^15 p is split into two f16 parts
+//     (hi + lo carries 22 bits of it), so the weights lose nothing that
+//     binary32 would keep.
+// The softmax is online, in log2 units, one step per chunk per head.  The
+// warps' states, then the cluster's CTAs' states, are merged at the end.
 #include <math.h>
 
 #include <cuda.h>
@@ -54,26 +63,62 @@ namespace {
 constexpr int AT_D = 128;
 constexpr int AT_WARPS = 4;
 constexpr int AT_THREADS = 32 * AT_WARPS;
-constexpr int AT_U = 4;                            // tokens per lane group per chunk
-constexpr int AT_CHUNK = 4 * AT_U;                 // tokens per chunk (4 lane groups)
+constexpr int AT_CHUNK = 16;                       // tokens per chunk: one k16 step of O += P V
 constexpr int AT_STAGES = 4;                       // ring depth per warp
 constexpr int AT_TILE = AT_CHUNK * AT_D;           // bytes of K (or of V) per chunk
 constexpr int AT_STAGE = 2 * AT_TILE;              // K tile, then V tile
 constexpr int AT_RING = AT_STAGES * AT_STAGE;      // per warp
 constexpr int AT_BAR_OFF = AT_WARPS * AT_RING;     // mbarriers after the rings
 constexpr int AT_SPLIT = 4;                        // CTAs (one cluster) per slice
-constexpr int AT_DYN_SMEM = AT_BAR_OFF + AT_WARPS * AT_STAGES * 8;
+// + 1024: the rings start at the first 1024-byte boundary of the dynamic
+// shared memory (which follows the kernel's static shared arrays)
+constexpr int AT_DYN_SMEM = AT_BAR_OFF + AT_WARPS * AT_STAGES * 8 + 1024;
 constexpr uint64_t AT_WAIT_LIMIT_NS = 2000000000ull;
-static_assert(AT_TILE % 128 == 0 && AT_STAGE % 128 == 0, "TMA destinations stay 128-byte aligned");
+constexpr float AT_P_LOG2 = 15.0f;                 // weights are formed as 2^15 p <= 2^15
+static_assert(AT_TILE % 1024 == 0 && AT_RING % 1024 == 0,
+              "128-byte-swizzled tiles start on 1024-byte boundaries");
 
-// 16 codes (one 16-byte vector) -> 8 pairs (even dim, odd dim), exactly.
-__device__ __forceinline__ void decode16(const uint4& c, float2 (&f)[8]) {
-  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i + 0] = e4m3x2_to_float2((uint16_t)(w[i] & 0xFFFFu));
-    f[2 * i + 1] = e4m3x2_to_float2((uint16_t)(w[i] >> 16));
-  }
+// two E4M3 codes (low byte first) -> f16x2, exactly
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t c16) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)c16));
+  return h2;
+}
+// (lo, hi) -> f16x2 with lo in the low half, round to nearest even
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t h2) {
+  float lo, hi;
+  asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h2));
+  return make_float2(lo, hi);
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+// (d0, d1) += A B on one m16n8k16 tile (f16 in, f32 accumulate) whose A
+// rows 8..15 are zero: a0 / a2 are the row-g fragments, the results of the
+// zero rows are dropped.
+__device__ __forceinline__ void mma_rows8(float& d0, float& d1, uint32_t a0, uint32_t a2,
+                                          uint32_t b0, uint32_t b1) {
+  asm("{\n\t.reg .f32 z2, z3;\n\t"  // results of the zero rows, dropped
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, z2, z3}, {%2, %3, %4, %3}, "
+      "{%5, %6}, {%0, %1, %7, %7};\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "r"(a0), "r"(0u), "r"(a2), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
 __device__ __forceinline__ uint16_t bf16_rn(float x) {
@@ -114,13 +159,13 @@ __global__ void __cluster_dims__(AT_SPLIT, 1, 1) __launch_bounds__(AT_THREADS, 2
                             const float* __restrict__ sk_p, const float* __restrict__ sv_p,
                             const int32_t* __restrict__ lens, int64_t smax, int hq, int hkv,
                             int hgroups, float softmax_scale, uint16_t* __restrict__ out) {
-  extern __shared__ __align__(1024) uint8_t at_smem[];
+  extern __shared__ __align__(16) uint8_t at_smem[];
   __shared__ float s_acc[AT_WARPS][GH][AT_D];
   __shared__ float s_ml[AT_WARPS][GH][2];
   __shared__ float s_ca[GH][AT_D];  // this CTA's merged state, read by the cluster
   __shared__ float s_cm[GH][2];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int grp = lane >> 3, l8 = lane & 7;
+  const int g = lane >> 2, tig = lane & 3;  // fragment row (query head) and column pair
   const int rank = blockIdx.x % AT_SPLIT;  // rank in the cluster (clusters run along x)
   const int unit = blockIdx.x / AT_SPLIT;
   const int hg = unit % hgroups;
@@ -138,8 +183,9 @@ __global__ void __cluster_dims__(AT_SPLIT, 1, 1) __launch_bounds__(AT_THREADS, 2
   const int per = (c_hi - c_lo + AT_WARPS - 1) / AT_WARPS;
   const int t0 = min(c_hi, c_lo + warp * per), t1 = min(c_hi, t0 + per);
   const int nch = (t1 - t0 + AT_CHUNK - 1) / AT_CHUNK;
-  const uint32_t ring = ptx::smem_addr(at_smem) + warp * AT_RING;
-  const uint32_t bar0 = ptx::smem_addr(at_smem) + AT_BAR_OFF + warp * AT_STAGES * 8;
+  const uint32_t base = (ptx::smem_addr(at_smem) + 1023u) & ~1023u;  // swizzle atoms: 1024-aligned
+  const uint32_t ring = base + warp * AT_RING;
+  const uint32_t bar0 = base + AT_BAR_OFF + warp * AT_STAGES * 8;
   // cache row of token t of this sequence is b * smax + t (fits: checked on the host)
   const int row0 = (int)(b * smax) + t0;
   const int x0 = kh * AT_D;  // byte column of this KV head: a multiple of 128
@@ -158,29 +204,36 @@ __global__ void __cluster_dims__(AT_SPLIT, 1, 1) __launch_bounds__(AT_THREADS, 2
     for (int c = 0; c < AT_STAGES && c < nch; ++c) issue(c);
   }
 
-  // query slice, all factors folded in: scores come out in log2 units
+  // Q as the A operand of S = Q K^T, row g = query head h0 + g (zero past
+  // GH).  The 16 dims of segment s map to the k slots as 2 tig + {0, 1} <->
+  // 16 s + 4 tig + {0, 1} and 2 tig + 8 + {0, 1} <-> 16 s + 4 tig + {2, 3},
+  // the order in which ldmatrix hands out the K bytes below.
+  uint32_t qa[8][2];
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const uint32_t w =
+        g < GH ? *reinterpret_cast<const uint32_t*>(q + ((b * hq) + h0 + g) * AT_D + 16 * s + 4 * tig)
+               : 0u;
+    qa[s][0] = e4m3x2_f16x2(w & 0xFFFFu);
+    qa[s][1] = e4m3x2_f16x2(w >> 16);
+  }
   const float qk = softmax_scale * sq_p[0] * sk_p[0] * 1.4426950408889634f;
-  float2 qf[GH][8];
+  // online-softmax state of head g (the 4 lanes of a row agree on m; each
+  // sums its own tokens into l), and O[g, d] for d = 16 s + 4 tig + e + 2 i
+  float m = -INFINITY, l = 0.0f;
+  float acc[8][2][2];
 #pragma unroll
-  for (int h = 0; h < GH; ++h) {
-    const uint4 c = *reinterpret_cast<const uint4*>(q + ((b * hq) + h0 + h) * AT_D + 16 * l8);
-    decode16(c, qf[h]);
+  for (int s = 0; s < 8; ++s)
 #pragma unroll
-    for (int i = 0; i < 8; ++i) qf[h][i] = __fmul2_rn(qf[h][i], make_float2(qk, qk));
-  }
-  float m[GH], l[GH];
-  float2 acc[GH][8];
-#pragma unroll
-  for (int h = 0; h < GH; ++h) {
-    m[h] = -INFINITY;
-    l[h] = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[h][i] = make_float2(0.0f, 0.0f);
-  }
+    for (int e = 0; e < 2; ++e) acc[s][e][0] = acc[s][e][1] = 0.0f;
   __syncwarp();  // the barriers are initialised before any lane polls them
 
-  // Every lane runs the same chunks (the warp-wide shuffles below need all
-  // 32 lanes); a lane group whose token is past the end skips the update.
+  // ldmatrix row address of this lane inside a tile: matrix lane / 8 holds
+  // tokens 8 ((lane / 8) & 1) + 0..7 of segment pair base + lane / 16; the
+  // 128-byte swizzle stores 16-byte chunk c of row r at chunk c ^ (r & 7)
+  const int mrow = (lane & 7) + ((lane >> 3) & 1) * 8;
+  const int mseg = lane >> 4;
+
   int c = 0;
   bool ok = true;
   for (; c < nch; ++c) {
@@ -190,61 +243,81 @@ __global__ void __cluster_dims__(AT_SPLIT, 1, 1) __launch_bounds__(AT_THREADS, 2
       ok = false;
       break;
     }
-    const uint32_t st = ring + s * AT_STAGE;
+    const uint32_t tk = ring + s * AT_STAGE, tv = tk + AT_TILE;
     const int tc = t0 + c * AT_CHUNK;
-    // the scores of the lane group's AT_U tokens for every head: independent
-    // chains, reduced over the 8 lanes of the group together
-    float sc[AT_U][GH];
+
+    // S for the chunk: n tile j holds tokens 8 j + 0..7; this lane gets
+    // head g, tokens 8 j + 2 tig + {0, 1}
+    float sc[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
 #pragma unroll
-    for (int u = 0; u < AT_U; ++u) {
-      float2 kf[8];
-      decode16(ptx::lds128(st + (grp + 4 * u) * AT_D + 16 * l8), kf);
+    for (int sp = 0; sp < 8; sp += 2) {
+      uint32_t r[4];  // tokens 0-7 / 8-15 of segment sp, then of segment sp + 1
+      ldsm_x4(tk + mrow * AT_D + (((sp + mseg) ^ (mrow & 7)) << 4), r);
 #pragma unroll
-      for (int h = 0; h < GH; ++h) {
-        float2 a = make_float2(0.0f, 0.0f);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) a = __ffma2_rn(qf[h][i], kf[i], a);
-        sc[u][h] = a.x + a.y;
+      for (int jj = 0; jj < 4; ++jj) {
+        const int j = jj & 1, seg = sp + (jj >> 1);
+        mma_rows8(sc[j][0], sc[j][1], qa[seg][0], qa[seg][1], e4m3x2_f16x2(r[jj] & 0xFFFFu),
+                  e4m3x2_f16x2(r[jj] >> 16));
       }
     }
+    // one online-softmax step over the chunk: scores in log2 units, tokens
+    // past the end weigh nothing; the maximum covers the chunk's first
+    // token, so it is finite
+    float mx = m;
 #pragma unroll
-    for (int o = 1; o < 8; o <<= 1)
+    for (int j = 0; j < 2; ++j)
 #pragma unroll
-      for (int u = 0; u < AT_U; ++u)
-#pragma unroll
-        for (int h = 0; h < GH; ++h) sc[u][h] += __shfl_xor_sync(0xFFFFFFFFu, sc[u][h], o);
-    // one online-softmax step per head over the chunk's tokens: the running
-    // maximum moves to the chunk's maximum (a factor of exactly 1 when it
-    // does not move), then each valid token adds its weight
-    float pw[AT_U][GH];
-#pragma unroll
-    for (int h = 0; h < GH; ++h) {
-      float mx = m[h];
-#pragma unroll
-      for (int u = 0; u < AT_U; ++u)
-        if (tc + grp + 4 * u < t1) mx = fmaxf(mx, sc[u][h]);
-      const float ms = mx == -INFINITY ? 0.0f : mx;  // no token yet: nothing to weigh
-      const float cr = exp2f(m[h] - ms);
-      float ps = 0.0f;
-#pragma unroll
-      for (int u = 0; u < AT_U; ++u) {
-        pw[u][h] = tc + grp + 4 * u < t1 ? exp2f(sc[u][h] - ms) : 0.0f;
-        ps += pw[u][h];
+      for (int e = 0; e < 2; ++e) {
+        const float x = tc + 8 * j + 2 * tig + e < t1 ? sc[j][e] * qk : -INFINITY;
+        sc[j][e] = x;
+        mx = fmaxf(mx, x);
       }
-      l[h] = __fmaf_rn(l[h], cr, ps);
+    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+    const float cr = exp2f(m - mx);  // 0 for the first step, exactly 1 if the maximum holds
+    float pp[2][2], ps = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[h][i] = __fmul2_rn(acc[h][i], make_float2(cr, cr));
-      m[h] = mx;
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        pp[j][e] = exp2f(sc[j][e] - mx + AT_P_LOG2);
+        ps += pp[j][e];
+      }
+    l = __fmaf_rn(l, cr, ps);
+    m = mx;
+    if (__any_sync(0xFFFFFFFFu, cr != 1.0f)) {
+#pragma unroll
+      for (int s2 = 0; s2 < 8; ++s2)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          acc[s2][e][0] *= cr;
+          acc[s2][e][1] *= cr;
+        }
     }
+    // P in the A layout of O += P V (k slots = the chunk's tokens, where the
+    // S tile left them), as hi + lo f16 parts
+    const uint32_t ph0 = pack_f16x2(pp[0][0], pp[0][1]), ph1 = pack_f16x2(pp[1][0], pp[1][1]);
+    const float2 f0 = unpack_f16x2(ph0), f1 = unpack_f16x2(ph1);
+    const uint32_t pl0 = pack_f16x2(pp[0][0] - f0.x, pp[0][1] - f0.y);
+    const uint32_t pl1 = pack_f16x2(pp[1][0] - f1.x, pp[1][1] - f1.y);
 #pragma unroll
-    for (int u = 0; u < AT_U; ++u) {
-      float2 vf[8];
-      decode16(ptx::lds128(st + AT_TILE + (grp + 4 * u) * AT_D + 16 * l8), vf);
+    for (int sp = 0; sp < 8; sp += 2) {
+      uint32_t r[4];  // transposed: tokens 2 tig + {0, 1} (+ 8) of dims 2 g, 2 g + 1 of a segment
+      ldsm_x4_trans(tv + mrow * AT_D + (((sp + mseg) ^ (mrow & 7)) << 4), r);
 #pragma unroll
-      for (int h = 0; h < GH; ++h)
+      for (int hs = 0; hs < 2; ++hs) {
+        const int seg = sp + hs;
+        // bytes (t, 2g) (t, 2g+1) (t+1, 2g) (t+1, 2g+1) -> (t, 2g) (t+1, 2g) | (t, 2g+1) (t+1, 2g+1)
+        const uint32_t x0v = __byte_perm(r[2 * hs], 0u, 0x3120u);
+        const uint32_t x1v = __byte_perm(r[2 * hs + 1], 0u, 0x3120u);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          acc[h][i] = __ffma2_rn(make_float2(pw[u][h], pw[u][h]), vf[i], acc[h][i]);
+        for (int e = 0; e < 2; ++e) {  // n tile of dims 16 seg + 2 n + e
+          const uint32_t b0 = e4m3x2_f16x2(e ? x0v >> 16 : x0v & 0xFFFFu);
+          const uint32_t b1 = e4m3x2_f16x2(e ? x1v >> 16 : x1v & 0xFFFFu);
+          mma_rows8(acc[seg][e][0], acc[seg][e][1], ph0, ph1, b0, b1);
+          mma_rows8(acc[seg][e][0], acc[seg][e][1], pl0, pl1, b0, b1);
+        }
+      }
     }
     // every lane has used this stage: lane 0 refills it with chunk c + AT_STAGES
     __syncwarp();
@@ -263,38 +336,20 @@ __global__ void __cluster_dims__(AT_SPLIT, 1, 1) __launch_bounds__(AT_THREADS, 2
         atomicCAS(&g_w8a8_attn_error, 0, 22);
   }
 
-  // merge the 4 lane groups of the warp (lanes with equal l8 hold equal dims)
+  // the warp's state: l summed over the 4 lanes of each row
+  l += __shfl_xor_sync(0xFFFFFFFFu, l, 1);
+  l += __shfl_xor_sync(0xFFFFFFFFu, l, 2);
+  if (g < GH) {
 #pragma unroll
-  for (int o = 8; o < 32; o <<= 1) {
+    for (int s2 = 0; s2 < 8; ++s2)
 #pragma unroll
-    for (int h = 0; h < GH; ++h) {
-      const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m[h], o);
-      const float l2 = __shfl_xor_sync(0xFFFFFFFFu, l[h], o);
-      float mt;
-      const float2 f = merge_factors(m[h], m2, mt);
-      l[h] = l[h] * f.x + l2 * f.y;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float ax = __shfl_xor_sync(0xFFFFFFFFu, acc[h][i].x, o);
-        const float ay = __shfl_xor_sync(0xFFFFFFFFu, acc[h][i].y, o);
-        acc[h][i].x = acc[h][i].x * f.x + ax * f.y;
-        acc[h][i].y = acc[h][i].y * f.x + ay * f.y;
+      for (int e = 0; e < 2; ++e) {
+        s_acc[warp][g][16 * s2 + 4 * tig + e] = acc[s2][e][0];
+        s_acc[warp][g][16 * s2 + 4 * tig + e + 2] = acc[s2][e][1];
       }
-      m[h] = mt;
-    }
-  }
-  if (grp == 0) {
-#pragma unroll
-    for (int h = 0; h < GH; ++h) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        s_acc[warp][h][16 * l8 + 2 * i] = acc[h][i].x;
-        s_acc[warp][h][16 * l8 + 2 * i + 1] = acc[h][i].y;
-      }
-      if (l8 == 0) {
-        s_ml[warp][h][0] = m[h];
-        s_ml[warp][h][1] = l[h];
-      }
+    if (tig == 0) {
+      s_ml[warp][g][0] = m;
+      s_ml[warp][g][1] = l;
     }
   }
   __syncthreads();
@@ -364,23 +419,25 @@ cudaError_t launch_decode_attention(const uint8_t* q, const float* sq, const uin
                                     cudaStream_t st) {
   if (batch == 0) return cudaSuccess;
   const int g = hq / hkv;
-  const int gh = g >= 4 ? 4 : g;
+  // query heads per CTA: the 8 used rows of the MMA tiles when they divide
+  // the group, else 4, else the whole group (1 or 2)
+  const int gh = g % 8 == 0 ? 8 : (g % 4 == 0 ? 4 : g);
   const int hgroups = g / gh;
   const int64_t grid = batch * hkv * hgroups * AT_SPLIT;
   // TMA row coordinates are 32-bit: the last chunk may start AT_CHUNK rows
   // before batch * smax and run past it (those rows read as zero)
   if (grid > 0x7FFFFFFFLL || batch * smax > 0x7FFFFFFFLL - AT_CHUNK) return cudaErrorInvalidValue;
   // K and V as 2-D row-major [batch * smax, hkv * 128] byte matrices; a box
-  // is 16 token rows of one KV head
+  // is 16 token rows of one KV head, stored with the 128-byte swizzle
   CUtensorMap tm_k, tm_v;
   const uint64_t rows = (uint64_t)(batch * smax), cols = (uint64_t)hkv * AT_D;
   if (rows == 0) {
     // no tokens at all: the kernel issues no load, but a map needs a row
-    if (!make_tmap_2d(&tm_k, k, 1, 1, cols, AT_CHUNK, AT_D, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_tmap_2d(&tm_v, v, 1, 1, cols, AT_CHUNK, AT_D, CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!make_tmap_2d(&tm_k, k, 1, 1, cols, AT_CHUNK, AT_D, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_2d(&tm_v, v, 1, 1, cols, AT_CHUNK, AT_D, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
-  } else if (!make_tmap_2d(&tm_k, k, 1, rows, cols, AT_CHUNK, AT_D, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-             !make_tmap_2d(&tm_v, v, 1, rows, cols, AT_CHUNK, AT_D, CU_TENSOR_MAP_SWIZZLE_NONE)) {
+  } else if (!make_tmap_2d(&tm_k, k, 1, rows, cols, AT_CHUNK, AT_D, CU_TENSOR_MAP_SWIZZLE_128B) ||
+             !make_tmap_2d(&tm_v, v, 1, rows, cols, AT_CHUNK, AT_D, CU_TENSOR_MAP_SWIZZLE_128B)) {
     return cudaErrorInvalidValue;
   }
   switch (gh) {
@@ -390,8 +447,11 @@ cudaError_t launch_decode_attention(const uint8_t* q, const float* sq, const uin
     case 2:
       return launch_attn<2>(tm_k, tm_v, q, sq, sk, sv, lens, smax, hq, hkv, hgroups, softmax_scale,
                             out, (unsigned)grid, st);
-    default:
+    case 4:
       return launch_attn<4>(tm_k, tm_v, q, sq, sk, sv, lens, smax, hq, hkv, hgroups, softmax_scale,
+                            out, (unsigned)grid, st);
+    default:
+      return launch_attn<8>(tm_k, tm_v, q, sq, sk, sv, lens, smax, hq, hkv, hgroups, softmax_scale,
                             out, (unsigned)grid, st);
   }
 }
