@@ -251,10 +251,12 @@ w8a8_status quant_error_report(const uint16_t *x_bf16, const uint8_t *q,
  * 1e-3 * sv * sum_t p_t |dec(v_t,d)| + half a BF16 ulp.
  * Rules: head_dim == 128 and num_q_heads / num_kv_heads in {1, 2} or a
  * multiple of 4 (else W8A8_ERR_UNSUPPORTED); batch * max_seq below
- * 2^31 - 16 (TMA row coordinates; else W8A8_ERR_UNSUPPORTED); q and the
+ * 2^31 - 32 (TMA row coordinates; else W8A8_ERR_UNSUPPORTED); q and the
  * caches 16-byte aligned, the rest 4-byte aligned.  Each (sequence, KV
- * head) slice of the cache is read once per 4 query heads, through TMA
- * tile loads of 16 tokens.
+ * head) slice of the cache is read once per 8 query heads (4 when the
+ * group is not a multiple of 8), through TMA tile loads of 32 tokens; the
+ * products run on the tensor cores (E4M3 codes for Q K^T, f16 for P V with
+ * the weights split in two f16 parts).
  * ---------------------------------------------------------------------- */
 w8a8_status fp8_decode_attention(const uint8_t *q, const float *q_scale,
                                  const uint8_t *k_cache, const float *k_scale,

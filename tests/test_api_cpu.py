@@ -130,7 +130,7 @@ def test_attention_argument_checks(L):
     assert a(A, A, None, A, A, A, A, 2, 64, 8, 2, 128, sc, A, None) == NULL
     assert a(A, A, A + 4, A, A, A, A, 2, 64, 8, 2, 128, sc, A, None) == ALIGN
     assert a(A, A, A, A, A, A, A, 2, 64, 8, 2, 128, sc, A + 2, None) == ALIGN
-    # TMA row coordinates are 32-bit: batch * max_seq must stay below 2^31 - 16
+    # TMA row coordinates are 32-bit: batch * max_seq must stay below 2^31 - 32
     assert a(A, A, A, A, A, A, A, 1 << 16, 1 << 15, 8, 2, 128, sc, A, None) == UNSUP
 
 

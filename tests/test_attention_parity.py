@@ -31,7 +31,14 @@ def _check(out, ref, ab, rel):
 
 CASES = [  # batch, max_seq, q heads, kv heads, lengths
     (2, 300, 8, 2, [300, 123]), (3, 64, 4, 4, [1, 64, 0]), (2, 40, 4, 2, [40, 17]),
-    (1, 1000, 32, 8, [997]), (2, 96, 16, 2, [96, 95]), (4, 7, 8, 8, [7, 1, 2, 3])]
+    (1, 1000, 32, 8, [997]), (2, 96, 16, 2, [96, 95]), (4, 7, 8, 8, [7, 1, 2, 3]),
+    # 320 (sequence, KV head) slices: enough that each slice is split over
+    # only 2 CTAs; ragged lengths from 0 to 64
+    (40, 64, 32, 8, [(7 * i) % 65 for i in range(40)]),
+    # 8 query heads per KV head: one CTA covers all 8 used MMA rows
+    (3, 200, 64, 8, [200, 77, 1]),
+    # 64 slices: each split over 4 CTAs
+    (8, 100, 32, 8, [100, 99, 64, 33, 32, 31, 17, 0])]
 
 
 @pytest.mark.parametrize("B,S,Hq,Hkv,lens", CASES)

@@ -212,7 +212,7 @@ W8A8_API w8a8_status fp8_decode_attention(const uint8_t* q, const float* q_scale
   if (head_dim != 128 || !(g == 1 || g == 2 || g % 4 == 0)) return W8A8_ERR_UNSUPPORTED;
   if (max_seq >= kMaxDim || batch >= kMaxDim) return W8A8_ERR_SHAPE;
   if (batch == 0) return W8A8_OK;
-  if (batch * max_seq > kMaxDim - 1 - 16) return W8A8_ERR_UNSUPPORTED;
+  if (batch * max_seq > kMaxDim - 1 - 32) return W8A8_ERR_UNSUPPORTED;
   if (!q || !q_scale || !k_cache || !k_scale || !v_cache || !v_scale || !seq_lens || !out_bf16)
     return W8A8_ERR_NULL;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out_bf16, 4) ||

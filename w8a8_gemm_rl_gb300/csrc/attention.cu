@@ -6,15 +6,15 @@
 //   out_d   = sv * sum_{t < len_b} softmax(score)_t * dec(v[b,t,kh,d])
 //
 // one query token per sequence, grouped-query heads (query head h reads KV
-// head h / (hq / hkv)), head dim 128.  A cluster of AT_SPLIT CTAs reads one
+// head h / (hq / hkv)), head dim 128.  A cluster of 2 to 8 CTAs reads one
 // (sequence, KV head) slice of K and V exactly once for up to 8 query
 // heads, so the kernel streams the cache and is HBM-bound.
 //
 // Each CTA takes a contiguous part of the slice's tokens and each of its 4
 // warps a contiguous quarter of that, streamed through the warp's own ring
-// of shared-memory stages: two TMA tile loads per chunk of 16 tokens (the
+// of shared-memory stages: two TMA tile loads per chunk of 32 tokens (the
 // 128-byte rows of one KV head sit hkv * 128 bytes apart in the cache, a
-// 2-D box of 16 rows x 128 bytes, stored with the 128-byte swizzle so that
+// 2-D box of 32 rows x 128 bytes, stored with the 128-byte swizzle so that
 // the 8-row matrix loads below hit distinct banks).  Lane 0 keeps
 // AT_STAGES - 1 chunks in flight while the warp computes on the oldest.
 //
@@ -63,13 +63,14 @@ namespace {
 constexpr int AT_D = 128;
 constexpr int AT_WARPS = 4;
 constexpr int AT_THREADS = 32 * AT_WARPS;
-constexpr int AT_CHUNK = 16;                       // tokens per chunk: one k16 step of O += P V
-constexpr int AT_STAGES = 4;                       // ring depth per warp
+constexpr int AT_CHUNK = 32;                       // tokens per chunk (a multiple of 16)
+constexpr int AT_NT = AT_CHUNK / 8;                // 8-token n tiles of S per chunk
+constexpr int AT_STAGES = 3;                       // ring depth per warp
 constexpr int AT_TILE = AT_CHUNK * AT_D;           // bytes of K (or of V) per chunk
 constexpr int AT_STAGE = 2 * AT_TILE;              // K tile, then V tile
 constexpr int AT_RING = AT_STAGES * AT_STAGE;      // per warp
 constexpr int AT_BAR_OFF = AT_WARPS * AT_RING;     // mbarriers after the rings
-constexpr int AT_SPLIT = 4;                        // CTAs (one cluster) per slice
+constexpr int AT_MAX_SPLIT = 8;                    // CTAs (one cluster) per slice, at most
 // + 1024: the rings start at the first 1024-byte boundary of the dynamic
 // shared memory (which follows the kernel's static shared arrays)
 constexpr int AT_DYN_SMEM = AT_BAR_OFF + AT_WARPS * AT_STAGES * 8 + 1024;
@@ -78,11 +79,20 @@ constexpr float AT_P_LOG2 = 15.0f;                 // weights are formed as 2^15
 static_assert(AT_TILE % 1024 == 0 && AT_RING % 1024 == 0,
               "128-byte-swizzled tiles start on 1024-byte boundaries");
 
-// two E4M3 codes (low byte first) -> f16x2, exactly
-__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t c16) {
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)c16));
-  return h2;
+// four E4M3 codes (bytes 0..3) -> f16x2 of bytes 0, 1 and f16x2 of bytes 2, 3,
+// exactly (every E4M3 value is an f16 value)
+__device__ __forceinline__ void e4m3x4_f16x2x2(uint32_t c, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(c));
+}
+// 2^x by the hardware approximation (relative error about 2^-22; 0 for
+// x = -inf and for results below the normal range)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 // (lo, hi) -> f16x2 with lo in the low half, round to nearest even
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
@@ -121,6 +131,18 @@ __device__ __forceinline__ void mma_rows8(float& d0, float& d1, uint32_t a0, uin
       : "r"(a0), "r"(0u), "r"(a2), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
+// (d0, d1) += A B on one m16n8k32 tile of E4M3 codes (f32 accumulate), A
+// rows 8..15 zero as above: a0 / a2 hold bytes 4 tig .. 4 tig + 3 of the
+// two 16-byte halves of row g's k range, b0 / b1 the same of column g.
+__device__ __forceinline__ void mma_e4m3_rows8(float& d0, float& d1, uint32_t a0, uint32_t a2,
+                                               uint32_t b0, uint32_t b1) {
+  asm("{\n\t.reg .f32 z2, z3;\n\t"
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, z2, z3}, {%2, %3, %4, %3}, "
+      "{%5, %6}, {%0, %1, %7, %7};\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "r"(a0), "r"(0u), "r"(a2), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
 __device__ __forceinline__ uint16_t bf16_rn(float x) {
   uint16_t r;
   asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(x));
@@ -152,13 +174,14 @@ __device__ __forceinline__ float2 merge_factors(float m, float m2, float& mt) {
 }  // namespace
 
 template <int GH>
-__global__ void __cluster_dims__(AT_SPLIT, 1, 1) __launch_bounds__(AT_THREADS, 2)
+__global__ void __launch_bounds__(AT_THREADS, 2)
     decode_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v,
                             const uint8_t* __restrict__ q, const float* __restrict__ sq_p,
                             const float* __restrict__ sk_p, const float* __restrict__ sv_p,
                             const int32_t* __restrict__ lens, int64_t smax, int hq, int hkv,
-                            int hgroups, float softmax_scale, uint16_t* __restrict__ out) {
+                            int hgroups, int nsplit, float softmax_scale,
+                            uint16_t* __restrict__ out) {
   extern __shared__ __align__(16) uint8_t at_smem[];
   __shared__ float s_acc[AT_WARPS][GH][AT_D];
   __shared__ float s_ml[AT_WARPS][GH][2];
@@ -166,8 +189,8 @@ __global__ void __cluster_dims__(AT_SPLIT, 1, 1) __launch_bounds__(AT_THREADS, 2
   __shared__ float s_cm[GH][2];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, tig = lane & 3;  // fragment row (query head) and column pair
-  const int rank = blockIdx.x % AT_SPLIT;  // rank in the cluster (clusters run along x)
-  const int unit = blockIdx.x / AT_SPLIT;
+  const int rank = blockIdx.x % nsplit;  // rank in the cluster of nsplit CTAs (along x)
+  const int unit = blockIdx.x / nsplit;
   const int hg = unit % hgroups;
   const int64_t bk = unit / hgroups;
   const int kh = (int)(bk % hkv);
@@ -176,9 +199,9 @@ __global__ void __cluster_dims__(AT_SPLIT, 1, 1) __launch_bounds__(AT_THREADS, 2
   // lengths are device data the host cannot check: clamp to [0, smax]
   const int len = (int)min((int64_t)max(lens[b], 0), smax);
 
-  // the cluster's CTAs split the tokens into AT_SPLIT contiguous parts,
-  // and each CTA's warps split its part into AT_WARPS
-  const int pc = (len + AT_SPLIT - 1) / AT_SPLIT;
+  // the cluster's CTAs split the tokens into nsplit contiguous parts, and
+  // each CTA's warps split its part into AT_WARPS
+  const int pc = (len + nsplit - 1) / nsplit;
   const int c_lo = min(len, rank * pc), c_hi = min(len, c_lo + pc);
   const int per = (c_hi - c_lo + AT_WARPS - 1) / AT_WARPS;
   const int t0 = min(c_hi, c_lo + warp * per), t1 = min(c_hi, t0 + per);
@@ -204,19 +227,16 @@ __global__ void __cluster_dims__(AT_SPLIT, 1, 1) __launch_bounds__(AT_THREADS, 2
     for (int c = 0; c < AT_STAGES && c < nch; ++c) issue(c);
   }
 
-  // Q as the A operand of S = Q K^T, row g = query head h0 + g (zero past
-  // GH).  The 16 dims of segment s map to the k slots as 2 tig + {0, 1} <->
-  // 16 s + 4 tig + {0, 1} and 2 tig + 8 + {0, 1} <-> 16 s + 4 tig + {2, 3},
-  // the order in which ldmatrix hands out the K bytes below.
-  uint32_t qa[8][2];
+  // Q as the A operand of S = Q K^T (raw E4M3 codes), row g = query head
+  // h0 + g (zero past GH); k step ks covers dims 32 ks .. 32 ks + 31
+  uint32_t qa[4][2];
 #pragma unroll
-  for (int s = 0; s < 8; ++s) {
-    const uint32_t w =
-        g < GH ? *reinterpret_cast<const uint32_t*>(q + ((b * hq) + h0 + g) * AT_D + 16 * s + 4 * tig)
-               : 0u;
-    qa[s][0] = e4m3x2_f16x2(w & 0xFFFFu);
-    qa[s][1] = e4m3x2_f16x2(w >> 16);
-  }
+  for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh)
+      qa[ks][hh] = g < GH ? *reinterpret_cast<const uint32_t*>(q + ((b * hq) + h0 + g) * AT_D +
+                                                              32 * ks + 16 * hh + 4 * tig)
+                          : 0u;
   const float qk = softmax_scale * sq_p[0] * sk_p[0] * 1.4426950408889634f;
   // online-softmax state of head g (the 4 lanes of a row agree on m; each
   // sums its own tokens into l), and O[g, d] for d = 16 s + 4 tig + e + 2 i
@@ -247,40 +267,59 @@ __global__ void __cluster_dims__(AT_SPLIT, 1, 1) __launch_bounds__(AT_THREADS, 2
     const int tc = t0 + c * AT_CHUNK;
 
     // S for the chunk: n tile j holds tokens 8 j + 0..7; this lane gets
-    // head g, tokens 8 j + 2 tig + {0, 1}
-    float sc[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
+    // head g, tokens 8 j + 2 tig + {0, 1}.  Two partial sums per tile (even
+    // and odd k steps) keep more MMA chains in flight.
+    float sp2[2][AT_NT][2] = {};
 #pragma unroll
-    for (int sp = 0; sp < 8; sp += 2) {
-      uint32_t r[4];  // tokens 0-7 / 8-15 of segment sp, then of segment sp + 1
-      ldsm_x4(tk + mrow * AT_D + (((sp + mseg) ^ (mrow & 7)) << 4), r);
+    for (int ks = 0; ks < 4; ++ks)
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const int j = jj & 1, seg = sp + (jj >> 1);
-        mma_rows8(sc[j][0], sc[j][1], qa[seg][0], qa[seg][1], e4m3x2_f16x2(r[jj] & 0xFFFFu),
-                  e4m3x2_f16x2(r[jj] >> 16));
+      for (int tb = 0; tb < AT_CHUNK / 16; ++tb) {
+        // tokens 16 tb + 0-7 / 8-15 of segment 2 ks, then of segment 2 ks + 1
+        uint32_t r[4];
+        const int row = 16 * tb + mrow;
+        ldsm_x4(tk + row * AT_D + (((2 * ks + mseg) ^ (row & 7)) << 4), r);
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj)
+          mma_e4m3_rows8(sp2[ks & 1][2 * tb + jj][0], sp2[ks & 1][2 * tb + jj][1], qa[ks][0],
+                         qa[ks][1], r[jj], r[jj + 2]);
       }
-    }
+    float sc[AT_NT][2];
+#pragma unroll
+    for (int j = 0; j < AT_NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) sc[j][e] = sp2[0][j][e] + sp2[1][j][e];
     // one online-softmax step over the chunk: scores in log2 units, tokens
     // past the end weigh nothing; the maximum covers the chunk's first
     // token, so it is finite
     float mx = m;
+    if (tc + AT_CHUNK <= t1) {  // a full chunk (all but a warp's last)
 #pragma unroll
-    for (int j = 0; j < 2; ++j)
+      for (int j = 0; j < AT_NT; ++j)
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float x = tc + 8 * j + 2 * tig + e < t1 ? sc[j][e] * qk : -INFINITY;
-        sc[j][e] = x;
-        mx = fmaxf(mx, x);
-      }
+        for (int e = 0; e < 2; ++e) {
+          sc[j][e] *= qk;
+          mx = fmaxf(mx, sc[j][e]);
+        }
+    } else {
+#pragma unroll
+      for (int j = 0; j < AT_NT; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float x = tc + 8 * j + 2 * tig + e < t1 ? sc[j][e] * qk : -INFINITY;
+          sc[j][e] = x;
+          mx = fmaxf(mx, x);
+        }
+    }
     mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
-    const float cr = exp2f(m - mx);  // 0 for the first step, exactly 1 if the maximum holds
-    float pp[2][2], ps = 0.0f;
+    // 0 for the first step, exactly 1 while the maximum holds
+    const float cr = m == mx ? 1.0f : ex2_approx(m - mx);
+    float pp[AT_NT][2], ps = 0.0f;
 #pragma unroll
-    for (int j = 0; j < 2; ++j)
+    for (int j = 0; j < AT_NT; ++j)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        pp[j][e] = exp2f(sc[j][e] - mx + AT_P_LOG2);
+        pp[j][e] = ex2_approx(sc[j][e] - mx + AT_P_LOG2);
         ps += pp[j][e];
       }
     l = __fmaf_rn(l, cr, ps);
@@ -294,37 +333,43 @@ __global__ void __cluster_dims__(AT_SPLIT, 1, 1) __launch_bounds__(AT_THREADS, 2
           acc[s2][e][1] *= cr;
         }
     }
-    // P in the A layout of O += P V (k slots = the chunk's tokens, where the
-    // S tile left them), as hi + lo f16 parts
-    const uint32_t ph0 = pack_f16x2(pp[0][0], pp[0][1]), ph1 = pack_f16x2(pp[1][0], pp[1][1]);
-    const float2 f0 = unpack_f16x2(ph0), f1 = unpack_f16x2(ph1);
-    const uint32_t pl0 = pack_f16x2(pp[0][0] - f0.x, pp[0][1] - f0.y);
-    const uint32_t pl1 = pack_f16x2(pp[1][0] - f1.x, pp[1][1] - f1.y);
+    // P in the A layout of O += P V, one k16 step per 16 tokens (k slots =
+    // the tokens, where the S tiles left them), as hi + lo f16 parts
 #pragma unroll
-    for (int sp = 0; sp < 8; sp += 2) {
-      uint32_t r[4];  // transposed: tokens 2 tig + {0, 1} (+ 8) of dims 2 g, 2 g + 1 of a segment
-      ldsm_x4_trans(tv + mrow * AT_D + (((sp + mseg) ^ (mrow & 7)) << 4), r);
+    for (int kk = 0; kk < AT_CHUNK / 16; ++kk) {
+      const uint32_t ph0 = pack_f16x2(pp[2 * kk][0], pp[2 * kk][1]);
+      const uint32_t ph1 = pack_f16x2(pp[2 * kk + 1][0], pp[2 * kk + 1][1]);
+      const float2 f0 = unpack_f16x2(ph0), f1 = unpack_f16x2(ph1);
+      const uint32_t pl0 = pack_f16x2(pp[2 * kk][0] - f0.x, pp[2 * kk][1] - f0.y);
+      const uint32_t pl1 = pack_f16x2(pp[2 * kk + 1][0] - f1.x, pp[2 * kk + 1][1] - f1.y);
 #pragma unroll
-      for (int hs = 0; hs < 2; ++hs) {
-        const int seg = sp + hs;
-        // bytes (t, 2g) (t, 2g+1) (t+1, 2g) (t+1, 2g+1) -> (t, 2g) (t+1, 2g) | (t, 2g+1) (t+1, 2g+1)
-        const uint32_t x0v = __byte_perm(r[2 * hs], 0u, 0x3120u);
-        const uint32_t x1v = __byte_perm(r[2 * hs + 1], 0u, 0x3120u);
+      for (int sp = 0; sp < 8; sp += 2) {
+        // transposed: tokens 16 kk + 2 tig + {0, 1} (+ 8) of dims 2 g, 2 g + 1 of a segment
+        uint32_t r[4];
+        const int row = 16 * kk + mrow;
+        ldsm_x4_trans(tv + row * AT_D + (((sp + mseg) ^ (row & 7)) << 4), r);
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {  // n tile of dims 16 seg + 2 n + e
-          const uint32_t b0 = e4m3x2_f16x2(e ? x0v >> 16 : x0v & 0xFFFFu);
-          const uint32_t b1 = e4m3x2_f16x2(e ? x1v >> 16 : x1v & 0xFFFFu);
-          mma_rows8(acc[seg][e][0], acc[seg][e][1], ph0, ph1, b0, b1);
-          mma_rows8(acc[seg][e][0], acc[seg][e][1], pl0, pl1, b0, b1);
+        for (int hs = 0; hs < 2; ++hs) {
+          const int seg = sp + hs;
+          // bytes (t, 2g) (t, 2g+1) (t+1, 2g) (t+1, 2g+1) -> (t, 2g) (t+1, 2g) | (t, 2g+1) (t+1, 2g+1)
+          const uint32_t x0v = __byte_perm(r[2 * hs], 0u, 0x3120u);
+          const uint32_t x1v = __byte_perm(r[2 * hs + 1], 0u, 0x3120u);
+          uint32_t b0[2], b1[2];  // [e]: n tile of dims 16 seg + 2 n + e
+          e4m3x4_f16x2x2(x0v, b0[0], b0[1]);
+          e4m3x4_f16x2x2(x1v, b1[0], b1[1]);
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            mma_rows8(acc[seg][e][0], acc[seg][e][1], ph0, ph1, b0[e], b1[e]);
+            mma_rows8(acc[seg][e][0], acc[seg][e][1], pl0, pl1, b0[e], b1[e]);
+          }
         }
       }
     }
-    // every lane has used this stage: lane 0 refills it with chunk c + AT_STAGES
+    // every lane has used this stage (each ldmatrix result has fed an MMA
+    // issued above, so the reads are complete): lane 0 refills it with
+    // chunk c + AT_STAGES
     __syncwarp();
-    if (lane == 0 && c + AT_STAGES < nch) {
-      ptx::fence_proxy_async_smem();
-      issue(c + AT_STAGES);
-    }
+    if (lane == 0 && c + AT_STAGES < nch) issue(c + AT_STAGES);
   }
   if (!ok && lane == 0) {
     // chunks c .. c + AT_STAGES - 1 may still be in flight: let them land
@@ -372,13 +417,12 @@ __global__ void __cluster_dims__(AT_SPLIT, 1, 1) __launch_bounds__(AT_THREADS, 2
       s_cm[h][1] = ll;
     }
   }
-  // then the cluster's CTAs in rank order: CTA r finishes heads r, r + AT_SPLIT, ...
+  // then the cluster's CTAs in rank order: CTA r finishes heads r, r + nsplit, ...
   cluster_sync_all();
   const float sv = sv_p[0];
-  for (int h = rank; h < GH; h += AT_SPLIT) {
+  for (int h = rank; h < GH; h += nsplit) {
     float mm = -INFINITY, ll = 0.0f, aa = 0.0f;
-#pragma unroll
-    for (int r = 0; r < AT_SPLIT; ++r) {
+    for (int r = 0; r < nsplit; ++r) {
       float mt;
       const float2 f = merge_factors(mm, ld_cluster_f32(&s_cm[h][0], r), mt);
       ll = ll * f.x + ld_cluster_f32(&s_cm[h][1], r) * f.y;
@@ -395,7 +439,7 @@ template <int GH>
 static cudaError_t launch_attn(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const uint8_t* q,
                                const float* sq, const float* sk, const float* sv,
                                const int32_t* lens, int64_t smax, int hq, int hkv, int hgroups,
-                               float softmax_scale, uint16_t* out, unsigned grid,
+                               int nsplit, float softmax_scale, uint16_t* out, unsigned grid,
                                cudaStream_t st) {
   static bool configured[64] = {};  // the attribute belongs to each device's context
   int dev = 0;
@@ -407,9 +451,20 @@ static cudaError_t launch_attn(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  decode_attention_kernel<GH><<<grid, AT_THREADS, AT_DYN_SMEM, st>>>(
-      tm_k, tm_v, q, sq, sk, sv, lens, smax, hq, hkv, hgroups, softmax_scale, out);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(AT_THREADS);
+  cfg.dynamicSmemBytes = AT_DYN_SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)nsplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_attention_kernel<GH>, tm_k, tm_v, q, sq, sk, sv, lens,
+                            smax, hq, hkv, hgroups, nsplit, softmax_scale, out);
 }
 
 cudaError_t launch_decode_attention(const uint8_t* q, const float* sq, const uint8_t* k,
@@ -423,7 +478,25 @@ cudaError_t launch_decode_attention(const uint8_t* q, const float* sq, const uin
   // the group, else 4, else the whole group (1 or 2)
   const int gh = g % 8 == 0 ? 8 : (g % 4 == 0 ? 4 : g);
   const int hgroups = g / gh;
-  const int64_t grid = batch * hkv * hgroups * AT_SPLIT;
+  // CTAs per slice (measured on the 32 x 8192 x 8 x 128 cache and its
+  // neighbours): each extra CTA costs a pipeline fill and a merge, so split
+  // finely only while SMs would otherwise idle; around one or two slices
+  // per SM take them whole (long ones in 4 parts, which pays for the
+  // fills), beyond that in 2 parts for a finer balance over the SMs
+  const int64_t units = batch * hkv * hgroups;
+  const int64_t sms = sm_count();
+  int nsplit;
+  if (units * 4 <= sms)
+    nsplit = AT_MAX_SPLIT;
+  else if (units * 2 <= sms)
+    nsplit = 4;
+  else if (units <= sms)
+    nsplit = 2;
+  else if (units <= 2 * sms)
+    nsplit = smax >= 16384 ? 4 : 1;
+  else
+    nsplit = 2;
+  const int64_t grid = units * nsplit;
   // TMA row coordinates are 32-bit: the last chunk may start AT_CHUNK rows
   // before batch * smax and run past it (those rows read as zero)
   if (grid > 0x7FFFFFFFLL || batch * smax > 0x7FFFFFFFLL - AT_CHUNK) return cudaErrorInvalidValue;
@@ -442,17 +515,17 @@ cudaError_t launch_decode_attention(const uint8_t* q, const float* sq, const uin
   }
   switch (gh) {
     case 1:
-      return launch_attn<1>(tm_k, tm_v, q, sq, sk, sv, lens, smax, hq, hkv, hgroups, softmax_scale,
-                            out, (unsigned)grid, st);
+      return launch_attn<1>(tm_k, tm_v, q, sq, sk, sv, lens, smax, hq, hkv, hgroups, nsplit,
+                            softmax_scale, out, (unsigned)grid, st);
     case 2:
-      return launch_attn<2>(tm_k, tm_v, q, sq, sk, sv, lens, smax, hq, hkv, hgroups, softmax_scale,
-                            out, (unsigned)grid, st);
+      return launch_attn<2>(tm_k, tm_v, q, sq, sk, sv, lens, smax, hq, hkv, hgroups, nsplit,
+                            softmax_scale, out, (unsigned)grid, st);
     case 4:
-      return launch_attn<4>(tm_k, tm_v, q, sq, sk, sv, lens, smax, hq, hkv, hgroups, softmax_scale,
-                            out, (unsigned)grid, st);
+      return launch_attn<4>(tm_k, tm_v, q, sq, sk, sv, lens, smax, hq, hkv, hgroups, nsplit,
+                            softmax_scale, out, (unsigned)grid, st);
     default:
-      return launch_attn<8>(tm_k, tm_v, q, sq, sk, sv, lens, smax, hq, hkv, hgroups, softmax_scale,
-                            out, (unsigned)grid, st);
+      return launch_attn<8>(tm_k, tm_v, q, sq, sk, sv, lens, smax, hq, hkv, hgroups, nsplit,
+                            softmax_scale, out, (unsigned)grid, st);
   }
 }
 
