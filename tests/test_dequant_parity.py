@@ -66,3 +66,32 @@ def test_quant_error_report_matches_oracle(W, rows, cols, qb, rb):
     assert np.allclose(st[..., 1:], want[..., 1:], rtol=1e-5, atol=0)
     # SQNR of E4M3 with block scales on N(0,1) data with outliers: 10-45 dB
     assert 10.0 < W.sqnr_db(torch.from_numpy(st)) < 45.0
+
+
+def test_weight_sync_rows_at_full_size(W):
+    """One Qwen3-8B gate_up matrix [24576, 4096] (the largest of the weight
+    sync): power-of-two block quantization, dequantization and the error
+    report, each checked against the oracle on sampled 128 x 128 blocks
+    (blocks are independent, so a block alone gives the same result); the
+    last block row and column included."""
+    n, k = 24576, 4096
+    w = synth.weights(n, k, seed=17, device="cuda")
+    wq, ws = W.quantize_weight_blockwise(w, pow2=True)
+    y = W.dequantize_blockwise(wq, ws, 128, 128)
+    st = W.quant_error_report(w, wq, ws, (128, 128), (128, 128))
+    torch.cuda.synchronize()
+    g = torch.Generator().manual_seed(5)
+    picks = [(0, 0), (n // 128 - 1, k // 128 - 1)] + [
+        (int(torch.randint(0, n // 128, (1,), generator=g)), int(torch.randint(0, k // 128, (1,), generator=g)))
+        for _ in range(6)]
+    for bi, bj in picks:
+        r, c = slice(128 * bi, 128 * bi + 128), slice(128 * bj, 128 * bj + 128)
+        xb = synth.bf16_bits(w[r, c])
+        q_ref, s_ref = O.quantize_blocks(xb, 128, 128, pow2=True)
+        assert (u8(wq[r, c]) == q_ref).all()
+        assert ws[bi, bj].item() == s_ref[0, 0]
+        assert (bits16(y[r, c]) == O.dequantize_blocks(q_ref, s_ref, 128, 128)).all()
+        want = O.quant_error(xb, q_ref, s_ref, 128, 128, 128, 128)[0, 0]
+        got = st[bi, bj].cpu().numpy()
+        assert got[0] == want[0]
+        assert np.allclose(got[1:], want[1:], rtol=1e-5, atol=0)
