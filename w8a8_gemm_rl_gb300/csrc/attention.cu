@@ -119,21 +119,20 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
                : "r"(addr)
                : "memory");
 }
-// (d0, d1) += A B on one m16n8k16 tile (f16 in, f32 accumulate) whose A
-// rows 8..15 are zero: a0 / a2 are the row-g fragments, the results of the
-// zero rows are dropped.
-__device__ __forceinline__ void mma_rows8(float& d0, float& d1, uint32_t a0, uint32_t a2,
-                                          uint32_t b0, uint32_t b1) {
-  asm("{\n\t.reg .f32 z2, z3;\n\t"  // results of the zero rows, dropped
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, z2, z3}, {%2, %3, %4, %3}, "
-      "{%5, %6}, {%0, %1, %7, %7};\n\t}"
-      : "+f"(d0), "+f"(d1)
-      : "r"(a0), "r"(0u), "r"(a2), "r"(b0), "r"(b1), "f"(0.0f));
+// d += A B on one full m16n8k16 tile (f16 in, f32 accumulate): a0 / a2 the
+// fragments of row g, a1 / a3 those of row g + 8; d0, d1 row g, d2, d3 row g + 8.
+__device__ __forceinline__ void mma_rows16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                           uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// (d0, d1) += A B on one m16n8k32 tile of E4M3 codes (f32 accumulate), A
-// rows 8..15 zero as above: a0 / a2 hold bytes 4 tig .. 4 tig + 3 of the
-// two 16-byte halves of row g's k range, b0 / b1 the same of column g.
+// (d0, d1) += A B on one m16n8k32 tile of E4M3 codes (f32 accumulate)
+// whose A rows 8..15 are zero (their results are dropped): a0 / a2 hold
+// bytes 4 tig .. 4 tig + 3 of the two 16-byte halves of row g's k range,
+// b0 / b1 the same of column g.
 __device__ __forceinline__ void mma_e4m3_rows8(float& d0, float& d1, uint32_t a0, uint32_t a2,
                                                uint32_t b0, uint32_t b1) {
   asm("{\n\t.reg .f32 z2, z3;\n\t"
@@ -240,12 +239,16 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
   const float qk = softmax_scale * sq_p[0] * sk_p[0] * 1.4426950408889634f;
   // online-softmax state of head g (the 4 lanes of a row agree on m; each
   // sums its own tokens into l), and O[g, d] for d = 16 s + 4 tig + e + 2 i
+  // in two parts: acc[s][e][i] from the high halves of the weights (MMA row
+  // g), acc[s][e][2 + i] from the low halves (row g + 8)
   float m = -INFINITY, l = 0.0f;
-  float acc[8][2][2];
+  float acc[8][2][4];
 #pragma unroll
   for (int s = 0; s < 8; ++s)
 #pragma unroll
-    for (int e = 0; e < 2; ++e) acc[s][e][0] = acc[s][e][1] = 0.0f;
+    for (int e = 0; e < 2; ++e)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[s][e][i] = 0.0f;
   __syncwarp();  // the barriers are initialised before any lane polls them
 
   // ldmatrix row address of this lane inside a tile: matrix lane / 8 holds
@@ -328,13 +331,14 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
 #pragma unroll
       for (int s2 = 0; s2 < 8; ++s2)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          acc[s2][e][0] *= cr;
-          acc[s2][e][1] *= cr;
-        }
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[s2][e][i] *= cr;
     }
     // P in the A layout of O += P V, one k16 step per 16 tokens (k slots =
-    // the tokens, where the S tiles left them), as hi + lo f16 parts
+    // the tokens, where the S tiles left them), as hi + lo f16 parts: the
+    // high parts in rows 0-7 and the low parts in rows 8-15 of one tile, so
+    // one MMA carries both
 #pragma unroll
     for (int kk = 0; kk < AT_CHUNK / 16; ++kk) {
       const uint32_t ph0 = pack_f16x2(pp[2 * kk][0], pp[2 * kk][1]);
@@ -358,10 +362,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
           e4m3x4_f16x2x2(x0v, b0[0], b0[1]);
           e4m3x4_f16x2x2(x1v, b1[0], b1[1]);
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            mma_rows8(acc[seg][e][0], acc[seg][e][1], ph0, ph1, b0[e], b1[e]);
-            mma_rows8(acc[seg][e][0], acc[seg][e][1], pl0, pl1, b0[e], b1[e]);
-          }
+          for (int e = 0; e < 2; ++e) mma_rows16(acc[seg][e], ph0, pl0, ph1, pl1, b0[e], b1[e]);
         }
       }
     }
@@ -389,8 +390,8 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
     for (int s2 = 0; s2 < 8; ++s2)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        s_acc[warp][g][16 * s2 + 4 * tig + e] = acc[s2][e][0];
-        s_acc[warp][g][16 * s2 + 4 * tig + e + 2] = acc[s2][e][1];
+        s_acc[warp][g][16 * s2 + 4 * tig + e] = acc[s2][e][0] + acc[s2][e][2];
+        s_acc[warp][g][16 * s2 + 4 * tig + e + 2] = acc[s2][e][1] + acc[s2][e][3];
       }
     if (tig == 0) {
       s_ml[warp][g][0] = m;
