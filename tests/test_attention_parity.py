@@ -97,3 +97,23 @@ def test_decode_attention_full_cache_sampled(W):
                                      v[b:b + 1].cpu().numpy(), 0.25, ln[b:b + 1].cpu().numpy(),
                                      1 / math.sqrt(128))
         _check(out[b:b + 1], ref, ab, 2.0 ** -14)
+
+
+def test_decode_attention_clamps_device_lengths(W):
+    """Lengths are device data the host cannot check: the kernel clamps them
+    to [0, max_seq], so a negative length gives zeros and one past max_seq
+    attends to the whole sequence (the oracle run with the clamped lengths)."""
+    g = torch.Generator().manual_seed(77)
+    B, S, Hq, Hkv = 3, 50, 8, 2
+    q, k, v = _codes((B, Hq, 128), g), _codes((B, S, Hkv, 128), g), _codes((B, S, Hkv, 128), g)
+    scales = torch.tensor([0.02, 0.03, 0.5], dtype=torch.float32)
+    ln = torch.tensor([-5, S + 100, 20], dtype=torch.int32)
+    dev = lambda t: t.cuda()
+    out = W.fp8_decode_attention(dev(q), dev(scales[0:1]), dev(k), dev(scales[1:2]), dev(v),
+                                 dev(scales[2:3]), dev(ln))
+    torch.cuda.synchronize()
+    clamped = np.array([0, S, 20], np.int32)
+    ref, ab = O.decode_attention(q.numpy(), scales[0].item(), k.numpy(), scales[1].item(), v.numpy(),
+                                 scales[2].item(), clamped, 1 / math.sqrt(128))
+    _check(out, ref, ab, 2.0 ** -14)
+    assert (bits16(out[0]) == 0).all()
