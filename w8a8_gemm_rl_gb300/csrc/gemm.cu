@@ -58,7 +58,7 @@ constexpr int THREADS = 32 * EPI_WARP0 + 32 * NUM_EPI_WARPS;
 constexpr int REGS_LAUNCH = 168, REGS_CTRL = 72, REGS_EPI = 216;
 static_assert(128 * REGS_CTRL + 256 * REGS_EPI <= THREADS * REGS_LAUNCH, "register split");
 constexpr int TMEM_COLS = 2 * BN;
-constexpr int RASTER_M = 16;
+constexpr int RASTER_M = 8;
 constexpr int MAX_GROUPS = 1024;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr uint64_t ABORT_DRAIN_LIMIT_NS = 10000000000ull;
