@@ -247,8 +247,11 @@ w8a8_status quant_error_report(const uint16_t *x_bf16, const uint8_t *q,
  *   seq_lens [batch] int32 (device), each in [0, max_seq]; an empty
  *            sequence gives zeros.
  *   out_bf16 [batch, num_q_heads, head_dim] (out).
- * Accuracy: binary32 arithmetic with an online softmax; |out - exact| <=
- * 1e-3 * sv * sum_t p_t |dec(v_t,d)| + half a BF16 ulp.
+ * Accuracy: FP32 accumulation throughout (the E4M3 products of Q K^T are
+ * exact; the softmax weights enter P V as two f16 parts, about 22 bits)
+ * with an online softmax; |out - exact| <= 1e-3 * sv * sum_t p_t
+ * |dec(v_t,d)| + half a BF16 ulp (the tests also hold 2^-14 of that sum).
+ * Lengths are read on the device and clamped to [0, max_seq].
  * Rules: head_dim == 128 and num_q_heads / num_kv_heads in {1, 2} or a
  * multiple of 4 (else W8A8_ERR_UNSUPPORTED); batch * max_seq below
  * 2^31 - 32 (TMA row coordinates; else W8A8_ERR_UNSUPPORTED); q and the
