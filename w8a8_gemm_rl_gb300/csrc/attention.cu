@@ -6,9 +6,10 @@
 //   out_d   = sv * sum_{t < len_b} softmax(score)_t * dec(v[b,t,kh,d])
 //
 // one query token per sequence, grouped-query heads (query head h reads KV
-// head h / (hq / hkv)), head dim 128.  A cluster of 2 to 8 CTAs reads one
-// (sequence, KV head) slice of K and V exactly once for up to 8 query
-// heads, so the kernel streams the cache and is HBM-bound.
+// head h / (hq / hkv)), head dim 128.  A cluster of 1 to 8 CTAs (chosen at
+// launch from the number of slices) reads one (sequence, KV head) slice of
+// K and V exactly once for up to 8 query heads, so the kernel streams the
+// cache and is HBM-bound.
 //
 // Each CTA takes a contiguous part of the slice's tokens and each of its 4
 // warps a contiguous quarter of that, streamed through the warp's own ring
@@ -18,19 +19,21 @@
 // the 8-row matrix loads below hit distinct banks).  Lane 0 keeps
 // AT_STAGES - 1 chunks in flight while the warp computes on the oldest.
 //
-// Both contractions of a chunk run on the tensor cores (mma.sync
-// m16n8k16, f16 operands, f32 accumulation), with the query heads as the
-// rows (8 of the 16 rows used):
-//   S[h, t] = sum_d q[h, d] k[t, d]: K fragments come from the raw E4M3
-//     tile by ldmatrix and are widened to f16 (exact: every E4M3 value is
-//     an f16 value), the products are exact;
-//   O[h, d] += P[h, t] v[t, d]: the accumulator of S is already laid out as
-//     the A operand P, V fragments come from ldmatrix.trans on the raw tile
-//     plus a byte permute, and P = 2^15 p is split into two f16 parts
-//     (hi + lo carries 22 bits of it), so the weights lose nothing that
-//     binary32 would keep.
+// Both contractions of a chunk run on the tensor cores (mma.sync), with the
+// query heads as the MMA rows:
+//   S[h, t] = sum_d q[h, d] k[t, d]: m16n8k32 on the raw E4M3 codes (the
+//     products are exact, f32 accumulation); K fragments come from the
+//     stage by ldmatrix, rows 8-15 of A are zero;
+//   O[h, d] += P[h, t] v[t, d]: m16n8k16 in f16 with f32 accumulation.  The
+//     accumulator of S is already laid out as the A operand P; V fragments
+//     come from ldmatrix.trans on the raw tile, a byte permute and one
+//     exact widening to f16.  P = 2^15 p is split into two f16 parts (hi +
+//     lo carries 22 bits of it, so the weights lose nothing that binary32
+//     would keep): the high parts fill A rows 0-7 and the low parts rows
+//     8-15, so one MMA carries both.
 // The softmax is online, in log2 units, one step per chunk per head.  The
-// warps' states, then the cluster's CTAs' states, are merged at the end.
+// warps' states, then the cluster's CTAs' states (through distributed
+// shared memory), are merged at the end.
 #include <math.h>
 
 #include <cuda.h>
@@ -76,7 +79,7 @@ constexpr int AT_MAX_SPLIT = 8;                    // CTAs (one cluster) per sli
 constexpr int AT_DYN_SMEM = AT_BAR_OFF + AT_WARPS * AT_STAGES * 8 + 1024;
 constexpr uint64_t AT_WAIT_LIMIT_NS = 2000000000ull;
 constexpr float AT_P_LOG2 = 15.0f;                 // weights are formed as 2^15 p <= 2^15
-static_assert(AT_TILE % 1024 == 0 && AT_RING % 1024 == 0,
+static_assert(AT_TILE % 1024 == 0 && AT_STAGE % 1024 == 0 && AT_RING % 1024 == 0,
               "128-byte-swizzled tiles start on 1024-byte boundaries");
 
 // four E4M3 codes (bytes 0..3) -> f16x2 of bytes 0, 1 and f16x2 of bytes 2, 3,
@@ -87,8 +90,9 @@ __device__ __forceinline__ void e4m3x4_f16x2x2(uint32_t c, uint32_t& lo, uint32_
       : "=r"(lo), "=r"(hi)
       : "r"(c));
 }
-// 2^x by the hardware approximation (relative error about 2^-22; 0 for
-// x = -inf and for results below the normal range)
+// 2^x by the hardware approximation (an error of a few ulp, far inside the
+// tolerance the parity tests hold; 0 for x = -inf and for results below the
+// normal range)
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
