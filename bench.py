@@ -16,7 +16,7 @@ input, with all inputs resident in HBM:
   4. KV-cache recalibration: per-tensor amax + E4M3 quantization of K and V,
      each [32, 8192, 8, 128].
 
-Metric: each phase is judged against its roofline time
+Metric: each phase is measured against its roofline time
 t_roof = max(flops / peak_fp8, bytes / peak_hbm) with algorithmic bytes and
 flops; `value` = 100 * (roofline time of the work all ranks did) / (wall time
 of the slowest rank), i.e. percent of one GB300's roofline, summed over GPUs.
@@ -727,7 +727,7 @@ def main():
     ap.add_argument("--no-next-rows", action="store_true",
                     help="skip the measurements of the rows past the hot path")
     ap.add_argument("--traffic", type=float, default=None,
-                    help="ncu dram bytes per launch of the dominant kernel, if measured for this build")
+                    help="ncu dram bytes per launch of the dominant kernel, if measured for the current sources")
     args = ap.parse_args()
     if args.impl == "reference":
         bench_reference(args)

@@ -51,7 +51,7 @@ typedef enum {
     W8A8_ERR_NULL = 1,        /* a required pointer is NULL */
     W8A8_ERR_SHAPE = 2,       /* a size is negative or breaks a stated rule */
     W8A8_ERR_ALIGN = 3,       /* a pointer is not aligned as stated */
-    W8A8_ERR_UNSUPPORTED = 4, /* valid request this build does not serve */
+    W8A8_ERR_UNSUPPORTED = 4, /* valid request the library does not serve */
     W8A8_ERR_CUDA = 5         /* the CUDA runtime reported an error */
 } w8a8_status;
 
