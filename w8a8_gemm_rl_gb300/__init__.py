@@ -224,8 +224,13 @@ def sqnr_db(stats):
 
 def fp8_decode_attention(q, q_scale, k_cache, k_scale, v_cache, v_scale, seq_lens,
                          softmax_scale=None, out=None, stream=None):
-    """q uint8 [B, Hq, 128]; k_cache, v_cache uint8 [B, S, Hkv, 128]; scales
-    float32 [1] (device); seq_lens int32 [B] -> BF16 [B, Hq, 128]."""
+    """Decode attention over the FP8 KV cache (one query token per sequence).
+
+    q uint8 [B, Hq, 128] E4M3 codes; k_cache, v_cache uint8 [B, S, Hkv, 128];
+    q_scale, k_scale, v_scale float32 [1] per-tensor scales (device); seq_lens
+    int32 [B] (device; clamped to [0, S] by the kernel) -> BF16 [B, Hq, 128].
+    Query head h reads KV head h // (Hq // Hkv); softmax_scale defaults to
+    1/sqrt(128)."""
     _need(q, torch.uint8, "q")
     _need(k_cache, torch.uint8, "k_cache")
     _need(v_cache, torch.uint8, "v_cache")
