@@ -67,7 +67,8 @@ const char *w8a8_last_cuda_error(void);
 
 /* Reads and clears the device-side error code that a kernel sets when a
  * bounded wait inside it gives up (0 = none; nonzero identifies the wait:
- * below 11 the GEMMs, 11..13 the weight quantizer, 21..22 the decode
+ * 1..8 the GEMMs of more than 256 rows and the grouped GEMM, 31..37 the
+ * GEMM of at most 256 rows, 11..13 the weight quantizer, 21..22 the decode
  * attention).  When several are set, the GEMMs' code is reported first,
  * then the quantizer's, and all are cleared.  Such a kernel stops early
  * and leaves its output incomplete.  Synchronous: blocks until the device
@@ -249,12 +250,16 @@ w8a8_status quant_error_report(const uint16_t *x_bf16, const uint8_t *q,
  *   out_bf16 [batch, num_q_heads, head_dim] (out).
  * Accuracy: FP32 accumulation throughout (the E4M3 products of Q K^T are
  * exact; the softmax weights enter P V as two f16 parts, about 22 bits)
- * with an online softmax; |out - exact| <= 1e-3 * sv * sum_t p_t
- * |dec(v_t,d)| + half a BF16 ulp (the tests also hold 2^-14 of that sum).
+ * with an online softmax whose exponentials use the hardware's approximate
+ * base-2 exponential (ex2.approx.ftz.f32, flushing subnormal results to
+ * zero); |out - exact| <= 1e-3 * sv * sum_t p_t |dec(v_t,d)| + half a BF16
+ * ulp (the tests also hold 2^-14 of that sum, which covers the error of
+ * the approximate exponential).
  * Lengths are read on the device and clamped to [0, max_seq].
  * Rules: head_dim == 128 and num_q_heads / num_kv_heads in {1, 2} or a
- * multiple of 4 (else W8A8_ERR_UNSUPPORTED); batch * max_seq below
- * 2^31 - 32 (TMA row coordinates; else W8A8_ERR_UNSUPPORTED); q and the
+ * multiple of 4 (else W8A8_ERR_UNSUPPORTED); batch, max_seq and
+ * batch * max_seq below 2^31 - 32 (TMA row coordinates; every over-size
+ * input gives W8A8_ERR_UNSUPPORTED); q and the
  * caches 16-byte aligned, the rest 4-byte aligned.  Each (sequence, KV
  * head) slice of the cache is read once per 8 query heads (4 when the
  * group is not a multiple of 8), through TMA tile loads of 32 tokens; the
@@ -289,6 +294,31 @@ w8a8_status fp8_block_gemm(const uint8_t *xq, const float *xs,
                            const uint8_t *wq, const float *ws,
                            uint16_t *y_bf16, int64_t m, int64_t n, int64_t k,
                            w8a8_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * fp8_block_gemm_ex -- fp8_block_gemm with option flags; the same result
+ * (bit for bit) for every flag value.  flags = 0 is fp8_block_gemm.
+ *
+ *   W8A8_GEMM_STATIC_WEIGHTS: the caller states that wq and ws are not
+ *     written by the kernel enqueued just before this call on `stream`
+ *     (nor by anything that kernel may still overlap) -- as holds for a
+ *     rollout's decode linears, whose weights change only at weight sync.
+ *     For m <= 256 the GEMM then starts reading its first weight slabs
+ *     while that previous kernel is finishing (programmatic dependent
+ *     launch); activations and scales of the tokens are read only after it
+ *     has completed.  Ignored for m > 256.
+ * Other flag bits give W8A8_ERR_UNSUPPORTED.
+ *
+ * Every call with m <= 256 (and k <= 32768) is launched as a programmatic
+ * dependent of the previous kernel on the stream: its prologue (barrier
+ * set-up, tensor-memory allocation) may overlap that kernel's end, and, with
+ * the flag, so may its first weight reads.
+ * ---------------------------------------------------------------------- */
+#define W8A8_GEMM_STATIC_WEIGHTS 1u
+w8a8_status fp8_block_gemm_ex(const uint8_t *xq, const float *xs,
+                              const uint8_t *wq, const float *ws,
+                              uint16_t *y_bf16, int64_t m, int64_t n,
+                              int64_t k, uint32_t flags, w8a8_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * fp8_grouped_gemm -- the MoE expert layers of [FP8-RL] section 1 (expert

@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_status_strings_and_version(L):
-    assert L.w8a8_version() == 100
+    assert L.w8a8_version() == 200
     for s in range(6):
         assert L.w8a8_status_string(s)
     assert L.w8a8_status_string(0) == b"ok"
@@ -132,6 +132,8 @@ def test_attention_argument_checks(L):
     assert a(A, A, A, A, A, A, A, 2, 64, 8, 2, 128, sc, A + 2, None) == ALIGN
     # TMA row coordinates are 32-bit: batch * max_seq must stay below 2^31 - 32
     assert a(A, A, A, A, A, A, A, 1 << 16, 1 << 15, 8, 2, 128, sc, A, None) == UNSUP
+    assert a(A, A, A, A, A, A, A, 1 << 31, 1, 8, 2, 128, sc, A, None) == UNSUP
+    assert a(A, A, A, A, A, A, A, 1, 1 << 31, 8, 2, 128, sc, A, None) == UNSUP
 
 
 def test_gemm_argument_checks(L):
@@ -146,6 +148,11 @@ def test_gemm_argument_checks(L):
     assert g(A, A, A, A, A + 8, 128, 256, 128, None) == ALIGN
     assert g(None, None, None, None, None, 0, 256, 128, None) == OK
     assert g(A, A, A, A, A, 1 << 31, 256, 128, None) == SHAPE
+    ge = L.fp8_block_gemm_ex
+    assert ge(A, A, A, A, A, 128, 256, 100, 0, None) == SHAPE
+    assert ge(A, A, A, A, A + 8, 64, 256, 128, 1, None) == ALIGN
+    assert ge(A, A, A, A, A, 64, 256, 128, 2, None) == UNSUP  # unknown flag bit
+    assert ge(None, None, None, None, None, 0, 256, 128, 1, None) == OK
     gg = L.fp8_grouped_gemm
     assert gg(A, A, 10, None, A, 2, 11, A, A, A, 256, 128, None) == SHAPE  # identity reads past rows_x
     assert gg(A, A, 10, None, None, 2, 10, A, A, A, 256, 128, None) == NULL

@@ -33,7 +33,14 @@ def _cdiv(a, b):
 
 
 GEMM_SHAPES = [(1, 16, 128), (3, 136, 256), (128, 256, 512), (200, 512, 384), (257, 264, 1024),
-               (64, 256, 144), (130, 520, 256), (1, 8, 16), (256, 1024, 4096), (129, 768, 12288)]
+               (64, 256, 144), (130, 520, 256), (1, 8, 16), (256, 1024, 4096), (129, 768, 12288),
+               # m <= 256 runs the weight-streaming kernel: token paddings 32/64/128/256,
+               # K splits of 1..8 (one 128-row tile over 32 slabs splits 8 ways), ragged
+               # N tiles and a partial last K slab
+               (32, 128, 4096), (33, 256, 1024), (65, 384, 2048), (255, 136, 12288),
+               (17, 1160, 400), (96, 128, 256),
+               # few rows but K past the weight-streaming kernel's reach: the general kernel
+               (3, 128, 32896)]
 
 
 @pytest.mark.parametrize("m,n,k", GEMM_SHAPES)
@@ -45,6 +52,46 @@ def test_block_gemm_small(W, m, n, k):
     assert W.consume_device_error() == 0
     y_ref, absref = O.block_gemm(xq, xs, wq, ws)
     assert_gemm_close(bits16(y), y_ref, absref, f"gemm {m}x{n}x{k}")
+
+
+@pytest.mark.parametrize("m,n,k", [sh for sh in GEMM_SHAPES if sh[0] <= 256])
+def test_block_gemm_static_weights_same_bits(W, m, n, k):
+    """The static-weights flag changes when the weights are read, not what
+    is computed: the same bits as without it."""
+    xq, wq = _codes((m, k), m + k), _codes((n, k), n + 7 * k)
+    xs, ws = _scales((m, _cdiv(k, 128)), 1), _scales((_cdiv(n, 128), _cdiv(k, 128)), 2)
+    args = (_dev(xq), _dev(xs), _dev(wq), _dev(ws))
+    y0 = W.fp8_block_gemm(*args)
+    y1 = W.fp8_block_gemm(*args, static_weights=True)
+    torch.cuda.synchronize()
+    assert W.consume_device_error() == 0
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+
+
+@pytest.mark.parametrize("m", [1, 64, 200])
+def test_decode_chain_static_weights(W, m):
+    """A chain of dependent linears on one stream, as in a decode step:
+    each GEMM's BF16 output is quantized (1x128) and feeds the next GEMM.
+    With static weights each GEMM may start streaming its weights while the
+    previous kernel runs, but must read its activations only after it: the
+    chain's result is bit-identical to the one without the flag."""
+    dims = [1024, 2048, 1024, 3072, 1024, 1024]
+    ws_ = [W.quantize_weight_blockwise(synth.weights(dims[i + 1], dims[i], seed=70 + i).cuda())
+           for i in range(len(dims) - 1)]
+    x0 = synth.activations(m, dims[0], seed=69).cuda()
+
+    def chain(static):
+        x = x0
+        for wq, wsc in ws_:
+            xq, xs = W.quantize_act_per_token_group(x)
+            x = W.fp8_block_gemm(xq, xs, wq, wsc, static_weights=static)
+        return x
+
+    ya = chain(False)
+    yb = chain(True)
+    torch.cuda.synchronize()
+    assert W.consume_device_error() == 0
+    assert torch.equal(ya.view(torch.int16), yb.view(torch.int16))
 
 
 def test_block_gemm_empty_and_k0(W):
@@ -106,7 +153,7 @@ def test_scale_power_of_two_is_exact(W):
     assert torch.equal(y1.float() * 4, y2.float())
 
 
-@pytest.mark.parametrize("m", [64, 256, 8192])
+@pytest.mark.parametrize("m", [1, 64, 128, 256, 8192])
 def test_block_gemm_qwen3_8b_shapes_sampled(W, m):
     """The four Qwen3-8B linears at M tokens, full size, checked on sampled
     entries: every tile corner of a tile row plus random positions."""

@@ -20,6 +20,7 @@ __all__ = [
     "quantize_act_per_token_group_gather", "dequantize_blockwise", "quant_error_report",
     "sqnr_db", "fp8_decode_attention", "fp8_block_gemm",
     "fp8_grouped_gemm", "kv_amax_quantize", "w8a8_linear", "consume_device_error",
+    "GEMM_STATIC_WEIGHTS",
     "KV_AMAX_AND_QUANT", "KV_AMAX_ONLY", "KV_QUANT_ONLY", "LIB_PATH",
 ]
 
@@ -61,6 +62,7 @@ _SIGNATURES = {
     "fp8_decode_attention": (_INT, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _I32,
                                     ctypes.c_float, _P, _P]),
     "fp8_block_gemm": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "fp8_block_gemm_ex": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_uint32, _P]),
     "fp8_grouped_gemm": (_INT, [_P, _P, _I64, _P, _P, _I32, _I64, _P, _P, _P, _I64, _I64, _P]),
     "kv_amax_quantize": (_INT, [_P, _I64, _P, _P, _P, _INT, _P]),
 }
@@ -248,15 +250,26 @@ def fp8_decode_attention(q, q_scale, k_cache, k_scale, v_cache, v_scale, seq_len
 
 # ------------------------------------------------------------------ GEMMs
 
-def fp8_block_gemm(xq, xs, wq, ws, y=None, stream=None):
-    """Y = X W^T with blockwise FP32 scales; returns BF16 [m, n]."""
+GEMM_STATIC_WEIGHTS = 1
+
+
+def fp8_block_gemm(xq, xs, wq, ws, y=None, stream=None, static_weights=False):
+    """Y = X W^T with blockwise FP32 scales; returns BF16 [m, n].
+    static_weights: the caller states that wq and ws are not written by the
+    kernel enqueued just before on the stream (fp8_block_gemm_ex's
+    W8A8_GEMM_STATIC_WEIGHTS); the result is the same either way."""
     _need(xq, torch.uint8, "xq")
     _need(wq, torch.uint8, "wq")
     m, k = xq.shape
     n = wq.shape[0]
     y = torch.empty((m, n), dtype=torch.bfloat16, device=xq.device) if y is None else y
-    _check("fp8_block_gemm", lib().fp8_block_gemm(_ptr(xq), _ptr(xs), _ptr(wq), _ptr(ws), _ptr(y),
-                                                  m, n, k, _stream(stream)))
+    if static_weights:
+        _check("fp8_block_gemm_ex",
+               lib().fp8_block_gemm_ex(_ptr(xq), _ptr(xs), _ptr(wq), _ptr(ws), _ptr(y), m, n, k,
+                                       GEMM_STATIC_WEIGHTS, _stream(stream)))
+    else:
+        _check("fp8_block_gemm", lib().fp8_block_gemm(_ptr(xq), _ptr(xs), _ptr(wq), _ptr(ws),
+                                                      _ptr(y), m, n, k, _stream(stream)))
     return y
 
 

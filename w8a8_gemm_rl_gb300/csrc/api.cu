@@ -11,6 +11,7 @@
 
 namespace w8a8 {
 cudaError_t consume_device_error(int* code);
+cudaError_t consume_small_gemm_error(int* code);
 cudaError_t consume_quant_error(int* code);
 cudaError_t consume_attention_error(int* code);
 int grouped_gemm_max_groups();
@@ -48,7 +49,7 @@ W8A8_API const char* w8a8_status_string(w8a8_status status) {
   return "unknown status";
 }
 
-W8A8_API int w8a8_version(void) { return 100; }
+W8A8_API int w8a8_version(void) { return 200; }
 
 W8A8_API const char* w8a8_last_cuda_error(void) { return g_last_cuda_error; }
 
@@ -210,7 +211,8 @@ W8A8_API w8a8_status fp8_decode_attention(const uint8_t* q, const float* q_scale
   if (num_q_heads % num_kv_heads != 0) return W8A8_ERR_SHAPE;
   const int32_t g = num_q_heads / num_kv_heads;
   if (head_dim != 128 || !(g == 1 || g == 2 || g % 4 == 0)) return W8A8_ERR_UNSUPPORTED;
-  if (max_seq >= kMaxDim || batch >= kMaxDim) return W8A8_ERR_SHAPE;
+  // over-size inputs (TMA row coordinates are 32-bit) share one status
+  if (max_seq >= kMaxDim || batch >= kMaxDim) return W8A8_ERR_UNSUPPORTED;
   if (batch == 0) return W8A8_OK;
   if (batch * max_seq > kMaxDim - 1 - 32) return W8A8_ERR_UNSUPPORTED;
   if (!q || !q_scale || !k_cache || !k_scale || !v_cache || !v_scale || !seq_lens || !out_bf16)
@@ -238,14 +240,25 @@ static w8a8_status check_gemm_common(const uint8_t* xq, const float* xs, const u
   return W8A8_OK;
 }
 
-W8A8_API w8a8_status fp8_block_gemm(const uint8_t* xq, const float* xs, const uint8_t* wq,
-                                    const float* ws, uint16_t* y_bf16, int64_t m, int64_t n,
-                                    int64_t k, w8a8_stream_t stream) {
+W8A8_API w8a8_status fp8_block_gemm_ex(const uint8_t* xq, const float* xs, const uint8_t* wq,
+                                       const float* ws, uint16_t* y_bf16, int64_t m, int64_t n,
+                                       int64_t k, uint32_t flags, w8a8_stream_t stream) {
   if (m < 0 || n < 0 || k < 0 || m >= kMaxDim) return W8A8_ERR_SHAPE;
+  if ((flags & ~(uint32_t)W8A8_GEMM_STATIC_WEIGHTS) != 0) return W8A8_ERR_UNSUPPORTED;
   if (m == 0 || n == 0) return (k % 16 == 0 && n % 8 == 0) ? W8A8_OK : W8A8_ERR_SHAPE;
   w8a8_status st = check_gemm_common(xq, xs, wq, ws, y_bf16, n, k);
   if (st != W8A8_OK) return st;
+  // few rows (decode-sized batches): the weight-streaming kernel
+  if (w8a8::block_gemm_small_m_serves(m, k))
+    return from_cuda(w8a8::launch_block_gemm_small_m(
+        xq, xs, wq, ws, y_bf16, m, n, k, (flags & W8A8_GEMM_STATIC_WEIGHTS) != 0, cs(stream)));
   return from_cuda(w8a8::launch_block_gemm(xq, xs, wq, ws, y_bf16, m, n, k, cs(stream)));
+}
+
+W8A8_API w8a8_status fp8_block_gemm(const uint8_t* xq, const float* xs, const uint8_t* wq,
+                                    const float* ws, uint16_t* y_bf16, int64_t m, int64_t n,
+                                    int64_t k, w8a8_stream_t stream) {
+  return fp8_block_gemm_ex(xq, xs, wq, ws, y_bf16, m, n, k, 0u, stream);
 }
 
 W8A8_API w8a8_status fp8_grouped_gemm(const uint8_t* xq, const float* xs, int64_t rows_x,
@@ -290,9 +303,12 @@ W8A8_API w8a8_status kv_amax_quantize(const uint16_t* x_bf16, int64_t numel, uin
 
 W8A8_API w8a8_status w8a8_consume_device_error(int* code) {
   if (!code) return W8A8_ERR_NULL;
-  int g = 0, q = 0, a = 0;
+  int g = 0, sg = 0, q = 0, a = 0;
   w8a8_status st = from_cuda(w8a8::consume_device_error(&g));
   if (st != W8A8_OK) return st;
+  st = from_cuda(w8a8::consume_small_gemm_error(&sg));
+  if (st != W8A8_OK) return st;
+  if (g == 0) g = sg;
   st = from_cuda(w8a8::consume_quant_error(&q));
   if (st != W8A8_OK) return st;
   st = from_cuda(w8a8::consume_attention_error(&a));

@@ -11,7 +11,7 @@
 // tensor memory and promoted into FP32 registers with its scale.
 //
 // Kernel structure (persistent, one CTA per SM, warp-specialized):
-//   warp 0      producer: TMA of the A and B K-slabs into a 4-stage
+//   warp 0      producer: TMA of the A and B K-slabs into a 3-stage
 //               shared-memory ring (for routed MoE rows, B by TMA and A rows
 //               0-63 by a cp.async gather);
 //   warp 1      allocates 512 TMEM columns; lane 0 issues 4 x
@@ -24,7 +24,7 @@
 //               FP32 registers (128 per thread), release the TMEM buffer,
 //               and after the last slab round to BF16 and store.
 // With two TMEM buffers the MMA of slab kb+1 overlaps the promotion of slab
-// kb.  Tiles are 128 x 256; tiles are visited in groups of 16 M-tiles so the
+// kb.  Tiles are 128 x 256; tiles are visited in groups of 8 M-tiles so the
 // CTAs running at once share A and B tiles through L2.
 //
 // Every mbarrier wait is bounded (2 s of wall time).  A wait that gives up
@@ -45,7 +45,7 @@ namespace gemm {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 128;  // FP8 elements = bytes = one 128-byte swizzle row
-constexpr int STAGES = 4;
+constexpr int STAGES = 3;
 constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;

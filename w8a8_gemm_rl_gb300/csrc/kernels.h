@@ -55,6 +55,15 @@ cudaError_t launch_block_gemm(const uint8_t* xq, const float* xs, const uint8_t*
                               const float* ws, uint16_t* y, int64_t m, int64_t n, int64_t k,
                               cudaStream_t st);
 
+// The same GEMM for m <= 256 rows (gemm_small_m.cu): weights streamed once
+// by every SM, K split over a thread-block cluster.  static_weights: wq and
+// ws may be read while the previous kernel on the stream is still running.
+cudaError_t launch_block_gemm_small_m(const uint8_t* xq, const float* xs, const uint8_t* wq,
+                                      const float* ws, uint16_t* y, int64_t m, int64_t n,
+                                      int64_t k, bool static_weights, cudaStream_t st);
+// Whether the kernel above serves m rows of depth k (m <= 256, k <= 32768).
+bool block_gemm_small_m_serves(int64_t m, int64_t k);
+
 cudaError_t launch_grouped_gemm(const uint8_t* xq, const float* xs, int64_t rows_x,
                                 const int32_t* row_idx, const int32_t* group_offsets, int32_t g,
                                 int64_t total_rows, const uint8_t* wq, const float* ws,
