@@ -341,72 +341,147 @@ def job_value(ms_total_local, steps, roof_step_s, world):
     return ms_total, ms_step, value
 
 
-def cpu_baseline_oracle(budget_s=12.0):
-    """The CPU oracle, as it stands, on a bounded sample of the same step's
-    phases; returns the same metric (roofline % of one GB300) and details."""
+# ------------------------------------------------------------ CPU baseline
+#
+# The CPU oracle as it stands, on a fixed, bounded sample of the step's
+# phases.  The sample is a number of identical-sized units; a unit holds a
+# strip of each phase's work (below), and the units are spread over one
+# process per host core (spawned, so no process is forked after the GPU is
+# in use).  The same sample is timed by --impl reference.
+
+CPU_UNIT_PARTS = (
+    "weight quant 256x4096 (o projection strip)",
+    "act quant 256x4096",
+    "dense GEMM 1024 outputs of the qkv linear (K=4096)",
+    "grouped GEMM 512 outputs of the MoE gate_up (K=2048)",
+    "KV amax + quant 262144 elements",
+)
+_CPU_UNIT = None
+
+
+def _cpu_unit_init():
+    """Inputs of the CPU sample's units, generated once per process."""
+    global _CPU_UNIT
     import oracle as O
     from w8a8_gemm_rl_gb300 import synth
+    O.lib()
+    w = synth.bf16_bits(synth.weights(4096, 4096, seed=1))
+    x = synth.bf16_bits(synth.activations(1024, 4096, seed=2))
+    xq, xs = O.quantize_act_per_token_group(x[:64])
+    wq, ws = O.quantize_weight_blockwise(w[:256])
+    gx = synth.bf16_bits(synth.activations(64, 2048, seed=4))
+    gw = synth.bf16_bits(synth.weights(256, 2048, seed=5))
+    gxq, gxs = O.quantize_act_per_token_group(gx)
+    gwq, gws = O.quantize_weight_blockwise(gw)
+    kv = synth.bf16_bits(synth.kv_cache(seed=3, shape=(1, 256, 8, 128)))
+    _CPU_UNIT = dict(w=w, x=x, g=(xq, xs, wq, ws), gg=(gxq, gxs, gwq, gws), kv=kv)
+
+
+def _cpu_unit_run(i):
+    """One unit of the CPU sample (index i picks the strips); returns its
+    wall time in seconds."""
+    import oracle as O
+    if _CPU_UNIT is None:
+        _cpu_unit_init()
+    u = _CPU_UNIT
+    rng = np.random.default_rng(i)
+    t0 = time.perf_counter()
+    r = 256 * (i % 16)
+    O.quantize_weight_blockwise(u["w"][r:r + 256])
+    r = 256 * (i % 4)
+    O.quantize_act_per_token_group(u["x"][r:r + 256])
+    O.block_gemm_entries(*u["g"], rng.integers(0, 64, 1024), rng.integers(0, 256, 1024))
+    O.block_gemm_entries(*u["gg"], rng.integers(0, 64, 512), rng.integers(0, 256, 512))
+    O.kv_amax_quantize(u["kv"])
+    return time.perf_counter() - t0
+
+
+def cpu_unit_roofline_s(peaks):
+    """GB300 roofline time of one unit's work (same accounting as the step)."""
+    return (t_roof(0, 3 * 256 * 4096 + 4 * 2 * 32, peaks)
+            + t_roof(0, 3 * 256 * 4096 + 4 * 256 * 32, peaks)
+            + t_roof(2 * 1024 * 4096, 0, peaks)
+            + t_roof(2 * 512 * 2048, 0, peaks)
+            + t_roof(0, 5 * 256 * 8 * 128, peaks))
+
+
+def host_cpu_info():
+    """(logical cores usable by this process, CPU model string)."""
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        cores = os.cpu_count() or 1
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for ln in f:
+                    if ln.lower().startswith("model name"):
+                        model = ln.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    if model is None:
+        import platform
+        model = platform.machine()
+    return cores, model
+
+
+class CpuSample:
+    """The CPU oracle on a fixed sample of `units_per_core` units per host
+    core, timed on all cores (one spawned process each) and on one core."""
+
+    def __init__(self, units_per_core=4):
+        import multiprocessing as mp
+        self.cores, self.model = host_cpu_info()
+        self.units = units_per_core * self.cores
+        self.pool = mp.get_context("spawn").Pool(self.cores, initializer=_cpu_unit_init)
+        # every worker has built its inputs before anything is timed
+        self.pool.map(_cpu_unit_run, range(self.cores), chunksize=1)
+        _cpu_unit_init()
+
+    def run_all_cores(self):
+        t0 = time.perf_counter()
+        self.pool.map(_cpu_unit_run, range(self.units), chunksize=1)
+        return time.perf_counter() - t0
+
+    def run_one_core(self, units=2):
+        return sum(_cpu_unit_run(i) for i in range(units)) / units
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+    def describe(self):
+        return (f"{self.units} units ({self.cores} cores x {self.units // self.cores}); "
+                f"a unit = " + "; ".join(CPU_UNIT_PARTS))
+
+
+def cpu_baseline_oracle(reps=1):
+    """The CPU oracle on the fixed sample: percent of one GB300's roofline
+    that the host's cores reach, with the single-core figure beside it."""
     peaks = load_peaks()
-    done_roof = 0.0
-    t_used = 0.0
-    parts = []
-    rng = np.random.default_rng(0)
-    per = budget_s / 4
-    # weight quant sample: 128-row strips of the o projection
-    t0 = time.perf_counter()
-    w = synth.weights(4096, 4096, seed=1)
-    wb = synth.bf16_bits(w)
-    rows = 0
-    t0 = time.perf_counter()
-    while time.perf_counter() - t0 < per and rows < 4096:
-        O.quantize_weight_blockwise(wb[rows:rows + 128])
-        rows += 128
-    dt = time.perf_counter() - t0
-    nb = 3 * rows * 4096 + 4 * (rows // 128) * 32
-    done_roof += t_roof(0, nb, peaks)
-    t_used += dt
-    parts.append(f"weight quant {rows}x4096")
-    # act quant sample: rows of an [8192, 4096] activation
-    x = synth.activations(1024, 4096, seed=2)
-    xb = synth.bf16_bits(x)
-    r = 0
-    t0 = time.perf_counter()
-    while time.perf_counter() - t0 < per / 2 and r < 1024:
-        O.quantize_act_per_token_group(xb[r:r + 64])
-        r += 64
-    dt = time.perf_counter() - t0
-    done_roof += t_roof(0, r * 4096 * 3 + 4 * r * 32, peaks)
-    t_used += dt
-    parts.append(f"act quant {r}x4096")
-    # GEMM sample: entries of the qkv linear at M=8192 (K=4096)
-    xq, xs = O.quantize_act_per_token_group(xb[:64])
-    wq, ws = O.quantize_weight_blockwise(wb[:256])
-    cnt = 0
-    t0 = time.perf_counter()
-    while time.perf_counter() - t0 < per:
-        ii = rng.integers(0, 64, 256)
-        jj = rng.integers(0, 256, 256)
-        O.block_gemm_entries(xq, xs, wq, ws, ii, jj)
-        cnt += 256
-    dt = time.perf_counter() - t0
-    done_roof += t_roof(2 * cnt * 4096, 0, peaks)
-    t_used += dt
-    parts.append(f"gemm {cnt} outputs of K=4096")
-    # KV sample: amax + code of a slice
-    kv = synth.kv_cache(seed=3, shape=(1, 1024, 8, 128))
-    kb = synth.bf16_bits(kv)
-    t0 = time.perf_counter()
-    reps = 0
-    while time.perf_counter() - t0 < per / 2:
-        O.kv_amax_quantize(kb)
-        reps += 1
-    dt = time.perf_counter() - t0
-    done_roof += t_roof(0, reps * 5 * kb.size, peaks)
-    t_used += dt
-    parts.append(f"kv {reps}x{kb.size} elements")
-    value = 100.0 * done_roof / t_used
-    return value, {"kind": "oracle", "cores": 1, "seconds": round(t_used, 2),
-                   "sample": "; ".join(parts) + " (single-threaded C oracle, same phases as the step)"}
+    smp = CpuSample()
+    try:
+        unit_roof = cpu_unit_roofline_s(peaks)
+        wall = min(smp.run_all_cores() for _ in range(reps))
+        one = smp.run_one_core()
+    finally:
+        smp.close()
+    value = 100.0 * smp.units * unit_roof / wall
+    info = {"kind": "oracle", "cores": smp.cores, "cpu_model": smp.model,
+            "seconds": round(wall, 2), "cpu_seconds": round(wall * smp.cores, 1),
+            "value_1core": round(100.0 * unit_roof / one, 6),
+            "sample": smp.describe() + " (C oracle as it stands, one process per core)"}
+    return value, info
 
 
 def bench_ours(args):
@@ -691,21 +766,26 @@ def measure_e2e(W, wl, args, roof_step, world, chunks=8, in_streams=1):
 # -------------------------------------------------------- reference arm
 
 def bench_reference(args):
-    """The oracle timed on the host cores, on a bounded sample of the same
-    workload per step (the reference arm of this metric)."""
+    """The oracle timed on the host cores, on the same fixed sample as
+    cpu_baseline per step (the reference arm of this metric)."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    vals = []
-    for _ in range(args.warmup):
-        cpu_baseline_oracle(budget_s=2.0)
-    t0 = time.perf_counter()
-    info = None
-    for _ in range(args.steps):
-        v, info = cpu_baseline_oracle(budget_s=8.0)
-        vals.append(v)
-    wall = time.perf_counter() - t0
-    value = float(np.mean(vals))
+    peaks = load_peaks()
+    smp = CpuSample()
+    try:
+        unit_roof = cpu_unit_roofline_s(peaks)
+        for _ in range(args.warmup):
+            smp.run_all_cores()
+        walls = [smp.run_all_cores() for _ in range(args.steps)]
+        one = smp.run_one_core()
+    finally:
+        smp.close()
+    wall = float(np.sum(walls))
+    value = 100.0 * smp.units * unit_roof * len(walls) / wall
+    info = {"kind": "oracle", "cores": smp.cores, "cpu_model": smp.model,
+            "value_1core": round(100.0 * unit_roof / one, 6),
+            "sample": smp.describe() + " (C oracle as it stands, one process per core)"}
     out = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": UNIT,
            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(1000 * wall / max(args.steps, 1), 1), "higher_is_better": True,
