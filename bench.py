@@ -14,7 +14,13 @@ input, with all inputs resident in HBM:
      gather fused into the quantizer), grouped gate_up GEMM, quantization of
      the [32768, 768] down input, grouped down GEMM;
   4. KV-cache recalibration: per-tensor amax + E4M3 quantization of K and V,
-     each [32, 8192, 8, 128].
+     each [32, 8192, 8, 128];
+  5. decode-sized Qwen3-8B linears at M = 64 and at M = 256 tokens: for each
+     of the 36 layers and each of its 4 linears, 1x128 activation
+     quantization then the blockwise FP8 GEMM with the layer's weights from
+     step 1 (6.3 GB of FP8 weights per pass, so every pass streams them from
+     HBM); each pass is one CUDA-graph replay of its 288 launches, the GEMMs
+     marked as reading static weights.
 
 Metric: each phase is measured against its roofline time
 t_roof = max(flops / peak_fp8, bytes / peak_hbm) with algorithmic bytes and
@@ -42,12 +48,15 @@ METRIC = "blockwise-FP8 GEMM TFLOP/s and FP8 quantize GB/s, as % of GB300 roofli
 UNIT = "% of GB300 roofline (sum over GPUs)"
 WORKLOAD = ("qwen3-8b weight sync (36 layers, 128x128 blockwise E4M3) + qwen3-8b W8A8 linears "
             "at M=8192 + qwen3-30b-a3b MoE layer (4096 tok, 128 experts, top-8) + FP8 KV "
-            "recalibration K,V [32,8192,8,128]")
+            "recalibration K,V [32,8192,8,128] + qwen3-8b W8A8 decode linears at M=64 and "
+            "M=256 over all 36 layers")
+DECODE_MS = (64, 256)
 
 # ------------------------------------------------------------------ peaks
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0  # nominal dense ratio, 4.5 / 2.25 PFLOP/s
+NOMINAL_FP8_TFLOPS = 4500.0
 
 
 def load_peaks():
@@ -101,12 +110,26 @@ def work_model():
     # 4. KV recalibration: amax pass (2 B/elem) then code pass (2 + 1 B/elem), K and V
     kv = int(np.prod(synth.KV_SHAPE))
     ph.append(("kv_quant", 0, 2 * 5 * kv))
+    # 5. decode linears: every layer's 4 linears at M tokens, act quant + GEMM
+    for M in DECODE_MS:
+        f = b = 0
+        for n, k in synth.QWEN3_8B_LINEARS.values():
+            f += 2 * M * n * k
+            b += 3 * M * k + 4 * M * cdiv(k, 128)  # act quant
+            b += M * k + n * k + 4 * (M * cdiv(k, 128) + cdiv(n, 128) * cdiv(k, 128)) + 2 * M * n
+        ph.append((f"decode_m{M}", f * synth.QWEN3_8B_LAYERS, b * synth.QWEN3_8B_LAYERS))
     return ph
 
 
-def t_roof(flops, nbytes, peaks, sustained=True):
-    fp8 = FP8_OVER_BF16 * (peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]) * 1e12
-    return max(flops / fp8, nbytes / (peaks["hbm_gbs"] * 1e9))
+def fp8_peak_tflops(peaks):
+    """Dense FP8 tensor peak: the measured BF16 burst peak (a cuBLAS GEMM
+    timed alone) x the nominal FP8/BF16 ratio.  The step is milliseconds
+    long, so the burst figure applies rather than the sustained one."""
+    return FP8_OVER_BF16 * peaks["bf16_tflops"]
+
+
+def t_roof(flops, nbytes, peaks):
+    return max(flops / (fp8_peak_tflops(peaks) * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9))
 
 
 # ---------------------------------------------------------------- clocks
@@ -127,7 +150,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "25"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -222,11 +245,47 @@ class Workload:
         self.kv_q = [torch.empty(t.shape, dtype=torch.uint8, device=dev) for t in self.kv]
         self.kv_s = [torch.empty(1, dtype=torch.float32, device=dev) for _ in self.kv]
         self.kv_a = [torch.empty(1, dtype=torch.float32, device=dev) for _ in self.kv]
+        # decode linears: one activation per (M, linear), shared by the layers
+        self.dec = {}
+        for M in DECODE_MS:
+            rows = []
+            for j, (n, k) in enumerate(synth.QWEN3_8B_LINEARS.values()):
+                rows.append(dict(x=synth.activations(M, k, seed=S + 80 + 10 * j + M, device=dev),
+                                 xq=torch.empty((M, k), dtype=torch.uint8, device=dev),
+                                 xs=torch.empty((M, cdiv(k, 128)), dtype=torch.float32, device=dev),
+                                 y=torch.empty((M, n), dtype=torch.bfloat16, device=dev)))
+            self.dec[M] = rows
+        self.graphs = {}
+        torch.cuda.synchronize()
+
+    def decode_pass(self, W, M):
+        """All 36 layers' 4 linears at M tokens: act quant, then the GEMM."""
+        nlin = len(self.synth.QWEN3_8B_LINEARS)
+        for l in range(self.synth.QWEN3_8B_LAYERS):
+            for j, d in enumerate(self.dec[M]):
+                wq, ws = self.wout[nlin * l + j]
+                W.quantize_act_per_token_group(d["x"], d["xq"], d["xs"])
+                W.fp8_block_gemm(d["xq"], d["xs"], wq, ws, d["y"], static_weights=True)
+
+    def capture_decode(self, W):
+        """One CUDA graph per decode pass (captured once, replayed per step)."""
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for M in DECODE_MS:
+                self.decode_pass(W, M)
+            torch.cuda.synchronize()
+            for M in DECODE_MS:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=side):
+                    self.decode_pass(W, M)
+                self.graphs[M] = g
+        torch.cuda.current_stream().wait_stream(side)
         torch.cuda.synchronize()
 
     def input_tensors(self):
         return ([*self.w] + [d["x"] for d in self.lin] + [self.moe_x, self.moe_d, self.row_idx, self.off]
-                + list(self.kv))
+                + list(self.kv) + [d["x"] for M in DECODE_MS for d in self.dec[M]])
 
     def output_tensors(self):
         outs = []
@@ -236,10 +295,13 @@ class Workload:
             outs += [d["y"]]
         outs += [self.y_gu, self.y_dn]
         outs += self.kv_q + self.kv_s + self.kv_a
+        outs += [d["y"] for M in DECODE_MS for d in self.dec[M]]
         return outs
 
 
-LAUNCHES_PER_STEP = 1 + 4 * 2 + 4 + 2 * 2  # weight batch (144 matrices), 4 x (act quant + GEMM), MoE 4, KV 2 x 2
+# weight batch (144 matrices), 4 x (act quant + GEMM), MoE 4, KV 2 x 2, and
+# per decode pass 36 layers x 4 linears x (act quant + GEMM)
+LAUNCHES_PER_STEP = 1 + 4 * 2 + 4 + 2 * 2 + len(DECODE_MS) * 36 * 4 * 2
 
 
 def run_step(W, wl, events=None, skip_weights=False):
@@ -270,10 +332,13 @@ def run_step(W, wl, events=None, skip_weights=False):
     for i in range(2):
         W.kv_amax_quantize(wl.kv[i], wl.kv_q[i], wl.kv_s[i], wl.kv_a[i])
     mark(6)
+    for i, M in enumerate(DECODE_MS):
+        wl.graphs[M].replay()
+        mark(7 + i)
 
 
 PHASE_ORDER = ["weight_quant", "act_quant_linears", "gemm_linears", "act_quant_moe", "grouped_gemm_moe",
-               "kv_quant"]
+               "kv_quant"] + [f"decode_m{M}" for M in DECODE_MS]
 
 
 def dist_setup(n_gpus):
@@ -496,12 +561,15 @@ def bench_ours(args):
     peaks = load_peaks()
     wl = Workload(dev, seed_base=0)
     stream = torch.cuda.current_stream()
+    W.quantize_weight_blockwise_batched(wl.w, wl.wout)  # the decode passes read these codes
+    wl.capture_decode(W)
     for _ in range(args.warmup):
         run_step(W, wl)
     torch.cuda.synchronize()
     assert W.consume_device_error() == 0
     # timed region: K steps, phase events in every step
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(PHASE_ORDER) + 1)]
+          for _ in range(args.steps)]
     clocks = ClockSampler(local)
     clocks.start()
     barrier(world)
@@ -548,9 +616,13 @@ def bench_ours(args):
                 "traffic": weight_quant_traffic(args)}
     gemm_roof = {"kernel": "fp8_gemm_kernel<DENSE> (4 launches, M=8192)", "bound": "tensor",
                  "achieved": round(model["gemm_linears"][0] / (phase_ms["gemm_linears"] * 1e-3) / 1e12, 1),
-                 "peak": round(FP8_OVER_BF16 * peaks["bf16_tflops_sustained"], 1), "unit": "TFLOP/s",
-                 "peak_note": "measured bf16 sustained x 2 (nominal fp8/bf16)"}
+                 "peak": round(fp8_peak_tflops(peaks), 1), "unit": "TFLOP/s",
+                 "peak_note": "measured bf16 burst x 2 (nominal fp8/bf16 ratio)",
+                 "peak_nominal": NOMINAL_FP8_TFLOPS,
+                 "peak_nominal_note": "GB300 dense FP8, vendor figure"}
     gemm_roof["frac"] = round(gemm_roof["achieved"] / gemm_roof["peak"], 4)
+    gemm_roof["frac_nominal"] = round(gemm_roof["achieved"] / NOMINAL_FP8_TFLOPS, 4)
+    decode_gemm = measure_decode_gemm_only(W, wl, peaks)
 
     next_rows = None if args.no_next_rows else measure_next_rows(W, wl, peaks)
     e2e = None
@@ -571,13 +643,63 @@ def bench_ours(args):
         "gemm_tflops": round(g_flops / (g_ms * 1e-3) / 1e12 * world, 1),
         "phases": phases, "roofline": roofline, "gemm_roofline": gemm_roof,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": LAUNCHES_PER_STEP * args.steps,
-        "clocks": clk, "peaks": peaks, "next_rows": next_rows,
+        "clocks": clk, "peaks": peaks, "next_rows": next_rows, "decode_gemm_only": decode_gemm,
     }
     if rank == 0:
         print(json.dumps(out))
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def measure_decode_gemm_only(W, wl, peaks, reps=5):
+    """The decode passes' GEMMs alone (activations quantized once before):
+    one CUDA graph per M of the 144 GEMMs, timed after the timed region, on
+    the GEMMs' own roofline (weight, activation and output bytes)."""
+    from w8a8_gemm_rl_gb300 import synth
+    out = {}
+    nlin = len(synth.QWEN3_8B_LINEARS)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    for M in DECODE_MS:
+        def gemms():
+            for l in range(synth.QWEN3_8B_LAYERS):
+                for j, d in enumerate(wl.dec[M]):
+                    wq, ws = wl.wout[nlin * l + j]
+                    W.fp8_block_gemm(d["xq"], d["xs"], wq, ws, d["y"], static_weights=True)
+        with torch.cuda.stream(side):
+            gemms()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                gemms()
+        torch.cuda.current_stream().wait_stream(side)
+        g.replay()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(reps):
+            g.replay()
+        t1.record()
+        torch.cuda.synchronize()
+        sec = t0.elapsed_time(t1) * 1e-3 / reps
+        per = {}
+        f = b = 0
+        for name, (n, k) in synth.QWEN3_8B_LINEARS.items():
+            fl = 2 * M * n * k
+            by = M * k + n * k + 4 * (M * cdiv(k, 128) + cdiv(n, 128) * cdiv(k, 128)) + 2 * M * n
+            f += fl
+            b += by
+            per[name] = round(1e6 * t_roof(fl, by, peaks), 2)
+        f *= synth.QWEN3_8B_LAYERS
+        b *= synth.QWEN3_8B_LAYERS
+        out[f"m{M}"] = {"workload": f"36 layers x 4 linears at M={M}, one graph of 144 GEMMs",
+                        "ms": round(sec * 1e3, 4), "us_per_gemm": round(sec * 1e6 / 144, 2),
+                        "pct_roofline": round(100 * t_roof(f, b, peaks) / sec, 2),
+                        "gbs": round(b / sec / 1e9, 1), "roofline_us_per_linear": per}
+    assert W.consume_device_error() == 0
+    return out
 
 
 def measure_next_rows(W, wl, peaks, reps=3):

@@ -59,10 +59,25 @@ def test_kv_recalibration_bytes():
     assert flops == 0 and nbytes == 2 * 5 * n
 
 
+def test_decode_passes():
+    # every layer's 4 linears at M tokens: the GEMM's codes, scale grids and
+    # BF16 output, plus the activation quantizer's 3 B per element and scales
+    shapes = [(6144, 4096), (4096, 4096), (24576, 4096), (4096, 12288)]
+    for M in bench.DECODE_MS:
+        flops, nbytes = phases()[f"decode_m{M}"]
+        assert flops == 36 * sum(2 * M * n * k for n, k in shapes)
+        want = 36 * sum(M * k + n * k + 4 * (M * (k // 128) + (n // 128) * (k // 128)) + 2 * M * n
+                        + 3 * M * k + 4 * M * (k // 128) for n, k in shapes)
+        assert nbytes == want
+        # the weights dominate: 36 x 176 MB of FP8 codes per pass
+        assert 36 * sum(n * k for n, k in shapes) == 6_945_767_424
+
+
 def test_roofline_time_takes_the_binding_resource():
     peaks = {"hbm_gbs": 1000.0, "bf16_tflops": 500.0, "bf16_tflops_sustained": 400.0}
-    # 1 GB at 1 TB/s = 1 ms; 1 TFLOP at 2 x 400 TF/s = 1.25 ms
+    # 1 GB at 1 TB/s = 1 ms; 1 TFLOP at 2 x 500 TF/s (the burst figure) = 1 ms;
+    # 2 TFLOP = 2 ms
     assert bench.t_roof(0, 1e9, peaks) == pytest.approx(1e-3)
-    assert bench.t_roof(1e12, 1e9, peaks) == pytest.approx(1e12 / (bench.FP8_OVER_BF16 * 400e12))
-    assert bench.t_roof(1e12, 1e9, peaks, sustained=False) == pytest.approx(
-        max(1e-3, 1e12 / (bench.FP8_OVER_BF16 * 500e12)))
+    assert bench.t_roof(2e12, 1e9, peaks) == pytest.approx(2e12 / (bench.FP8_OVER_BF16 * 500e12))
+    assert bench.t_roof(1e11, 1e9, peaks) == pytest.approx(1e-3)
+    assert bench.fp8_peak_tflops(peaks) == pytest.approx(1000.0)

@@ -249,7 +249,7 @@ W8A8_API w8a8_status fp8_block_gemm_ex(const uint8_t* xq, const float* xs, const
   w8a8_status st = check_gemm_common(xq, xs, wq, ws, y_bf16, n, k);
   if (st != W8A8_OK) return st;
   // few rows (decode-sized batches): the weight-streaming kernel
-  if (w8a8::block_gemm_small_m_serves(m, k))
+  if (w8a8::block_gemm_small_m_serves(m, n, k))
     return from_cuda(w8a8::launch_block_gemm_small_m(
         xq, xs, wq, ws, y_bf16, m, n, k, (flags & W8A8_GEMM_STATIC_WEIGHTS) != 0, cs(stream)));
   return from_cuda(w8a8::launch_block_gemm(xq, xs, wq, ws, y_bf16, m, n, k, cs(stream)));

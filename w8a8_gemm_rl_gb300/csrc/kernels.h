@@ -61,8 +61,9 @@ cudaError_t launch_block_gemm(const uint8_t* xq, const float* xs, const uint8_t*
 cudaError_t launch_block_gemm_small_m(const uint8_t* xq, const float* xs, const uint8_t* wq,
                                       const float* ws, uint16_t* y, int64_t m, int64_t n,
                                       int64_t k, bool static_weights, cudaStream_t st);
-// Whether the kernel above serves m rows of depth k (m <= 256, k <= 32768).
-bool block_gemm_small_m_serves(int64_t m, int64_t k);
+// Whether the kernel above is the one for an m x n x k product (m <= 256,
+// k <= 32768, and past m = 128 only where the general kernel has few tiles).
+bool block_gemm_small_m_serves(int64_t m, int64_t n, int64_t k);
 
 cudaError_t launch_grouped_gemm(const uint8_t* xq, const float* xs, int64_t rows_x,
                                 const int32_t* row_idx, const int32_t* group_offsets, int32_t g,
