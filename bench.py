@@ -16,11 +16,12 @@ input, with all inputs resident in HBM:
   4. KV-cache recalibration: per-tensor amax + E4M3 quantization of K and V,
      each [32, 8192, 8, 128];
   5. decode-sized Qwen3-8B linears at M = 64 and at M = 256 tokens: for each
-     of the 36 layers and each of its 4 linears, 1x128 activation
-     quantization then the blockwise FP8 GEMM with the layer's weights from
-     step 1 (6.3 GB of FP8 weights per pass, so every pass streams them from
-     HBM); each pass is one CUDA-graph replay of its 288 launches, the GEMMs
-     marked as reading static weights.
+     of the 36 layers and each of its 4 linears, the W8A8 linear from BF16
+     activations (1x128 activation quantization, then the blockwise FP8 GEMM
+     with the layer's weights from step 1, chained as programmatic
+     dependents).  6.3 GB of FP8 weights per pass,
+     so every pass streams them from HBM; each pass is one CUDA-graph replay,
+     the linears marked as reading static weights.
 
 Metric: each phase is measured against its roofline time
 t_roof = max(flops / peak_fp8, bytes / peak_hbm) with algorithmic bytes and
@@ -259,13 +260,14 @@ class Workload:
         torch.cuda.synchronize()
 
     def decode_pass(self, W, M):
-        """All 36 layers' 4 linears at M tokens: act quant, then the GEMM."""
+        """All 36 layers' 4 linears at M tokens, each the W8A8 linear from
+        BF16 activations (w8a8_linear): the activation quantizer, then the
+        GEMM, chained as programmatic dependents."""
         nlin = len(self.synth.QWEN3_8B_LINEARS)
         for l in range(self.synth.QWEN3_8B_LAYERS):
             for j, d in enumerate(self.dec[M]):
                 wq, ws = self.wout[nlin * l + j]
-                W.quantize_act_per_token_group(d["x"], d["xq"], d["xs"])
-                W.fp8_block_gemm(d["xq"], d["xs"], wq, ws, d["y"], static_weights=True)
+                W.w8a8_linear(d["x"], wq, ws, d["y"], d["xq"], d["xs"], static_weights=True)
 
     def capture_decode(self, W):
         """One CUDA graph per decode pass (captured once, replayed per step)."""
@@ -662,6 +664,9 @@ def measure_decode_gemm_only(W, wl, peaks, reps=5):
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     for M in DECODE_MS:
+        for d in wl.dec[M]:
+            W.quantize_act_per_token_group(d["x"], d["xq"], d["xs"])
+
         def gemms():
             for l in range(synth.QWEN3_8B_LAYERS):
                 for j, d in enumerate(wl.dec[M]):
@@ -698,6 +703,33 @@ def measure_decode_gemm_only(W, wl, peaks, reps=5):
                         "ms": round(sec * 1e3, 4), "us_per_gemm": round(sec * 1e6 / 144, 2),
                         "pct_roofline": round(100 * t_roof(f, b, peaks) / sec, 2),
                         "gbs": round(b / sec / 1e9, 1), "roofline_us_per_linear": per}
+        if M <= 128:
+            # the same decode pass with each linear as ONE kernel (the
+            # quantization fused into the GEMM) instead of quantizer + GEMM
+            def single():
+                for l in range(synth.QWEN3_8B_LAYERS):
+                    for j, d in enumerate(wl.dec[M]):
+                        wq, ws = wl.wout[nlin * l + j]
+                        W.w8a8_linear(d["x"], wq, ws, d["y"], static_weights=True, single_kernel=True)
+            with torch.cuda.stream(side):
+                single()
+                torch.cuda.synchronize()
+                g1 = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g1, stream=side):
+                    single()
+            torch.cuda.current_stream().wait_stream(side)
+            g1.replay()
+            torch.cuda.synchronize()
+            t0.record()
+            for _ in range(reps):
+                g1.replay()
+            t1.record()
+            torch.cuda.synchronize()
+            out[f"m{M}"]["single_kernel_linear_ms"] = round(t0.elapsed_time(t1) / reps, 4)
+            out[f"m{M}"]["single_kernel_note"] = (
+                "the decode pass with each linear as one kernel quantizing its own token rows "
+                "(every 128-column weight tile repeats the quantization); the phase runs "
+                "quantizer + GEMM instead")
     assert W.consume_device_error() == 0
     return out
 

@@ -321,6 +321,41 @@ w8a8_status fp8_block_gemm_ex(const uint8_t *xq, const float *xs,
                               int64_t k, uint32_t flags, w8a8_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * w8a8_linear -- the whole W8A8 linear of [FP8-RL] section 1 from BF16
+ * activations: 1 x 128 per-token activation quantization ([NeMo] Table 1,
+ * as quantize_act_per_token_group) followed by fp8_block_gemm.
+ *
+ *   x_bf16 [m, k] BF16 activations; wq [n, k], ws [ceil(n/128),
+ *   ceil(k/128)] the quantized weights; y_bf16 [m, n] (out).
+ *   xq [m, k], xs [m, ceil(k/128)]: the activations' codes and scales (out),
+ *   bit-exact with quantize_act_per_token_group.  Both NULL, or both not.
+ *   flags: W8A8_GEMM_STATIC_WEIGHTS (as fp8_block_gemm_ex) and/or
+ *   W8A8_LINEAR_SINGLE_KERNEL.
+ *
+ * Two ways to run it:
+ *  - one kernel (m <= 128, k <= 32768): the GEMM's token loaders read the
+ *    BF16 rows and quantize them on the way into shared memory, so the codes
+ *    make no round trip through HBM and xq, xs may be NULL.  Every 128
+ *    output columns repeat that quantization, so it is chosen by default
+ *    only for n <= 1024; W8A8_LINEAR_SINGLE_KERNEL asks for it wherever it
+ *    can run.
+ *  - otherwise the activation quantizer, then the GEMM (xq and xs are
+ *    required: the library allocates nothing).  Both are launched as
+ *    programmatic dependents, so the GEMM's set-up (and, with static
+ *    weights, its first weight reads) overlaps the quantizer.
+ * y is within fp8_block_gemm's accuracy of the exact product of the codes.
+ * Rules: as fp8_block_gemm (k % 16 == 0, n % 8 == 0); x_bf16, wq, y_bf16
+ * and xq 16-byte aligned, ws and xs 4-byte aligned; xq and xs both NULL or
+ * both not, and not NULL for the two-kernel way (else W8A8_ERR_NULL).
+ * m == 0 or n == 0 does nothing; k == 0 writes zeros to y.
+ * ---------------------------------------------------------------------- */
+#define W8A8_LINEAR_SINGLE_KERNEL 2u
+w8a8_status w8a8_linear(const uint16_t *x_bf16, int64_t m, int64_t k,
+                        const uint8_t *wq, const float *ws, int64_t n,
+                        uint16_t *y_bf16, uint8_t *xq, float *xs,
+                        uint32_t flags, w8a8_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * fp8_grouped_gemm -- the MoE expert layers of [FP8-RL] section 1 (expert
  * layers are quantized) and section 3 (30B-A3B MoE): fp8_block_gemm per
  * expert over that expert's routed rows.

@@ -148,6 +148,14 @@ def test_gemm_argument_checks(L):
     assert g(A, A, A, A, A + 8, 128, 256, 128, None) == ALIGN
     assert g(None, None, None, None, None, 0, 256, 128, None) == OK
     assert g(A, A, A, A, A, 1 << 31, 256, 128, None) == SHAPE
+    li = L.w8a8_linear
+    assert li(A, 64, 100, A, A, 256, A, None, None, 0, None) == SHAPE   # k % 16
+    assert li(A, 64, 128, A, A, 256, A, A, None, 0, None) == NULL       # xq without xs
+    assert li(A, 300, 128, A, A, 256, A, None, None, 0, None) == NULL   # m > 128 needs xq, xs
+    assert li(A + 2, 64, 128, A, A, 256, A, None, None, 0, None) == ALIGN
+    assert li(A, 64, 128, A, A, 2048, A, None, None, 0, None) == NULL   # wide n: two kernels
+    assert li(A, 64, 128, A, A, 256, A, None, None, 4, None) == UNSUP
+    assert li(None, 0, 128, None, None, 256, None, None, None, 0, None) == OK
     ge = L.fp8_block_gemm_ex
     assert ge(A, A, A, A, A, 128, 256, 100, 0, None) == SHAPE
     assert ge(A, A, A, A, A + 8, 64, 256, 128, 1, None) == ALIGN

@@ -20,7 +20,7 @@ __all__ = [
     "quantize_act_per_token_group_gather", "dequantize_blockwise", "quant_error_report",
     "sqnr_db", "fp8_decode_attention", "fp8_block_gemm",
     "fp8_grouped_gemm", "kv_amax_quantize", "w8a8_linear", "consume_device_error",
-    "GEMM_STATIC_WEIGHTS",
+    "GEMM_STATIC_WEIGHTS", "LINEAR_SINGLE_KERNEL",
     "KV_AMAX_AND_QUANT", "KV_AMAX_ONLY", "KV_QUANT_ONLY", "LIB_PATH",
 ]
 
@@ -63,6 +63,7 @@ _SIGNATURES = {
                                     ctypes.c_float, _P, _P]),
     "fp8_block_gemm": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "fp8_block_gemm_ex": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_uint32, _P]),
+    "w8a8_linear": (_INT, [_P, _I64, _I64, _P, _P, _I64, _P, _P, _P, ctypes.c_uint32, _P]),
     "fp8_grouped_gemm": (_INT, [_P, _P, _I64, _P, _P, _I32, _I64, _P, _P, _P, _I64, _I64, _P]),
     "kv_amax_quantize": (_INT, [_P, _I64, _P, _P, _P, _INT, _P]),
 }
@@ -288,10 +289,30 @@ def fp8_grouped_gemm(xq, xs, row_idx, group_offsets, total_rows, wq, ws, y=None,
     return y
 
 
-def w8a8_linear(x, wq, ws, stream=None):
-    """BF16 activations -> 1x128 quantization -> blockwise FP8 GEMM, on one stream."""
-    xq, xs = quantize_act_per_token_group(x, stream=stream)
-    return fp8_block_gemm(xq, xs, wq, ws, stream=stream)
+LINEAR_SINGLE_KERNEL = 2
+
+
+def w8a8_linear(x, wq, ws, y=None, xq=None, xs=None, stream=None, static_weights=False,
+                single_kernel=False, return_codes=False):
+    """BF16 activations [m, k] -> 1x128 quantization -> blockwise FP8 GEMM
+    (the C entry point w8a8_linear).  xq/xs, the activations' codes and
+    scales, are written when given; they are allocated here unless the one
+    kernel way runs (m <= 128 and k <= 32768, with n <= 1024 or
+    single_kernel) and return_codes is off.  Returns y, or (y, xq, xs) with
+    return_codes."""
+    _need(x, torch.bfloat16, "x")
+    _need(wq, torch.uint8, "wq")
+    m, k = x.shape
+    n = wq.shape[0]
+    y = torch.empty((m, n), dtype=torch.bfloat16, device=x.device) if y is None else y
+    one_kernel = m <= 128 and k <= 32768 and (single_kernel or n <= 1024)
+    if xq is None and (return_codes or not one_kernel):
+        xq = torch.empty((m, k), dtype=torch.uint8, device=x.device)
+        xs = torch.empty((m, _cdiv(k, 128)), dtype=torch.float32, device=x.device)
+    flags = (GEMM_STATIC_WEIGHTS if static_weights else 0) | (LINEAR_SINGLE_KERNEL if single_kernel else 0)
+    _check("w8a8_linear", lib().w8a8_linear(_ptr(x), m, k, _ptr(wq), _ptr(ws), n, _ptr(y),
+                                            _ptr(xq), _ptr(xs), flags, _stream(stream)))
+    return (y, xq, xs) if return_codes else y
 
 
 # --------------------------------------------------------------- KV cache

@@ -261,6 +261,34 @@ W8A8_API w8a8_status fp8_block_gemm(const uint8_t* xq, const float* xs, const ui
   return fp8_block_gemm_ex(xq, xs, wq, ws, y_bf16, m, n, k, 0u, stream);
 }
 
+W8A8_API w8a8_status w8a8_linear(const uint16_t* x_bf16, int64_t m, int64_t k, const uint8_t* wq,
+                                 const float* ws, int64_t n, uint16_t* y_bf16, uint8_t* xq,
+                                 float* xs, uint32_t flags, w8a8_stream_t stream) {
+  if (m < 0 || n < 0 || k < 0 || m >= kMaxDim) return W8A8_ERR_SHAPE;
+  if ((flags & ~(uint32_t)(W8A8_GEMM_STATIC_WEIGHTS | W8A8_LINEAR_SINGLE_KERNEL)) != 0)
+    return W8A8_ERR_UNSUPPORTED;
+  if (k % 16 != 0 || n % 8 != 0 || n >= kMaxDim || k >= kMaxDim) return W8A8_ERR_SHAPE;
+  if (m == 0 || n == 0) return W8A8_OK;
+  if ((xq == nullptr) != (xs == nullptr)) return W8A8_ERR_NULL;
+  if (!y_bf16 || (k > 0 && (!x_bf16 || !wq || !ws))) return W8A8_ERR_NULL;
+  if (!aligned(y_bf16, 16) || (k > 0 && (!aligned(x_bf16, 16) || !aligned(wq, 16) ||
+                                         !aligned(ws, 4))))
+    return W8A8_ERR_ALIGN;
+  if (xq && (!aligned(xq, 16) || !aligned(xs, 4))) return W8A8_ERR_ALIGN;
+  const bool stat = (flags & W8A8_GEMM_STATIC_WEIGHTS) != 0;
+  const bool single = (flags & W8A8_LINEAR_SINGLE_KERNEL) != 0;
+  if (k > 0 && (single ? w8a8::linear_fused_possible(m, n, k) : w8a8::linear_fused_serves(m, n, k)))
+    return from_cuda(w8a8::launch_linear_fused(x_bf16, wq, ws, y_bf16, xq, xs, m, n, k, stat,
+                                               cs(stream)));
+  // two kernels: the activation quantizer writes xq and xs, then the GEMM
+  if (k > 0 && !xq) return W8A8_ERR_NULL;
+  if (k == 0) return from_cuda(cudaMemsetAsync(y_bf16, 0, (size_t)(m * n * 2), cs(stream)));
+  w8a8_status st = from_cuda(w8a8::launch_act_quant(x_bf16, m, k, xq, xs, cs(stream)));
+  if (st != W8A8_OK) return st;
+  return fp8_block_gemm_ex(xq, xs, wq, ws, y_bf16, m, n, k, flags & W8A8_GEMM_STATIC_WEIGHTS,
+                           stream);
+}
+
 W8A8_API w8a8_status fp8_grouped_gemm(const uint8_t* xq, const float* xs, int64_t rows_x,
                                       const int32_t* row_idx, const int32_t* group_offsets,
                                       int32_t g, int64_t total_rows, const uint8_t* wq,

@@ -45,6 +45,7 @@
 // so no CTA of the cluster is left waiting.
 #include <algorithm>
 
+#include "common.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tmap.h"
@@ -62,11 +63,15 @@ constexpr int W_BYTES = BW * BK;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr int MAX_SPLIT = 8;  // portable cluster size
 
-template <int NT>
+// kFused: the token rows come as BF16 and are quantized (1 x 128 groups) by
+// the loader warps on their way into shared memory.
+template <int NT, bool kFused = false>
 struct Cfg {
   static constexpr int X_BYTES = NT * BK;
-  static constexpr int STAGE_BYTES = W_BYTES + X_BYTES;
-  static constexpr int STAGES = 4;
+  // fused: each stage also holds the slab's BF16 token rows (NT x 256 B)
+  static constexpr int XB_BYTES = kFused ? NT * BK * 2 : 0;
+  static constexpr int STAGE_BYTES = W_BYTES + X_BYTES + XB_BYTES;
+  static constexpr int STAGES = kFused && NT >= 128 ? 3 : 4;
   // The CTA's scales are loaded once, at the start: xs of every token for
   // each of the CTA's slabs, transposed to [slab][token], and the tile's ws
   // per slab.  A CTA takes at most MAX_SLABS slabs (the split is chosen so,
@@ -74,7 +79,12 @@ struct Cfg {
   static constexpr int MAX_SLABS = 32;
   static constexpr int XS_BYTES = MAX_SLABS * NT * 4;
   static constexpr int WS_BYTES = MAX_SLABS * 4;
-  static constexpr int XW = NT >= 128 ? 2 : 1;  // token-loader warps
+  static constexpr int XW = kFused ? (NT >= 128 ? 4 : 2) : (NT >= 128 ? 2 : 1);  // token loaders
+  // Fused: the loaders' group scales pass to the promotion warps through a
+  // ring of scale slots (each slab's NT scales), deep enough that the
+  // loaders never wait on it in steady state: they run at most STAGES slabs
+  // ahead of the MMA, and the MMA at most 2 ahead of the promotion.
+  static constexpr int SLOTS = STAGES + 2;
   static constexpr int EPI_WARPS = NT >= 256 ? 8 : 4;
   static constexpr int EPI_WARP0 = 2 + XW;
   static constexpr int COLS = NT >= 256 ? 128 : NT;  // token columns per promotion thread
@@ -90,8 +100,8 @@ struct Cfg {
   static constexpr int OFF_XS = RING > RED_BYTES ? RING : RED_BYTES;
   static constexpr int OFF_WS = OFF_XS + XS_BYTES;
   static constexpr int OFF_BARS = OFF_WS + WS_BYTES;
-  // full, empty, tfull[2], tempty[2], done, recv
-  static constexpr int NUM_BARS = 2 * STAGES + 4 + 2;
+  // full, empty, sfull, sempty, tfull[2], tempty[2], done, recv
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * SLOTS + 4 + 2;
   static constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
   static constexpr int SMEM = 1024 + OFF_MISC + 16;
   static constexpr uint32_t IDESC = ptx::idesc_e4m3_f32(BW, NT);
@@ -99,6 +109,8 @@ struct Cfg {
   static_assert(SMEM <= 232448, "shared memory");
   static_assert(COLS % 16 == 0 && COLS >= 32, "TMEM loads: 16 columns each, at least two");
   static_assert(NT % (4 * XW) == 0, "token rows split evenly over the loader warps");
+  static_assert(!kFused || (NT <= 128 && NT % (8 * XW) == 0 && SLOTS <= MAX_SLABS),
+                "fused: up to 128 tokens, 8 rows per loader warp step");
   // Registers: with 256 tokens the 8 promotion warps hold 128 FP32 sums
   // each; during the main loop the first warpgroup (producer, MMA, loaders)
   // gives them its share: 128 * 64 + 256 * 216 <= 384 * 168 (the launch's
@@ -112,6 +124,9 @@ struct Cfg {
 struct Params {
   const uint8_t* xq;
   const float* xs;
+  const uint16_t* xb;  // fused: BF16 tokens [m, k]
+  uint8_t* xq_out;     // fused: codes and scales written here when not NULL
+  float* xs_out;
   const float* ws;
   uint16_t* y;
   int32_t m, n, k, nkb, split;
@@ -151,12 +166,12 @@ __device__ __forceinline__ int owned_lo(int r, int m, int split) {
 // sums (kAcc), the others take part in the barriers and the final sums.
 // Each role calls it from its own branch, so that it runs with the registers
 // that role holds.
-template <int NT, bool kAcc>
+template <int NT, bool kFused, bool kAcc>
 __device__ __forceinline__ void reduce_store(const Params& p, uint8_t* smem, uint32_t sbase,
                                              uint32_t recv_bar, int rank, int split, int n0,
                                              int warp, int lane, int c0,
-                                             const float2 (&acc)[Cfg<NT>::COLS / 2]) {
-  using C = Cfg<NT>;
+                                             const float2 (&acc)[Cfg<NT, kFused>::COLS / 2]) {
+  using C = Cfg<NT, kFused>;
   // -------------------------------------------------- cluster reduction
   // In rounds of up to 128 token rows (two rounds when NT = 256):
   //  1. a cluster barrier: every CTA has finished its main loop (or the
@@ -232,11 +247,11 @@ __device__ __forceinline__ void reduce_store(const Params& p, uint8_t* smem, uin
   if (split > 1) ptx::cluster_sync();
 }
 
-template <int NT>
-__global__ void __launch_bounds__(Cfg<NT>::THREADS, NT <= 64 ? 2 : 1)
+template <int NT, bool kFused>
+__global__ void __launch_bounds__(Cfg<NT, kFused>::THREADS, NT <= 64 ? 2 : 1)
     fp8_gemm_small_m_kernel(const __grid_constant__ CUtensorMap tmap_w,
                             const __grid_constant__ Params p) {
-  using C = Cfg<NT>;
+  using C = Cfg<NT, kFused>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -244,14 +259,17 @@ __global__ void __launch_bounds__(Cfg<NT>::THREADS, NT <= 64 ? 2 : 1)
   const uint32_t bar0 = sbase + C::OFF_BARS;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
-  constexpr int TB0 = 2 * C::STAGES;
+  auto sfull_bar = [&](int s) { return bar0 + 8u * (2 * C::STAGES + s); };
+  auto sempty_bar = [&](int s) { return bar0 + 8u * (2 * C::STAGES + C::SLOTS + s); };
+  constexpr int TB0 = 2 * C::STAGES + 2 * C::SLOTS;
   auto tfull_bar = [&](int b) { return bar0 + 8u * (TB0 + b); };
   auto tempty_bar = [&](int b) { return bar0 + 8u * (TB0 + 2 + b); };
   const uint32_t done_bar = bar0 + 8u * (TB0 + 4);
   const uint32_t recv_bar = bar0 + 8u * (TB0 + 5);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-  float* xs_tab = reinterpret_cast<float*>(smem + C::OFF_XS);  // [slab][token]
+  // unfused: xs of every slab [slab][token]; fused: the scale-slot ring
+  float* xs_tab = reinterpret_cast<float*>(smem + C::OFF_XS);
   float* ws_tab = reinterpret_cast<float*>(smem + C::OFF_WS);   // [slab]
 
   const int warp = threadIdx.x >> 5;
@@ -269,6 +287,10 @@ __global__ void __launch_bounds__(Cfg<NT>::THREADS, NT <= 64 ? 2 : 1)
     for (int s = 0; s < C::STAGES; ++s) {
       ptx::mbar_init(full_bar(s), 1 + 32 * C::XW);  // W expect_tx + token loaders' lanes
       ptx::mbar_init(empty_bar(s), 1);
+    }
+    for (int s = 0; s < C::SLOTS; ++s) {
+      ptx::mbar_init(sfull_bar(s), 32 * C::XW);  // the token loaders' lanes
+      ptx::mbar_init(sempty_bar(s), C::EPI_WARPS);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(tfull_bar(b), 1);
@@ -314,10 +336,11 @@ __global__ void __launch_bounds__(Cfg<NT>::THREADS, NT <= 64 ? 2 : 1)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // the CTA's scales: xs[token][kb0 .. kb0 + nsl) transposed to [slab][token]
   // (tokens past m read as 0), and ws[tile][kb0 .. kb0 + nsl)
-  for (int i = threadIdx.x; i < NT * nsl; i += C::THREADS) {
-    const int t = i / nsl, j = i - t * nsl;
-    xs_tab[j * NT + t] = t < p.m ? p.xs[(int64_t)t * p.nkb + kb0 + j] : 0.0f;
-  }
+  if (!kFused)
+    for (int i = threadIdx.x; i < NT * nsl; i += C::THREADS) {
+      const int t = i / nsl, j = i - t * nsl;
+      xs_tab[j * NT + t] = t < p.m ? p.xs[(int64_t)t * p.nkb + kb0 + j] : 0.0f;
+    }
   if (!p.static_weights)
     for (int j = threadIdx.x; j < nsl; j += C::THREADS)
       ws_tab[j] = p.ws[(int64_t)tile * p.nkb + kb0 + j];
@@ -392,6 +415,112 @@ __global__ void __launch_bounds__(Cfg<NT>::THREADS, NT <= 64 ? 2 : 1)
         }
       }
       __syncwarp();
+    } else if (kFused) {
+      // ------------------------------------------- token loaders + quantizer
+      // Loader warp w owns token rows 8 (i XW + w) + [0, 8), i = 0, 1, ...
+      // It copies them, BF16, into the stage's staging area by 16-byte
+      // cp.async, STAGES slabs ahead (one copy group per slab), and codes
+      // them from there once they have landed:
+      //  * four lanes take one 1 x 128 group (row r, slab kb); lane `sub`
+      //    holds elements [32 sub, 32 sub + 32);
+      //  * the group's amax is reduced over the four lanes, S = RN32(amax /
+      //    448) (S = 1 for an all-zero group), and each element is coded as
+      //    E4M3(RN32(x / S)) -- the activation quantizer's arithmetic, bit
+      //    for bit;
+      //  * lane `sub`'s 32 codes (code chunks 2 sub, 2 sub + 1) go to chunk
+      //    c ^ (r % 8) of the row (the 128-byte swizzle), S to the slab's
+      //    scale slot.
+      // Rows past m and elements past k read as zero (codes 0, S = 1).  In
+      // the staging area chunk c of row r sits at (c & 8) | ((c ^ r) & 7), so
+      // the 8 rows a warp reads at once fall in distinct banks.  The CTAs of
+      // the first weight tile also write the codes and scales out.
+      const int w = warp - 2;
+      const int sub = lane & 3, gi = lane >> 2;
+      constexpr int ITERS = NT / (8 * C::XW);
+      const bool write_out = tile == 0 && p.xq_out != nullptr;
+      auto staging = [&](int st) { return sbase + st * C::STAGE_BYTES + W_BYTES + C::X_BYTES; };
+      // copies of slab j (this warp's rows) into stage j % STAGES
+      auto copy_slab = [&](int j) {
+        const uint32_t xb = staging(j % C::STAGES);
+        const int c = lane & 15;
+        const int col = (kb0 + j) * BK + 8 * c;
+  #pragma unroll
+        for (int it = 0; it < ITERS; ++it) {
+  #pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int r = 8 * (it * C::XW + w) + 2 * t + (lane >> 4);
+            const bool in = r < p.m && col < p.k;
+            ptx::cp_async_16(xb + (uint32_t)(r * 256 + (((c & 8) | ((c ^ r) & 7)) << 4)),
+                             in ? p.xb + (int64_t)r * p.k + col : p.xb, in ? 16u : 0u);
+          }
+        }
+        ptx::cp_async_commit();
+      };
+      for (int j = 0; j < min(C::STAGES, nsl); ++j) copy_slab(j);
+      uint32_t stage = 0, phase = 0;
+      for (int j = 0; j < nsl; ++j) {
+        const int sl = j % C::SLOTS;
+        // this lane's copies of slab j have landed, then every lane's
+        if (nsl - 1 - j >= C::STAGES - 1) ptx::cp_async_wait_group<C::STAGES - 1>();
+        else ptx::cp_async_wait_group<0>();
+        __syncwarp();
+        uint32_t okw = 1;
+        if (lane == 0)
+          okw = (wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, 31) &&
+                 wait_bar(sempty_bar(sl), (uint32_t)(((j / C::SLOTS) & 1) ^ 1), abort_flag, 31))
+                    ? 1u : 0u;
+        okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+        if (!okw) break;
+        const int kb = kb0 + j;
+        const uint32_t sx = sbase + stage * C::STAGE_BYTES + W_BYTES;
+        const uint32_t xb = staging(stage);
+        float* slot = xs_tab + sl * NT;
+  #pragma unroll
+        for (int it = 0; it < ITERS; ++it) {
+          const int r = 8 * (it * C::XW + w) + gi;
+          const bool rin = r < p.m;
+          const int col = kb * BK + 32 * sub;
+          uint4 v[4];
+  #pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int c = 4 * sub + i;
+            v[i] = ptx::lds128(xb + (uint32_t)(r * 256 + (((c & 8) | ((c ^ r) & 7)) << 4)));
+          }
+          float a = absmax_bf16x8_tree<4>(v);
+          a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+          a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+          const float S = scale_from_amax(a);
+          const QuantScale qs = make_quant_scale(S);
+          uint32_t cw[8];
+  #pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            cw[2 * i] = quant_bf16x4(v[i].x, v[i].y, qs);
+            cw[2 * i + 1] = quant_bf16x4(v[i].z, v[i].w, qs);
+          }
+          const uint32_t rb = sx + (uint32_t)(r * 128);
+          ptx::sts128(rb + ((uint32_t)((2 * sub) ^ (r & 7)) << 4), cw[0], cw[1], cw[2], cw[3]);
+          ptx::sts128(rb + ((uint32_t)((2 * sub + 1) ^ (r & 7)) << 4), cw[4], cw[5], cw[6], cw[7]);
+          if (sub == 0) slot[r] = S;
+          if (write_out && rin) {
+            uint8_t* dst = p.xq_out + (int64_t)r * p.k + col;
+            if (col < p.k) *reinterpret_cast<uint4*>(dst) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+            if (col + 16 < p.k)
+              *reinterpret_cast<uint4*>(dst + 16) = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+            if (sub == 0) p.xs_out[(int64_t)r * p.nkb + kb] = S;
+          }
+        }
+        // the codes were written by the generic proxy; the MMA reads them
+        // through the async proxy
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(full_bar(stage));
+        ptx::mbar_arrive(sfull_bar(sl));
+        // the staging rows of this stage are free again: next slab for it
+        __syncwarp();
+        if (j + C::STAGES < nsl) copy_slab(j + C::STAGES);
+        if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+      }
+      ptx::cp_async_wait_all();
+      __syncwarp();
     } else {
       // -------------------------------------------------------- token loaders
       // Lane l of loader warp w copies 16-byte chunk l % 8 of token rows
@@ -424,7 +553,7 @@ __global__ void __launch_bounds__(Cfg<NT>::THREADS, NT <= 64 ? 2 : 1)
       __syncwarp();
     }
     const float2 none[C::COLS / 2] = {};
-    reduce_store<NT, false>(p, smem, sbase, recv_bar, rank, split, n0, warp, lane, 0, none);
+    reduce_store<NT, kFused, false>(p, smem, sbase, recv_bar, rank, split, n0, warp, lane, 0, none);
   } else {
     // ------------------------------------------------------------ promotion
     const int ew = warp - C::EPI_WARP0;
@@ -435,12 +564,17 @@ __global__ void __launch_bounds__(Cfg<NT>::THREADS, NT <= 64 ? 2 : 1)
     for (int i = 0; i < C::COLS / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
     uint32_t tb = 0, tphase = 0;
     for (int j = 0; j < nsl; ++j) {
+      const int sl = j % C::SLOTS;
       uint32_t okw = 1;
-      if (lane == 0) okw = wait_bar(tfull_bar(tb), tphase, abort_flag, 32) ? 1u : 0u;
+      if (lane == 0)
+        okw = (wait_bar(tfull_bar(tb), tphase, abort_flag, 32) &&
+               (!kFused ||
+                wait_bar(sfull_bar(sl), (uint32_t)((j / C::SLOTS) & 1), abort_flag, 32)))
+                  ? 1u : 0u;
       okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
       if (!okw) break;
       ptx::tc_fence_after();
-      const float* slot = xs_tab + j * NT;
+      const float* slot = xs_tab + (kFused ? sl : j) * NT;
       const float2 w2 = make_float2(ws_tab[j], ws_tab[j]);
       const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + tb * NT + c0;
       uint32_t ra[16], rb[16];
@@ -471,9 +605,14 @@ __global__ void __launch_bounds__(Cfg<NT>::THREADS, NT <= 64 ? 2 : 1)
           if (lane == 0) ptx::mbar_arrive(tempty_bar(tb));
         }
       }
+      if (kFused) {
+        // the slab's scales have been read: hand the slot back to the loaders
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(sempty_bar(sl));
+      }
       if (++tb == 2) { tb = 0; tphase ^= 1u; }
     }
-    reduce_store<NT, true>(p, smem, sbase, recv_bar, rank, split, n0, warp, lane, c0, acc);
+    reduce_store<NT, kFused, true>(p, smem, sbase, recv_bar, rank, split, n0, warp, lane, c0, acc);
   }
 
   ptx::tc_fence_before();
@@ -486,7 +625,7 @@ __global__ void __launch_bounds__(Cfg<NT>::THREADS, NT <= 64 ? 2 : 1)
 
 // Most clusters of `split` CTAs that fit on the device at once (cached per
 // device).
-template <int NT>
+template <int NT, bool kFused>
 static int max_active_clusters(int split) {
   static int cache[64][MAX_SPLIT + 1] = {};
   int dev = 0;
@@ -494,8 +633,8 @@ static int max_active_clusters(int split) {
   if (cache[dev][split] > 0) return cache[dev][split];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)split, 1, 1);
-  cfg.blockDim = dim3(Cfg<NT>::THREADS, 1, 1);
-  cfg.dynamicSmemBytes = Cfg<NT>::SMEM;
+  cfg.blockDim = dim3(Cfg<NT, kFused>::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<NT, kFused>::SMEM;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)split;
@@ -504,7 +643,8 @@ static int max_active_clusters(int split) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_small_m_kernel<NT>, &cfg) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_small_m_kernel<NT, kFused>, &cfg) !=
+          cudaSuccess ||
       n <= 0) {
     cudaGetLastError();  // the query failed: assume one cluster per `split` SMs
     n = std::max(1, sm_count() / split);
@@ -517,13 +657,13 @@ static int max_active_clusters(int split) {
 // comes from the occupancy query) times the slabs of each CTA, plus a small
 // cost per extra CTA of a split (its pipeline fill and its share of the
 // reduction), is made smallest.
-template <int NT>
+template <int NT, bool kFused>
 static int choose_split(int tiles, int nkb) {
   int best = MAX_SPLIT;
   double best_cost = 1e30;
   for (int s = 1; s <= std::min(MAX_SPLIT, nkb); ++s) {
-    if ((nkb + s - 1) / s > Cfg<NT>::MAX_SLABS) continue;  // the scale table holds MAX_SLABS
-    const int fit = max_active_clusters<NT>(s);
+    if ((nkb + s - 1) / s > Cfg<NT, kFused>::MAX_SLABS) continue;  // the scale table's size
+    const int fit = max_active_clusters<NT, kFused>(s);
     const double waves = (double)((tiles + fit - 1) / fit);
     const double cost = waves * (double)((nkb + s - 1) / s) + 0.5 * (double)(s - 1) / MAX_SPLIT;
     if (cost < best_cost - 1e-9) { best_cost = cost; best = s; }
@@ -531,31 +671,26 @@ static int choose_split(int tiles, int nkb) {
   return best;
 }
 
-template <int NT>
-static cudaError_t launch_nt(const uint8_t* xq, const float* xs, const uint8_t* wq,
-                             const float* ws, uint16_t* y, int64_t m, int64_t n, int64_t k,
-                             bool static_weights, cudaStream_t st) {
-  using C = Cfg<NT>;
+// p: every field but split set by the caller.
+template <int NT, bool kFused>
+static cudaError_t launch_nt(Params p, const uint8_t* wq, cudaStream_t st) {
+  using C = Cfg<NT, kFused>;
   CUtensorMap tw;
-  if (!make_tmap_2d(&tw, wq, 1, (uint64_t)n, (uint64_t)k, BW, BK, CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!make_tmap_2d(&tw, wq, 1, (uint64_t)p.n, (uint64_t)p.k, BW, BK,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   static int configured[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(fp8_gemm_small_m_kernel<NT>,
+    e = cudaFuncSetAttribute(fp8_gemm_small_m_kernel<NT, kFused>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = 1;
   }
-  Params p{};
-  p.xq = xq; p.xs = xs; p.ws = ws; p.y = y;
-  p.m = (int32_t)m; p.n = (int32_t)n; p.k = (int32_t)k;
-  p.nkb = (int32_t)((k + BK - 1) / BK);
-  p.static_weights = static_weights ? 1 : 0;
-  const int tiles = (int)((n + BW - 1) / BW);
-  p.split = choose_split<NT>(tiles, p.nkb);
+  const int tiles = (p.n + BW - 1) / BW;
+  p.split = choose_split<NT, kFused>(tiles, p.nkb);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(p.split * tiles), 1, 1);
   cfg.blockDim = dim3(C::THREADS, 1, 1);
@@ -572,12 +707,25 @@ static cudaError_t launch_nt(const uint8_t* xq, const float* xs, const uint8_t* 
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, fp8_gemm_small_m_kernel<NT>, tw, p);
+  e = cudaLaunchKernelEx(&cfg, fp8_gemm_small_m_kernel<NT, kFused>, tw, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
+static Params make_params(const float* ws, uint16_t* y, int64_t m, int64_t n, int64_t k,
+                          bool static_weights) {
+  Params p{};
+  p.ws = ws; p.y = y;
+  p.m = (int32_t)m; p.n = (int32_t)n; p.k = (int32_t)k;
+  p.nkb = (int32_t)((k + BK - 1) / BK);
+  p.static_weights = static_weights ? 1 : 0;
+  return p;
+}
+
 }  // namespace sgemm
+
+constexpr int BW_TILE = sgemm::BW;
+constexpr int FUSED_MAX_TILES = 8;
 
 bool block_gemm_small_m_serves(int64_t m, int64_t n, int64_t k) {
   // a split of at most MAX_SPLIT CTAs must leave each at most MAX_SLABS slabs
@@ -611,10 +759,39 @@ cudaError_t launch_block_gemm_small_m(const uint8_t* xq, const float* xs, const 
                                       int64_t k, bool static_weights, cudaStream_t st) {
   using namespace sgemm;
   if (!block_gemm_small_m_serves(m, n, k) || n <= 0) return cudaErrorInvalidValue;
-  if (m <= 32) return launch_nt<32>(xq, xs, wq, ws, y, m, n, k, static_weights, st);
-  if (m <= 64) return launch_nt<64>(xq, xs, wq, ws, y, m, n, k, static_weights, st);
-  if (m <= 128) return launch_nt<128>(xq, xs, wq, ws, y, m, n, k, static_weights, st);
-  return launch_nt<256>(xq, xs, wq, ws, y, m, n, k, static_weights, st);
+  Params p = make_params(ws, y, m, n, k, static_weights);
+  p.xq = xq; p.xs = xs;
+  if (m <= 32) return launch_nt<32, false>(p, wq, st);
+  if (m <= 64) return launch_nt<64, false>(p, wq, st);
+  if (m <= 128) return launch_nt<128, false>(p, wq, st);
+  return launch_nt<256, false>(p, wq, st);
+}
+
+bool linear_fused_possible(int64_t m, int64_t n, int64_t k);
+
+bool linear_fused_serves(int64_t m, int64_t n, int64_t k) {
+  // Every weight-tile CTA quantizes the token rows of its slabs, so the
+  // quantization is repeated once per 128 output columns: measured on the
+  // Qwen3-8B linears at m = 64 (48 to 192 tiles) the single kernel took 55
+  // to 73 us a linear against 19 us for quantizer + GEMM.  It is kept for
+  // narrow outputs, where that repetition is small.
+  return linear_fused_possible(m, n, k) && (n + BW_TILE - 1) / BW_TILE <= FUSED_MAX_TILES;
+}
+
+bool linear_fused_possible(int64_t m, int64_t n, int64_t k) {
+  return m <= 128 && block_gemm_small_m_serves(m, n, k);
+}
+
+cudaError_t launch_linear_fused(const uint16_t* x, const uint8_t* wq, const float* ws,
+                                uint16_t* y, uint8_t* xq_out, float* xs_out, int64_t m,
+                                int64_t n, int64_t k, bool static_weights, cudaStream_t st) {
+  using namespace sgemm;
+  if (!linear_fused_possible(m, n, k) || n <= 0) return cudaErrorInvalidValue;
+  Params p = make_params(ws, y, m, n, k, static_weights);
+  p.xb = x; p.xq_out = xq_out; p.xs_out = xs_out;
+  if (m <= 32) return launch_nt<32, true>(p, wq, st);
+  if (m <= 64) return launch_nt<64, true>(p, wq, st);
+  return launch_nt<128, true>(p, wq, st);
 }
 
 }  // namespace w8a8

@@ -61,6 +61,17 @@ cudaError_t launch_block_gemm(const uint8_t* xq, const float* xs, const uint8_t*
 cudaError_t launch_block_gemm_small_m(const uint8_t* xq, const float* xs, const uint8_t* wq,
                                       const float* ws, uint16_t* y, int64_t m, int64_t n,
                                       int64_t k, bool static_weights, cudaStream_t st);
+// The same kernel fed with BF16 activations x [m, k]: the 1 x 128 activation
+// quantization happens inside it (bit-exact with launch_act_quant); its codes
+// and scales are also written to xq_out / xs_out when those are not NULL.
+cudaError_t launch_linear_fused(const uint16_t* x, const uint8_t* wq, const float* ws,
+                                uint16_t* y, uint8_t* xq_out, float* xs_out, int64_t m,
+                                int64_t n, int64_t k, bool static_weights, cudaStream_t st);
+// Whether that kernel is the faster choice (narrow outputs), and whether it
+// can run at all (m <= 128, k <= 32768).
+bool linear_fused_serves(int64_t m, int64_t n, int64_t k);
+bool linear_fused_possible(int64_t m, int64_t n, int64_t k);
+
 // Whether the kernel above is the one for an m x n x k product (m <= 256,
 // k <= 32768, and past m = 128 only where the general kernel has few tiles).
 bool block_gemm_small_m_serves(int64_t m, int64_t n, int64_t k);

@@ -238,10 +238,18 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const uint16_t* __restri
 // spreads the per-group work -- two butterfly steps, S and the reciprocal --
 // over 32 values per lane; a warp covers 8 consecutive groups (2 KB) per
 // unit and U units are loaded before any is used.
+//
+// Launched as a programmatic dependent, and letting the next kernel on the
+// stream launch at once: in a chain quantizer -> GEMM the GEMM's prologue
+// (and, with static weights, its first weight reads) overlaps this kernel,
+// and this kernel's launch overlaps the end of the one before it.  Nothing
+// is read or written before that previous kernel has completed.
 template <int U, bool kPow2>
 __global__ void __launch_bounds__(256) act_quant_k128_kernel(const uint16_t* __restrict__ x,
                                                              int64_t G, uint8_t* __restrict__ q,
                                                              float* __restrict__ s) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int sub = lane & 3, gi = lane >> 2;
   const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -337,7 +345,17 @@ static cudaError_t launch_act_quant_t(const uint16_t* x, int64_t m, int64_t k, u
   if (k % 128 == 0) {
     constexpr int U = 2;
     const unsigned grid = grid_for(G, 8 * 8 * U, 8);  // 8 warps x 8 groups x U per CTA pass
-    act_quant_k128_kernel<U, kPow2><<<grid, 256, 0, st>>>(x, G, q, s);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, act_quant_k128_kernel<U, kPow2>, x, G, q, s);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
   const unsigned grid = grid_for(G, 8 * 8, 16);  // 8 warps x 8 groups per CTA iteration
