@@ -75,6 +75,16 @@ const char *w8a8_last_cuda_error(void);
  * has finished prior work on the legacy stream. */
 w8a8_status w8a8_consume_device_error(int *code);
 
+/* Test hook for the abort paths: while `on` is nonzero, every later launch
+ * of the GEMMs and of the weight quantizer behaves as if one of its bounded
+ * waits had run out of time at once (the GEMMs' MMA issuer before its first
+ * slab: code 5, or 35 for m <= 256; the weight quantizer's consumers on
+ * their first block: code 13).  The kernel then stops as it would after a
+ * real time-out -- the other roles stop, copies and MMAs in flight are
+ * drained, tensor memory is freed -- and its output is incomplete.  Nothing
+ * faults or hangs.  Synchronous; call with 0 to return to normal. */
+w8a8_status w8a8_debug_force_wait_timeout(int on);
+
 /* ------------------------------------------------------------------------
  * E4M3 codec ([UFP8] "FP8 data formats", referring to the OCP FP8 spec;
  * [FP8-RL] section 1 range +-448).

@@ -1,0 +1,83 @@
+"""The kernels' abort paths, run on demand: with the test hook on, a bounded
+wait behaves as if it had run out of time.  The kernel must return (no
+hang), report the documented code through w8a8_consume_device_error, and
+leave the GPU usable: the next normal call passes parity.  Nothing here
+faults or hangs a GPU: the hook only makes one wait give up early."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from parity_util import assert_gemm_close, bits16
+from w8a8_gemm_rl_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _gemm_case(m, n, k, seed):
+    g = torch.Generator().manual_seed(seed)
+    xq = (torch.randn(m, k, generator=g) * 60).clamp_(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    wq = (torch.randn(n, k, generator=g) * 60).clamp_(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    xs = (torch.rand(m, -(-k // 128), generator=g) * 0.01 + 0.001).numpy()
+    ws = (torch.rand(-(-n // 128), -(-k // 128), generator=g) * 0.01 + 0.001).numpy()
+    return xq, xs, wq, ws
+
+
+@pytest.mark.parametrize("m,code", [(300, 5), (64, 35)])
+def test_gemm_abort_then_recover(W, m, code):
+    n, k = 512, 1024
+    xq, xs, wq, ws = _gemm_case(m, n, k, seed=m)
+    dev = [torch.from_numpy(a).cuda() for a in (xq, xs, wq, ws)]
+    assert W.consume_device_error() == 0
+    W.debug_force_wait_timeout(True)
+    try:
+        W.fp8_block_gemm(*dev)
+        torch.cuda.synchronize()
+    finally:
+        W.debug_force_wait_timeout(False)
+    assert W.consume_device_error() == code
+    y = W.fp8_block_gemm(*dev)
+    torch.cuda.synchronize()
+    assert W.consume_device_error() == 0
+    y_ref, absref = O.block_gemm(xq, xs, wq, ws)
+    assert_gemm_close(bits16(y), y_ref, absref, f"after abort m={m}")
+
+
+def test_grouped_gemm_abort_then_recover(W):
+    g, n, k, rows = 4, 256, 512, 200
+    xq, xs, _, _ = _gemm_case(rows, n, k, seed=9)
+    rng = np.random.default_rng(9)
+    wq = np.stack([_gemm_case(1, n, k, seed=20 + e)[2] for e in range(g)])
+    ws = np.stack([_gemm_case(1, n, k, seed=30 + e)[3] for e in range(g)])
+    off = np.array([0, 37, 37, 120, rows], np.int32)
+    ridx = rng.integers(0, rows, rows).astype(np.int32)
+    args = [torch.from_numpy(xq).cuda(), torch.from_numpy(xs).cuda(), torch.from_numpy(ridx).cuda(),
+            torch.from_numpy(off).cuda(), rows, torch.from_numpy(wq).cuda(), torch.from_numpy(ws).cuda()]
+    W.debug_force_wait_timeout(True)
+    try:
+        W.fp8_grouped_gemm(*args)
+        torch.cuda.synchronize()
+    finally:
+        W.debug_force_wait_timeout(False)
+    assert W.consume_device_error() == 5
+    y = W.fp8_grouped_gemm(*args)
+    torch.cuda.synchronize()
+    assert W.consume_device_error() == 0
+    y_ref, absref = O.grouped_gemm(xq, xs, ridx, off, wq, ws)
+    assert_gemm_close(bits16(y), y_ref, absref, "grouped after abort")
+
+
+def test_weight_quant_abort_then_recover(W):
+    w = synth.weights(384, 1024, seed=5)
+    W.debug_force_wait_timeout(True)
+    try:
+        W.quantize_weight_blockwise(w.cuda())
+        torch.cuda.synchronize()   # the producer gives up on its own bounded wait (2 s)
+    finally:
+        W.debug_force_wait_timeout(False)
+    assert W.consume_device_error() in (13, 11)
+    wq, ws = W.quantize_weight_blockwise(w.cuda())
+    torch.cuda.synchronize()
+    assert W.consume_device_error() == 0
+    wq_ref, ws_ref = O.quantize_weight_blockwise(synth.bf16_bits(w))
+    assert (wq.cpu().numpy() == wq_ref).all() and (ws.cpu().numpy() == ws_ref).all()

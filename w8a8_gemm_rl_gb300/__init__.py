@@ -20,7 +20,7 @@ __all__ = [
     "quantize_act_per_token_group_gather", "dequantize_blockwise", "quant_error_report",
     "sqnr_db", "fp8_decode_attention", "fp8_block_gemm",
     "fp8_grouped_gemm", "kv_amax_quantize", "w8a8_linear", "consume_device_error",
-    "GEMM_STATIC_WEIGHTS", "LINEAR_SINGLE_KERNEL",
+    "GEMM_STATIC_WEIGHTS", "LINEAR_SINGLE_KERNEL", "debug_force_wait_timeout",
     "KV_AMAX_AND_QUANT", "KV_AMAX_ONLY", "KV_QUANT_ONLY", "LIB_PATH",
 ]
 
@@ -48,6 +48,7 @@ _SIGNATURES = {
     "w8a8_version": (_INT, []),
     "w8a8_last_cuda_error": (ctypes.c_char_p, []),
     "w8a8_consume_device_error": (_INT, [_P]),
+    "w8a8_debug_force_wait_timeout": (_INT, [_INT]),
     "e4m3_encode_f32": (_INT, [_P, _I64, _P, _P]),
     "e4m3_decode_f32": (_INT, [_P, _I64, _P, _P]),
     "quantize_weight_blockwise": (_INT, [_P, _I64, _I64, _P, _P, _P]),
@@ -338,3 +339,9 @@ def consume_device_error():
     v = ctypes.c_int(0)
     _check("w8a8_consume_device_error", lib().w8a8_consume_device_error(ctypes.byref(v)))
     return v.value
+
+
+def debug_force_wait_timeout(on):
+    """Test hook: while on, the GEMMs and the weight quantizer behave as if a
+    bounded wait had run out of time (see w8a8_debug_force_wait_timeout)."""
+    _check("w8a8_debug_force_wait_timeout", lib().w8a8_debug_force_wait_timeout(1 if on else 0))

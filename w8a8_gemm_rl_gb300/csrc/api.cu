@@ -12,6 +12,9 @@
 namespace w8a8 {
 cudaError_t consume_device_error(int* code);
 cudaError_t consume_small_gemm_error(int* code);
+cudaError_t set_gemm_force_timeout(int on);
+cudaError_t set_small_gemm_force_timeout(int on);
+cudaError_t set_quant_force_timeout(int on);
 cudaError_t consume_quant_error(int* code);
 cudaError_t consume_attention_error(int* code);
 int grouped_gemm_max_groups();
@@ -342,4 +345,13 @@ W8A8_API w8a8_status w8a8_consume_device_error(int* code) {
   st = from_cuda(w8a8::consume_attention_error(&a));
   *code = g != 0 ? g : (q != 0 ? q : a);
   return st;
+}
+
+W8A8_API w8a8_status w8a8_debug_force_wait_timeout(int on) {
+  const int v = on ? 1 : 0;
+  w8a8_status st = from_cuda(w8a8::set_gemm_force_timeout(v));
+  if (st != W8A8_OK) return st;
+  st = from_cuda(w8a8::set_small_gemm_force_timeout(v));
+  if (st != W8A8_OK) return st;
+  return from_cuda(w8a8::set_quant_force_timeout(v));
 }

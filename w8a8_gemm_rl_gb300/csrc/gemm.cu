@@ -39,6 +39,10 @@
 namespace w8a8 {
 
 __device__ int g_w8a8_gemm_error = 0;
+// Test hook (w8a8_debug_force_wait_timeout): when set, the MMA issuer's
+// first wait gives up at once, as if its time limit had passed, so that the
+// abort path (stop, drain copies and MMAs, free TMEM) runs on demand.
+__device__ int g_w8a8_gemm_force_timeout = 0;
 
 namespace gemm {
 
@@ -396,6 +400,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
         for (int kb = 0; kb < nkb; ++kb) {
           if (!wait_bar(tempty_bar(tb), tphase ^ 1u, abort_flag, 4)) { ok = false; break; }
+          if (g_w8a8_gemm_force_timeout) { record_error(5); *abort_flag = 1; ok = false; break; }
           if (!wait_bar(full_bar(stage), phase, abort_flag, 5)) { ok = false; break; }
           // gathered A rows were written by cp.async (generic proxy); the
           // MMA reads them through the async proxy
@@ -690,6 +695,10 @@ cudaError_t launch_grouped_gemm(const uint8_t* xq, const float* xs, int64_t rows
 }
 
 int grouped_gemm_max_groups() { return gemm::MAX_GROUPS; }
+
+cudaError_t set_gemm_force_timeout(int on) {
+  return cudaMemcpyToSymbol(g_w8a8_gemm_force_timeout, &on, sizeof(int));
+}
 
 cudaError_t consume_device_error(int* code) {
   int v = 0;

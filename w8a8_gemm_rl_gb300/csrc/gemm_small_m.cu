@@ -54,6 +54,9 @@ namespace w8a8 {
 
 // Device error word of this kernel (each translation unit has its own).
 __device__ int g_w8a8_small_gemm_error = 0;
+// Test hook (w8a8_debug_force_wait_timeout): when set, the MMA issuer's
+// first wait gives up at once, so that the abort path runs on demand.
+__device__ int g_w8a8_small_gemm_force_timeout = 0;
 
 namespace sgemm {
 
@@ -391,6 +394,7 @@ __global__ void __launch_bounds__(Cfg<NT, kFused>::THREADS, NT <= 64 ? 2 : 1)
         uint32_t stage = 0, phase = 0, tb = 0, tphase = 0;
         for (int j = 0; j < nsl; ++j) {
           if (!wait_bar(tempty_bar(tb), tphase ^ 1u, abort_flag, 34)) break;
+          if (g_w8a8_small_gemm_force_timeout) { record_error(35); *abort_flag = 1; break; }
           if (!wait_bar(full_bar(stage), phase, abort_flag, 35)) break;
           // the token rows were written by cp.async (generic proxy); the MMA
           // reads them through the async proxy
@@ -740,6 +744,10 @@ bool block_gemm_small_m_serves(int64_t m, int64_t n, int64_t k) {
   // tiles each, 21.6 and 39.5 us here against 22.6 and 54.2 us there).
   if (m > 128) return ((m + 127) / 128) * ((n + 255) / 256) * 4 < (int64_t)sm_count();
   return true;
+}
+
+cudaError_t set_small_gemm_force_timeout(int on) {
+  return cudaMemcpyToSymbol(g_w8a8_small_gemm_force_timeout, &on, sizeof(int));
 }
 
 cudaError_t consume_small_gemm_error(int* code) {

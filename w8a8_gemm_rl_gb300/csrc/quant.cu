@@ -25,6 +25,14 @@ namespace w8a8 {
 
 // Set (first error wins) when a bounded wait in a quantization kernel gives up.
 __device__ int g_w8a8_quant_error = 0;
+// Test hook (w8a8_debug_force_wait_timeout): when set, the weight
+// quantizer's consumers give up on their first block at once, as if the
+// wait's time limit had passed, so that the abort path runs on demand.
+__device__ int g_w8a8_quant_force_timeout = 0;
+
+cudaError_t set_quant_force_timeout(int on) {
+  return cudaMemcpyToSymbol(g_w8a8_quant_force_timeout, &on, sizeof(int));
+}
 
 cudaError_t consume_quant_error(int* code) {
   int v = 0;
@@ -529,7 +537,9 @@ __global__ void __launch_bounds__(WQ_THREADS, 2)
     const int s = (int)(it % WQ_STAGES);
     const uint32_t par = (uint32_t)((it / WQ_STAGES) & 1);
     uint32_t ok = 1;
-    if (lane == 0) ok = ptx::mbar_wait(full_bar(s), par, WQ_WAIT_NS) ? 1u : 0u;
+    if (lane == 0)
+      ok = (it == 0 && g_w8a8_quant_force_timeout) ? 0u
+                                                    : (ptx::mbar_wait(full_bar(s), par, WQ_WAIT_NS) ? 1u : 0u);
     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
     if (!ok && lane == 0) atomicCAS(&g_w8a8_quant_error, 0, 13);
     const uint32_t stage = sbase + s * WQ_STAGE_BYTES;
