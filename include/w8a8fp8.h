@@ -69,7 +69,7 @@ const char *w8a8_last_cuda_error(void);
  * bounded wait inside it gives up (0 = none; nonzero identifies the wait:
  * 1..8 the GEMMs of more than 256 rows and the grouped GEMM, 31..37 the
  * GEMM of at most 256 rows, 11..13 the weight quantizer, 21..22 the decode
- * attention).  When several are set, the GEMMs' code is reported first,
+ * attention, 41..43 the batched dequantizer and error report).  When several are set, the GEMMs' code is reported first,
  * then the quantizer's, and all are cleared.  Such a kernel stops early
  * and leaves its output incomplete.  Synchronous: blocks until the device
  * has finished prior work on the legacy stream. */
@@ -242,6 +242,38 @@ w8a8_status quant_error_report(const uint16_t *x_bf16, const uint8_t *q,
                                int64_t report_block_rows,
                                int64_t report_block_cols, double *stats,
                                w8a8_stream_t stream);
+
+/* dequantize_blockwise and quant_error_report over `count` weight matrices
+ * with 128 x 128 scale blocks (and, for the report, 128 x 128 report
+ * blocks) in as few launches as the kernel-parameter space allows: every
+ * matrix of a whole-model weight sync in one call each.  The same
+ * arithmetic as the one-matrix calls: y bit-identical; the report's maxima
+ * identical and its sums within a few binary32 roundings (the order of
+ * summation differs).  descs is a HOST array, read before the call
+ * returns.  Rules: n, k >= 0 and k % 16 == 0 for the dequantizer, k % 8 == 0
+ * for the report; q, y_bf16 and x_bf16 16-byte aligned, s 4-byte aligned,
+ * stats 8-byte aligned; count >= 0.  A bounded wait that gives up records
+ * code 41..43 (w8a8_consume_device_error). */
+typedef struct {
+    const uint8_t *q;       /* [n, k] E4M3 codes */
+    const float *s;         /* [ceil(n/128), ceil(k/128)] scales */
+    uint16_t *y_bf16;       /* [n, k] (out) */
+    int64_t n;
+    int64_t k;
+} w8a8_dequant_desc;
+w8a8_status dequantize_blockwise_batched(const w8a8_dequant_desc *descs,
+                                         int32_t count, w8a8_stream_t stream);
+
+typedef struct {
+    const uint16_t *x_bf16; /* [n, k] the BF16 matrix that was quantized */
+    const uint8_t *q;       /* [n, k] its E4M3 codes */
+    const float *s;         /* [ceil(n/128), ceil(k/128)] its scales */
+    double *stats;          /* [ceil(n/128), ceil(k/128), 3] (out) */
+    int64_t n;
+    int64_t k;
+} w8a8_error_desc;
+w8a8_status quant_error_report_batched(const w8a8_error_desc *descs,
+                                       int32_t count, w8a8_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * fp8_decode_attention -- attention of one new query token per sequence

@@ -95,3 +95,42 @@ def test_weight_sync_rows_at_full_size(W):
         got = st[bi, bj].cpu().numpy()
         assert got[0] == want[0]
         assert np.allclose(got[1:], want[1:], rtol=1e-5, atol=0)
+
+
+BATCH_SHAPES = [(256, 512), (300, 208), (129, 1024), (8, 128), (0, 256), (384, 4096), (131, 16)]
+
+
+def test_batched_dequantize_and_report(W):
+    """Many matrices in one call each (128 x 128 blocks), ragged edges
+    included: the dequantized BF16 bit-exact with the oracle, the report's
+    maxima exact and sums within 1e-5, per matrix."""
+    xs, qs, ss = [], [], []
+    for i, (n, k) in enumerate(BATCH_SHAPES):
+        x = synth.activations(n, k, seed=40 + i) if n else torch.zeros((0, k), dtype=torch.bfloat16)
+        q_ref, s_ref = O.quantize_blocks(synth.bf16_bits(x), 128, 128)
+        xs.append(x.cuda())
+        qs.append(torch.from_numpy(q_ref).cuda())
+        ss.append(torch.from_numpy(s_ref).cuda())
+    ys = W.dequantize_blockwise_batched(qs, ss)
+    sts = W.quant_error_report_batched(xs, qs, ss)
+    torch.cuda.synchronize()
+    assert W.consume_device_error() == 0
+    for x, q, s, y, st in zip(xs, qs, ss, ys, sts):
+        if x.shape[0] == 0:
+            continue
+        q_ref, s_ref = q.cpu().numpy(), s.cpu().numpy()
+        assert (bits16(y) == O.dequantize_blocks(q_ref, s_ref, 128, 128)).all()
+        want = O.quant_error(synth.bf16_bits(x.cpu()), q_ref, s_ref, 128, 128, 128, 128)
+        got = st.cpu().numpy()
+        assert (got[..., 0] == want[..., 0]).all()
+        assert np.allclose(got[..., 1:], want[..., 1:], rtol=1e-5, atol=0)
+
+
+def test_batched_equals_one_matrix_calls(W):
+    """The batched dequantizer gives the one-matrix call's bits on a weight
+    sync's matrices (one Qwen3-8B layer)."""
+    ws_ = [W.quantize_weight_blockwise(synth.weights(n, k, seed=50 + i, device="cuda"))
+           for i, (n, k) in enumerate(synth.QWEN3_8B_LINEARS.values())]
+    ys = W.dequantize_blockwise_batched([q for q, _ in ws_], [s for _, s in ws_])
+    for (q, s), y in zip(ws_, ys):
+        assert torch.equal(y.view(torch.int16), W.dequantize_blockwise(q, s, 128, 128).view(torch.int16))

@@ -18,7 +18,7 @@ __all__ = [
     "lib", "W8A8Error", "e4m3_encode_f32", "e4m3_decode_f32", "quantize_weight_blockwise",
     "quantize_weight_blockwise_batched", "quantize_act_per_token_group",
     "quantize_act_per_token_group_gather", "dequantize_blockwise", "quant_error_report",
-    "sqnr_db", "fp8_decode_attention", "fp8_block_gemm",
+    "sqnr_db", "fp8_decode_attention", "dequantize_blockwise_batched", "quant_error_report_batched", "fp8_block_gemm",
     "fp8_grouped_gemm", "kv_amax_quantize", "w8a8_linear", "consume_device_error",
     "GEMM_STATIC_WEIGHTS", "LINEAR_SINGLE_KERNEL", "debug_force_wait_timeout",
     "KV_AMAX_AND_QUANT", "KV_AMAX_ONLY", "KV_QUANT_ONLY", "LIB_PATH",
@@ -67,6 +67,8 @@ _SIGNATURES = {
     "w8a8_linear": (_INT, [_P, _I64, _I64, _P, _P, _I64, _P, _P, _P, ctypes.c_uint32, _P]),
     "fp8_grouped_gemm": (_INT, [_P, _P, _I64, _P, _P, _I32, _I64, _P, _P, _P, _I64, _I64, _P]),
     "kv_amax_quantize": (_INT, [_P, _I64, _P, _P, _P, _INT, _P]),
+    "dequantize_blockwise_batched": (_INT, [_P, _I32, _P]),
+    "quant_error_report_batched": (_INT, [_P, _I32, _P]),
 }
 
 
@@ -215,6 +217,49 @@ def quant_error_report(x, q, s, scale_block, report_block, stats=None, stream=No
     _check("quant_error_report",
            lib().quant_error_report(_ptr(x), _ptr(q), _ptr(s), rows, cols, scale_block[0],
                                     scale_block[1], rbr, rbc, _ptr(stats), _stream(stream)))
+    return stats
+
+
+class DequantDesc(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("s", ctypes.c_void_p), ("y_bf16", ctypes.c_void_p),
+                ("n", ctypes.c_int64), ("k", ctypes.c_int64)]
+
+
+class ErrorDesc(ctypes.Structure):
+    _fields_ = [("x_bf16", ctypes.c_void_p), ("q", ctypes.c_void_p), ("s", ctypes.c_void_p),
+                ("stats", ctypes.c_void_p), ("n", ctypes.c_int64), ("k", ctypes.c_int64)]
+
+
+def dequantize_blockwise_batched(qs, ss, ys=None, stream=None):
+    """dequantize_blockwise over many matrices with 128 x 128 scale blocks in
+    one call: qs uint8 [n, k] codes, ss their scale grids; returns the BF16
+    outputs (allocated unless ys is given)."""
+    if ys is None:
+        ys = [torch.empty(q.shape, dtype=torch.bfloat16, device=q.device) for q in qs]
+    arr = (DequantDesc * len(qs))()
+    for i, (q, s, y) in enumerate(zip(qs, ss, ys)):
+        _need(q, torch.uint8, "q")
+        arr[i] = DequantDesc(q.data_ptr(), s.data_ptr(), y.data_ptr(), q.shape[0], q.shape[1])
+    _check("dequantize_blockwise_batched",
+           lib().dequantize_blockwise_batched(arr, len(qs), _stream(stream)))
+    return ys
+
+
+def quant_error_report_batched(xs, qs, ss, stats=None, stream=None):
+    """quant_error_report over many matrices with 128 x 128 scale and report
+    blocks in one call; returns the float64 [ceil(n/128), ceil(k/128), 3]
+    reports (allocated unless stats is given)."""
+    if stats is None:
+        stats = [torch.empty((_cdiv(x.shape[0], 128), _cdiv(x.shape[1], 128), 3),
+                             dtype=torch.float64, device=x.device) for x in xs]
+    arr = (ErrorDesc * len(xs))()
+    for i, (x, q, s, st) in enumerate(zip(xs, qs, ss, stats)):
+        _need(x, torch.bfloat16, "x")
+        _need(q, torch.uint8, "q")
+        arr[i] = ErrorDesc(x.data_ptr(), q.data_ptr(), s.data_ptr(), st.data_ptr(), x.shape[0],
+                           x.shape[1])
+    _check("quant_error_report_batched",
+           lib().quant_error_report_batched(arr, len(xs), _stream(stream)))
     return stats
 
 

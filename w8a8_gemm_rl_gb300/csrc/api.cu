@@ -15,6 +15,7 @@ cudaError_t consume_small_gemm_error(int* code);
 cudaError_t set_gemm_force_timeout(int on);
 cudaError_t set_small_gemm_force_timeout(int on);
 cudaError_t set_quant_force_timeout(int on);
+cudaError_t consume_batch_error(int* code);
 cudaError_t consume_quant_error(int* code);
 cudaError_t consume_attention_error(int* code);
 int grouped_gemm_max_groups();
@@ -199,6 +200,68 @@ W8A8_API w8a8_status quant_error_report(const uint16_t* x_bf16, const uint8_t* q
                                             report_block_cols, stats, cs(stream)));
 }
 
+template <typename Desc, typename Fill>
+static w8a8_status block_batch(const Desc* descs, int32_t count, Fill fill, bool report,
+                               w8a8_stream_t stream) {
+  if (count < 0) return W8A8_ERR_SHAPE;
+  if (count == 0) return W8A8_OK;
+  if (!descs) return W8A8_ERR_NULL;
+  constexpr int kChunk = 256;
+  w8a8::BlockJob jobs[kChunk];
+  int nj = 0;
+  for (int32_t i = 0; i < count; ++i) {
+    w8a8::BlockJob j{};
+    w8a8_status st = fill(descs[i], j);
+    if (st != W8A8_OK) return st;
+    if (j.n == 0 || j.k == 0) continue;
+    jobs[nj++] = j;
+    if (nj == kChunk || i == count - 1) {
+      st = from_cuda(report ? w8a8::launch_quant_error_batch(jobs, nj, cs(stream))
+                            : w8a8::launch_dequant_batch(jobs, nj, cs(stream)));
+      if (st != W8A8_OK) return st;
+      nj = 0;
+    }
+  }
+  if (nj > 0)
+    return from_cuda(report ? w8a8::launch_quant_error_batch(jobs, nj, cs(stream))
+                            : w8a8::launch_dequant_batch(jobs, nj, cs(stream)));
+  return W8A8_OK;
+}
+
+W8A8_API w8a8_status dequantize_blockwise_batched(const w8a8_dequant_desc* descs, int32_t count,
+                                                  w8a8_stream_t stream) {
+  // every entry is checked before anything is queued
+  for (int32_t i = 0; descs && i < count; ++i) {
+    const w8a8_dequant_desc& d = descs[i];
+    if (d.n < 0 || d.k < 0 || d.n >= kMaxDim || d.k >= kMaxDim) return W8A8_ERR_SHAPE;
+    if (d.n == 0 || d.k == 0) continue;
+    if (d.k % 16 != 0) return W8A8_ERR_SHAPE;
+    if (!d.q || !d.s || !d.y_bf16) return W8A8_ERR_NULL;
+    if (!aligned(d.q, 16) || !aligned(d.y_bf16, 16) || !aligned(d.s, 4)) return W8A8_ERR_ALIGN;
+  }
+  return block_batch(descs, count, [](const w8a8_dequant_desc& d, w8a8::BlockJob& j) {
+    j.q = d.q; j.s = d.s; j.y = d.y_bf16; j.n = d.n; j.k = d.k;
+    return W8A8_OK;
+  }, false, stream);
+}
+
+W8A8_API w8a8_status quant_error_report_batched(const w8a8_error_desc* descs, int32_t count,
+                                                w8a8_stream_t stream) {
+  for (int32_t i = 0; descs && i < count; ++i) {
+    const w8a8_error_desc& d = descs[i];
+    if (d.n < 0 || d.k < 0 || d.n >= kMaxDim || d.k >= kMaxDim) return W8A8_ERR_SHAPE;
+    if (d.n == 0 || d.k == 0) continue;
+    if (d.k % 8 != 0) return W8A8_ERR_SHAPE;
+    if (!d.x_bf16 || !d.q || !d.s || !d.stats) return W8A8_ERR_NULL;
+    if (!aligned(d.x_bf16, 16) || !aligned(d.q, 16) || !aligned(d.s, 4) || !aligned(d.stats, 8))
+      return W8A8_ERR_ALIGN;
+  }
+  return block_batch(descs, count, [](const w8a8_error_desc& d, w8a8::BlockJob& j) {
+    j.x = d.x_bf16; j.q = d.q; j.s = d.s; j.stats = d.stats; j.n = d.n; j.k = d.k;
+    return W8A8_OK;
+  }, true, stream);
+}
+
 // --------------------------------------------------------------- attention
 
 W8A8_API w8a8_status fp8_decode_attention(const uint8_t* q, const float* q_scale,
@@ -334,16 +397,18 @@ W8A8_API w8a8_status kv_amax_quantize(const uint16_t* x_bf16, int64_t numel, uin
 
 W8A8_API w8a8_status w8a8_consume_device_error(int* code) {
   if (!code) return W8A8_ERR_NULL;
-  int g = 0, sg = 0, q = 0, a = 0;
+  int g = 0, sg = 0, q = 0, a = 0, bt = 0;
   w8a8_status st = from_cuda(w8a8::consume_device_error(&g));
   if (st != W8A8_OK) return st;
   st = from_cuda(w8a8::consume_small_gemm_error(&sg));
   if (st != W8A8_OK) return st;
   if (g == 0) g = sg;
+  st = from_cuda(w8a8::consume_batch_error(&bt));
+  if (st != W8A8_OK) return st;
   st = from_cuda(w8a8::consume_quant_error(&q));
   if (st != W8A8_OK) return st;
   st = from_cuda(w8a8::consume_attention_error(&a));
-  *code = g != 0 ? g : (q != 0 ? q : a);
+  *code = g != 0 ? g : (q != 0 ? q : (a != 0 ? a : bt));
   return st;
 }
 

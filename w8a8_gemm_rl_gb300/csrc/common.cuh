@@ -188,6 +188,19 @@ __device__ __forceinline__ float absmax_bf16x8_tree(const uint4 (&v)[N]) {
   return absmax_finish(m0 & 0x7FFF7FFFu);
 }
 
+// ---- dequantization: RN32(dec(code) * S), then BF16 round to nearest even ----
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Two codes (bits 0..7, 8..15) times S, rounded once to binary32 each, then
+// to BF16: the BF16 pair for output positions (lo, hi).
+__device__ __forceinline__ uint32_t dequant_pair(uint32_t codes16, float S) {
+  const float2 d = e4m3x2_to_float2((uint16_t)codes16);
+  return pack_bf16x2_rn(__fmul_rn(d.x, S), __fmul_rn(d.y, S));
+}
+
 // ---- cache-hinted vector access for data touched once ----
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   uint4 v;

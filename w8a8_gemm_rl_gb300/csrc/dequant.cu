@@ -14,19 +14,6 @@ namespace w8a8 {
 
 namespace {
 
-__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-// Two codes (bits 0..7, 8..15) times S, rounded once to binary32 each, then
-// to BF16: the BF16 pair for output positions (lo, hi).
-__device__ __forceinline__ uint32_t dequant_pair(uint32_t codes16, float S) {
-  const float2 d = e4m3x2_to_float2((uint16_t)codes16);
-  return pack_bf16x2_rn(__fmul_rn(d.x, S), __fmul_rn(d.y, S));
-}
-
 inline unsigned grid_for(int64_t work, int64_t per_cta) {
   const int64_t need = (work + per_cta - 1) / per_cta;
   const int64_t cap = (int64_t)sm_count() * 8;

@@ -40,6 +40,19 @@ cudaError_t launch_kv_amax_quantize(const uint16_t* x, int64_t n, uint8_t* q, fl
 // per-report-block error statistics [max |x - x_hat|, sum e^2, sum x^2].
 cudaError_t launch_dequant(const uint8_t* q, const float* s, int64_t rows, int64_t cols,
                            int64_t br, int64_t bc, uint16_t* y, cudaStream_t st);
+// batch.cu: the same two over many matrices at once, 128 x 128 scale blocks
+// (and, for the report, 128 x 128 report blocks).
+struct BlockJob {
+  const uint16_t* x;  // report: BF16 inputs [n, k]
+  const uint8_t* q;   // codes [n, k]
+  const float* s;     // scales [ceil(n/128), ceil(k/128)]
+  uint16_t* y;        // dequantize: BF16 output [n, k]
+  double* stats;      // report: [ceil(n/128), ceil(k/128), 3]
+  int64_t n, k;
+};
+cudaError_t launch_dequant_batch(const BlockJob* jobs, int count, cudaStream_t st);
+cudaError_t launch_quant_error_batch(const BlockJob* jobs, int count, cudaStream_t st);
+
 cudaError_t launch_quant_error(const uint16_t* x, const uint8_t* q, const float* s, int64_t rows,
                                int64_t cols, int64_t sbr, int64_t sbc, int64_t rbr, int64_t rbc,
                                double* stats, cudaStream_t st);
