@@ -94,6 +94,22 @@ def test_decode_chain_static_weights(W, m):
     assert torch.equal(ya.view(torch.int16), yb.view(torch.int16))
 
 
+@pytest.mark.parametrize("m,n,k", [(2305, 2312, 48), (5000, 776, 32)])
+def test_block_gemm_partial_last_n_tile_several_waves(W, m, n, k):
+    """More tiles than SMs, with a last N tile of 8 columns: a CTA's epilogue
+    stores that tile with a single TMA store and starts its next tile at once.
+    Called three times, since a staging-buffer race shows only in some runs."""
+    xq, wq = _codes((m, k), m + k), _codes((n, k), n + 7 * k)
+    xs, ws = _scales((m, _cdiv(k, 128)), 1), _scales((_cdiv(n, 128), _cdiv(k, 128)), 2)
+    y_ref, absref = O.block_gemm(xq, xs, wq, ws)
+    args = (_dev(xq), _dev(xs), _dev(wq), _dev(ws))
+    for rep in range(3):
+        y = W.fp8_block_gemm(*args)
+        torch.cuda.synchronize()
+        assert W.consume_device_error() == 0
+        assert_gemm_close(bits16(y), y_ref, absref, f"gemm {m}x{n}x{k} call {rep}")
+
+
 def test_block_gemm_empty_and_k0(W):
     y = W.fp8_block_gemm(torch.empty(0, 128, dtype=torch.uint8, device="cuda"),
                          torch.empty(0, 1, device="cuda"),
@@ -185,6 +201,20 @@ def _grouped_case(g, n, k, rows_x, total, seed, gather=True, bad_rows=False):
         row_idx[::17] = -1
         row_idx[5::23] = rows_x
     return xq, xs, wq, ws, off, row_idx
+
+
+def test_grouped_gemm_partial_last_n_tile_several_waves(W):
+    """Grouped tiles outnumbering the SMs, each expert's last N tile 8 columns
+    wide; three calls (the staging-buffer race showed only in some runs)."""
+    g, n, k, rows_x, total = 4, 520, 32, 3000, 8000
+    xq, xs, wq, ws, off, row_idx = _grouped_case(g, n, k, rows_x, total, seed=77)
+    y_ref, absref = O.grouped_gemm(xq, xs, row_idx, off, wq, ws)
+    args = (_dev(xq), _dev(xs), _dev(row_idx), _dev(off), total, _dev(wq), _dev(ws))
+    for rep in range(3):
+        y = W.fp8_grouped_gemm(*args)
+        torch.cuda.synchronize()
+        assert W.consume_device_error() == 0
+        assert_gemm_close(bits16(y), y_ref, absref, f"grouped partial-N call {rep}")
 
 
 @pytest.mark.parametrize("g,n,k,rows_x,total,gather", [

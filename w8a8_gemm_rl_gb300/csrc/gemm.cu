@@ -482,6 +482,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr int SWZ_SHIFT = CPR == 8 ? 0 : (CPR == 4 ? 1 : 2);  // 128/64/32-byte swizzle
     constexpr uint32_t BUF_BYTES = 32 * SC * 2;
     const uint32_t stg0 = sbase + OFF_STAGE + (uint32_t)ew * STAGE_BUFS * BUF_BYTES;
+    static_assert(STAGE_BUFS == 2, "one staging buffer in flight, one being written");
+    uint32_t nstores = 0;  // TMA stores this warp has issued (over all its tiles)
     for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
       const int64_t cur_row0 = T.row0;
       const int cur_rows = T.rows;
@@ -536,9 +538,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (t + gridDim.x < num_tiles) setup_tile(t + gridDim.x);
 #pragma unroll
       for (int pass = 0; pass < 128 / SC; ++pass) {
-        const uint32_t stg = stg0 + (uint32_t)(pass % STAGE_BUFS) * BUF_BYTES;
-        // the TMA store issued from this buffer two passes ago must have read
-        // it (the store from the other buffer may still be reading)
+        const int col0 = c0 + pass * SC;
+        if (col0 >= p.n) break;  // columns past n (warp-uniform)
+        // the buffers alternate per TMA store issued, not per pass: the one
+        // written now is never the source of the newest store (which may
+        // still be reading the other), and every older store has read its
+        // source once all but the newest have
+        const uint32_t stg = stg0 + (nstores % STAGE_BUFS) * BUF_BYTES;
         if (lane == 0) ptx::bulk_wait_read_1();
         __syncwarp();
 #pragma unroll
@@ -551,14 +557,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                       ptx::pack_bf16x2(acc[v * 4 + 2].x, acc[v * 4 + 2].y),
                       ptx::pack_bf16x2(acc[v * 4 + 3].x, acc[v * 4 + 3].y));
         }
-        const int col0 = c0 + pass * SC;
         if (full_rows) {
           ptx::fence_proxy_async_smem();  // staging writes -> TMA (async proxy)
           __syncwarp();
-          if (lane == 0 && col0 < p.n) {
+          if (lane == 0) {
             ptx::tma_store_2d(&tmap_y, stg, col0, (int)(cur_row0 + quarter * 32));
             ptx::bulk_commit();
           }
+          ++nstores;
         } else {
           __syncwarp();
 #pragma unroll
