@@ -808,6 +808,7 @@ def measure_next_rows(W, wl, peaks, reps=3):
         "workload": "32 sequences x 8192 tokens, 32 query heads over 8 KV heads, head dim 128",
         "us": round(sec * 1e6, 1), "gbs": round(nb / sec / 1e9, 1),
         "pct_roofline": round(100 * nb / sec / 1e9 / peaks["hbm_gbs"], 2), "bytes_per_call": nb}
+    out["fp8_block_gemm_pow2"] = measure_pow2_gemm(W, wl, peaks, reps)
     W.quantize_weight_blockwise_batched(wl.w, wl.wout)
     for kind, nbytes in (("dequant", 3 * elems + 4 * blocks),
                          ("quant_error_report", 3 * elems + 4 * blocks + 24 * blocks)):
@@ -829,6 +830,42 @@ def measure_next_rows(W, wl, peaks, reps=3):
     del yall, sall
     assert W.consume_device_error() == 0
     return out
+
+
+def measure_pow2_gemm(W, wl, peaks, reps=3):
+    """The power-of-two-scale GEMM (block-scaled MMA) on the four Qwen3-8B
+    linears at M=8192, operands quantized with power-of-two scales, timed
+    beside the FP32-scale GEMM on the same codes and scales (both compute
+    the same product; only the scaling hardware differs)."""
+    ops = []
+    for j, d in enumerate(wl.lin):
+        m, k = d["x"].shape
+        xq, xs = W.quantize_act_per_token_group(d["x"], pow2=True)
+        wq, ws = W.quantize_weight_blockwise(wl.w[j], pow2=True)
+        ops.append((xq, xs, wq, ws, torch.empty_like(d["y"])))
+    flops = sum(2 * o[0].shape[0] * o[0].shape[1] * o[2].shape[0] for o in ops)
+    res = {"workload": "Qwen3-8B qkv/o/gate_up/down linears at M=8192, power-of-two scales, 4 launches"}
+    for name, fn in (("pow2", W.fp8_block_gemm_pow2), ("fp32_scale_kernel", W.fp8_block_gemm)):
+        for o in ops:
+            fn(*o[:4], y=o[4])
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(reps):
+            for o in ops:
+                fn(*o[:4], y=o[4])
+        t1.record()
+        torch.cuda.synchronize()
+        sec = t0.elapsed_time(t1) * 1e-3 / reps
+        tf = flops / sec / 1e12
+        res[name] = {"ms": round(sec * 1e3, 3), "tflops": round(tf, 1),
+                     "frac": round(tf / fp8_peak_tflops(peaks), 4)}
+    res["peak_tflops"] = round(fp8_peak_tflops(peaks), 1)
+    res["peak_note"] = "measured bf16 burst x 2 (nominal fp8/bf16 ratio)"
+    assert W.consume_device_error() == 0
+    del ops
+    return res
 
 
 def measure_e2e(W, wl, args, roof_step, world, chunks=8, in_streams=1):

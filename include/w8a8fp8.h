@@ -68,9 +68,11 @@ const char *w8a8_last_cuda_error(void);
 /* Reads and clears the device-side error code that a kernel sets when a
  * bounded wait inside it gives up (0 = none; nonzero identifies the wait:
  * 1..8 the GEMMs of more than 256 rows and the grouped GEMM, 31..37 the
- * GEMM of at most 256 rows, 11..13 the weight quantizer, 21..22 the decode
- * attention, 41..43 the batched dequantizer and error report).  When several are set, the GEMMs' code is reported first,
- * then the quantizer's, and all are cleared.  Such a kernel stops early
+ * GEMM of at most 256 rows, 51..58 the power-of-two GEMM (59: a scale it
+ * cannot hold), 11..13 the weight quantizer, 21..22 the decode attention,
+ * 41..43 the batched dequantizer and error report).  When several are set,
+ * the GEMMs' code is reported first, then the quantizer's, and all are
+ * cleared.  Such a kernel stops early
  * and leaves its output incomplete.  Synchronous: blocks until the device
  * has finished prior work on the legacy stream. */
 w8a8_status w8a8_consume_device_error(int *code);
@@ -78,7 +80,8 @@ w8a8_status w8a8_consume_device_error(int *code);
 /* Test hook for the abort paths: while `on` is nonzero, every later launch
  * of the GEMMs and of the weight quantizer behaves as if one of its bounded
  * waits had run out of time at once (the GEMMs' MMA issuer before its first
- * slab: code 5, or 35 for m <= 256; the weight quantizer's consumers on
+ * slab: code 5, 35 for m <= 256, 55 for fp8_block_gemm_pow2; the weight
+ * quantizer's consumers on
  * their first block: code 13).  The kernel then stops as it would after a
  * real time-out -- the other roles stop, copies and MMAs in flight are
  * drained, tensor memory is freed -- and its output is incomplete.  Nothing
@@ -361,6 +364,32 @@ w8a8_status fp8_block_gemm_ex(const uint8_t *xq, const float *xs,
                               const uint8_t *wq, const float *ws,
                               uint16_t *y_bf16, int64_t m, int64_t n,
                               int64_t k, uint32_t flags, w8a8_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * fp8_block_gemm_pow2 -- fp8_block_gemm for power-of-two scales (the
+ * "Power-of-2 Scaling Factor" recipe option of the [NeMo] blog, as made by
+ * the *_pow2 quantizers), with the scaling done inside the tensor cores:
+ * every scale is a UE8M0 factor of a block-scaled MMA ([UFP8] "FP8 scale
+ * choice" names E8M0 as the alternative to FP32 scales), and the FP32
+ * accumulator spans the whole K extent instead of being promoted through
+ * registers once per 128-wide slab.
+ *
+ *   y[i,j] = BF16( sum_kb xs[i,kb] * ws[j/128,kb]
+ *                        * sum_{k in slab kb} dec(xq[i,k]) * dec(wq[j,k]) )
+ *
+ * Arguments, layouts, rules and accuracy bound as fp8_block_gemm, plus:
+ * every xs and ws value must be +2^e with -127 <= e <= 127.  The *_pow2
+ * quantizers give such scales except for a block whose amax is below
+ * 448 * 2^-127 (nonzero); a scale outside the rule makes that tile's rows
+ * of y_bf16 wrong and records device error 59 (w8a8_consume_device_error),
+ * nothing else.  Results differ from fp8_block_gemm's only in rounding
+ * order (both within the bound).  Any m is served; for m <= 256 the weight
+ * stream bounds both GEMMs and fp8_block_gemm is the faster.
+ * ---------------------------------------------------------------------- */
+w8a8_status fp8_block_gemm_pow2(const uint8_t *xq, const float *xs,
+                                const uint8_t *wq, const float *ws,
+                                uint16_t *y_bf16, int64_t m, int64_t n,
+                                int64_t k, w8a8_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * w8a8_linear -- the whole W8A8 linear of [FP8-RL] section 1 from BF16

@@ -43,6 +43,28 @@ def test_gemm_abort_then_recover(W, m, code):
     assert_gemm_close(bits16(y), y_ref, absref, f"after abort m={m}")
 
 
+def test_pow2_gemm_abort_then_recover(W):
+    m, n, k = 300, 512, 1024
+    xq, _, wq, _ = _gemm_case(m, n, k, seed=17)
+    rng = np.random.default_rng(17)
+    xs = np.ldexp(np.float32(1), rng.integers(-12, -4, (m, k // 128))).astype(np.float32)
+    ws = np.ldexp(np.float32(1), rng.integers(-12, -4, (n // 128, k // 128))).astype(np.float32)
+    dev = [torch.from_numpy(a).cuda() for a in (xq, xs, wq, ws)]
+    assert W.consume_device_error() == 0
+    W.debug_force_wait_timeout(True)
+    try:
+        W.fp8_block_gemm_pow2(*dev)
+        torch.cuda.synchronize()
+    finally:
+        W.debug_force_wait_timeout(False)
+    assert W.consume_device_error() == 55
+    y = W.fp8_block_gemm_pow2(*dev)
+    torch.cuda.synchronize()
+    assert W.consume_device_error() == 0
+    y_ref, absref = O.block_gemm(xq, xs, wq, ws)
+    assert_gemm_close(bits16(y), y_ref, absref, "pow2 after abort")
+
+
 def test_grouped_gemm_abort_then_recover(W):
     g, n, k, rows = 4, 256, 512, 200
     xq, xs, _, _ = _gemm_case(rows, n, k, seed=9)

@@ -18,7 +18,8 @@ __all__ = [
     "lib", "W8A8Error", "e4m3_encode_f32", "e4m3_decode_f32", "quantize_weight_blockwise",
     "quantize_weight_blockwise_batched", "quantize_act_per_token_group",
     "quantize_act_per_token_group_gather", "dequantize_blockwise", "quant_error_report",
-    "sqnr_db", "fp8_decode_attention", "dequantize_blockwise_batched", "quant_error_report_batched", "fp8_block_gemm",
+    "sqnr_db", "fp8_decode_attention", "dequantize_blockwise_batched", "quant_error_report_batched",
+    "fp8_block_gemm", "fp8_block_gemm_pow2",
     "fp8_grouped_gemm", "kv_amax_quantize", "w8a8_linear", "consume_device_error",
     "GEMM_STATIC_WEIGHTS", "LINEAR_SINGLE_KERNEL", "debug_force_wait_timeout",
     "KV_AMAX_AND_QUANT", "KV_AMAX_ONLY", "KV_QUANT_ONLY", "LIB_PATH",
@@ -64,6 +65,7 @@ _SIGNATURES = {
                                     ctypes.c_float, _P, _P]),
     "fp8_block_gemm": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "fp8_block_gemm_ex": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_uint32, _P]),
+    "fp8_block_gemm_pow2": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "w8a8_linear": (_INT, [_P, _I64, _I64, _P, _P, _I64, _P, _P, _P, ctypes.c_uint32, _P]),
     "fp8_grouped_gemm": (_INT, [_P, _P, _I64, _P, _P, _I32, _I64, _P, _P, _P, _I64, _I64, _P]),
     "kv_amax_quantize": (_INT, [_P, _I64, _P, _P, _P, _INT, _P]),
@@ -317,6 +319,19 @@ def fp8_block_gemm(xq, xs, wq, ws, y=None, stream=None, static_weights=False):
     else:
         _check("fp8_block_gemm", lib().fp8_block_gemm(_ptr(xq), _ptr(xs), _ptr(wq), _ptr(ws),
                                                       _ptr(y), m, n, k, _stream(stream)))
+    return y
+
+
+def fp8_block_gemm_pow2(xq, xs, wq, ws, y=None, stream=None):
+    """Y = X W^T for power-of-two scales (the *_pow2 quantizers' output) on
+    the block-scaled MMA; returns BF16 [m, n]."""
+    _need(xq, torch.uint8, "xq")
+    _need(wq, torch.uint8, "wq")
+    m, k = xq.shape
+    n = wq.shape[0]
+    y = torch.empty((m, n), dtype=torch.bfloat16, device=xq.device) if y is None else y
+    _check("fp8_block_gemm_pow2", lib().fp8_block_gemm_pow2(_ptr(xq), _ptr(xs), _ptr(wq), _ptr(ws),
+                                                            _ptr(y), m, n, k, _stream(stream)))
     return y
 
 

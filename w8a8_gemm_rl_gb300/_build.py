@@ -14,7 +14,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "libw8a8fp8.so")
 BUILD = os.path.join(ROOT, "_build")
-SOURCES = ["api.cu", "quant.cu", "gemm.cu", "gemm_small_m.cu", "dequant.cu", "batch.cu", "attention.cu"]
+SOURCES = ["api.cu", "quant.cu", "gemm.cu", "gemm_small_m.cu", "gemm_pow2.cu", "dequant.cu", "batch.cu", "attention.cu"]
 HEADERS = ["common.cuh", "ptx.cuh", "kernels.h"]
 
 NVCC = os.environ.get("NVCC", shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc")

@@ -12,6 +12,8 @@
 namespace w8a8 {
 cudaError_t consume_device_error(int* code);
 cudaError_t consume_small_gemm_error(int* code);
+cudaError_t consume_pow2_gemm_error(int* code);
+cudaError_t set_pow2_gemm_force_timeout(int on);
 cudaError_t set_gemm_force_timeout(int on);
 cudaError_t set_small_gemm_force_timeout(int on);
 cudaError_t set_quant_force_timeout(int on);
@@ -327,6 +329,16 @@ W8A8_API w8a8_status fp8_block_gemm(const uint8_t* xq, const float* xs, const ui
   return fp8_block_gemm_ex(xq, xs, wq, ws, y_bf16, m, n, k, 0u, stream);
 }
 
+W8A8_API w8a8_status fp8_block_gemm_pow2(const uint8_t* xq, const float* xs, const uint8_t* wq,
+                                         const float* ws, uint16_t* y_bf16, int64_t m, int64_t n,
+                                         int64_t k, w8a8_stream_t stream) {
+  if (m < 0 || n < 0 || k < 0 || m >= kMaxDim) return W8A8_ERR_SHAPE;
+  if (m == 0 || n == 0) return (k % 16 == 0 && n % 8 == 0) ? W8A8_OK : W8A8_ERR_SHAPE;
+  w8a8_status st = check_gemm_common(xq, xs, wq, ws, y_bf16, n, k);
+  if (st != W8A8_OK) return st;
+  return from_cuda(w8a8::launch_block_gemm_pow2(xq, xs, wq, ws, y_bf16, m, n, k, cs(stream)));
+}
+
 W8A8_API w8a8_status w8a8_linear(const uint16_t* x_bf16, int64_t m, int64_t k, const uint8_t* wq,
                                  const float* ws, int64_t n, uint16_t* y_bf16, uint8_t* xq,
                                  float* xs, uint32_t flags, w8a8_stream_t stream) {
@@ -397,12 +409,14 @@ W8A8_API w8a8_status kv_amax_quantize(const uint16_t* x_bf16, int64_t numel, uin
 
 W8A8_API w8a8_status w8a8_consume_device_error(int* code) {
   if (!code) return W8A8_ERR_NULL;
-  int g = 0, sg = 0, q = 0, a = 0, bt = 0;
+  int g = 0, sg = 0, pg = 0, q = 0, a = 0, bt = 0;
   w8a8_status st = from_cuda(w8a8::consume_device_error(&g));
   if (st != W8A8_OK) return st;
   st = from_cuda(w8a8::consume_small_gemm_error(&sg));
   if (st != W8A8_OK) return st;
-  if (g == 0) g = sg;
+  st = from_cuda(w8a8::consume_pow2_gemm_error(&pg));
+  if (st != W8A8_OK) return st;
+  if (g == 0) g = sg != 0 ? sg : pg;
   st = from_cuda(w8a8::consume_batch_error(&bt));
   if (st != W8A8_OK) return st;
   st = from_cuda(w8a8::consume_quant_error(&q));
@@ -417,6 +431,8 @@ W8A8_API w8a8_status w8a8_debug_force_wait_timeout(int on) {
   w8a8_status st = from_cuda(w8a8::set_gemm_force_timeout(v));
   if (st != W8A8_OK) return st;
   st = from_cuda(w8a8::set_small_gemm_force_timeout(v));
+  if (st != W8A8_OK) return st;
+  st = from_cuda(w8a8::set_pow2_gemm_force_timeout(v));
   if (st != W8A8_OK) return st;
   return from_cuda(w8a8::set_quant_force_timeout(v));
 }

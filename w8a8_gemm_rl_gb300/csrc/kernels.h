@@ -68,6 +68,13 @@ cudaError_t launch_block_gemm(const uint8_t* xq, const float* xs, const uint8_t*
                               const float* ws, uint16_t* y, int64_t m, int64_t n, int64_t k,
                               cudaStream_t st);
 
+// The same GEMM for power-of-two scales on the block-scaled MMA
+// (gemm_pow2.cu): the scales become UE8M0 factors of the tensor cores'
+// products and the accumulator spans all of K.
+cudaError_t launch_block_gemm_pow2(const uint8_t* xq, const float* xs, const uint8_t* wq,
+                                   const float* ws, uint16_t* y, int64_t m, int64_t n, int64_t k,
+                                   cudaStream_t st);
+
 // The same GEMM for m <= 256 rows (gemm_small_m.cu): weights streamed once
 // by every SM, K split over a thread-block cluster.  static_weights: wq and
 // ws may be read while the previous kernel on the stream is still running.
