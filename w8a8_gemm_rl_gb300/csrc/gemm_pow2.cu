@@ -22,14 +22,14 @@
 //
 // Roles (persistent, one CTA per SM, 128 x 256 tiles):
 //   warps 0-3   scale factors: warp q writes each slab's factors into lane
-//               quarter q of a ring of 4 TMEM slots; lane 0 of warp 0 is also
-//               the producer: TMA of the A and B slabs into a 4-stage ring;
+//               quarter q of a ring of 4 TMEM slots;
 //   warps 4-11  epilogue: wait for a tile's accumulator, read it (32 rows x
 //               128 columns per warp), hand the accumulator back, round to
 //               BF16 and store through a swizzled staging area by TMA;
 //   warp 12     allocates 512 TMEM columns (accumulator 0..255, scale slots
 //               256..319); lane 0 issues 4 block-scaled MMAs per slab and
-//               commits.
+//               commits;
+//   warp 13     producer: TMA of the A and B slabs into a 3-stage ring.
 // Every mbarrier wait is bounded (2 s); a wait that gives up records an
 // error code (51..58) in this kernel's device error word, stops the other
 // roles, drains copies and MMAs in flight and frees TMEM.  A scale that is
@@ -51,7 +51,7 @@ __device__ int g_w8a8_pow2_gemm_force_timeout = 0;
 namespace p2 {
 
 constexpr int BM = 128, BN = 256, BK = 128;
-constexpr int STAGES = 4;
+constexpr int STAGES = 3;
 constexpr int A_BYTES = BM * BK, B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int SF_SLOTS = 4;
@@ -62,7 +62,9 @@ constexpr int TMEM_COLS = 512;
 constexpr int SF_WARPS = 4;
 constexpr int EPI_WARP0 = 4, NUM_EPI_WARPS = 8;
 constexpr int MMA_WARP = EPI_WARP0 + NUM_EPI_WARPS;
-constexpr int THREADS = 32 * (MMA_WARP + 1);
+constexpr int TMA_WARP = MMA_WARP + 1;
+constexpr int THREADS = 32 * (TMA_WARP + 1);
+constexpr int SF_AHEAD = 4;  // slabs of scales held in registers ahead of use
 constexpr int RASTER_M = 8;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr int STORE_COLS = 32;  // BF16 columns per TMA store box
@@ -179,7 +181,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
+  if (warp == TMA_WARP && lane == 0) {
     ptx::prefetch_tmap(&tmap_a);
     ptx::prefetch_tmap(&tmap_b);
     ptx::prefetch_tmap(&tmap_y);
@@ -196,15 +198,17 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int nkb = p.nkb;
 
   if (warp < SF_WARPS) {
-    // -------------------------------------------- scale factors + producer
+    // --------------------------------------------------------- scale factors
+    // Each slab's scales come from a register ring filled SF_AHEAD slabs
+    // ahead, so no slab waits for its loads; the ring index is static (the
+    // inner loop is unrolled).
     const uint32_t lane_q = (uint32_t)(warp * 32) << 16;  // this warp's lane quarter
-    uint32_t stage = 0, phase = 0, slot = 0, sphase = 0;
-    int64_t issued = 0;
+    uint32_t slot = 0, sphase = 0;
     bool ok = true;
     for (uint32_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
       const Tile T = decode_tile(p, t);
       const int nb0 = T.n0 / BN * 2;  // first 128-column weight-scale block
-      // lane l handles A rows 32c + l (c = 0..3); rows past m read row 0's
+      // lane l takes A rows 32c + l (c = 0..3); rows past m read row 0's
       // scale (their codes are zero, so any factor gives zero)
       const float* xsr[4];
 #pragma unroll
@@ -214,64 +218,80 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       const float* wsr0 = p.ws + (int64_t)min(nb0, p.nnb - 1) * nkb;
       const float* wsr1 = p.ws + (int64_t)min(nb0 + 1, p.nnb - 1) * nkb;
-      // scales of the next slab are loaded one slab ahead
-      float na[4], nw0, nw1;
+      float ra[SF_AHEAD][4], rw[SF_AHEAD][2];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) na[c] = xsr[c][0];
-      nw0 = wsr0[0];
-      nw1 = wsr1[0];
-      for (int kb = 0; kb < nkb; ++kb) {
-        float a[4];
+      for (int u = 0; u < SF_AHEAD; ++u) {
+        if (u < nkb) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) a[c] = na[c];
-        const float w0 = nw0, w1 = nw1;
-        if (kb + 1 < nkb) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) na[c] = xsr[c][kb + 1];
-          nw0 = wsr0[kb + 1];
-          nw1 = wsr1[kb + 1];
+          for (int c = 0; c < 4; ++c) ra[u][c] = xsr[c][u];
+          rw[u][0] = wsr0[u];
+          rw[u][1] = wsr1[u];
         }
-        uint32_t okw = 1;
-        if (lane == 0)
-          okw = ((warp != 0 || wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, 51)) &&
-                 wait_bar(sf_empty_bar(slot), sphase ^ 1u, abort_flag, 52)) ? 1u : 0u;
-        okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
-        if (!okw) { ok = false; break; }
-        ptx::tc_fence_after();
-        if (warp == 0 && lane == 0) {
+      }
+      for (int kb0 = 0; kb0 < nkb && ok; kb0 += SF_AHEAD) {
+#pragma unroll
+        for (int u = 0; u < SF_AHEAD; ++u) {
+          const int kb = kb0 + u;
+          if (kb >= nkb) break;
+          uint32_t okw = 1;
+          if (lane == 0) okw = wait_bar(sf_empty_bar(slot), sphase ^ 1u, abort_flag, 52) ? 1u : 0u;
+          okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+          if (!okw) { ok = false; break; }
+          ptx::tc_fence_after();
+          if (warp == 0 && !(ue8m0_exact(ra[u][0]) && ue8m0_exact(ra[u][1]) &&
+                             ue8m0_exact(ra[u][2]) && ue8m0_exact(ra[u][3]) &&
+                             ue8m0_exact(rw[u][0]) && ue8m0_exact(rw[u][1])))
+            record_error(59);
+          // slot `slot` of this warp's lane quarter: A columns 0..3, B
+          // columns 8..15 (B columns 0..127 of the tile take weight block
+          // nb0, 128..255 block nb0 + 1)
+          const uint32_t col = tmem_base + lane_q + SF_COL0 + slot * SF_SLOT_COLS;
+          const uint32_t b0 = ue8m0_x4(rw[u][0]), b1 = ue8m0_x4(rw[u][1]);
+          asm volatile(
+              "tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(col),
+              "r"(ue8m0_x4(ra[u][0])), "r"(ue8m0_x4(ra[u][1])), "r"(ue8m0_x4(ra[u][2])),
+              "r"(ue8m0_x4(ra[u][3]))
+              : "memory");
+          asm volatile(
+              "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
+                  col + SF_B_COL),
+              "r"(b0), "r"(b0), "r"(b0), "r"(b0), "r"(b1), "r"(b1), "r"(b1), "r"(b1)
+              : "memory");
+          // refill this ring entry with slab kb + SF_AHEAD
+          if (kb + SF_AHEAD < nkb) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) ra[u][c] = xsr[c][kb + SF_AHEAD];
+            rw[u][0] = wsr0[kb + SF_AHEAD];
+            rw[u][1] = wsr1[kb + SF_AHEAD];
+          }
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(sf_full_bar(slot));
+          if (++slot == SF_SLOTS) { slot = 0; sphase ^= 1u; }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == TMA_WARP) {
+    // -------------------------------------------------------------- producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      for (uint32_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        const Tile T = decode_tile(p, t);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, 51)) { ok = false; break; }
           const uint32_t sa = sbase + stage * STAGE_BYTES;
           ptx::mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
           ptx::tma_load_2d(sa, &tmap_a, full_bar(stage), kb * BK, (int)T.row0);
           ptx::tma_load_2d(sa + A_BYTES, &tmap_b, full_bar(stage), kb * BK, T.n0);
+          ++issued;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
-        ++issued;
-        // scale factors into TMEM slot `slot` (this warp's lane quarter): A
-        // columns 0..3, B columns 8..15 (B columns 0..127 of the tile take
-        // weight block nb0, 128..255 block nb0 + 1)
-        if (warp == 0 && !(ue8m0_exact(a[0]) && ue8m0_exact(a[1]) && ue8m0_exact(a[2]) && ue8m0_exact(a[3]) &&
-              ue8m0_exact(w0) && ue8m0_exact(w1)))
-          record_error(59);
-        const uint32_t col = tmem_base + lane_q + SF_COL0 + slot * SF_SLOT_COLS;
-        const uint32_t b0 = ue8m0_x4(w0), b1 = ue8m0_x4(w1);
-        asm volatile(
-            "tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(col),
-            "r"(ue8m0_x4(a[0])), "r"(ue8m0_x4(a[1])), "r"(ue8m0_x4(a[2])), "r"(ue8m0_x4(a[3]))
-            : "memory");
-        asm volatile(
-            "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
-                col + SF_B_COL),
-            "r"(b0), "r"(b0), "r"(b0), "r"(b0), "r"(b1), "r"(b1), "r"(b1), "r"(b1)
-            : "memory");
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(sf_full_bar(slot));
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-        if (++slot == SF_SLOTS) { slot = 0; sphase ^= 1u; }
       }
-    }
-    // no TMA copy may still be landing when the CTA retires
-    if (warp == 0 && lane == 0 && issued > 0) {
+      // no TMA copy may still be landing when the CTA retires
       const int64_t first = issued > STAGES ? issued - STAGES : 0;
       for (int64_t i = first; i < issued; ++i) {
         const uint64_t t0 = ptx::globaltimer();
