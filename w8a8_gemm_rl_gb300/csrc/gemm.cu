@@ -78,16 +78,18 @@ constexpr int NUM_BARS = 2 * STAGES + 4 + 1;  // full, empty, tfull[2], tempty[2
 constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
 enum Mode { DENSE = 0, GROUPED = 1, GATHER = 2 };
 // Output staging: each promotion warp writes its 32 rows x 128 columns, in
-// 128 / store_cols passes, into one of two private buffers of 32 rows x
-// store_cols BF16 columns laid out as the TMA's 64-byte (dense) or 32-byte
-// (grouped) swizzle, and one lane stores the box to global memory by TMA
-// while the next pass fills the other buffer (narrower for the grouped
-// modes, whose group tables also need room).
-constexpr int STAGE_BUFS = 2;
+// 128 / store_cols passes, into private boxes of 32 rows x store_cols BF16
+// columns laid out as the TMA's 64-byte (dense) or 32-byte (grouped)
+// swizzle, one box per pass, and one lane stores each box to global memory
+// by TMA.  The boxes hold the warp's whole share of a tile, so a tile's
+// stores never wait for one another: the only wait, before the first pass,
+// is for the previous tile's stores to have read their boxes, long done.
+// The MMA meanwhile runs ahead into the next tile's first slabs, so a short
+// store phase keeps it from stalling at tile boundaries.
 __host__ __device__ constexpr int store_cols(int mode) { return mode == DENSE ? 32 : 16; }
 constexpr int OFF_STAGE = (OFF_MISC + 16 + 1023) / 1024 * 1024;  // swizzle atoms: 1024-byte aligned
 __host__ __device__ constexpr int stage_bytes(int mode) {
-  return NUM_EPI_WARPS * STAGE_BUFS * 32 * store_cols(mode) * 2;
+  return NUM_EPI_WARPS * 32 * 128 * 2;  // (128 / store_cols) boxes of 32 x store_cols per warp
 }
 __host__ __device__ constexpr int off_groups(int mode) { return OFF_STAGE + stage_bytes(mode); }
 __host__ __device__ constexpr int smem_bytes(int mode, int g) { return 1024 + off_groups(mode) + 2 * 4 * (g + 1); }
@@ -481,9 +483,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr int RPI = 32 / CPR;  // rows per warp-wide copy (partial-tile path)
     constexpr int SWZ_SHIFT = CPR == 8 ? 0 : (CPR == 4 ? 1 : 2);  // 128/64/32-byte swizzle
     constexpr uint32_t BUF_BYTES = 32 * SC * 2;
-    const uint32_t stg0 = sbase + OFF_STAGE + (uint32_t)ew * STAGE_BUFS * BUF_BYTES;
-    static_assert(STAGE_BUFS == 2, "one staging buffer in flight, one being written");
-    uint32_t nstores = 0;  // TMA stores this warp has issued (over all its tiles)
+    constexpr int PASSES = 128 / SC;
+    const uint32_t stg0 = sbase + OFF_STAGE + (uint32_t)ew * PASSES * BUF_BYTES;
     for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
       const int64_t cur_row0 = T.row0;
       const int cur_rows = T.rows;
@@ -536,17 +537,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       // the next tile's decode and first scale loads overlap the stores
       // (started inside the last slab instead, they slowed it down)
       if (t + gridDim.x < num_tiles) setup_tile(t + gridDim.x);
+      // the previous tile's TMA stores have read this warp's boxes
+      if (lane == 0) ptx::bulk_wait_read_0();
+      __syncwarp();
 #pragma unroll
-      for (int pass = 0; pass < 128 / SC; ++pass) {
+      for (int pass = 0; pass < PASSES; ++pass) {
         const int col0 = c0 + pass * SC;
         if (col0 >= p.n) break;  // columns past n (warp-uniform)
-        // the buffers alternate per TMA store issued, not per pass: the one
-        // written now is never the source of the newest store (which may
-        // still be reading the other), and every older store has read its
-        // source once all but the newest have
-        const uint32_t stg = stg0 + (nstores % STAGE_BUFS) * BUF_BYTES;
-        if (lane == 0) ptx::bulk_wait_read_1();
-        __syncwarp();
+        const uint32_t stg = stg0 + (uint32_t)pass * BUF_BYTES;
 #pragma unroll
         for (int ch = 0; ch < CPR; ++ch) {
           const int v = pass * CPR + ch;
@@ -564,7 +562,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             ptx::tma_store_2d(&tmap_y, stg, col0, (int)(cur_row0 + quarter * 32));
             ptx::bulk_commit();
           }
-          ++nstores;
         } else {
           __syncwarp();
 #pragma unroll
