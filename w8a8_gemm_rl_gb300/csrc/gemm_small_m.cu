@@ -119,6 +119,9 @@ struct Cfg {
   // gives them its share: 128 * 64 + 256 * 216 <= 384 * 168 (the launch's
   // register budget), and every warp returns to 168 for the reduction.
   static constexpr bool SPLIT_REGS = NT >= 256;
+  // unfused 256 tokens: the scale tables are loaded by every thread before
+  // the roles split; otherwise the promotion warps fetch them asynchronously
+  static constexpr bool SYNC_SCALES = NT >= 256 && !kFused;
   static constexpr int REGS_CTRL = 64, REGS_EPI = 216;
   static_assert(!SPLIT_REGS || (EPI_WARP0 == 4 && 128 * REGS_CTRL + 256 * REGS_EPI <= THREADS * 168),
                 "register split");
@@ -330,32 +333,28 @@ __global__ void __launch_bounds__(Cfg<NT, kFused>::THREADS, NT <= 64 ? 2 : 1)
       ptx::tma_load_2d(sbase + j * C::STAGE_BYTES, &tmap_w, full_bar(j), (kb0 + j) * BK, n0);
     }
   }
-  if (p.static_weights)
-    for (int j = threadIdx.x; j < nsl; j += C::THREADS)
-      ws_tab[j] = p.ws[(int64_t)tile * p.nkb + kb0 + j];
   // Launched as a programmatic dependent: everything above may overlap the
   // end of the previous kernel on the stream; nothing below runs before that
   // kernel has completed and its memory is visible.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // the CTA's scales: xs[token][kb0 .. kb0 + nsl) transposed to [slab][token]
-  // (tokens past m read as 0), and ws[tile][kb0 .. kb0 + nsl)
-  if (!kFused)
+  if (C::SYNC_SCALES) {
+    // 256 tokens: every thread loads the CTA's scales here (the promotion
+    // warps' register share has no room for the asynchronous fetch below)
     for (int i = threadIdx.x; i < NT * nsl; i += C::THREADS) {
       const int t = i / nsl, j = i - t * nsl;
       xs_tab[j * NT + t] = t < p.m ? p.xs[(int64_t)t * p.nkb + kb0 + j] : 0.0f;
     }
-  if (!p.static_weights)
     for (int j = threadIdx.x; j < nsl; j += C::THREADS)
       ws_tab[j] = p.ws[(int64_t)tile * p.nkb + kb0 + j];
+  }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  if (C::SPLIT_REGS) {
-    if (warp < 4) ptx::reg_dealloc<C::REGS_CTRL>(); else ptx::reg_alloc<C::REGS_EPI>();
-  }
-
+  // The register re-split is issued at the top of each side's branch: code
+  // after a join of the two would compile at the smaller share.
   if (warp < C::EPI_WARP0) {
+    if (C::SPLIT_REGS) ptx::reg_dealloc<C::REGS_CTRL>();
     if (warp == 0) {
       // ------------------------------------------------------------ producer
       // slabs [0, pre) were issued before the wait (pre <= STAGES)
@@ -559,10 +558,31 @@ __global__ void __launch_bounds__(Cfg<NT, kFused>::THREADS, NT <= 64 ? 2 : 1)
     const float2 none[C::COLS / 2] = {};
     reduce_store<NT, kFused, false>(p, smem, sbase, recv_bar, rank, split, n0, warp, lane, 0, none);
   } else {
+    if (C::SPLIT_REGS) ptx::reg_alloc<C::REGS_EPI>();
     // ------------------------------------------------------------ promotion
     const int ew = warp - C::EPI_WARP0;
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int c0 = (ew >> 2) * C::COLS;  // first token column of this warp
+    // The CTA's scales, fetched by these warps alone while the first slabs
+    // stream in: xs[token][kb0 .. kb0 + nsl) transposed to [slab][token]
+    // (tokens past m read as 0; thread et takes token et % NT, every
+    // (ET / NT)-th slab) and ws[tile][kb0 .. kb0 + nsl).
+    if (!C::SYNC_SCALES) {
+      const int et = threadIdx.x - 32 * C::EPI_WARP0;
+      constexpr int ET = 32 * C::EPI_WARPS;
+      static_assert(ET % NT == 0 || kFused, "whole tokens per thread group");
+      if (!kFused) {
+        const int t = et % NT;
+        const bool in = t < p.m;
+        const float* src = p.xs + (in ? (int64_t)t * p.nkb + kb0 : 0);
+        for (int j = et / NT; j < nsl; j += ET / NT)
+          ptx::cp_async_4(ptx::smem_addr(xs_tab + j * NT + t), in ? src + j : p.xs, in ? 4u : 0u);
+      }
+      for (int j = et; j < nsl; j += ET)
+        ptx::cp_async_4(ptx::smem_addr(ws_tab + j), p.ws + (int64_t)tile * p.nkb + kb0 + j, 4u);
+      ptx::cp_async_wait_all();
+      ptx::named_bar_sync(1, ET);
+    }
     float2 acc[C::COLS / 2];
 #pragma unroll
     for (int i = 0; i < C::COLS / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
@@ -657,19 +677,23 @@ static int max_active_clusters(int split) {
   return n;
 }
 
-// Split of K over a cluster: the waves of clusters (how many fit at once
-// comes from the occupancy query) times the slabs of each CTA, plus a small
-// cost per extra CTA of a split (its pipeline fill and its share of the
-// reduction), is made smallest.
+// Split of K over a cluster, chosen by a cost model fitted to timings of
+// the Qwen3-8B decode linears on GB300: a wave of clusters costs a fixed
+// part (launch, prologue, pipeline fill, reduction) worth FILL slabs plus
+// the slabs of each CTA, and the model makes waves x (FILL + slabs per CTA)
+// smallest.  The occupancy query counts one CTA per SM; up to 64 tokens two
+// CTAs share an SM, which doubles the clusters resident at once.
 template <int NT, bool kFused>
 static int choose_split(int tiles, int nkb) {
+  constexpr double FILL = NT <= 64 ? 23.0 : (NT <= 128 ? 20.0 : 13.0);
+  constexpr int PER_SM = (NT <= 64 && !kFused) ? 2 : 1;
   int best = MAX_SPLIT;
   double best_cost = 1e30;
   for (int s = 1; s <= std::min(MAX_SPLIT, nkb); ++s) {
     if ((nkb + s - 1) / s > Cfg<NT, kFused>::MAX_SLABS) continue;  // the scale table's size
-    const int fit = max_active_clusters<NT, kFused>(s);
+    const int fit = PER_SM * max_active_clusters<NT, kFused>(s);
     const double waves = (double)((tiles + fit - 1) / fit);
-    const double cost = waves * (double)((nkb + s - 1) / s) + 0.5 * (double)(s - 1) / MAX_SPLIT;
+    const double cost = waves * (FILL + (double)((nkb + s - 1) / s));
     if (cost < best_cost - 1e-9) { best_cost = cost; best = s; }
   }
   return best;
