@@ -373,13 +373,16 @@ def max_over_ranks(v, world):
 
 # DRAM bytes (read + written) of one launch of the batched weight quantizer
 # (144 matrices), from an ncu capture of the same kernel on one Qwen3-8B
-# layer's 4 matrices scaled by the 36 layers (traffic grows with the
-# elements), keyed by a hash of the kernel's sources: any change to them
-# makes the figure stale, and it is then reported as null.
+# layer's 4 matrices, repeated launches with ncu's cache control off (so a
+# launch's writes include the codes the previous one left dirty in L2, and
+# a read-only flush after the last launch shows what it left), scaled by the
+# 36 layers (traffic grows with the elements).  Keyed by a hash of the
+# kernel's sources: any change to them makes the figure stale, and it is
+# then reported as null.
 WEIGHT_QUANT_SOURCES = ("quant.cu", "common.cuh", "ptx.cuh", "tmap.h")
 WEIGHT_QUANT_TRAFFIC = {
-    # profiles/weight_quant_batched_qwen3_8b_layer.md: 36 x (385.9 + 151.4) MB
-    "8a0837605b3b16d0": 36 * (385918976 + 151399680),
+    # profiles/weight_quant_batched_qwen3_8b_layer.md: 36 x (385.9 + 192.2) MB
+    "b415e07fd20282fb": 36 * (385890816 + 192173056),
 }
 
 
