@@ -104,7 +104,7 @@ struct Cfg {
   static constexpr int OFF_WS = OFF_XS + XS_BYTES;
   static constexpr int OFF_BARS = OFF_WS + WS_BYTES;
   // full, empty, sfull, sempty, tfull[2], tempty[2], done, recv
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * SLOTS + 4 + 2;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * SLOTS + 4 + 3;  // + done, recv, scales
   static constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
   static constexpr int SMEM = 1024 + OFF_MISC + 16;
   static constexpr uint32_t IDESC = ptx::idesc_e4m3_f32(BW, NT);
@@ -119,9 +119,11 @@ struct Cfg {
   // gives them its share: 128 * 64 + 256 * 216 <= 384 * 168 (the launch's
   // register budget), and every warp returns to 168 for the reduction.
   static constexpr bool SPLIT_REGS = NT >= 256;
-  // unfused 256 tokens: the scale tables are loaded by every thread before
-  // the roles split; otherwise the promotion warps fetch them asynchronously
-  static constexpr bool SYNC_SCALES = NT >= 256 && !kFused;
+  // Who fetches the CTA's scale tables (asynchronously, after the
+  // dependency wait): with 256 tokens the token loaders, which signal the
+  // promotion warps through an mbarrier (the promotion warps' register share
+  // has no room for the fetch); otherwise the promotion warps themselves.
+  static constexpr bool LOADER_SCALES = NT >= 256 && !kFused;
   static constexpr int REGS_CTRL = 64, REGS_EPI = 216;
   static_assert(!SPLIT_REGS || (EPI_WARP0 == 4 && 128 * REGS_CTRL + 256 * REGS_EPI <= THREADS * 168),
                 "register split");
@@ -272,6 +274,7 @@ __global__ void __launch_bounds__(Cfg<NT, kFused>::THREADS, NT <= 64 ? 2 : 1)
   auto tempty_bar = [&](int b) { return bar0 + 8u * (TB0 + 2 + b); };
   const uint32_t done_bar = bar0 + 8u * (TB0 + 4);
   const uint32_t recv_bar = bar0 + 8u * (TB0 + 5);
+  const uint32_t scales_bar = bar0 + 8u * (TB0 + 6);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   // unfused: xs of every slab [slab][token]; fused: the scale-slot ring
@@ -307,6 +310,7 @@ __global__ void __launch_bounds__(Cfg<NT, kFused>::THREADS, NT <= 64 ? 2 : 1)
     // CTA owns (armed before any peer can send: they send only after a
     // cluster barrier that follows this)
     ptx::mbar_init(recv_bar, 1);
+    ptx::mbar_init(scales_bar, 32 * C::XW);  // the token loaders' lanes
     {
       const int mh = min(128, p.m);
       const int cnt = owned_lo(rank + 1, mh, split) - owned_lo(rank, mh, split);
@@ -337,16 +341,6 @@ __global__ void __launch_bounds__(Cfg<NT, kFused>::THREADS, NT <= 64 ? 2 : 1)
   // end of the previous kernel on the stream; nothing below runs before that
   // kernel has completed and its memory is visible.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (C::SYNC_SCALES) {
-    // 256 tokens: every thread loads the CTA's scales here (the promotion
-    // warps' register share has no room for the asynchronous fetch below)
-    for (int i = threadIdx.x; i < NT * nsl; i += C::THREADS) {
-      const int t = i / nsl, j = i - t * nsl;
-      xs_tab[j * NT + t] = t < p.m ? p.xs[(int64_t)t * p.nkb + kb0 + j] : 0.0f;
-    }
-    for (int j = threadIdx.x; j < nsl; j += C::THREADS)
-      ws_tab[j] = p.ws[(int64_t)tile * p.nkb + kb0 + j];
-  }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -533,6 +527,23 @@ __global__ void __launch_bounds__(Cfg<NT, kFused>::THREADS, NT <= 64 ? 2 : 1)
       const int w = warp - 2;
       const int q = lane >> 3, c = lane & 7;
       constexpr int ITERS = NT / (4 * C::XW);
+      if (C::LOADER_SCALES) {
+        // the CTA's scale tables first: xs[token][kb0 .. kb0 + nsl) transposed
+        // to [slab][token] (tokens past m read as 0; loader thread lt takes
+        // token lt % 32 + 32 i, every slab) and ws[tile][kb0 .. kb0 + nsl);
+        // their arrival is signalled on scales_bar
+        const int lt = threadIdx.x - 64;
+        constexpr int LT = 32 * C::XW;
+        for (int t = lt; t < NT; t += LT) {
+          const bool in = t < p.m;
+          const float* src = p.xs + (in ? (int64_t)t * p.nkb + kb0 : 0);
+          for (int j = 0; j < nsl; ++j)
+            ptx::cp_async_4(ptx::smem_addr(xs_tab + j * NT + t), in ? src + j : p.xs, in ? 4u : 0u);
+        }
+        for (int j = lt; j < nsl; j += LT)
+          ptx::cp_async_4(ptx::smem_addr(ws_tab + j), p.ws + (int64_t)tile * p.nkb + kb0 + j, 4u);
+        ptx::cp_async_arrive_noinc(scales_bar);
+      }
       uint32_t stage = 0, phase = 0;
       for (int j = 0; j < nsl; ++j) {
         uint32_t okw = 1;
@@ -567,7 +578,13 @@ __global__ void __launch_bounds__(Cfg<NT, kFused>::THREADS, NT <= 64 ? 2 : 1)
     // stream in: xs[token][kb0 .. kb0 + nsl) transposed to [slab][token]
     // (tokens past m read as 0; thread et takes token et % NT, every
     // (ET / NT)-th slab) and ws[tile][kb0 .. kb0 + nsl).
-    if (!C::SYNC_SCALES) {
+    if (C::LOADER_SCALES) {
+      // the token loaders' fetch of the scale tables has landed
+      uint32_t okw = 1;
+      if (lane == 0) okw = wait_bar(scales_bar, 0, abort_flag, 32) ? 1u : 0u;
+      okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+      (void)okw;  // on a timeout the abort flag stops the loop below
+    } else {
       const int et = threadIdx.x - 32 * C::EPI_WARP0;
       constexpr int ET = 32 * C::EPI_WARPS;
       static_assert(ET % NT == 0 || kFused, "whole tokens per thread group");
