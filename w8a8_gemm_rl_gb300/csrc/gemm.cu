@@ -80,16 +80,21 @@ enum Mode { DENSE = 0, GROUPED = 1, GATHER = 2 };
 // Output staging: each promotion warp writes its 32 rows x 128 columns, in
 // 128 / store_cols passes, into private boxes of 32 rows x store_cols BF16
 // columns laid out as the TMA's 64-byte (dense) or 32-byte (grouped)
-// swizzle, one box per pass, and one lane stores each box to global memory
-// by TMA.  The boxes hold the warp's whole share of a tile, so a tile's
-// stores never wait for one another: the only wait, before the first pass,
-// is for the previous tile's stores to have read their boxes, long done.
-// The MMA meanwhile runs ahead into the next tile's first slabs, so a short
-// store phase keeps it from stalling at tile boundaries.
+// swizzle, and one lane stores each box to global memory by TMA.
+//  * dense: two boxes, alternating per TMA store issued (not per pass: a
+//    partial last N tile issues fewer stores than passes, and the box
+//    written next must never be the source of the newest store, which
+//    cp.async.bulk.wait_group.read 1 does not retire);
+//  * grouped: one box per pass, the warp's whole share of a tile, so a
+//    tile's stores never wait for one another (the one wait, before the
+//    first pass, is for the previous tile's stores).
+// Measured: two boxes are 1.5% faster for the dense GEMM, whole-tile boxes
+// 2-3% faster for the grouped one.
 __host__ __device__ constexpr int store_cols(int mode) { return mode == DENSE ? 32 : 16; }
+__host__ __device__ constexpr int stage_boxes(int mode) { return mode == DENSE ? 2 : 128 / store_cols(mode); }
 constexpr int OFF_STAGE = (OFF_MISC + 16 + 1023) / 1024 * 1024;  // swizzle atoms: 1024-byte aligned
 __host__ __device__ constexpr int stage_bytes(int mode) {
-  return NUM_EPI_WARPS * 32 * 128 * 2;  // (128 / store_cols) boxes of 32 x store_cols per warp
+  return NUM_EPI_WARPS * stage_boxes(mode) * 32 * store_cols(mode) * 2;
 }
 __host__ __device__ constexpr int off_groups(int mode) { return OFF_STAGE + stage_bytes(mode); }
 __host__ __device__ constexpr int smem_bytes(int mode, int g) { return 1024 + off_groups(mode) + 2 * 4 * (g + 1); }
@@ -484,7 +489,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr int SWZ_SHIFT = CPR == 8 ? 0 : (CPR == 4 ? 1 : 2);  // 128/64/32-byte swizzle
     constexpr uint32_t BUF_BYTES = 32 * SC * 2;
     constexpr int PASSES = 128 / SC;
-    const uint32_t stg0 = sbase + OFF_STAGE + (uint32_t)ew * PASSES * BUF_BYTES;
+    constexpr int NBOX = stage_boxes(kMode);
+    constexpr bool WHOLE_TILE = NBOX == PASSES;
+    const uint32_t stg0 = sbase + OFF_STAGE + (uint32_t)ew * NBOX * BUF_BYTES;
+    uint32_t nstores = 0;  // TMA stores this warp has issued (over all its tiles)
     for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
       const int64_t cur_row0 = T.row0;
       const int cur_rows = T.rows;
@@ -537,14 +545,22 @@ __global__ void __launch_bounds__(THREADS, 1)
       // the next tile's decode and first scale loads overlap the stores
       // (started inside the last slab instead, they slowed it down)
       if (t + gridDim.x < num_tiles) setup_tile(t + gridDim.x);
-      // the previous tile's TMA stores have read this warp's boxes
-      if (lane == 0) ptx::bulk_wait_read_0();
-      __syncwarp();
+      if (WHOLE_TILE) {
+        // the previous tile's TMA stores have read this warp's boxes
+        if (lane == 0) ptx::bulk_wait_read_0();
+        __syncwarp();
+      }
 #pragma unroll
       for (int pass = 0; pass < PASSES; ++pass) {
         const int col0 = c0 + pass * SC;
         if (col0 >= p.n) break;  // columns past n (warp-uniform)
-        const uint32_t stg = stg0 + (uint32_t)pass * BUF_BYTES;
+        const uint32_t stg =
+            stg0 + (WHOLE_TILE ? (uint32_t)pass : (nstores & 1u)) * BUF_BYTES;
+        if (!WHOLE_TILE) {
+          // every store but the newest (from the other box) has read its box
+          if (lane == 0) ptx::bulk_wait_read_1();
+          __syncwarp();
+        }
 #pragma unroll
         for (int ch = 0; ch < CPR; ++ch) {
           const int v = pass * CPR + ch;
@@ -562,6 +578,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             ptx::tma_store_2d(&tmap_y, stg, col0, (int)(cur_row0 + quarter * 32));
             ptx::bulk_commit();
           }
+          ++nstores;
         } else {
           __syncwarp();
 #pragma unroll
