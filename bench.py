@@ -812,6 +812,7 @@ def measure_next_rows(W, wl, peaks, reps=3):
         "us": round(sec * 1e6, 1), "gbs": round(nb / sec / 1e9, 1),
         "pct_roofline": round(100 * nb / sec / 1e9 / peaks["hbm_gbs"], 2), "bytes_per_call": nb}
     out["fp8_block_gemm_pow2"] = measure_pow2_gemm(W, wl, peaks, reps)
+    out["config1_single_linear"] = measure_single_linear(W, peaks)
     W.quantize_weight_blockwise_batched(wl.w, wl.wout)
     for kind, nbytes in (("dequant", 3 * elems + 4 * blocks),
                          ("quant_error_report", 3 * elems + 4 * blocks + 24 * blocks)):
@@ -833,6 +834,77 @@ def measure_next_rows(W, wl, peaks, reps=3):
     del yall, sall
     assert W.consume_device_error() == 0
     return out
+
+
+def single_linear_work():
+    """Algorithmic work of one W8A8 linear of X [128, 512] and W [256, 512]
+    (both quantized, then the GEMM): FLOPs and bytes."""
+    m, n, k = 128, 256, 512
+    q_x = 2 * m * k + m * k + 4 * m * cdiv(k, 128)
+    q_w = 2 * n * k + n * k + 4 * cdiv(n, 128) * cdiv(k, 128)
+    g = m * k + n * k + 4 * (m * cdiv(k, 128) + cdiv(n, 128) * cdiv(k, 128)) + 2 * m * n
+    return 2 * m * n * k, q_x + q_w + g
+
+
+def measure_single_linear(W, peaks, reps=200):
+    """One W8A8 linear at the smallest configuration the pages give, X
+    [128, 512] ~ N(0,1) with 0.1% x50 outliers and W [256, 512] ~ N(0, 0.02)
+    (seeds 0 and 1): quantize W, quantize X, then the GEMM, as three eager
+    launches and as one CUDA-graph replay, and w8a8_linear (one kernel that
+    quantizes X on the way into the GEMM, W already quantized).  Latency-bound: microseconds per call
+    are the figure; the roofline share is nominal."""
+    from w8a8_gemm_rl_gb300 import synth
+    m, n, k = 128, 256, 512
+    x = synth.activations(m, k, seed=0, device="cuda")
+    w = synth.weights(n, k, seed=1, device="cuda")
+    xq = torch.empty((m, k), dtype=torch.uint8, device="cuda")
+    xs = torch.empty((m, cdiv(k, 128)), dtype=torch.float32, device="cuda")
+    wq = torch.empty((n, k), dtype=torch.uint8, device="cuda")
+    ws = torch.empty((cdiv(n, 128), cdiv(k, 128)), dtype=torch.float32, device="cuda")
+    y = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+
+    def three():
+        W.quantize_weight_blockwise(w, wq, ws)
+        W.quantize_act_per_token_group(x, xq, xs)
+        W.fp8_block_gemm(xq, xs, wq, ws, y)
+
+    def linear():
+        W.w8a8_linear(x, wq, ws, y)
+
+    def timed(fn):
+        for _ in range(10):
+            fn()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(reps):
+            fn()
+        t1.record()
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) * 1e3 / reps
+
+    us_eager = timed(three)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        three()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            three()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    us_graph = timed(graph.replay)
+    us_linear = timed(linear)
+    assert W.consume_device_error() == 0
+    f, b = single_linear_work()
+    troof_us = t_roof(f, b, peaks) * 1e6
+    return {"workload": "X [128, 512] and W [256, 512], both quantized (1x128, 128x128) then the GEMM",
+            "us_three_launches": round(us_eager, 2), "us_graph": round(us_graph, 2),
+            "us_w8a8_linear": round(us_linear, 2), "troof_us": round(troof_us, 3),
+            "pct_roofline_graph": round(100 * troof_us / us_graph, 2),
+            "note": "launch- and latency-bound: the microseconds are the figure"}
 
 
 def measure_pow2_gemm(W, wl, peaks, reps=3):

@@ -81,3 +81,16 @@ def test_roofline_time_takes_the_binding_resource():
     assert bench.t_roof(2e12, 1e9, peaks) == pytest.approx(2e12 / (bench.FP8_OVER_BF16 * 500e12))
     assert bench.t_roof(1e11, 1e9, peaks) == pytest.approx(1e-3)
     assert bench.fp8_peak_tflops(peaks) == pytest.approx(1000.0)
+
+
+def test_single_linear_work():
+    """X [128, 512], W [256, 512]: 2 m n k FLOPs; the bytes of both
+    quantizers (2 B read + 1 B written per element + scales) and of the
+    GEMM (codes, scales, BF16 output)."""
+    f, b = bench.single_linear_work()
+    assert f == 2 * 128 * 256 * 512
+    q_x = 131072 + 65536 + 4 * 128 * 4
+    q_w = 262144 + 131072 + 4 * 2 * 4
+    gemm = 65536 + 131072 + 4 * (128 * 4 + 2 * 4) + 65536
+    assert b == q_x + q_w + gemm
+
