@@ -39,6 +39,9 @@ GEMM_SHAPES = [(1, 16, 128), (3, 136, 256), (128, 256, 512), (200, 512, 384), (2
                # N tiles and a partial last K slab
                (32, 128, 4096), (33, 256, 1024), (65, 384, 2048), (255, 136, 12288),
                (17, 1160, 400), (96, 128, 256),
+               # 256 rows: the cluster reduction in one round (splits up to 4) or in
+               # rounds of 128 rows
+               (256, 4096, 1024), (250, 2048, 2048),
                # few rows but K past the weight-streaming kernel's reach: the general kernel
                (3, 128, 32896)]
 

@@ -95,8 +95,10 @@ struct Cfg {
   static constexpr int TMEM_COLS = 2 * NT;  // a power of two >= 64
   static constexpr int RING = STAGES * STAGE_BYTES;
   // The reduction reuses the ring: a send area of up to NTR = min(NT, 128)
-  // token rows of 128 FP32, then a receive area of `split` slots of the
+  // token rows of 128 FP32, then a receive area of split - 1 slots of the
   // ceil(rows / split) token rows a CTA owns, at most NTR + split rows.
+  // With 256 tokens all rows go in one round where the send area and the
+  // slots fit below the barriers (the ring and the scale tables).
   static constexpr int NTR = NT < 128 ? NT : 128;
   static constexpr int RECV_OFF = NTR * BW * 4;
   static constexpr int RED_BYTES = RECV_OFF + (NTR + MAX_SPLIT) * BW * 4;
@@ -125,9 +127,26 @@ struct Cfg {
   // has no room for the fetch); otherwise the promotion warps themselves.
   static constexpr bool LOADER_SCALES = NT >= 256 && !kFused;
   static constexpr int REGS_CTRL = 64, REGS_EPI = 216;
+  // TMEM columns per promotion load step: 32 for 128 token columns (fewer,
+  // longer load round trips; measured 3-5% faster with 256 tokens), else 16
+  // (the fused kernel's registers hold no two 32-column buffers next to 128
+  // sums)
+  static constexpr int PROM_STEP = COLS >= 128 && !kFused ? 32 : 16;
   static_assert(!SPLIT_REGS || (EPI_WARP0 == 4 && 128 * REGS_CTRL + 256 * REGS_EPI <= THREADS * 168),
                 "register split");
 };
+
+// tcgen05.ld of N (16 or 32) consecutive columns, and the wait for it
+template <int N>
+__device__ __forceinline__ void tmem_load(uint32_t taddr, uint32_t (&r)[N]) {
+  if constexpr (N == 32) ptx::tmem_ld_32x32b_x32(taddr, r);
+  else ptx::tmem_ld_32x32b_x16(taddr, r);
+}
+template <int N>
+__device__ __forceinline__ void tmem_wait(uint32_t (&r)[N]) {
+  if constexpr (N == 32) ptx::tmem_wait_ld_dep32(r);
+  else ptx::tmem_wait_ld_dep(r);
+}
 
 struct Params {
   const uint8_t* xq;
@@ -169,6 +188,17 @@ __device__ __forceinline__ int owned_lo(int r, int m, int split) {
   return (int)((uint32_t)(r * m) / (uint32_t)split);
 }
 
+// Token rows the cluster reduction takes per round: all m at once where the
+// send area (m rows of 128 FP32) and the receive slots of the split - 1 peers
+// fit in the shared memory the main loop has finished with (the ring and the
+// scale tables), else rounds of 128.
+template <int NT, bool kFused>
+__device__ __forceinline__ int reduce_rows_per_round(int m, int split) {
+  if (NT <= 128) return m;
+  const int own = (m + split - 1) / split;
+  return (m + (split - 1) * own) * BW * 4 <= Cfg<NT, kFused>::OFF_BARS ? m : 128;
+}
+
 // The cluster reduction and the store of the output rows, run by every warp
 // of the CTA after its role in the main loop: the promotion warps pass their
 // sums (kAcc), the others take part in the barriers and the final sums.
@@ -181,58 +211,76 @@ __device__ __forceinline__ void reduce_store(const Params& p, uint8_t* smem, uin
                                              const float2 (&acc)[Cfg<NT, kFused>::COLS / 2]) {
   using C = Cfg<NT, kFused>;
   // -------------------------------------------------- cluster reduction
-  // In rounds of up to 128 token rows (two rounds when NT = 256):
-  //  1. a cluster barrier: every CTA has finished its main loop (or the
-  //     previous round), so its ring is free to stage and to receive;
+  // Per round of token rows (one round unless the shared memory is short):
+  //  1. arrive on the cluster barrier: this thread is past the main loop (or
+  //     the previous round's sums) -- every copy and MMA touching the ring
+  //     has been seen complete on an mbarrier, so the arrive is relaxed;
   //  2. the promotion threads store their partial sums as FP32 rows
-  //     [token][weight row] in the send area (consecutive lanes: consecutive
-  //     words);
-  //  3. one thread sends each peer the rows that peer owns with one bulk
-  //     copy into the peer's receive area, slot [sender rank], completing on
-  //     the peer's receive mbarrier;
-  //  4. once its own rows have arrived from every peer, a CTA adds them in
-  //     rank order (its own partial read in place), rounds to BF16 and
-  //     stores them.
-  // A last cluster barrier keeps every CTA alive until all copies out of it
-  // have landed (each receiver waits for its bytes before arriving there).
+  //     [token][weight row] in the send area at the start of the ring
+  //     (consecutive lanes: consecutive words) -- the ring is this CTA's own
+  //     and every slab in it has been consumed;
+  //  3. wait on the cluster barrier: every peer is past its main loop, so
+  //     its receive area (after its send area) is free;
+  //  4. lane q of warp 0 sends peer q the rows that peer owns with one bulk
+  //     copy into the peer's receive slot for this sender, completing on
+  //     the peer's receive mbarrier; lane 0 waits for this CTA's own rows;
+  //  5. arrive (relaxed) on the cluster barrier again: every copy into this
+  //     CTA has landed, as its receive mbarrier showed, so the senders'
+  //     areas are free;
+  //  6. the CTA adds its rows' partials in rank order (its own read in
+  //     place), rounds to BF16 and stores them;
+  //  7. wait on the cluster barrier: every copy out of this CTA has landed,
+  //     so it may reuse its send area or exit.
   const int m = p.m;
-  const int rounds = NT > 128 ? (m + 127) / 128 : 1;
+  const int rr = reduce_rows_per_round<NT, kFused>(m, split);
+  const int rounds = (m + rr - 1) / rr;
+  const int recv_off = rr * BW * 4;
   for (int h = 0; h < rounds; ++h) {
-    const int t0 = 128 * h;
-    const int mh = min(128, m - t0);
+    const int t0 = rr * h;
+    const int mh = min(rr, m - t0);
     const int own_rows = (mh + split - 1) / split;
     const int mlo = owned_lo(rank, mh, split), mhi = owned_lo(rank + 1, mh, split);
-    if (split > 1) ptx::cluster_sync(); else __syncthreads();
-    if (kAcc && c0 == t0) {
+    if (split > 1) ptx::cluster_arrive_relaxed();
+    if (kAcc && c0 < t0 + mh && c0 + C::COLS > t0) {
       const int row = (warp & 3) * 32 + lane;
       float* send = reinterpret_cast<float*>(smem);
 #pragma unroll
       for (int i = 0; i < C::COLS; ++i) {
-        if (i < mh) send[i * BW + row] = (i & 1) ? acc[i >> 1].y : acc[i >> 1].x;
+        const int u = c0 + i - t0;
+        if (u >= 0 && u < mh) send[u * BW + row] = (i & 1) ? acc[i >> 1].y : acc[i >> 1].x;
       }
       ptx::fence_proxy_async_smem();  // generic writes -> the bulk copies' reads
     }
     __syncthreads();
-    if (split > 1 && threadIdx.x == 0) {
-      for (int q = 0; q < split; ++q) {
+    if (split > 1) ptx::cluster_wait();
+    if (split > 1 && warp == 0) {
+      const int q = lane;
+      if (q < split && q != rank) {
         const int qlo = owned_lo(q, mh, split), qhi = owned_lo(q + 1, mh, split);
-        if (q == rank || qhi == qlo) continue;
-        const uint32_t dst = sbase + (uint32_t)(C::RECV_OFF + rank * own_rows * BW * 4);
-        ptx::bulk_copy_to_peer(ptx::mapa_shared(dst, (uint32_t)q),
-                               sbase + (uint32_t)(qlo * BW * 4), (uint32_t)((qhi - qlo) * BW * 4),
-                               ptx::mapa_shared(recv_bar, (uint32_t)q));
+        if (qhi > qlo) {
+          // a receiver's slots skip its own rank
+          const int slot = rank < q ? rank : rank - 1;
+          const uint32_t dst = sbase + (uint32_t)(recv_off + slot * own_rows * BW * 4);
+          ptx::bulk_copy_to_peer(ptx::mapa_shared(dst, (uint32_t)q),
+                                 sbase + (uint32_t)(qlo * BW * 4),
+                                 (uint32_t)((qhi - qlo) * BW * 4),
+                                 ptx::mapa_shared(recv_bar, (uint32_t)q));
+        }
       }
+    }
+    if (split > 1 && threadIdx.x == 0) {
       const uint64_t tw = ptx::globaltimer();
       while (!ptx::mbar_try_wait(recv_bar, (uint32_t)(h & 1))) {
         if (ptx::globaltimer() - tw > WAIT_LIMIT_NS) { record_error(37); break; }
       }
       if (h + 1 < rounds) {
-        const int mn = min(128, m - t0 - 128);
+        const int mn = min(rr, m - t0 - rr);
         const int cnt = owned_lo(rank + 1, mn, split) - owned_lo(rank, mn, split);
         ptx::mbar_arrive_expect_tx(recv_bar, (uint32_t)((split - 1) * cnt * BW * 4));
       }
     }
     __syncthreads();
+    if (split > 1) ptx::cluster_arrive_relaxed();
     // warp = token row, lane = 4 consecutive weight rows: 16-byte shared
     // loads, and a warp stores one 256-byte output row segment
     const int col4 = lane * 4;
@@ -240,7 +288,7 @@ __device__ __forceinline__ void reduce_store(const Params& p, uint8_t* smem, uin
       float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int q = 0; q < split; ++q) {
         const int off = q == rank ? (u * BW + col4) * 4
-                                  : C::RECV_OFF + ((q * own_rows + (u - mlo)) * BW + col4) * 4;
+                                  : recv_off + (((q < rank ? q : q - 1) * own_rows + (u - mlo)) * BW + col4) * 4;
         const float4 v = *reinterpret_cast<const float4*>(smem + off);
         s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
       }
@@ -251,8 +299,8 @@ __device__ __forceinline__ void reduce_store(const Params& p, uint8_t* smem, uin
         *reinterpret_cast<uint2*>(p.y + (int64_t)(t0 + u) * p.n + n0 + col4) = o;
       }
     }
+    if (split > 1) ptx::cluster_wait();
   }
-  if (split > 1) ptx::cluster_sync();
 }
 
 template <int NT, bool kFused>
@@ -312,7 +360,7 @@ __global__ void __launch_bounds__(Cfg<NT, kFused>::THREADS, NT <= 64 ? 2 : 1)
     ptx::mbar_init(recv_bar, 1);
     ptx::mbar_init(scales_bar, 32 * C::XW);  // the token loaders' lanes
     {
-      const int mh = min(128, p.m);
+      const int mh = reduce_rows_per_round<NT, kFused>(p.m, split);
       const int cnt = owned_lo(rank + 1, mh, split) - owned_lo(rank, mh, split);
       ptx::mbar_arrive_expect_tx(recv_bar, (uint32_t)((split - 1) * cnt * BW * 4));
     }
@@ -578,15 +626,14 @@ __global__ void __launch_bounds__(Cfg<NT, kFused>::THREADS, NT <= 64 ? 2 : 1)
     // stream in: xs[token][kb0 .. kb0 + nsl) transposed to [slab][token]
     // (tokens past m read as 0; thread et takes token et % NT, every
     // (ET / NT)-th slab) and ws[tile][kb0 .. kb0 + nsl).
+    const int et = threadIdx.x - 32 * C::EPI_WARP0;
+    constexpr int ET = 32 * C::EPI_WARPS;
     if (C::LOADER_SCALES) {
-      // the token loaders' fetch of the scale tables has landed
-      uint32_t okw = 1;
-      if (lane == 0) okw = wait_bar(scales_bar, 0, abort_flag, 32) ? 1u : 0u;
-      okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
-      (void)okw;  // on a timeout the abort flag stops the loop below
+      // the token loaders' fetch of the scale tables has landed: every lane
+      // waits on the barrier itself, since every lane reads the tables next
+      // (on a timeout the abort flag stops the loop below)
+      wait_bar(scales_bar, 0, abort_flag, 32);
     } else {
-      const int et = threadIdx.x - 32 * C::EPI_WARP0;
-      constexpr int ET = 32 * C::EPI_WARPS;
       static_assert(ET % NT == 0 || kFused, "whole tokens per thread group");
       if (!kFused) {
         const int t = et % NT;
@@ -598,6 +645,13 @@ __global__ void __launch_bounds__(Cfg<NT, kFused>::THREADS, NT <= 64 ? 2 : 1)
       for (int j = et; j < nsl; j += ET)
         ptx::cp_async_4(ptx::smem_addr(ws_tab + j), p.ws + (int64_t)tile * p.nkb + kb0 + j, 4u);
       ptx::cp_async_wait_all();
+      ptx::named_bar_sync(1, ET);
+    }
+    if (!kFused) {
+      // Each slab's token scales times the tile's weight scale, once per
+      // CTA: s[j][t] = xs[t][kb0 + j] * ws[tile][kb0 + j], the factor every
+      // partial of slab j, token t is multiplied by.
+      for (int i = et; i < nsl * NT; i += ET) xs_tab[i] *= ws_tab[i / NT];
       ptx::named_bar_sync(1, ET);
     }
     float2 acc[C::COLS / 2];
@@ -618,33 +672,42 @@ __global__ void __launch_bounds__(Cfg<NT, kFused>::THREADS, NT <= 64 ? 2 : 1)
       const float* slot = xs_tab + (kFused ? sl : j) * NT;
       const float2 w2 = make_float2(ws_tab[j], ws_tab[j]);
       const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + tb * NT + c0;
-      uint32_t ra[16], rb[16];
-      ptx::tmem_ld_32x32b_x16(tcol, ra);
-      ptx::tmem_wait_ld_dep(ra);
+      // The slab's partial comes out of TMEM STEP columns at a time, the
+      // next step's load in flight while the current one is multiplied in.
+      constexpr int STEP = C::PROM_STEP, NSTEP = C::COLS / STEP;
+      auto hand_back = [&]() {
+        // the buffer's last load has landed: hand it back to the MMA
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(tempty_bar(tb));
+      };
+      uint32_t ra[STEP], rb[STEP];
+      tmem_load<STEP>(tcol, ra);
+      tmem_wait<STEP>(ra);
+      if (NSTEP == 1) hand_back();
 #pragma unroll
-      for (int cc = 0; cc < C::COLS / 16; ++cc) {
-        uint32_t(&cur)[16] = (cc & 1) ? rb : ra;
-        uint32_t(&nxt)[16] = (cc & 1) ? ra : rb;
-        if (cc + 1 < C::COLS / 16) ptx::tmem_ld_32x32b_x16(tcol + (cc + 1) * 16, nxt);
+      for (int cc = 0; cc < NSTEP; ++cc) {
+        uint32_t(&cur)[STEP] = (cc & 1) ? rb : ra;
+        uint32_t(&nxt)[STEP] = (cc & 1) ? ra : rb;
+        if (cc + 1 < NSTEP) tmem_load<STEP>(tcol + (cc + 1) * STEP, nxt);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float4 x4 = *reinterpret_cast<const float4*>(slot + c0 + cc * 16 + 4 * e);
-          const float2 s01 = __fmul2_rn(make_float2(x4.x, x4.y), w2);
-          const float2 s23 = __fmul2_rn(make_float2(x4.z, x4.w), w2);
-          acc[cc * 8 + 2 * e] = __ffma2_rn(
+        for (int e = 0; e < STEP / 4; ++e) {
+          const float4 x4 = *reinterpret_cast<const float4*>(slot + c0 + cc * STEP + 4 * e);
+          float2 s01 = make_float2(x4.x, x4.y), s23 = make_float2(x4.z, x4.w);
+          if (kFused) {  // unfused: the table holds the products already
+            s01 = __fmul2_rn(s01, w2);
+            s23 = __fmul2_rn(s23, w2);
+          }
+          const int a = cc * (STEP / 2) + 2 * e;
+          acc[a] = __ffma2_rn(
               make_float2(__uint_as_float(cur[4 * e]), __uint_as_float(cur[4 * e + 1])), s01,
-              acc[cc * 8 + 2 * e]);
-          acc[cc * 8 + 2 * e + 1] = __ffma2_rn(
+              acc[a]);
+          acc[a + 1] = __ffma2_rn(
               make_float2(__uint_as_float(cur[4 * e + 2]), __uint_as_float(cur[4 * e + 3])), s23,
-              acc[cc * 8 + 2 * e + 1]);
+              acc[a + 1]);
         }
-        if (cc + 1 < C::COLS / 16) ptx::tmem_wait_ld_dep(nxt);
-        if (cc + 2 == C::COLS / 16) {
-          // the buffer's last load has landed: hand it back to the MMA
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(tempty_bar(tb));
-        }
+        if (cc + 1 < NSTEP) tmem_wait<STEP>(nxt);
+        if (cc + 2 == NSTEP) hand_back();
       }
       if (kFused) {
         // the slab's scales have been read: hand the slot back to the loaders

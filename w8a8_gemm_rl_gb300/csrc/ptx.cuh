@@ -173,6 +173,19 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// The two halves of cluster_sync, for work that fits between them: arrive
+// says this thread has reached a point; wait (acquire) returns once every
+// thread of the cluster has arrived.  Each thread alternates them.  The
+// relaxed arrive orders none of the thread's earlier memory operations: for
+// points whose preconditions were already observed complete through
+// mbarriers (copies and MMAs finished), where a release would only add the
+// cost of draining the thread's outstanding accesses.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 // Address of the same shared-memory location in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   uint32_t r;
