@@ -381,8 +381,8 @@ def max_over_ranks(v, world):
 # then reported as null.
 WEIGHT_QUANT_SOURCES = ("quant.cu", "common.cuh", "ptx.cuh", "tmap.h")
 WEIGHT_QUANT_TRAFFIC = {
-    # profiles/weight_quant_batched_qwen3_8b_layer.md: 36 x (385.9 + 192.2) MB
-    "b415e07fd20282fb": 36 * (385890816 + 192173056),
+    # profiles/weight_quant_batched_qwen3_8b_layer.md: 36 x (385.9 + 192.3) MB
+    "831b98e3d9eef423": 36 * (385895168 + 192344832),
 }
 
 
