@@ -67,7 +67,7 @@ const char *w8a8_last_cuda_error(void);
 
 /* Reads and clears the device-side error code that a kernel sets when a
  * bounded wait inside it gives up (0 = none; nonzero identifies the wait:
- * 1..8 the GEMMs of more than 256 rows and the grouped GEMM, 31..37 the
+ * 1..10 the GEMMs of more than 256 rows and the grouped GEMM, 31..37 the
  * GEMM of at most 256 rows, 51..58 the power-of-two GEMM (59: a scale it
  * cannot hold), 11..13 the weight quantizer, 21..22 the decode attention,
  * 41..43 the batched dequantizer and error report).  When several are set,

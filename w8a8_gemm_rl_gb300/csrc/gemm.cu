@@ -19,7 +19,10 @@
 //               of two 256-column TMEM buffers, then commits to mbarriers;
 //   warp 2      waits for each slab's MMAs and releases the promotion warps
 //               through a named barrier per TMEM buffer;
-//   warp 3      routed MoE rows: gathers A rows 64-127; otherwise idle;
+//   warp 3      stages each slab's scales (xs of the tile's rows, ws of its
+//               two column blocks) into a shared-memory ring, two slabs ahead;
+//               for routed MoE rows it gathers A rows 64-127 instead, and
+//               warp 2 stages the scales;
 //   warps 4..11 promotion: tcgen05.ld of the slab partial, acc += P * s in
 //               FP32 registers (128 per thread), release the TMEM buffer,
 //               and after the last slab round to BF16 and store.
@@ -74,7 +77,8 @@ constexpr uint32_t IDESC = ptx::idesc_e4m3_f32(BM, BN);
 
 // shared-memory map (offsets from a 1024-byte aligned base)
 constexpr int OFF_BARS = STAGES * STAGE_BYTES;
-constexpr int NUM_BARS = 2 * STAGES + 4 + 1;  // full, empty, tfull[2], tempty[2], done
+// full, empty, tfull[2], tempty[2], done, then the scale slots' sfull, sempty
+constexpr int NUM_BARS = 2 * STAGES + 4 + 1 + 2 * 4;
 constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
 enum Mode { DENSE = 0, GROUPED = 1, GATHER = 2 };
 // Output staging: each promotion warp writes its 32 rows x 128 columns, in
@@ -96,7 +100,19 @@ constexpr int OFF_STAGE = (OFF_MISC + 16 + 1023) / 1024 * 1024;  // swizzle atom
 __host__ __device__ constexpr int stage_bytes(int mode) {
   return NUM_EPI_WARPS * stage_boxes(mode) * 32 * store_cols(mode) * 2;
 }
-__host__ __device__ constexpr int off_groups(int mode) { return OFF_STAGE + stage_bytes(mode); }
+// The promotion's per-slab scales, staged by the hand-off warp: SCALE_SLOTS
+// slots, each the 128 row scales xs[row, kb] of the tile and its two
+// column-block scales ws[nb, kb] (padded to 16 bytes), filled
+// SCALE_LOOKAHEAD slabs ahead of the slab being released.
+constexpr int SCALE_SLOTS = 4;
+static_assert(NUM_BARS == 2 * STAGES + 5 + 2 * SCALE_SLOTS, "barrier count");
+constexpr int SCALE_LOOKAHEAD = 2;
+constexpr int SCALE_SLOT_FLOATS = 132;
+static_assert(SCALE_SLOTS >= SCALE_LOOKAHEAD + 2, "slots staged ahead plus the two in use");
+__host__ __device__ constexpr int off_scales(int mode) { return OFF_STAGE + stage_bytes(mode); }
+__host__ __device__ constexpr int off_groups(int mode) {
+  return off_scales(mode) + SCALE_SLOTS * SCALE_SLOT_FLOATS * 4;
+}
 __host__ __device__ constexpr int smem_bytes(int mode, int g) { return 1024 + off_groups(mode) + 2 * 4 * (g + 1); }
 static_assert(smem_bytes(DENSE, 1) <= 232448, "shared memory");
 static_assert(smem_bytes(GATHER, MAX_GROUPS) <= 232448, "shared memory");
@@ -183,6 +199,58 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, int64_t t, const in
   return T;
 }
 
+// A lane's share of one tile's scale sources: rows lane + 32 i (i < 4) of
+// xs (row index, or invalid: past the tile, past rows_x, or a routed index
+// out of range) and the tile's two column blocks of ws (first element of the
+// block's row of slabs, or invalid: past n).
+struct ScaleSrc {
+  int32_t row[4];
+  uint32_t row_ok;  // bit i: row[i] valid
+  int64_t blk[2];
+  uint32_t blk_ok;  // bit h: blk[h] valid
+};
+
+template <int kMode>
+__device__ __forceinline__ ScaleSrc scale_sources(const Params& p, const Tile& T, int lane) {
+  ScaleSrc S;
+  S.row_ok = 0;
+  S.blk_ok = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = lane + 32 * i;
+    int64_t sr = -1;
+    if (r < T.rows) sr = kMode == GATHER ? (int64_t)p.row_idx[T.row0 + r] : T.row0 + r;
+    const bool v = sr >= 0 && sr < p.rows_x;
+    S.row[i] = v ? (int32_t)sr : 0;
+    S.row_ok |= (v ? 1u : 0u) << i;
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int nb = (T.n0 >> 7) + h;
+    const bool v = nb < p.nnb;
+    S.blk[h] = ((int64_t)T.e * p.nnb + (v ? nb : 0)) * p.nkb;
+    S.blk_ok |= (v ? 1u : 0u) << h;
+  }
+  return S;
+}
+
+// Slab kb's scales into a slot: 128 row scales, then the two block scales
+// (4-byte cp.async; invalid sources write 0).
+__device__ __forceinline__ void stage_scales(const Params& p, const ScaleSrc& S, int kb,
+                                             uint32_t slot, int lane) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const bool v = (S.row_ok >> i) & 1u;
+    ptx::cp_async_4(slot + 4u * (uint32_t)(lane + 32 * i),
+                    v ? p.xs + (int64_t)S.row[i] * p.nkb + kb : p.xs, v ? 4u : 0u);
+  }
+  if (lane < 2) {
+    const bool v = (S.blk_ok >> lane) & 1u;
+    const int64_t b = lane == 0 ? S.blk[0] : S.blk[1];
+    ptx::cp_async_4(slot + 4u * (uint32_t)(128 + lane), v ? p.ws + b + kb : p.ws, v ? 4u : 0u);
+  }
+}
+
 template <int kMode>
 __global__ void __launch_bounds__(THREADS, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -198,6 +266,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
   auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
   const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 4);
+  auto sfull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 5 + s); };
+  auto sempty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 5 + SCALE_SLOTS + s); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
   int32_t* s_prefix = reinterpret_cast<int32_t*>(smem + off_groups(kMode));
@@ -216,6 +286,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       ptx::mbar_init(tempty_bar(b), NUM_EPI_WARPS);
     }
     ptx::mbar_init(done_bar, 1);
+    for (int s = 0; s < SCALE_SLOTS; ++s) {
+      ptx::mbar_init(sfull_bar(s), 32);  // the scale stager's lanes (cp.async arrivals)
+      ptx::mbar_init(sempty_bar(s), 1);  // the hand-off warp, once the slot is read
+    }
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -385,20 +459,94 @@ __global__ void __launch_bounds__(THREADS, 1)
     // abort (no more MMAs to wait for) the warp waits for that release
     // itself, which the promotion warps always make: they wait on nothing
     // but these barriers.
+    //
+    // Each slab's scales reach the promotion warps through shared memory, so
+    // that those warps keep no global load in flight across their barriers
+    // and fences (each of which would wait for it): slot j % SCALE_SLOTS (j
+    // counts the CTA's slabs) holds the tile's 128 row scales xs[source row,
+    // kb] and its two column-block scales ws[e, nb, kb]; rows past the tile or
+    // the operand, routed rows whose index lies outside [0, rows_x), and
+    // blocks past n read as 0 (their partial sums are 0).  The slots are
+    // filled SCALE_LOOKAHEAD slabs ahead by warp 3, which takes part in no
+    // barrier of the slab loop, and handed over through the sfull / sempty
+    // mbarriers: this warp releases slab j only once slab j's slot is full
+    // (every lane waits, so that the release follows the copies in each
+    // lane), and frees slab j - 2's slot once slab j's MMAs have finished
+    // (the promotion warps are then done with slab j - 2).  With routed rows
+    // warp 3 gathers operand rows instead, and this warp stages the scales
+    // itself with cp.async groups: slab j's copies are waited for before its
+    // release, and slab j + SCALE_LOOKAHEAD is staged right after it (issued
+    // before, they held the release up).
+    const uint32_t scale_ring = sbase + (uint32_t)off_scales(kMode);
+    auto slot_addr = [&](int64_t j) {
+      return scale_ring + (uint32_t)((j % SCALE_SLOTS) * SCALE_SLOT_FLOATS * 4);
+    };
+    // routed rows: load cursor (tile, slab, CTA slab count) for the staging
+    int64_t lt = blockIdx.x;
+    int lkb = 0;
+    int64_t lj = 0;
+    ScaleSrc src{};
+    auto stage_next = [&]() {  // one commit group per call (empty past the end)
+      if (lt < num_tiles) {
+        stage_scales(p, src, lkb, slot_addr(lj), lane);
+        ++lj;
+        if (++lkb == nkb) {
+          lkb = 0;
+          lt += gridDim.x;
+          if (lt < num_tiles) src = scale_sources<kMode>(p, decode_tile<kMode>(p, lt, s_prefix, s_start), lane);
+        }
+      }
+      ptx::cp_async_commit();
+    };
+    if (kMode == GATHER) {
+      if (lt < num_tiles) src = scale_sources<kMode>(p, decode_tile<kMode>(p, lt, s_prefix, s_start), lane);
+#pragma unroll 1
+      for (int i = 0; i < SCALE_LOOKAHEAD; ++i) stage_next();
+    }
     uint32_t tb = 0, tphase = 0;
     bool ok = true;
+    int64_t j = 0;
     for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-      for (int kb = 0; kb < nkb; ++kb) {
+      for (int kb = 0; kb < nkb; ++kb, ++j) {
         if (lane == 0) {
           if (ok) ok = wait_bar(tfull_bar(tb), tphase, abort_flag, 7);
           if (!ok && !ptx::mbar_wait(tempty_bar(tb), tphase ^ 1u, ABORT_DRAIN_LIMIT_NS))
             record_error(8);
         }
+        if (kMode == GATHER) {
+          ptx::cp_async_wait_group<SCALE_LOOKAHEAD - 1>();
+        } else if (!*abort_flag) {
+          wait_bar(sfull_bar((int)(j % SCALE_SLOTS)), (uint32_t)((j / SCALE_SLOTS) & 1), abort_flag,
+                   10);
+        }
         __syncwarp();
         ptx::named_bar_arrive(BAR_SLAB + tb, BAR_SLAB_THREADS);
+        if (kMode == GATHER) stage_next();
+        else if (lane == 0 && j >= 2) ptx::mbar_arrive(sempty_bar((int)((j - 2) % SCALE_SLOTS)));
         if (++tb == 2) { tb = 0; tphase ^= 1u; }
       }
     }
+    if (kMode == GATHER) ptx::cp_async_wait_all();
+  } else if (kMode != GATHER && warp == 3) {
+    // ------------------------------------------------------ scale staging
+    // Fills slab j's slot (above) once slab j - SCALE_SLOTS's slot is free,
+    // by 4-byte cp.async whose completion arrives on the slot's sfull.
+    // Every lane waits for the slot itself, before its copies overwrite it.
+    const uint32_t scale_ring = sbase + (uint32_t)off_scales(kMode);
+    int64_t j = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      const ScaleSrc src = scale_sources<kMode>(p, decode_tile<kMode>(p, t, s_prefix, s_start), lane);
+      for (int kb = 0; kb < nkb; ++kb, ++j) {
+        const int sl = (int)(j % SCALE_SLOTS);
+        const bool okl = wait_bar(sempty_bar(sl), (uint32_t)(((j / SCALE_SLOTS) & 1) ^ 1),
+                                  abort_flag, 9);
+        if (!__all_sync(0xFFFFFFFFu, okl)) { ok = false; break; }
+        stage_scales(p, src, kb, scale_ring + (uint32_t)(sl * SCALE_SLOT_FLOATS * 4), lane);
+        ptx::cp_async_arrive_noinc(sfull_bar(sl));
+      }
+    }
+    ptx::cp_async_wait_all();
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issue
     if (lane == 0) {
@@ -452,37 +600,11 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     // per-tile state, filled for the next tile before the current one is stored
     Tile T;
-    bool row_ok = false, src_ok = false, nb_ok = false;
-    int64_t yrow = 0;
-    const float* xsr = p.xs;
-    const float* wsr = p.ws;
-    float a0 = 0.f, w0 = 0.f, a1 = 0.f, w1 = 0.f;
-    auto setup_tile = [&](int64_t t) {
-      T = decode_tile<kMode>(p, t, s_prefix, s_start);
-      row_ok = lrow < T.rows;
-      yrow = T.row0 + lrow;
-      int64_t src = yrow;
-      src_ok = row_ok;
-      if (kMode == GATHER && row_ok) {
-        src = p.row_idx[yrow];
-        src_ok = src >= 0 && src < p.rows_x;
-      }
-      const int nb = (T.n0 >> 7) + half;
-      nb_ok = nb < p.nnb;
-      // A row or B column outside the operands reads zeros (TMA fill or the
-      // gather's zero fill), so its partial is 0 whatever the scale: such a
-      // row takes row 0's scales (a valid address) and the loads need no
-      // condition -- a select on a load result would wait for the load here
-      xsr = p.xs + (src_ok ? src : 0) * (int64_t)nkb;
-      wsr = p.ws + ((int64_t)T.e * p.nnb + (nb_ok ? nb : 0)) * nkb;
-      a0 = xsr[0];
-      w0 = wsr[0];
-      if (nkb > 1) {
-        a1 = xsr[1];
-        w1 = wsr[1];
-      }
-    };
+    auto setup_tile = [&](int64_t t) { T = decode_tile<kMode>(p, t, s_prefix, s_start); };
     if ((int64_t)blockIdx.x < num_tiles) setup_tile(blockIdx.x);
+    // this thread's row scale and column-block scale in each staged slot
+    const float* scales = reinterpret_cast<const float*>(smem + off_scales(kMode));
+    uint32_t js = 0;  // slabs of this CTA so far (slot = js % SCALE_SLOTS)
     constexpr int SC = store_cols(kMode);
     constexpr int CPR = SC / 8;  // 16-byte chunks per staged row
     constexpr int RPI = 32 / CPR;  // rows per warp-wide copy (partial-tile path)
@@ -501,15 +623,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int j = 0; j < 64; ++j) acc[j] = make_float2(0.0f, 0.0f);
       for (int kb = 0; kb < nkb; ++kb) {
-        const float s = a0 * w0;
-        a0 = a1;
-        w0 = w1;
-        if (kb + 2 < nkb) {
-          a1 = xsr[kb + 2];
-          w1 = wsr[kb + 2];
-        }
-        // the next tile's decode and first scale loads overlap the last slab
         ptx::named_bar_sync(BAR_SLAB + tb, BAR_SLAB_THREADS);  // slab kb is in TMEM buffer tb
+        const float* slot = scales + (js % SCALE_SLOTS) * SCALE_SLOT_FLOATS;
+        const float s = slot[lrow] * slot[128 + half];
+        ++js;
         ptx::tc_fence_after();
         const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + tb * BN + half * 128;
         const float2 s2 = make_float2(s, s);
