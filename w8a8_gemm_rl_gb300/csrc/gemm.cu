@@ -508,16 +508,18 @@ __global__ void __launch_bounds__(THREADS, 1)
     int64_t j = 0;
     for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
       for (int kb = 0; kb < nkb; ++kb, ++j) {
-        if (lane == 0) {
-          if (ok) ok = wait_bar(tfull_bar(tb), tphase, abort_flag, 7);
-          if (!ok && !ptx::mbar_wait(tempty_bar(tb), tphase ^ 1u, ABORT_DRAIN_LIMIT_NS))
-            record_error(8);
-        }
+        // slab j's scales first: they are normally staged long before its
+        // MMAs finish, and the check then stays off the release's path
         if (kMode == GATHER) {
           ptx::cp_async_wait_group<SCALE_LOOKAHEAD - 1>();
         } else if (!*abort_flag) {
           wait_bar(sfull_bar((int)(j % SCALE_SLOTS)), (uint32_t)((j / SCALE_SLOTS) & 1), abort_flag,
                    10);
+        }
+        if (lane == 0) {
+          if (ok) ok = wait_bar(tfull_bar(tb), tphase, abort_flag, 7);
+          if (!ok && !ptx::mbar_wait(tempty_bar(tb), tphase ^ 1u, ABORT_DRAIN_LIMIT_NS))
+            record_error(8);
         }
         __syncwarp();
         ptx::named_bar_arrive(BAR_SLAB + tb, BAR_SLAB_THREADS);
