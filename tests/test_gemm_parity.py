@@ -97,11 +97,12 @@ def test_decode_chain_static_weights(W, m):
     assert torch.equal(ya.view(torch.int16), yb.view(torch.int16))
 
 
-@pytest.mark.parametrize("m,n,k", [(2305, 2312, 48), (5000, 776, 32)])
+@pytest.mark.parametrize("m,n,k", [(2305, 2312, 48), (5000, 776, 32), (1100, 2312, 48)])
 def test_block_gemm_partial_last_n_tile_several_waves(W, m, n, k):
     """More tiles than SMs, with a last N tile of 8 columns: a CTA's epilogue
     stores that tile with a single TMA store and starts its next tile at once.
-    Called three times, since a staging-buffer race shows only in some runs."""
+    Called three times, since a staging-buffer race shows only in some runs.
+    1100 x 2312 runs the 128-wide tiles (90 tiles 256 wide, 171 128 wide)."""
     xq, wq = _codes((m, k), m + k), _codes((n, k), n + 7 * k)
     xs, ws = _scales((m, _cdiv(k, 128)), 1), _scales((_cdiv(n, 128), _cdiv(k, 128)), 2)
     y_ref, absref = O.block_gemm(xq, xs, wq, ws)

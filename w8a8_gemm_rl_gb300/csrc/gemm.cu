@@ -50,12 +50,15 @@ __device__ int g_w8a8_gemm_force_timeout = 0;
 namespace gemm {
 
 constexpr int BM = 128;
+// Tile width: 256 columns, or 128 for the dense GEMM when 256-wide tiles
+// would leave SMs idle (few rows); each of the 8 promotion warps takes half.
 constexpr int BN = 256;
+constexpr int BN_NARROW = 128;
 constexpr int BK = 128;  // FP8 elements = bytes = one 128-byte swizzle row
 constexpr int STAGES = 3;
 constexpr int A_BYTES = BM * BK;
-constexpr int B_BYTES = BN * BK;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+__host__ __device__ constexpr int b_bytes(int bn) { return bn * BK; }
+__host__ __device__ constexpr int ring_stage_bytes(int bn) { return A_BYTES + b_bytes(bn); }
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int EPI_WARP0 = 4;  // warpgroup 0: producer, MMA, hand-off, gather
 constexpr int THREADS = 32 * EPI_WARP0 + 32 * NUM_EPI_WARPS;
@@ -64,7 +67,6 @@ constexpr int THREADS = 32 * EPI_WARP0 + 32 * NUM_EPI_WARPS;
 // 128 * 72 + 256 * 216 = 64512.
 constexpr int REGS_LAUNCH = 168, REGS_CTRL = 72, REGS_EPI = 216;
 static_assert(128 * REGS_CTRL + 256 * REGS_EPI <= THREADS * REGS_LAUNCH, "register split");
-constexpr int TMEM_COLS = 2 * BN;
 constexpr int RASTER_M = 8;
 constexpr int MAX_GROUPS = 1024;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
@@ -73,16 +75,15 @@ constexpr uint64_t ABORT_DRAIN_LIMIT_NS = 10000000000ull;
 // TMEM buffer b to the promotion warps on barrier BAR_SLAB + b
 constexpr uint32_t BAR_SLAB = 1;
 constexpr uint32_t BAR_SLAB_THREADS = 32 * (1 + NUM_EPI_WARPS);
-constexpr uint32_t IDESC = ptx::idesc_e4m3_f32(BM, BN);
 
 // shared-memory map (offsets from a 1024-byte aligned base)
-constexpr int OFF_BARS = STAGES * STAGE_BYTES;
+__host__ __device__ constexpr int off_bars(int bn) { return STAGES * ring_stage_bytes(bn); }
 // full, empty, tfull[2], tempty[2], done, then the scale slots' sfull, sempty
 constexpr int NUM_BARS = 2 * STAGES + 4 + 1 + 2 * 4;
-constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
+__host__ __device__ constexpr int off_misc(int bn) { return off_bars(bn) + NUM_BARS * 8; }
 enum Mode { DENSE = 0, GROUPED = 1, GATHER = 2 };
-// Output staging: each promotion warp writes its 32 rows x 128 columns, in
-// 128 / store_cols passes, into private boxes of 32 rows x store_cols BF16
+// Output staging: each promotion warp writes its 32 rows x bn / 2 columns, in
+// bn / 2 / store_cols passes, into private boxes of 32 rows x store_cols BF16
 // columns laid out as the TMA's 64-byte (dense) or 32-byte (grouped)
 // swizzle, and one lane stores each box to global memory by TMA.
 //  * dense: two boxes, alternating per TMA store issued (not per pass: a
@@ -95,10 +96,13 @@ enum Mode { DENSE = 0, GROUPED = 1, GATHER = 2 };
 // Measured: two boxes are 1.5% faster for the dense GEMM, whole-tile boxes
 // 2-3% faster for the grouped one.
 __host__ __device__ constexpr int store_cols(int mode) { return mode == DENSE ? 32 : 16; }
-__host__ __device__ constexpr int stage_boxes(int mode) { return mode == DENSE ? 2 : 128 / store_cols(mode); }
-constexpr int OFF_STAGE = (OFF_MISC + 16 + 1023) / 1024 * 1024;  // swizzle atoms: 1024-byte aligned
-__host__ __device__ constexpr int stage_bytes(int mode) {
-  return NUM_EPI_WARPS * stage_boxes(mode) * 32 * store_cols(mode) * 2;
+__host__ __device__ constexpr int stage_boxes(int mode, int bn) {
+  return mode == DENSE ? 2 : bn / 2 / store_cols(mode);
+}
+// swizzle atoms: 1024-byte aligned
+__host__ __device__ constexpr int off_stage(int bn) { return (off_misc(bn) + 16 + 1023) / 1024 * 1024; }
+__host__ __device__ constexpr int stage_bytes(int mode, int bn) {
+  return NUM_EPI_WARPS * stage_boxes(mode, bn) * 32 * store_cols(mode) * 2;
 }
 // The promotion's per-slab scales, staged by the hand-off warp: SCALE_SLOTS
 // slots, each the 128 row scales xs[row, kb] of the tile and its two
@@ -109,13 +113,16 @@ static_assert(NUM_BARS == 2 * STAGES + 5 + 2 * SCALE_SLOTS, "barrier count");
 constexpr int SCALE_LOOKAHEAD = 2;
 constexpr int SCALE_SLOT_FLOATS = 132;
 static_assert(SCALE_SLOTS >= SCALE_LOOKAHEAD + 2, "slots staged ahead plus the two in use");
-__host__ __device__ constexpr int off_scales(int mode) { return OFF_STAGE + stage_bytes(mode); }
-__host__ __device__ constexpr int off_groups(int mode) {
-  return off_scales(mode) + SCALE_SLOTS * SCALE_SLOT_FLOATS * 4;
+__host__ __device__ constexpr int off_scales(int mode, int bn) { return off_stage(bn) + stage_bytes(mode, bn); }
+__host__ __device__ constexpr int off_groups(int mode, int bn) {
+  return off_scales(mode, bn) + SCALE_SLOTS * SCALE_SLOT_FLOATS * 4;
 }
-__host__ __device__ constexpr int smem_bytes(int mode, int g) { return 1024 + off_groups(mode) + 2 * 4 * (g + 1); }
-static_assert(smem_bytes(DENSE, 1) <= 232448, "shared memory");
-static_assert(smem_bytes(GATHER, MAX_GROUPS) <= 232448, "shared memory");
+__host__ __device__ constexpr int smem_bytes(int mode, int g, int bn) {
+  return 1024 + off_groups(mode, bn) + 2 * 4 * (g + 1);
+}
+static_assert(smem_bytes(DENSE, 1, BN) <= 232448, "shared memory");
+static_assert(smem_bytes(DENSE, 1, BN_NARROW) <= 232448, "shared memory");
+static_assert(smem_bytes(GATHER, MAX_GROUPS, BN) <= 232448, "shared memory");
 
 struct Params {
   const uint8_t* xq;
@@ -161,7 +168,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   }
 }
 
-template <int kMode>
+template <int kMode, int kBN>
 __device__ __forceinline__ Tile decode_tile(const Params& p, int64_t t, const int32_t* s_prefix,
                                             const int32_t* s_start) {
   Tile T;
@@ -179,7 +186,7 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, int64_t t, const in
     T.e = 0;
     T.row0 = (int64_t)mt * BM;
     T.rows = (int32_t)min64(BM, p.m - T.row0);
-    T.n0 = nt * BN;
+    T.n0 = nt * kBN;
   } else {
     const int32_t mt_all = (int32_t)(tt / (uint32_t)p.num_n_tiles);
     const int32_t nt = (int32_t)(tt - (uint32_t)mt_all * (uint32_t)p.num_n_tiles);
@@ -194,7 +201,7 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, int64_t t, const in
     T.e = lo;
     T.row0 = gstart + (int64_t)mt * BM;
     T.rows = (int32_t)min64(BM, gend - T.row0);
-    T.n0 = nt * BN;
+    T.n0 = nt * kBN;
   }
   return T;
 }
@@ -251,7 +258,7 @@ __device__ __forceinline__ void stage_scales(const Params& p, const ScaleSrc& S,
   }
 }
 
-template <int kMode>
+template <int kMode, int kBN>
 __global__ void __launch_bounds__(THREADS, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b,
@@ -260,7 +267,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = ptx::smem_addr(smem);
-  const uint32_t bar0 = sbase + OFF_BARS;
+  constexpr int STAGE_BYTES = ring_stage_bytes(kBN);
+  constexpr int TMEM_COLS = 2 * kBN;
+  constexpr uint32_t IDESC = ptx::idesc_e4m3_f32(BM, kBN);
+  constexpr int OFF_MISC = off_misc(kBN);
+  const uint32_t bar0 = sbase + off_bars(kBN);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
   auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
@@ -270,7 +281,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   auto sempty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 5 + SCALE_SLOTS + s); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
-  int32_t* s_prefix = reinterpret_cast<int32_t*>(smem + off_groups(kMode));
+  int32_t* s_prefix = reinterpret_cast<int32_t*>(smem + off_groups(kMode, kBN));
   int32_t* s_start = s_prefix + (p.g + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -359,7 +370,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (kMode != GATHER) {
       if (lane == 0) {
         for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-          const Tile T = decode_tile<kMode>(p, t, s_prefix, s_start);
+          const Tile T = decode_tile<kMode, kBN>(p, t, s_prefix, s_start);
           const int brow = T.e * p.n + T.n0;
           for (int kb = 0; kb < nkb; ++kb) {
             if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, 1)) { ok = false; break; }
@@ -388,7 +399,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t dofs_even = (uint32_t)((64 * w + q) * 128 + ((c ^ q) << 4));
       const uint32_t dofs_odd = (uint32_t)((64 * w + q) * 128 + ((c ^ (q | 4)) << 4));
       for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        const Tile T = decode_tile<kMode>(p, t, s_prefix, s_start);
+        const Tile T = decode_tile<kMode, kBN>(p, t, s_prefix, s_start);
         const int brow = T.e * p.n + T.n0;
         int32_t src_row[16];
         uint32_t valid = 0;
@@ -408,7 +419,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (!okw) { ok = false; break; }
           const uint32_t sa = sbase + stage * STAGE_BYTES;
           if (warp == 0 && lane == 0) {
-            ptx::mbar_arrive_expect_tx(full_bar(stage), B_BYTES);
+            ptx::mbar_arrive_expect_tx(full_bar(stage), b_bytes(kBN));
             ptx::tma_load_2d(sa + A_BYTES, &tmap_b, full_bar(stage), kb * BK, brow);
             ++issued;
           }
@@ -477,7 +488,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // itself with cp.async groups: slab j's copies are waited for before its
     // release, and slab j + SCALE_LOOKAHEAD is staged right after it (issued
     // before, they held the release up).
-    const uint32_t scale_ring = sbase + (uint32_t)off_scales(kMode);
+    const uint32_t scale_ring = sbase + (uint32_t)off_scales(kMode, kBN);
     auto slot_addr = [&](int64_t j) {
       return scale_ring + (uint32_t)((j % SCALE_SLOTS) * SCALE_SLOT_FLOATS * 4);
     };
@@ -493,13 +504,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (++lkb == nkb) {
           lkb = 0;
           lt += gridDim.x;
-          if (lt < num_tiles) src = scale_sources<kMode>(p, decode_tile<kMode>(p, lt, s_prefix, s_start), lane);
+          if (lt < num_tiles) src = scale_sources<kMode>(p, decode_tile<kMode, kBN>(p, lt, s_prefix, s_start), lane);
         }
       }
       ptx::cp_async_commit();
     };
     if (kMode == GATHER) {
-      if (lt < num_tiles) src = scale_sources<kMode>(p, decode_tile<kMode>(p, lt, s_prefix, s_start), lane);
+      if (lt < num_tiles) src = scale_sources<kMode>(p, decode_tile<kMode, kBN>(p, lt, s_prefix, s_start), lane);
 #pragma unroll 1
       for (int i = 0; i < SCALE_LOOKAHEAD; ++i) stage_next();
     }
@@ -534,11 +545,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     // Fills slab j's slot (above) once slab j - SCALE_SLOTS's slot is free,
     // by 4-byte cp.async whose completion arrives on the slot's sfull.
     // Every lane waits for the slot itself, before its copies overwrite it.
-    const uint32_t scale_ring = sbase + (uint32_t)off_scales(kMode);
+    const uint32_t scale_ring = sbase + (uint32_t)off_scales(kMode, kBN);
     int64_t j = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-      const ScaleSrc src = scale_sources<kMode>(p, decode_tile<kMode>(p, t, s_prefix, s_start), lane);
+      const ScaleSrc src = scale_sources<kMode>(p, decode_tile<kMode, kBN>(p, t, s_prefix, s_start), lane);
       for (int kb = 0; kb < nkb; ++kb, ++j) {
         const int sl = (int)(j % SCALE_SLOTS);
         const bool okl = wait_bar(sempty_bar(sl), (uint32_t)(((j / SCALE_SLOTS) & 1) ^ 1),
@@ -566,7 +577,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t sa = sbase + stage * STAGE_BYTES;
           const uint64_t adesc = ptx::smem_desc_kmajor_sw128(sa);
           const uint64_t bdesc = ptx::smem_desc_kmajor_sw128(sa + A_BYTES);
-          const uint32_t dcol = tmem_base + tb * BN;
+          const uint32_t dcol = tmem_base + tb * kBN;
 #pragma unroll
           for (int kk = 0; kk < BK / 32; ++kk)  // K = 32 bytes per MMA: +2 in the >>4 field
             ptx::mma_f8f6f4(dcol, adesc + 2u * kk, bdesc + 2u * kk, IDESC, kk > 0 ? 1u : 0u);
@@ -596,57 +607,58 @@ __global__ void __launch_bounds__(THREADS, 1)
     // load has landed.
     const int ew = warp - EPI_WARP0;
     const int quarter = warp & 3;  // TMEM lanes this warp may access
-    const int half = ew >> 2;      // which 128 of the 256 tile columns
+    const int half = ew >> 2;      // which half of the tile's columns
+    constexpr int COLS = kBN / 2;  // columns per promotion warp
     const int lrow = quarter * 32 + lane;
     uint32_t tb = 0;
 
     // per-tile state, filled for the next tile before the current one is stored
     Tile T;
-    auto setup_tile = [&](int64_t t) { T = decode_tile<kMode>(p, t, s_prefix, s_start); };
+    auto setup_tile = [&](int64_t t) { T = decode_tile<kMode, kBN>(p, t, s_prefix, s_start); };
     if ((int64_t)blockIdx.x < num_tiles) setup_tile(blockIdx.x);
     // this thread's row scale and column-block scale in each staged slot
-    const float* scales = reinterpret_cast<const float*>(smem + off_scales(kMode));
+    const float* scales = reinterpret_cast<const float*>(smem + off_scales(kMode, kBN));
     uint32_t js = 0;  // slabs of this CTA so far (slot = js % SCALE_SLOTS)
     constexpr int SC = store_cols(kMode);
     constexpr int CPR = SC / 8;  // 16-byte chunks per staged row
     constexpr int RPI = 32 / CPR;  // rows per warp-wide copy (partial-tile path)
     constexpr int SWZ_SHIFT = CPR == 8 ? 0 : (CPR == 4 ? 1 : 2);  // 128/64/32-byte swizzle
     constexpr uint32_t BUF_BYTES = 32 * SC * 2;
-    constexpr int PASSES = 128 / SC;
-    constexpr int NBOX = stage_boxes(kMode);
+    constexpr int PASSES = COLS / SC;
+    constexpr int NBOX = stage_boxes(kMode, kBN);
     constexpr bool WHOLE_TILE = NBOX == PASSES;
-    const uint32_t stg0 = sbase + OFF_STAGE + (uint32_t)ew * NBOX * BUF_BYTES;
+    const uint32_t stg0 = sbase + off_stage(kBN) + (uint32_t)ew * NBOX * BUF_BYTES;
     uint32_t nstores = 0;  // TMA stores this warp has issued (over all its tiles)
     for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
       const int64_t cur_row0 = T.row0;
       const int cur_rows = T.rows;
-      const int c0 = T.n0 + half * 128;
-      float2 acc[64];
+      const int c0 = T.n0 + half * COLS;
+      float2 acc[COLS / 2];
 #pragma unroll
-      for (int j = 0; j < 64; ++j) acc[j] = make_float2(0.0f, 0.0f);
+      for (int j = 0; j < COLS / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
       for (int kb = 0; kb < nkb; ++kb) {
         ptx::named_bar_sync(BAR_SLAB + tb, BAR_SLAB_THREADS);  // slab kb is in TMEM buffer tb
         const float* slot = scales + (js % SCALE_SLOTS) * SCALE_SLOT_FLOATS;
-        const float s = slot[lrow] * slot[128 + half];
+        const float s = slot[lrow] * slot[128 + half * COLS / 128];
         ++js;
         ptx::tc_fence_after();
-        const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + tb * BN + half * 128;
+        const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + tb * kBN + half * COLS;
         const float2 s2 = make_float2(s, s);
         uint32_t ra[16], rb[16];
         ptx::tmem_ld_32x32b_x16(tcol, ra);
         ptx::tmem_wait_ld_dep(ra);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < COLS / 16; ++c) {
           uint32_t(&cur)[16] = (c & 1) ? rb : ra;
           uint32_t(&nxt)[16] = (c & 1) ? ra : rb;
-          if (c < 7) ptx::tmem_ld_32x32b_x16(tcol + (c + 1) * 16, nxt);
+          if (c + 1 < COLS / 16) ptx::tmem_ld_32x32b_x16(tcol + (c + 1) * 16, nxt);
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             acc[c * 8 + j] = __ffma2_rn(
                 make_float2(__uint_as_float(cur[2 * j]), __uint_as_float(cur[2 * j + 1])), s2,
                 acc[c * 8 + j]);
-          if (c < 7) ptx::tmem_wait_ld_dep(nxt);
-          if (c == 6) {
+          if (c + 1 < COLS / 16) ptx::tmem_wait_ld_dep(nxt);
+          if (c + 2 == COLS / 16) {
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(tempty_bar(tb));
@@ -738,7 +750,7 @@ static bool make_tmap_u8(CUtensorMap* map, const void* base, uint64_t rows, uint
   return make_tmap_2d(map, base, 1, rows, cols, box_rows, 128, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int kMode>
+template <int kMode, int kBN>
 static cudaError_t prepare_kernel(int smem) {
   // Raise the dynamic shared-memory limit once per device and size class.
   static int configured[64] = {0};
@@ -746,12 +758,30 @@ static cudaError_t prepare_kernel(int smem) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || smem > configured[dev]) {
-    e = cudaFuncSetAttribute(gemm::fp8_gemm_kernel<kMode>,
+    e = cudaFuncSetAttribute(gemm::fp8_gemm_kernel<kMode, kBN>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = smem;
   }
   return cudaSuccess;
+}
+
+// p: every field but num_n_tiles set by the caller.
+template <int kBN>
+static cudaError_t launch_dense(const CUtensorMap& ta, const CUtensorMap& ty, const uint8_t* wq,
+                                gemm::Params p, cudaStream_t st) {
+  using namespace gemm;
+  CUtensorMap tb;
+  if (!make_tmap_u8(&tb, wq, (uint64_t)p.n, (uint64_t)p.k, kBN)) return cudaErrorInvalidValue;
+  p.num_n_tiles = (int32_t)((p.n + kBN - 1) / kBN);
+  const int64_t tiles = (int64_t)p.num_m_tiles * p.num_n_tiles;
+  if (tiles > INT32_MAX) return cudaErrorNotSupported;  // 2^31 tiles of output cannot exist
+  const int smem = smem_bytes(DENSE, 1, kBN);
+  cudaError_t e = prepare_kernel<DENSE, kBN>(smem);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)std::min<int64_t>(tiles, sm_count());
+  fp8_gemm_kernel<DENSE, kBN><<<grid, THREADS, smem, st>>>(ta, tb, ty, p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_block_gemm(const uint8_t* xq, const float* xs, const uint8_t* wq,
@@ -760,9 +790,8 @@ cudaError_t launch_block_gemm(const uint8_t* xq, const float* xs, const uint8_t*
   using namespace gemm;
   if (m == 0 || n == 0) return cudaSuccess;
   if (k == 0) return cudaMemsetAsync(y, 0, (size_t)(m * n * 2), st);
-  CUtensorMap ta, tb;
+  CUtensorMap ta;
   if (!make_tmap_u8(&ta, xq, (uint64_t)m, (uint64_t)k, BM)) return cudaErrorInvalidValue;
-  if (!make_tmap_u8(&tb, wq, (uint64_t)n, (uint64_t)k, BN)) return cudaErrorInvalidValue;
   CUtensorMap ty;
   if (!make_tmap_2d(&ty, y, 2, (uint64_t)m, (uint64_t)n, 32, store_cols(DENSE),
                     CU_TENSOR_MAP_SWIZZLE_64B))
@@ -776,15 +805,11 @@ cudaError_t launch_block_gemm(const uint8_t* xq, const float* xs, const uint8_t*
   p.nnb = (int32_t)((n + 127) / 128);
   p.g = 1;
   p.num_m_tiles = (int32_t)((m + BM - 1) / BM);
-  p.num_n_tiles = (int32_t)((n + BN - 1) / BN);
-  const int64_t tiles = (int64_t)p.num_m_tiles * p.num_n_tiles;
-  if (tiles > INT32_MAX) return cudaErrorNotSupported;  // 2^31 tiles of output cannot exist
-  const int smem = smem_bytes(DENSE, 1);
-  cudaError_t e = prepare_kernel<DENSE>(smem);
-  if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)std::min<int64_t>(tiles, sm_count());
-  fp8_gemm_kernel<DENSE><<<grid, THREADS, smem, st>>>(ta, tb, ty, p);
-  return cudaGetLastError();
+  // 128-wide tiles where 256-wide ones would not give every SM a tile: twice
+  // the CTAs, and each promotion warp's chain per slab half as long
+  const int64_t wide_tiles = (int64_t)p.num_m_tiles * ((n + BN - 1) / BN);
+  if (wide_tiles < (int64_t)sm_count()) return launch_dense<BN_NARROW>(ta, ty, wq, p, st);
+  return launch_dense<BN>(ta, ty, wq, p, st);
 }
 
 cudaError_t launch_grouped_gemm(const uint8_t* xq, const float* xs, int64_t rows_x,
@@ -818,17 +843,17 @@ cudaError_t launch_grouped_gemm(const uint8_t* xq, const float* xs, int64_t rows
   p.num_n_tiles = (int32_t)((n + BN - 1) / BN);
   const int64_t max_tiles = ((total_rows + BM - 1) / BM + g) * (int64_t)p.num_n_tiles;
   if (max_tiles > INT32_MAX) return cudaErrorNotSupported;
-  const int smem = smem_bytes(gather ? GATHER : GROUPED, g);
+  const int smem = smem_bytes(gather ? GATHER : GROUPED, g, BN);
   const unsigned grid = (unsigned)std::min<int64_t>(max_tiles, sm_count());
   cudaError_t e;
   if (gather) {
-    e = prepare_kernel<GATHER>(smem);
+    e = prepare_kernel<GATHER, BN>(smem);
     if (e != cudaSuccess) return e;
-    fp8_gemm_kernel<GATHER><<<grid, THREADS, smem, st>>>(ta, tb, ty, p);
+    fp8_gemm_kernel<GATHER, BN><<<grid, THREADS, smem, st>>>(ta, tb, ty, p);
   } else {
-    e = prepare_kernel<GROUPED>(smem);
+    e = prepare_kernel<GROUPED, BN>(smem);
     if (e != cudaSuccess) return e;
-    fp8_gemm_kernel<GROUPED><<<grid, THREADS, smem, st>>>(ta, tb, ty, p);
+    fp8_gemm_kernel<GROUPED, BN><<<grid, THREADS, smem, st>>>(ta, tb, ty, p);
   }
   return cudaGetLastError();
 }
