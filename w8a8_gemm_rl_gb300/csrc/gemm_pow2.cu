@@ -239,8 +239,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     // --------------------------------------------------------- scale factors
     // Warp q writes its lane quarter: A column q (the CTA's rows 32q + lane)
     // and all 8 B columns.  The scales of a group of SF_GROUP slabs are
-    // loaded while the previous group is written, into a register ring
-    // indexed statically (the inner loops are unrolled).
+    // loaded into a register ring indexed statically (the inner loops are
+    // unrolled), right after the previous group's handover: issued before
+    // it, they held up that arrive, which waits for the warp's loads in
+    // flight.
     const uint32_t lane_q = (uint32_t)(warp * 32) << 16;  // this warp's lane quarter
     const uint32_t lead_sf_full0 = lead_bar0 + 8u * (2 * STAGES);
     uint32_t slot = 0, sphase = 0;
@@ -289,12 +291,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                     cu + SF_B_COL),
                 "r"(b0), "r"(b0), "r"(b0), "r"(b0), "r"(b1), "r"(b1), "r"(b1), "r"(b1)
                 : "memory");
-            // the same ring entry for the next group
-            if (kb + SF_GROUP < nkb) {
-              ra[u] = xsr[kb + SF_GROUP];
-              rw0[u] = wsr0[kb + SF_GROUP];
-              rw1[u] = wsr1[kb + SF_GROUP];
-            }
           }
         }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -302,6 +298,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive_cluster(lead_sf_full0 + 8u * slot);
         if (++slot == SF_SLOTS) { slot = 0; sphase ^= 1u; }
+        // the next group's scales
+#pragma unroll
+        for (int u = 0; u < SF_GROUP; ++u) {
+          const int kb = kb0 + SF_GROUP + u;
+          if (kb < nkb) {
+            ra[u] = xsr[kb];
+            rw0[u] = wsr0[kb];
+            rw1[u] = wsr1[kb];
+          }
+        }
       }
     }
     __syncwarp();
