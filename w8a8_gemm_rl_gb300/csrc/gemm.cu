@@ -84,22 +84,18 @@ __host__ __device__ constexpr int off_misc(int bn) { return off_bars(bn) + NUM_B
 enum Mode { DENSE = 0, GROUPED = 1, GATHER = 2 };
 // Output staging: each promotion warp writes its 32 rows x bn / 2 columns, in
 // bn / 2 / store_cols passes, into private boxes of 32 rows x store_cols BF16
-// columns laid out as the TMA's 64-byte swizzle, and one lane stores each
-// box to global memory by TMA (32-column boxes: 3-6% faster for the grouped
-// GEMM than 16-column ones).
-//  * dense: two boxes, alternating per TMA store issued (not per pass: a
-//    partial last N tile issues fewer stores than passes, and the box
-//    written next must never be the source of the newest store, which
-//    cp.async.bulk.wait_group.read 1 does not retire);
-//  * grouped: one box per pass, the warp's whole share of a tile, so a
-//    tile's stores never wait for one another (the one wait, before the
-//    first pass, is for the previous tile's stores).
-// Measured: two boxes are 1.5% faster for the dense GEMM, whole-tile boxes
-// 2-3% faster for the grouped one.
-__host__ __device__ constexpr int store_cols(int) { return 32; }
-__host__ __device__ constexpr int stage_boxes(int mode, int bn) {
-  return mode == DENSE ? 2 : bn / 2 / store_cols(mode);
-}
+// columns laid out as the TMA's 128-byte swizzle, and one lane stores each
+// box to global memory by TMA (64-column boxes: 2% faster than 32-column
+// ones, which were 3-6% faster for the grouped GEMM than 16-column ones).
+// Each warp has two boxes.  Where a warp's share of a tile takes two passes
+// (tiles 256 wide) each pass has its own box, so a tile's stores never wait
+// for one another (the one wait, before the first pass, is for the previous
+// tile's stores).  With one pass per tile (128 wide) the boxes alternate per
+// TMA store issued (not per pass: a partial last N tile issues fewer stores
+// than passes, and the box written next must never be the source of the
+// newest store, which cp.async.bulk.wait_group.read 1 does not retire).
+__host__ __device__ constexpr int store_cols(int) { return 64; }
+__host__ __device__ constexpr int stage_boxes(int, int) { return 2; }
 // swizzle atoms: 1024-byte aligned
 __host__ __device__ constexpr int off_stage(int bn) { return (off_misc(bn) + 16 + 1023) / 1024 * 1024; }
 __host__ __device__ constexpr int stage_bytes(int mode, int bn) {
@@ -795,7 +791,7 @@ cudaError_t launch_block_gemm(const uint8_t* xq, const float* xs, const uint8_t*
   if (!make_tmap_u8(&ta, xq, (uint64_t)m, (uint64_t)k, BM)) return cudaErrorInvalidValue;
   CUtensorMap ty;
   if (!make_tmap_2d(&ty, y, 2, (uint64_t)m, (uint64_t)n, 32, store_cols(DENSE),
-                    CU_TENSOR_MAP_SWIZZLE_64B))
+                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   Params p{};
   p.xq = xq; p.xs = xs; p.ws = ws; p.y = y;
@@ -830,7 +826,7 @@ cudaError_t launch_grouped_gemm(const uint8_t* xq, const float* xs, int64_t rows
     return cudaErrorInvalidValue;
   CUtensorMap ty;
   if (!make_tmap_2d(&ty, y, 2, (uint64_t)total_rows, (uint64_t)n, 32, store_cols(GROUPED),
-                    CU_TENSOR_MAP_SWIZZLE_64B))
+                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   Params p{};
   p.xq = xq; p.xs = xs; p.ws = ws; p.y = y;
