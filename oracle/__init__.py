@@ -52,6 +52,9 @@ def lib():
             "oracle_decode_attention": (ctypes.c_int, [P, ctypes.c_float, P, ctypes.c_float, P,
                                                         ctypes.c_float, P, i64, i64, i64, i64, i64,
                                                         ctypes.c_double, P, P]),
+            "oracle_prefill_attention": (ctypes.c_int, [P, ctypes.c_float, P, ctypes.c_float, P,
+                                                         ctypes.c_float, i64, i64, i64, i64, i64,
+                                                         ctypes.c_double, P, P]),
             "oracle_bf16_from_f64": (u16, [ctypes.c_double]),
             "oracle_bf16_from_f64_array": (None, [P, i64, P]),
         }
@@ -276,6 +279,23 @@ def decode_attention(q, sq, k, sk, v, sv, lens, softmax_scale):
     ab = np.empty((B, Hq, D), np.float64)
     rc = lib().oracle_decode_attention(_p(q), float(sq), _p(k), float(sk), _p(v), float(sv), _p(lens),
                                        B, S, Hq, Hkv, D, float(softmax_scale), _p(out), _p(ab))
+    assert rc == 0
+    return out, ab
+
+
+def prefill_attention(q, sq, k, sk, v, sv, softmax_scale):
+    """Causal prefill attention over FP8 Q, K, V (NeMo blog Table 3, per-tensor
+    scales): q [B, S, Hq, D], k and v [B, S, Hkv, D] E4M3 codes; query token i
+    reads tokens 0..i.  Returns (out, absout) float64 [B, S, Hq, D]: the
+    exact-math output and the bound sv * sum_j p_j |dec(v_j)| for its
+    tolerance."""
+    q, k, v = _c(q, np.uint8), _c(k, np.uint8), _c(v, np.uint8)
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    out = np.empty((B, S, Hq, D), np.float64)
+    ab = np.empty((B, S, Hq, D), np.float64)
+    rc = lib().oracle_prefill_attention(_p(q), float(sq), _p(k), float(sk), _p(v), float(sv),
+                                        B, S, Hq, Hkv, D, float(softmax_scale), _p(out), _p(ab))
     assert rc == 0
     return out, ab
 

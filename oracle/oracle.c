@@ -36,6 +36,7 @@
  * multiply-add is fused.
  */
 #include <math.h>
+#include <stdlib.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -536,6 +537,67 @@ ORACLE_EXPORT int oracle_decode_attention(const uint8_t *q, float sq, const uint
             }
         }
     }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Prefill (causal) attention over FP8 Q, K and V                            */
+/* ------------------------------------------------------------------------ */
+
+/* [NeMo] Table 3: Q, K and V carry one FP32 scale each (per tensor); the
+ * prompt's tokens attend causally: query token i of sequence b, query head h,
+ * reads the keys and values of tokens 0..i of the same sequence, KV head
+ * h / (hq / hkv).  q [batch, seq, hq, d], k and v [batch, seq, hkv, d]:
+ *   score_j = softmax_scale * sq * sk * sum_d dec(q[b,i,h,d]) dec(k[b,j,kh,d])
+ *   p_j     = exp(score_j - max) / sum_{u <= i} exp(score_u - max),  j <= i
+ *   out_d   = sv * sum_{j <= i} p_j dec(v[b,j,kh,d])
+ * all in FP64; absout_d = sv * sum_j p_j |dec(v)| bounds the rounding.  The
+ * scores of a row are formed once and kept (seq <= 1 << 20). */
+ORACLE_EXPORT int oracle_prefill_attention(const uint8_t *q, float sq, const uint8_t *k, float sk,
+                                           const uint8_t *v, float sv, int64_t batch, int64_t seq,
+                                           int64_t hq, int64_t hkv, int64_t d,
+                                           double softmax_scale, double *out, double *absout) {
+    int64_t b, h, i, j, e;
+    double dec[256];
+    double *sc;
+    if (batch < 0 || seq < 0 || seq > (1 << 20) || hq <= 0 || hkv <= 0 || d <= 0 || hq % hkv)
+        return -1;
+    for (e = 0; e < 256; ++e) dec[e] = oracle_e4m3_decode((uint8_t)e);
+    sc = (double *)malloc(sizeof(double) * (size_t)(seq > 0 ? seq : 1));
+    if (!sc) return -3;
+    for (b = 0; b < batch; ++b)
+        for (i = 0; i < seq; ++i)
+            for (h = 0; h < hq; ++h) {
+                const int64_t kh = h / (hq / hkv);
+                const uint8_t *qv = q + ((b * seq + i) * hq + h) * d;
+                double *o = out + ((b * seq + i) * hq + h) * d;
+                double *ao = absout + ((b * seq + i) * hq + h) * d;
+                double mx = -HUGE_VAL, den = 0.0;
+                for (e = 0; e < d; ++e) o[e] = ao[e] = 0.0;
+                for (j = 0; j <= i; ++j) {
+                    const uint8_t *kv = k + ((b * seq + j) * hkv + kh) * d;
+                    double s = 0.0;
+                    for (e = 0; e < d; ++e) s += dec[qv[e]] * dec[kv[e]];
+                    s *= softmax_scale * (double)sq * (double)sk;
+                    sc[j] = s;
+                    if (s > mx) mx = s;
+                }
+                for (j = 0; j <= i; ++j) {
+                    const uint8_t *vv = v + ((b * seq + j) * hkv + kh) * d;
+                    const double pj = exp(sc[j] - mx);
+                    den += pj;
+                    for (e = 0; e < d; ++e) {
+                        const double x = dec[vv[e]];
+                        o[e] += pj * x;
+                        ao[e] += pj * fabs(x);
+                    }
+                }
+                for (e = 0; e < d; ++e) {
+                    o[e] = o[e] / den * (double)sv;
+                    ao[e] = ao[e] / den * fabs((double)sv);
+                }
+            }
+    free(sc);
     return 0;
 }
 

@@ -317,6 +317,70 @@ def test_attention_matches_library_softmax():
         assert (ab[b] >= np.abs(out[b]) * (1 - 1e-12)).all()
 
 
+# ------------------------------------------------------ prefill attention
+
+def test_prefill_attention_pins():
+    """Causal prefill attention against what fixes it:
+    * query token 0 has one key, so its output is that token's dequantized V;
+    * a zero query weighs keys 0..i uniformly: the mean of those V rows;
+    * query token S-1 sees the whole sequence: the (separately pinned) decode
+      attention over all S tokens;
+    * causality: changing K and V of tokens after i leaves row i unchanged;
+    * grouped heads: Hkv = 2 KV heads give what Hkv = 8 with each KV head
+      repeated for its 4 query heads gives."""
+    rng = np.random.default_rng(40)
+    B, S, Hq, Hkv = 2, 19, 8, 2
+    qd, k, v = _attn_inputs(rng, B * S, S, Hq, Hkv)
+    q = qd.reshape(B, S, Hq, 128)
+    k, v = k[:B], v[:B]
+    sq, sk, sv = (float(np.float32(t)) for t in (0.02, 0.05, 0.375))
+    sc = 1 / np.sqrt(128)
+    out, ab = O.prefill_attention(q, sq, k, sk, v, sv, sc)
+    for b in range(B):
+        for h in range(Hq):
+            assert np.array_equal(out[b, 0, h], sv * O.e4m3_decode(v[b, 0, h // 4]))
+    assert (ab >= np.abs(out) * (1 - 1e-12)).all()
+    outz, _ = O.prefill_attention(np.zeros_like(q), 1.0, k, 1.0, v, sv, 1.0)
+    for i in (0, 5, S - 1):
+        for h in range(Hq):
+            want = sv * O.e4m3_decode(v[1, : i + 1, h // 4]).mean(axis=0)
+            assert np.allclose(outz[1, i, h], want, rtol=1e-14, atol=1e-300)
+    lens = np.full(B, S, np.int32)
+    dec, _ = O.decode_attention(np.ascontiguousarray(q[:, S - 1]), sq, k, sk, v, sv, lens, sc)
+    assert np.allclose(out[:, S - 1], dec, rtol=1e-13, atol=1e-13 * np.abs(dec).max())
+    i = 7
+    k2, v2 = k.copy(), v.copy()
+    k2[:, i + 1 :] = rng.integers(0, 0x7E, k2[:, i + 1 :].shape)
+    v2[:, i + 1 :] = rng.integers(0, 0x7E, v2[:, i + 1 :].shape)
+    out2, _ = O.prefill_attention(q, sq, k2, sk, v2, sv, sc)
+    assert np.array_equal(out2[:, : i + 1], out[:, : i + 1])
+    assert not np.array_equal(out2[:, i + 1 :], out[:, i + 1 :])
+    out8, _ = O.prefill_attention(q, sq, np.repeat(k, 4, axis=2), sk, np.repeat(v, 4, axis=2), sv, sc)
+    assert np.array_equal(out8, out)
+
+
+def test_prefill_attention_matches_library_softmax():
+    """Against torch: a float64 causal softmax (masked with -inf) and einsum
+    over the dequantized tensors, library routines written independently."""
+    rng = np.random.default_rng(41)
+    B, S, Hq, Hkv = 2, 23, 4, 4
+    qd, k, v = _attn_inputs(rng, B * S, S, Hq, Hkv)
+    q = qd.reshape(B, S, Hq, 128)
+    k, v = k[:B], v[:B]
+    sq, sk, sv = (float(np.float32(t)) for t in (0.03, 0.04, 0.5))
+    sc = 1 / np.sqrt(128)
+    out, _ = O.prefill_attention(q, sq, k, sk, v, sv, sc)
+    dq = torch.from_numpy(O.e4m3_decode(q)) * sq
+    dk = torch.from_numpy(O.e4m3_decode(k)) * sk
+    dv = torch.from_numpy(O.e4m3_decode(v)) * sv
+    mask = torch.triu(torch.ones(S, S, dtype=torch.bool), diagonal=1)
+    for b in range(B):
+        s = torch.einsum("ihd,jhd->hij", dq[b], dk[b]) * sc
+        p = torch.softmax(s.masked_fill(mask, float("-inf")), dim=-1)
+        want = torch.einsum("hij,jhd->ihd", p, dv[b]).numpy()
+        assert np.allclose(out[b], want, rtol=1e-12, atol=1e-12 * np.abs(want).max())
+
+
 # ------------------------------------------------------ power-of-two scales
 
 def test_pow2_scale_hand_values_and_definition():
