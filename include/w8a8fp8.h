@@ -69,7 +69,8 @@ const char *w8a8_last_cuda_error(void);
  * bounded wait inside it gives up (0 = none; nonzero identifies the wait:
  * 1..10 the GEMMs of more than 256 rows and the grouped GEMM, 31..37 the
  * GEMM of at most 256 rows, 51..58 the power-of-two GEMM (59: a scale it
- * cannot hold), 11..13 the weight quantizer, 21..22 the decode attention,
+ * cannot hold), 11..13 the weight quantizer, 21..24 the decode and prefill
+ * attention,
  * 41..43 the batched dequantizer and error report).  When several are set,
  * the GEMMs' code is reported first, then the quantizer's, and all are
  * cleared.  Such a kernel stops early
@@ -298,8 +299,10 @@ w8a8_status quant_error_report_batched(const w8a8_error_desc *descs,
  * with an online softmax whose exponentials use the hardware's approximate
  * base-2 exponential (ex2.approx.ftz.f32, flushing subnormal results to
  * zero); |out - exact| <= 1e-3 * sv * sum_t p_t |dec(v_t,d)| + half a BF16
- * ulp (the tests also hold 2^-14 of that sum, which covers the error of
- * the approximate exponential).
+ * ulp + 2^-39 * sv * sum_t |dec(v_t,d)| (the tests also hold 2^-14 of the
+ * first sum, which covers the error of the approximate exponential; the
+ * last term is the weights below 2^-39 of the largest, which f16 cannot
+ * hold and which are left out).
  * Lengths are read on the device and clamped to [0, max_seq].
  * Rules: head_dim == 128 and num_q_heads / num_kv_heads in {1, 2} or a
  * multiple of 4 (else W8A8_ERR_UNSUPPORTED); batch, max_seq and
@@ -319,6 +322,41 @@ w8a8_status fp8_decode_attention(const uint8_t *q, const float *q_scale,
                                  int32_t num_kv_heads, int32_t head_dim,
                                  float softmax_scale, uint16_t *out_bf16,
                                  w8a8_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * fp8_prefill_attention -- causal attention of a prompt's tokens over FP8
+ * Q, K and V, with the per-tensor FP32 scales of [NeMo] Table 3:
+ *
+ *   score_j = softmax_scale * sq * sk * sum_d dec(q[b,i,h,d]) dec(k[b,j,kh,d])
+ *   out[b,i,h,d] = BF16( sv * sum_{j <= i} softmax_j(score) dec(v[b,j,kh,d]) )
+ *
+ * query token i of sequence b reading tokens 0..i of the same sequence, with
+ * kh = h / (num_q_heads / num_kv_heads) (grouped-query heads).
+ *   q        [batch, seq, num_q_heads, head_dim] E4M3; q_scale one FP32 (device).
+ *   k, v     [batch, seq, num_kv_heads, head_dim] E4M3 (the KV cache's
+ *            layout, as written by kv_amax_quantize); k_scale, v_scale one
+ *            FP32 each (device).
+ *   out_bf16 [batch, seq, num_q_heads, head_dim] (out).
+ * Accuracy: as fp8_decode_attention (FP32 accumulation, exact E4M3
+ * products for Q K^T, the weights in two f16 parts for P V, the hardware's
+ * approximate base-2 exponential): |out - exact| <= 1e-3 * sv * sum_j p_j
+ * |dec(v_j,d)| + half a BF16 ulp + 2^-39 * sv * sum_{j <= i} |dec(v_j,d)|
+ * (weights below 2^-39 of the row's largest, which f16 cannot hold, are
+ * left out).
+ * Rules: head_dim == 128 (else W8A8_ERR_UNSUPPORTED); num_q_heads and
+ * batch at most 65535, seq and batch * seq below 2^31 - 64 (grid and TMA
+ * coordinate limits; over-size inputs give W8A8_ERR_UNSUPPORTED); q, k and
+ * v 16-byte aligned, the rest 4-byte aligned.  A CTA takes 64 query tokens
+ * of one (sequence, query head) and streams the keys and values up to them
+ * in chunks of 64 tokens (TMA tiles), on the tensor cores (E4M3 for Q K^T,
+ * f16 for P V).  A bounded wait that gives up records device error 23 or 24.
+ * ---------------------------------------------------------------------- */
+w8a8_status fp8_prefill_attention(const uint8_t *q, const float *q_scale,
+                                  const uint8_t *k, const float *k_scale,
+                                  const uint8_t *v, const float *v_scale, int64_t batch,
+                                  int64_t seq, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, float softmax_scale, uint16_t *out_bf16,
+                                  w8a8_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * fp8_block_gemm -- the W8A8 linear of [FP8-RL] section 1 / arXiv abstract

@@ -136,6 +136,25 @@ def test_attention_argument_checks(L):
     assert a(A, A, A, A, A, A, A, 1, 1 << 31, 8, 2, 128, sc, A, None) == UNSUP
 
 
+def test_prefill_attention_argument_checks(L):
+    import ctypes
+    a = L.fp8_prefill_attention
+    sc = ctypes.c_float(0.088)
+    assert a(A, A, A, A, A, A, 2, 64, 8, 2, 64, sc, A, None) == UNSUP    # head dim
+    assert a(A, A, A, A, A, A, 2, 64, 8, 3, 128, sc, A, None) == SHAPE   # 8 % 3
+    assert a(A, A, A, A, A, A, -1, 64, 8, 2, 128, sc, A, None) == SHAPE
+    assert a(A, A, A, A, A, A, 2, -5, 8, 2, 128, sc, A, None) == SHAPE
+    assert a(None, None, None, None, None, None, 0, 64, 8, 2, 128, sc, None, None) == OK
+    assert a(None, None, None, None, None, None, 3, 0, 8, 2, 128, sc, None, None) == OK
+    assert a(A, A, None, A, A, A, 2, 64, 8, 2, 128, sc, A, None) == NULL
+    assert a(A, A, A + 4, A, A, A, 2, 64, 8, 2, 128, sc, A, None) == ALIGN
+    assert a(A, A, A, A, A, A, 2, 64, 8, 2, 128, sc, A + 2, None) == ALIGN
+    # grid limits and 32-bit TMA row coordinates
+    assert a(A, A, A, A, A, A, 1 << 16, 1, 8, 2, 128, sc, A, None) == UNSUP
+    assert a(A, A, A, A, A, A, 2, 64, 1 << 16, 2, 128, sc, A, None) == UNSUP
+    assert a(A, A, A, A, A, A, 1 << 15, 1 << 16, 8, 2, 128, sc, A, None) == UNSUP
+
+
 def test_gemm_argument_checks(L):
     g = L.fp8_block_gemm
     assert g(A, A, A, A, A, 128, 256, 100, None) == SHAPE  # k % 16

@@ -21,10 +21,12 @@ def _codes(shape, g):
     return c.to(torch.uint8)
 
 
-def _check(out, ref, ab, rel):
+def _check(out, ref, ab, rel, dropped=0.0):
+    """dropped: the bound on the weights too small for f16 (below 2^-39 of
+    the row's largest), which the kernels leave out."""
     got = bf16_to_f64(bits16(out)).reshape(ref.shape)
     err = np.abs(got - ref)
-    bound = rel * ab + 0.5 * ulp_bf16(ref)
+    bound = rel * ab + 0.5 * ulp_bf16(ref) + dropped
     bad = err > bound
     assert not bad.any(), (int(bad.sum()), float((err - bound).max()))
 
@@ -117,3 +119,56 @@ def test_decode_attention_clamps_device_lengths(W):
                                  scales[2].item(), clamped, 1 / math.sqrt(128))
     _check(out, ref, ab, 2.0 ** -14)
     assert (bits16(out[0]) == 0).all()
+
+
+# ------------------------------------------------------------------ prefill
+
+def _dropped_bound(v, sv, hq):
+    """sv * 2^-39 * sum over keys j <= i of max_d |dec(v_j)|, per [b, i, h, 1]:
+    the most that weights below 2^-39 of a row's largest can carry."""
+    dv = np.abs(O.e4m3_decode(v)).max(axis=3)           # [B, S, Hkv]
+    cum = np.cumsum(dv, axis=1)                          # keys 0..i
+    cum = np.repeat(cum, hq // v.shape[2], axis=2)       # query head h reads KV head h // g
+    return abs(sv) * 2.0 ** -39 * cum[..., None]
+
+PREFILL_CASES = [  # batch, tokens per sequence, q heads, kv heads
+    (1, 1, 4, 4), (2, 63, 8, 2), (1, 64, 4, 1), (2, 65, 4, 4), (1, 200, 8, 2),
+    (3, 130, 32, 8), (1, 700, 8, 8)]
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv", PREFILL_CASES)
+def test_prefill_attention_matches_oracle(W, B, S, Hq, Hkv):
+    """Causal prefill over random E4M3 codes (every finite code): a single
+    token, partial and whole 64-token query blocks, grouped heads."""
+    g = torch.Generator().manual_seed(B * 100 + S + Hq)
+    q, k, v = _codes((B, S, Hq, 128), g), _codes((B, S, Hkv, 128), g), _codes((B, S, Hkv, 128), g)
+    scales = torch.tensor([0.02, 0.03, 0.5], dtype=torch.float32)
+    dev = lambda t: t.cuda()
+    out = W.fp8_prefill_attention(dev(q), dev(scales[0:1]), dev(k), dev(scales[1:2]), dev(v),
+                                  dev(scales[2:3]))
+    torch.cuda.synchronize()
+    assert W.consume_device_error() == 0
+    ref, ab = O.prefill_attention(q.numpy(), scales[0].item(), k.numpy(), scales[1].item(),
+                                  v.numpy(), scales[2].item(), 1 / math.sqrt(128))
+    drop = _dropped_bound(v.numpy(), scales[2].item(), Hq)
+    _check(out, ref, ab, 1e-3, drop)
+    _check(out, ref, ab, 2.0 ** -14, drop)
+
+
+def test_prefill_attention_over_quantized_activations(W):
+    """Q, K and V from N(0, 1) activations with 0.1% x50 outliers, each
+    quantized per tensor by kv_amax_quantize (as the rollout stores them):
+    the softmax is not dominated by a few keys here."""
+    B, S, Hq, Hkv = 2, 300, 16, 4
+    x = [synth.activations(B * S * h, 128, seed=90 + i).reshape(B, S, h, 128).cuda()
+         for i, h in enumerate((Hq, Hkv, Hkv))]
+    qkv = [W.kv_amax_quantize(t) for t in x]
+    out = W.fp8_prefill_attention(qkv[0][0], qkv[0][1], qkv[1][0], qkv[1][1], qkv[2][0], qkv[2][1])
+    torch.cuda.synchronize()
+    assert W.consume_device_error() == 0
+    sc = [t[1].item() for t in qkv]
+    ref, ab = O.prefill_attention(qkv[0][0].cpu().numpy(), sc[0], qkv[1][0].cpu().numpy(), sc[1],
+                                  qkv[2][0].cpu().numpy(), sc[2], 1 / math.sqrt(128))
+    drop = _dropped_bound(qkv[2][0].cpu().numpy(), sc[2], Hq)
+    _check(out, ref, ab, 1e-3, drop)
+    _check(out, ref, ab, 2.0 ** -14, drop)

@@ -18,7 +18,7 @@ __all__ = [
     "lib", "W8A8Error", "e4m3_encode_f32", "e4m3_decode_f32", "quantize_weight_blockwise",
     "quantize_weight_blockwise_batched", "quantize_act_per_token_group",
     "quantize_act_per_token_group_gather", "dequantize_blockwise", "quant_error_report",
-    "sqnr_db", "fp8_decode_attention", "dequantize_blockwise_batched", "quant_error_report_batched",
+    "sqnr_db", "fp8_decode_attention", "fp8_prefill_attention", "dequantize_blockwise_batched", "quant_error_report_batched",
     "fp8_block_gemm", "fp8_block_gemm_pow2",
     "fp8_grouped_gemm", "kv_amax_quantize", "w8a8_linear", "consume_device_error",
     "GEMM_STATIC_WEIGHTS", "LINEAR_SINGLE_KERNEL", "debug_force_wait_timeout",
@@ -63,6 +63,8 @@ _SIGNATURES = {
     "quant_error_report": (_INT, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, _P]),
     "fp8_decode_attention": (_INT, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _I32,
                                     ctypes.c_float, _P, _P]),
+    "fp8_prefill_attention": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _I32,
+                                     ctypes.c_float, _P, _P]),
     "fp8_block_gemm": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "fp8_block_gemm_ex": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_uint32, _P]),
     "fp8_block_gemm_pow2": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
@@ -294,6 +296,29 @@ def fp8_decode_attention(q, q_scale, k_cache, k_scale, v_cache, v_scale, seq_len
            lib().fp8_decode_attention(_ptr(q), _ptr(q_scale), _ptr(k_cache), _ptr(k_scale),
                                       _ptr(v_cache), _ptr(v_scale), _ptr(seq_lens), B, S, Hq, Hkv,
                                       D, sc, _ptr(out), _stream(stream)))
+    return out
+
+
+def fp8_prefill_attention(q, q_scale, k, k_scale, v, v_scale, softmax_scale=None, out=None,
+                          stream=None):
+    """Causal prefill attention over FP8 Q, K and V.
+
+    q uint8 [B, S, Hq, 128] E4M3 codes; k, v uint8 [B, S, Hkv, 128]; q_scale,
+    k_scale, v_scale float32 [1] per-tensor scales (device) -> BF16
+    [B, S, Hq, 128].  Query token i reads tokens 0..i of its sequence; query
+    head h reads KV head h // (Hq // Hkv); softmax_scale defaults to
+    1/sqrt(128)."""
+    _need(q, torch.uint8, "q")
+    _need(k, torch.uint8, "k")
+    _need(v, torch.uint8, "v")
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    sc = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    out = torch.empty((B, S, Hq, D), dtype=torch.bfloat16, device=q.device) if out is None else out
+    _check("fp8_prefill_attention",
+           lib().fp8_prefill_attention(_ptr(q), _ptr(q_scale), _ptr(k), _ptr(k_scale), _ptr(v),
+                                       _ptr(v_scale), B, S, Hq, Hkv, D, sc, _ptr(out),
+                                       _stream(stream)))
     return out
 
 

@@ -294,6 +294,29 @@ W8A8_API w8a8_status fp8_decode_attention(const uint8_t* q, const float* q_scale
                                                  cs(stream)));
 }
 
+W8A8_API w8a8_status fp8_prefill_attention(const uint8_t* q, const float* q_scale,
+                                           const uint8_t* k, const float* k_scale,
+                                           const uint8_t* v, const float* v_scale, int64_t batch,
+                                           int64_t seq, int32_t num_q_heads, int32_t num_kv_heads,
+                                           int32_t head_dim, float softmax_scale,
+                                           uint16_t* out_bf16, w8a8_stream_t stream) {
+  if (batch < 0 || seq < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+    return W8A8_ERR_SHAPE;
+  if (num_q_heads % num_kv_heads != 0) return W8A8_ERR_SHAPE;
+  if (head_dim != 128) return W8A8_ERR_UNSUPPORTED;
+  // over-size inputs (grid dimensions; TMA row coordinates are 32-bit) share one status
+  if (num_q_heads > 65535 || batch > 65535 || seq >= kMaxDim) return W8A8_ERR_UNSUPPORTED;
+  if (batch == 0 || seq == 0) return W8A8_OK;
+  if (batch * seq > kMaxDim - 1 - 64) return W8A8_ERR_UNSUPPORTED;
+  if (!q || !q_scale || !k || !k_scale || !v || !v_scale || !out_bf16) return W8A8_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out_bf16, 4) ||
+      !aligned(q_scale, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4))
+    return W8A8_ERR_ALIGN;
+  return from_cuda(w8a8::launch_prefill_attention(q, q_scale, k, k_scale, v, v_scale, batch, seq,
+                                                  num_q_heads, num_kv_heads, softmax_scale,
+                                                  out_bf16, cs(stream)));
+}
+
 // ------------------------------------------------------------------ GEMMs
 
 static w8a8_status check_gemm_common(const uint8_t* xq, const float* xs, const uint8_t* wq,

@@ -146,6 +146,18 @@ __device__ __forceinline__ void mma_e4m3_rows8(float& d0, float& d1, uint32_t a0
       : "r"(a0), "r"(0u), "r"(a2), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
+// d += A B on one full m16n8k32 tile of E4M3 codes (f32 accumulate): a[0] /
+// a[2] bytes 4 tig .. 4 tig + 3 of the two 16-byte halves of row g's k
+// range, a[1] / a[3] the same of row g + 8; d[0], d[1] row g, d[2], d[3] row
+// g + 8.
+__device__ __forceinline__ void mma_e4m3_rows16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                                uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 __device__ __forceinline__ uint16_t bf16_rn(float x) {
   uint16_t r;
   asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(x));
@@ -532,6 +544,280 @@ cudaError_t launch_decode_attention(const uint8_t* q, const float* sq, const uin
       return launch_attn<8>(tm_k, tm_v, q, sq, sk, sv, lens, smax, hq, hkv, hgroups, nsplit,
                             softmax_scale, out, (unsigned)grid, st);
   }
+}
+
+
+// ================================================================ prefill
+// Causal prefill attention (NeMo RL FP8 blog, Table 3: per-tensor Q, K and V
+// scales): the prompt's tokens attend to their sequence's tokens up to
+// themselves,
+//   score_j = softmax_scale * sq * sk * sum_d dec(q[b,i,h,d]) * dec(k[b,j,kh,d])
+//   out_d   = sv * sum_{j <= i} softmax(score)_j * dec(v[b,j,kh,d]),
+// q [batch, seq, hq, 128], k and v [batch, seq, hkv, 128] (the KV cache's
+// layout), out [batch, seq, hq, 128] BF16.
+//
+// A CTA takes 64 query tokens of one (sequence, query head); each of its 4
+// warps 16 of them, as the rows of m16 MMA tiles.  The keys come in chunks
+// of 64 tokens (K and V tiles by TMA, 128-byte swizzle, a 3-stage ring
+// shared by the warps): S = Q K^T on the raw E4M3 codes (m16n8k32, f32
+// accumulation), one online-softmax step per chunk in log2 units, then
+// O += P V in f16 with the weights P = 2^15 p split into high and low f16
+// parts (two MMAs; together they carry 22 bits of each weight), V widened
+// exactly from E4M3.  The diagonal chunk masks the keys after each query.
+// Query blocks are launched longest (most keys) first.
+namespace {
+constexpr int PF_ROWS = 64;                    // query tokens per CTA
+constexpr int PF_KEYS = 64;                    // keys per chunk (= PF_ROWS: chunk qb is the diagonal)
+constexpr int PF_STAGES = 3;
+constexpr int PF_TILE = PF_KEYS * AT_D;        // bytes of K (or of V) per chunk
+constexpr int PF_STAGE = 2 * PF_TILE;
+constexpr int PF_BAR_OFF = PF_STAGES * PF_STAGE;
+constexpr int PF_DYN_SMEM = PF_BAR_OFF + PF_STAGES * 8 + 1024;
+static_assert(PF_TILE % 1024 == 0, "128-byte-swizzled tiles start on 1024-byte boundaries");
+static_assert(PF_ROWS == 16 * AT_WARPS && PF_KEYS == PF_ROWS, "one diagonal chunk per query block");
+}  // namespace
+
+__global__ void __launch_bounds__(AT_THREADS)
+    prefill_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
+                             const __grid_constant__ CUtensorMap tm_v,
+                             const uint8_t* __restrict__ q, const float* __restrict__ sq_p,
+                             const float* __restrict__ sk_p, const float* __restrict__ sv_p,
+                             int seq, int hq, int hkv, int nqb, float softmax_scale,
+                             uint16_t* __restrict__ out) {
+  extern __shared__ __align__(16) uint8_t at_smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, tig = lane & 3;
+  const int qb = nqb - 1 - (int)blockIdx.x;  // the longest blocks first
+  const int h = (int)blockIdx.y;
+  const int64_t b = blockIdx.z;
+  const int kh = h / (hq / hkv);
+  const int r0 = qb * PF_ROWS + 16 * warp;  // this warp's first query token
+  const int nch = qb + 1;                   // key chunks 0 .. qb
+  const uint32_t base = (ptx::smem_addr(at_smem) + 1023u) & ~1023u;
+  const uint32_t bar0 = base + PF_BAR_OFF;
+  // cache row of token t of this sequence is b * seq + t (fits: checked on the host)
+  const int krow0 = (int)(b * seq);
+  const int x0 = kh * AT_D;
+  auto issue = [&](int c) {
+    const uint32_t st = base + (c % PF_STAGES) * PF_STAGE;
+    const uint32_t bar = bar0 + (c % PF_STAGES) * 8;
+    ptx::mbar_arrive_expect_tx(bar, PF_STAGE);
+    ptx::tma_load_2d(st, &tm_k, bar, x0, krow0 + c * PF_KEYS);
+    ptx::tma_load_2d(st + PF_TILE, &tm_v, bar, x0, krow0 + c * PF_KEYS);
+  };
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < PF_STAGES; ++s) ptx::mbar_init(bar0 + s * 8, 1);
+    ptx::fence_mbar_init();
+    for (int c = 0; c < PF_STAGES && c < nch; ++c) issue(c);
+  }
+  __syncthreads();  // the barriers are initialised before any thread polls them
+
+  // Q as the A operand of S = Q K^T (raw E4M3 codes): rows g and g + 8 are
+  // query tokens r0 + g and r0 + g + 8 (zero past the sequence); k step ks
+  // covers dims 32 ks .. 32 ks + 31
+  uint32_t qa[4][4];
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int tok = r0 + g + 8 * hh;
+    const uint8_t* qp = q + (((b * seq + tok) * hq) + h) * (int64_t)AT_D + 4 * tig;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      qa[ks][hh] = tok < seq ? *reinterpret_cast<const uint32_t*>(qp + 32 * ks) : 0u;
+      qa[ks][2 + hh] = tok < seq ? *reinterpret_cast<const uint32_t*>(qp + 32 * ks + 16) : 0u;
+    }
+  }
+  const float qk = softmax_scale * sq_p[0] * sk_p[0] * 1.4426950408889634f;
+  // online-softmax state of rows g (index 0) and g + 8 (index 1): the 4
+  // lanes of a row agree on m, each sums its own keys into l; O[row, d] for
+  // d = 16 s + 4 tig + e + 2 i: acc[s][e][i] (row g), acc[s][e][2 + i] (row g + 8)
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f};
+  float acc[8][2][4];
+#pragma unroll
+  for (int s = 0; s < 8; ++s)
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[s][e][i] = 0.0f;
+  // ldmatrix row address of this lane inside a tile (as in the decode kernel)
+  const int mrow = (lane & 7) + ((lane >> 3) & 1) * 8;
+  const int mseg = lane >> 4;
+
+  int c = 0;
+  bool ok = true;
+  for (; c < nch; ++c) {
+    const int s = c % PF_STAGES;
+    const bool landed = ptx::mbar_wait(bar0 + s * 8, (uint32_t)(c / PF_STAGES) & 1u, AT_WAIT_LIMIT_NS);
+    if (!__syncthreads_and(landed ? 1 : 0)) {
+      ok = false;
+      break;
+    }
+    const uint32_t tk = base + s * PF_STAGE, tv = tk + PF_TILE;
+    const bool diag = c == qb;
+    // S for the chunk: n tile j holds keys 64 c + 8 j + 0..7; this lane gets
+    // keys 64 c + 8 j + 2 tig + {0, 1} of rows g and g + 8
+    float sp[PF_KEYS / 8][4];
+#pragma unroll
+    for (int j = 0; j < PF_KEYS / 8; ++j)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sp[j][i] = 0.0f;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+      for (int tb = 0; tb < PF_KEYS / 16; ++tb) {
+        uint32_t r[4];
+        const int row = 16 * tb + mrow;
+        ldsm_x4(tk + row * AT_D + (((2 * ks + mseg) ^ (row & 7)) << 4), r);
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) mma_e4m3_rows16(sp[2 * tb + jj], qa[ks], r[jj], r[jj + 2]);
+      }
+    // one online-softmax step per row: scores in log2 units, keys after the
+    // query weigh nothing (the diagonal chunk only); every row has key 0 in
+    // chunk 0, so its maximum is finite from the first step on
+    float mx[2] = {m[0], m[1]};
+#pragma unroll
+    for (int j = 0; j < PF_KEYS / 8; ++j)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int key = c * PF_KEYS + 8 * j + 2 * tig + (i & 1);
+        const int row = r0 + g + 8 * (i >> 1);
+        const float x = diag && key > row ? -INFINITY : sp[j][i] * qk;
+        sp[j][i] = x;
+        mx[i >> 1] = fmaxf(mx[i >> 1], x);
+      }
+    float cr[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xFFFFFFFFu, mx[hh], 1));
+      mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xFFFFFFFFu, mx[hh], 2));
+      // 0 for the first step, exactly 1 while the maximum holds
+      cr[hh] = m[hh] == mx[hh] ? 1.0f : ex2_approx(m[hh] - mx[hh]);
+    }
+    float ps[2] = {0.0f, 0.0f};
+#pragma unroll
+    for (int j = 0; j < PF_KEYS / 8; ++j)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        sp[j][i] = ex2_approx(sp[j][i] - mx[i >> 1] + AT_P_LOG2);
+        ps[i >> 1] += sp[j][i];
+      }
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      l[hh] = __fmaf_rn(l[hh], cr[hh], ps[hh]);
+      m[hh] = mx[hh];
+    }
+    if (__any_sync(0xFFFFFFFFu, cr[0] != 1.0f || cr[1] != 1.0f)) {
+#pragma unroll
+      for (int s2 = 0; s2 < 8; ++s2)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[s2][e][i] *= cr[i >> 1];
+    }
+    // O += P V, one k16 step per 16 keys: P in the A layout (rows g, g + 8;
+    // k slots = the keys, where the S tiles left them), as high and low f16
+    // parts, each one MMA against the same V fragments
+#pragma unroll
+    for (int kk = 0; kk < PF_KEYS / 16; ++kk) {
+      uint32_t ah[4], al[4];  // a0: row g keys 0-7 of the step, a1: row g + 8, a2 / a3: keys 8-15
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const float p0 = sp[2 * kk + t][2 * hh], p1 = sp[2 * kk + t][2 * hh + 1];
+          const uint32_t hi = pack_f16x2(p0, p1);
+          const float2 f = unpack_f16x2(hi);
+          ah[2 * t + hh] = hi;
+          al[2 * t + hh] = pack_f16x2(p0 - f.x, p1 - f.y);
+        }
+#pragma unroll
+      for (int spg = 0; spg < 8; spg += 2) {
+        // transposed: keys 16 kk + 2 tig + {0, 1} (+ 8) of dims 2 g, 2 g + 1 of a segment
+        uint32_t r[4];
+        const int row = 16 * kk + mrow;
+        ldsm_x4_trans(tv + row * AT_D + (((spg + mseg) ^ (row & 7)) << 4), r);
+#pragma unroll
+        for (int hs = 0; hs < 2; ++hs) {
+          const int seg = spg + hs;
+          const uint32_t x0v = __byte_perm(r[2 * hs], 0u, 0x3120u);
+          const uint32_t x1v = __byte_perm(r[2 * hs + 1], 0u, 0x3120u);
+          uint32_t b0[2], b1[2];  // [e]: n tile of dims 16 seg + 2 n + e
+          e4m3x4_f16x2x2(x0v, b0[0], b0[1]);
+          e4m3x4_f16x2x2(x1v, b1[0], b1[1]);
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            mma_rows16(acc[seg][e], ah[0], ah[1], ah[2], ah[3], b0[e], b1[e]);
+            mma_rows16(acc[seg][e], al[0], al[1], al[2], al[3], b0[e], b1[e]);
+          }
+        }
+      }
+    }
+    // every warp has used this stage (each ldmatrix result has fed an MMA
+    // above): refill it with chunk c + PF_STAGES
+    __syncthreads();
+    if (threadIdx.x == 0 && c + PF_STAGES < nch) issue(c + PF_STAGES);
+  }
+  if (!ok && threadIdx.x == 0) {
+    // chunks c .. c + PF_STAGES - 1 may still be in flight: let them land
+    // (bounded) before the shared memory is given up
+    atomicCAS(&g_w8a8_attn_error, 0, 23);
+    for (int j = c; j < nch && j < c + PF_STAGES; ++j)
+      if (!ptx::mbar_wait(bar0 + (j % PF_STAGES) * 8, (uint32_t)(j / PF_STAGES) & 1u,
+                          AT_WAIT_LIMIT_NS))
+        atomicCAS(&g_w8a8_attn_error, 0, 24);
+  }
+  if (!ok) return;
+  const float sv = sv_p[0];
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    float lt = l[hh];
+    lt += __shfl_xor_sync(0xFFFFFFFFu, lt, 1);
+    lt += __shfl_xor_sync(0xFFFFFFFFu, lt, 2);
+    const int tok = r0 + g + 8 * hh;
+    if (tok >= seq) continue;
+    const float f = sv / lt;
+    uint16_t* o = out + (((b * seq + tok) * hq) + h) * (int64_t)AT_D;
+#pragma unroll
+    for (int s2 = 0; s2 < 8; ++s2)
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        // dims 16 s2 + 4 tig + 2 i + {0, 1}
+        const uint32_t v2 = (uint32_t)bf16_rn(acc[s2][0][2 * hh + i] * f) |
+                            ((uint32_t)bf16_rn(acc[s2][1][2 * hh + i] * f) << 16);
+        *reinterpret_cast<uint32_t*>(o + 16 * s2 + 4 * tig + 2 * i) = v2;
+      }
+  }
+}
+
+cudaError_t launch_prefill_attention(const uint8_t* q, const float* sq, const uint8_t* k,
+                                     const float* sk, const uint8_t* v, const float* sv,
+                                     int64_t batch, int64_t seq, int hq, int hkv,
+                                     float softmax_scale, uint16_t* out, cudaStream_t st) {
+  if (batch == 0 || seq == 0) return cudaSuccess;
+  const int64_t nqb = (seq + PF_ROWS - 1) / PF_ROWS;
+  // grid y / z limits; TMA row coordinates are 32-bit: the last chunk may
+  // run PF_KEYS rows past batch * seq (those rows read as zero)
+  if (hq > 65535 || batch > 65535 || nqb > 0x7FFFFFFFLL ||
+      batch * seq > 0x7FFFFFFFLL - PF_KEYS)
+    return cudaErrorInvalidValue;
+  CUtensorMap tm_k, tm_v;
+  const uint64_t rows = (uint64_t)(batch * seq), cols = (uint64_t)hkv * AT_D;
+  if (!make_tmap_2d(&tm_k, k, 1, rows, cols, PF_KEYS, AT_D, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d(&tm_v, v, 1, rows, cols, PF_KEYS, AT_D, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    e = cudaFuncSetAttribute(prefill_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             PF_DYN_SMEM);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev] = true;
+  }
+  const dim3 grid((unsigned)nqb, (unsigned)hq, (unsigned)batch);
+  prefill_attention_kernel<<<grid, AT_THREADS, PF_DYN_SMEM, st>>>(
+      tm_k, tm_v, q, sq, sk, sv, (int)seq, hq, hkv, (int)nqb, softmax_scale, out);
+  return cudaGetLastError();
 }
 
 }  // namespace w8a8

@@ -57,6 +57,12 @@ cudaError_t launch_quant_error(const uint16_t* x, const uint8_t* q, const float*
                                int64_t cols, int64_t sbr, int64_t sbc, int64_t rbr, int64_t rbc,
                                double* stats, cudaStream_t st);
 
+// attention.cu: causal prefill attention over FP8 Q, K, V (head dim 128).
+cudaError_t launch_prefill_attention(const uint8_t* q, const float* sq, const uint8_t* k,
+                                     const float* sk, const uint8_t* v, const float* sv,
+                                     int64_t batch, int64_t seq, int hq, int hkv,
+                                     float softmax_scale, uint16_t* out, cudaStream_t st);
+
 // attention.cu: decode attention over the FP8 KV cache (head dim 128).
 cudaError_t launch_decode_attention(const uint8_t* q, const float* sq, const uint8_t* k,
                                     const float* sk, const uint8_t* v, const float* sv,
