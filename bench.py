@@ -811,6 +811,7 @@ def measure_next_rows(W, wl, peaks, reps=3):
         "workload": "32 sequences x 8192 tokens, 32 query heads over 8 KV heads, head dim 128",
         "us": round(sec * 1e6, 1), "gbs": round(nb / sec / 1e9, 1),
         "pct_roofline": round(100 * nb / sec / 1e9 / peaks["hbm_gbs"], 2), "bytes_per_call": nb}
+    out["fp8_prefill_attention"] = measure_prefill_attention(W, peaks)
     out["fp8_block_gemm_pow2"] = measure_pow2_gemm(W, wl, peaks, reps)
     out["config1_single_linear"] = measure_single_linear(W, peaks)
     W.quantize_weight_blockwise_batched(wl.w, wl.wout)
@@ -834,6 +835,45 @@ def measure_next_rows(W, wl, peaks, reps=3):
     del yall, sall
     assert W.consume_device_error() == 0
     return out
+
+
+def prefill_attention_flops(B, S, Hq, D=128):
+    """Causal attention: query token i meets keys 0..i, 2 D FLOPs each for
+    Q K^T and for P V."""
+    return 4 * D * Hq * B * S * (S + 1) // 2
+
+
+def measure_prefill_attention(W, peaks, reps=10):
+    """Causal prefill attention for a rollout prompt batch on Qwen3-8B's
+    attention shape: 4 sequences x 2048 tokens, 32 query heads over 8 KV
+    heads, head dim 128; Q, K, V per-tensor-quantized N(0, 1) activations.
+    Tensor work (Q K^T on E4M3, P V in f16 with the weights in two parts),
+    against the FP8 peak."""
+    from w8a8_gemm_rl_gb300 import synth
+    B, S, Hq, Hkv = 4, 2048, 32, 8
+    x = [synth.activations(B * S * h, 128, seed=95 + i, device="cuda").reshape(B, S, h, 128)
+         for i, h in enumerate((Hq, Hkv, Hkv))]
+    qkv = [W.kv_amax_quantize(t) for t in x]
+    args = (qkv[0][0], qkv[0][1], qkv[1][0], qkv[1][1], qkv[2][0], qkv[2][1])
+    att = W.fp8_prefill_attention(*args)
+    for _ in range(3):
+        W.fp8_prefill_attention(*args, out=att)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(reps):
+        W.fp8_prefill_attention(*args, out=att)
+    t1.record()
+    torch.cuda.synchronize()
+    assert W.consume_device_error() == 0
+    sec = t0.elapsed_time(t1) * 1e-3 / reps
+    f = prefill_attention_flops(B, S, Hq)
+    tf = f / sec / 1e12
+    return {"workload": "4 sequences x 2048 tokens, causal, 32 query heads over 8 KV heads, "
+                        "head dim 128", "us": round(sec * 1e6, 1), "tflops": round(tf, 1),
+            "pct_roofline": round(100 * tf / fp8_peak_tflops(peaks), 2), "flops_per_call": f,
+            "note": "mma.sync tensor path (E4M3 Q K^T, f16 P V with two-part weights)"}
 
 
 def single_linear_work():

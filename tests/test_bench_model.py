@@ -94,3 +94,10 @@ def test_single_linear_work():
     gemm = 65536 + 131072 + 4 * (128 * 4 + 2 * 4) + 65536
     assert b == q_x + q_w + gemm
 
+
+def test_prefill_attention_flops():
+    """Causal: query token i meets i + 1 keys, 4 D FLOPs per (query, key,
+    head): S (S + 1) / 2 pairs per sequence and head."""
+    assert bench.prefill_attention_flops(1, 1, 1) == 4 * 128
+    assert bench.prefill_attention_flops(2, 3, 4) == 4 * 128 * 4 * 2 * 6
+

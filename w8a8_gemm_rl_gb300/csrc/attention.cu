@@ -577,7 +577,8 @@ static_assert(PF_TILE % 1024 == 0, "128-byte-swizzled tiles start on 1024-byte b
 static_assert(PF_ROWS == 16 * AT_WARPS && PF_KEYS == PF_ROWS, "one diagonal chunk per query block");
 }  // namespace
 
-__global__ void __launch_bounds__(AT_THREADS)
+// 3 CTAs per SM (168 registers): 6-7% faster than 2 (180 registers)
+__global__ void __launch_bounds__(AT_THREADS, 3)
     prefill_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                              const __grid_constant__ CUtensorMap tm_v,
                              const uint8_t* __restrict__ q, const float* __restrict__ sq_p,
