@@ -69,7 +69,7 @@ const char *w8a8_last_cuda_error(void);
  * bounded wait inside it gives up (0 = none; nonzero identifies the wait:
  * 1..10 the GEMMs of more than 256 rows and the grouped GEMM, 31..37 the
  * GEMM of at most 256 rows, 51..58 the power-of-two GEMM (59: a scale it
- * cannot hold), 11..13 the weight quantizer, 21..24 the decode and prefill
+ * cannot hold), 11..13 the weight quantizer, 21..23 the decode and prefill
  * attention,
  * 41..43 the batched dequantizer and error report).  When several are set,
  * the GEMMs' code is reported first, then the quantizer's, and all are
@@ -344,12 +344,14 @@ w8a8_status fp8_decode_attention(const uint8_t *q, const float *q_scale,
  * (weights below 2^-39 of the row's largest, which f16 cannot hold, are
  * left out).
  * Rules: head_dim == 128 (else W8A8_ERR_UNSUPPORTED); num_q_heads and
- * batch at most 65535, seq and batch * seq below 2^31 - 64 (grid and TMA
- * coordinate limits; over-size inputs give W8A8_ERR_UNSUPPORTED); q, k and
- * v 16-byte aligned, the rest 4-byte aligned.  A CTA takes 64 query tokens
- * of one (sequence, query head) and streams the keys and values up to them
- * in chunks of 64 tokens (TMA tiles), on the tensor cores (E4M3 for Q K^T,
- * f16 for P V).  A bounded wait that gives up records device error 23 or 24.
+ * batch at most 65535, seq and batch * seq below 2^31 - 128 (grid and TMA
+ * coordinate limits; over-size inputs give W8A8_ERR_UNSUPPORTED); q, k, v
+ * and out_bf16 16-byte aligned, the scales 4-byte aligned.  A CTA takes 128
+ * query tokens of one (sequence, query head) and streams the keys and
+ * values up to them in chunks of 128 tokens (TMA tiles); both products run
+ * on the tcgen05 tensor cores with the accumulators in tensor memory (E4M3
+ * for Q K^T, f16 for P V).  A bounded wait that gives up records device
+ * error 23.
  * ---------------------------------------------------------------------- */
 w8a8_status fp8_prefill_attention(const uint8_t *q, const float *q_scale,
                                   const uint8_t *k, const float *k_scale,

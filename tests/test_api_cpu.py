@@ -149,10 +149,13 @@ def test_prefill_attention_argument_checks(L):
     assert a(A, A, None, A, A, A, 2, 64, 8, 2, 128, sc, A, None) == NULL
     assert a(A, A, A + 4, A, A, A, 2, 64, 8, 2, 128, sc, A, None) == ALIGN
     assert a(A, A, A, A, A, A, 2, 64, 8, 2, 128, sc, A + 2, None) == ALIGN
+    assert a(A, A, A, A, A, A, 2, 64, 8, 2, 128, sc, A + 8, None) == ALIGN  # out: 16 bytes
     # grid limits and 32-bit TMA row coordinates
     assert a(A, A, A, A, A, A, 1 << 16, 1, 8, 2, 128, sc, A, None) == UNSUP
     assert a(A, A, A, A, A, A, 2, 64, 1 << 16, 2, 128, sc, A, None) == UNSUP
     assert a(A, A, A, A, A, A, 1 << 15, 1 << 16, 8, 2, 128, sc, A, None) == UNSUP
+    # the last key tile of the last sequence starts below 2^31 - 128
+    assert a(A, A, A, A, A, A, 2, (1 << 30) - 63, 8, 2, 128, sc, A, None) == UNSUP
 
 
 def test_gemm_argument_checks(L):

@@ -307,13 +307,13 @@ W8A8_API w8a8_status fp8_prefill_attention(const uint8_t* q, const float* q_scal
   // over-size inputs (grid dimensions; TMA row coordinates are 32-bit) share one status
   if (num_q_heads > 65535 || batch > 65535 || seq >= kMaxDim) return W8A8_ERR_UNSUPPORTED;
   if (batch == 0 || seq == 0) return W8A8_OK;
-  if (batch * seq > kMaxDim - 1 - 64) return W8A8_ERR_UNSUPPORTED;
+  if (batch * seq > kMaxDim - 1 - 128) return W8A8_ERR_UNSUPPORTED;
   if (!q || !q_scale || !k || !k_scale || !v || !v_scale || !out_bf16) return W8A8_ERR_NULL;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out_bf16, 4) ||
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out_bf16, 16) ||
       !aligned(q_scale, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4))
     return W8A8_ERR_ALIGN;
-  return from_cuda(w8a8::launch_prefill_attention(q, q_scale, k, k_scale, v, v_scale, batch, seq,
-                                                  num_q_heads, num_kv_heads, softmax_scale,
+  return from_cuda(w8a8::launch_prefill_attention(q, q_scale, k, k_scale, v, v_scale, batch,
+                                                  seq, num_q_heads, num_kv_heads, softmax_scale,
                                                   out_bf16, cs(stream)));
 }
 

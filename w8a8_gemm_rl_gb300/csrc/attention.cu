@@ -146,18 +146,6 @@ __device__ __forceinline__ void mma_e4m3_rows8(float& d0, float& d1, uint32_t a0
       : "r"(a0), "r"(0u), "r"(a2), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
-// d += A B on one full m16n8k32 tile of E4M3 codes (f32 accumulate): a[0] /
-// a[2] bytes 4 tig .. 4 tig + 3 of the two 16-byte halves of row g's k
-// range, a[1] / a[3] the same of row g + 8; d[0], d[1] row g, d[2], d[3] row
-// g + 8.
-__device__ __forceinline__ void mma_e4m3_rows16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                                uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 __device__ __forceinline__ uint16_t bf16_rn(float x) {
   uint16_t r;
   asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(x));
@@ -556,236 +544,413 @@ cudaError_t launch_decode_attention(const uint8_t* q, const float* sq, const uin
 // q [batch, seq, hq, 128], k and v [batch, seq, hkv, 128] (the KV cache's
 // layout), out [batch, seq, hq, 128] BF16.
 //
-// A CTA takes 64 query tokens of one (sequence, query head); each of its 4
-// warps 16 of them, as the rows of m16 MMA tiles.  The keys come in chunks
-// of 64 tokens (K and V tiles by TMA, 128-byte swizzle, a 3-stage ring
-// shared by the warps): S = Q K^T on the raw E4M3 codes (m16n8k32, f32
-// accumulation), one online-softmax step per chunk in log2 units, then
-// O += P V in f16 with the weights P = 2^15 p split into high and low f16
-// parts (two MMAs; together they carry 22 bits of each weight), V widened
-// exactly from E4M3.  The diagonal chunk masks the keys after each query.
-// Query blocks are launched longest (most keys) first.
+// Both contractions run on the 5th-generation tensor cores with the
+// accumulators in tensor memory.  A CTA takes 128 query tokens of one
+// (sequence, query head); keys come in chunks of 128 tokens, so chunk qb is
+// the diagonal one; query blocks are launched longest (most keys) first.
+//   warp 0     TMA: the Q tile once, then K and V tiles (E4M3, 128-byte
+//              swizzle) into a 2-stage ring;
+//   warp 1     allocates 512 TMEM columns; lane 0 issues S(j) = Q K_j^T on
+//              the raw E4M3 codes (kind::f8f6f4, M = 128 queries, N = 128
+//              keys, f32 accumulation) into one of two S buffers, and
+//              PV(j) = P_j V_j (kind::f16, M = 128 queries, N = 128 dims,
+//              K = 128 keys, the weights' high and low f16 parts in turn)
+//              into the PV buffer;
+//   warps 2-3  widen each V tile to f16, transposed (V^T [dim][key], the
+//              K-major B operand), exactly;
+//   warps 4-7  one query row per thread: the row of S(j) out of TMEM, its
+//              maximum and weights P = 2^15 p (online softmax in log2 units,
+//              later keys masked in the diagonal chunk) as high and low f16
+//              parts (together 22 bits of each weight) into shared memory
+//              (the A operand), then the row of PV(j):
+//              O = O * correction + PV(j) in FP32 registers.
+// The softmax passes keep their 32-column loops rolled: fully unrolled, the
+// loop body outgrew the instruction cache and the kernel ran ~30% slower.
+// Every mbarrier wait is bounded; a wait that gives up records error 23 and
+// stops the CTA's roles.
 namespace {
-constexpr int PF_ROWS = 64;                    // query tokens per CTA
-constexpr int PF_KEYS = 64;                    // keys per chunk (= PF_ROWS: chunk qb is the diagonal)
-constexpr int PF_STAGES = 3;
-constexpr int PF_TILE = PF_KEYS * AT_D;        // bytes of K (or of V) per chunk
-constexpr int PF_STAGE = 2 * PF_TILE;
-constexpr int PF_BAR_OFF = PF_STAGES * PF_STAGE;
-constexpr int PF_DYN_SMEM = PF_BAR_OFF + PF_STAGES * 8 + 1024;
-static_assert(PF_TILE % 1024 == 0, "128-byte-swizzled tiles start on 1024-byte boundaries");
-static_assert(PF_ROWS == 16 * AT_WARPS && PF_KEYS == PF_ROWS, "one diagonal chunk per query block");
+constexpr int PT_ROWS = 128;                        // query tokens per CTA
+constexpr int PT_KEYS = 128;                        // keys per chunk
+constexpr int PT_TILE = PT_KEYS * AT_D;             // 16 KB: a Q, K or V tile (E4M3)
+constexpr int PT_HALF = 128 * 128;                  // 16 KB: 128 rows x 64 f16 (128 bytes)
+constexpr int PT_OFF_Q = 0;
+constexpr int PT_OFF_KV = PT_OFF_Q + PT_TILE;       // 2 stages of (K, V)
+constexpr int PT_OFF_VT = PT_OFF_KV + 4 * PT_TILE;  // 2 buffers of V^T f16 (2 halves each)
+constexpr int PT_OFF_P = PT_OFF_VT + 4 * PT_HALF;   // P high (2 halves), P low (2 halves)
+constexpr int PT_OFF_BAR = PT_OFF_P + 4 * PT_HALF;
+constexpr int PT_NBAR = 18;
+constexpr int PT_OFF_MISC = PT_OFF_BAR + PT_NBAR * 8;
+constexpr int PT_DYN_SMEM = PT_OFF_MISC + 16 + 1024;
+constexpr int PT_THREADS = 256;
+constexpr uint32_t PT_IDESC = ptx::idesc_e4m3_f32(128, 128);  // also kind::f16 with F16 A, B
+static_assert(PT_OFF_KV % 1024 == 0 && PT_OFF_VT % 1024 == 0 && PT_OFF_P % 1024 == 0,
+              "swizzled tiles start on 1024-byte boundaries");
+static_assert(PT_DYN_SMEM <= 232448, "shared memory");
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// bounded mbarrier wait that also gives up once another role has
+__device__ __forceinline__ bool pt_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (ptx::globaltimer() - t0 > AT_WAIT_LIMIT_NS) {
+      atomicCAS(&g_w8a8_attn_error, 0, 23);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
 }  // namespace
 
-// 3 CTAs per SM (168 registers): 6-7% faster than 2 (180 registers)
-__global__ void __launch_bounds__(AT_THREADS, 3)
-    prefill_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
-                             const __grid_constant__ CUtensorMap tm_v,
-                             const uint8_t* __restrict__ q, const float* __restrict__ sq_p,
-                             const float* __restrict__ sk_p, const float* __restrict__ sv_p,
-                             int seq, int hq, int hkv, int nqb, float softmax_scale,
-                             uint16_t* __restrict__ out) {
+__global__ void __launch_bounds__(PT_THREADS, 1)
+    prefill_attention_kernel(const __grid_constant__ CUtensorMap tm_q,
+                                const __grid_constant__ CUtensorMap tm_k,
+                                const __grid_constant__ CUtensorMap tm_v,
+                                const float* __restrict__ sq_p, const float* __restrict__ sk_p,
+                                const float* __restrict__ sv_p, int seq, int hq, int hkv, int nqb,
+                                float softmax_scale, uint16_t* __restrict__ out) {
   extern __shared__ __align__(16) uint8_t at_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, tig = lane & 3;
   const int qb = nqb - 1 - (int)blockIdx.x;  // the longest blocks first
   const int h = (int)blockIdx.y;
   const int64_t b = blockIdx.z;
   const int kh = h / (hq / hkv);
-  const int r0 = qb * PF_ROWS + 16 * warp;  // this warp's first query token
-  const int nch = qb + 1;                   // key chunks 0 .. qb
+  const int q0 = qb * PT_ROWS;
+  const int nch = qb + 1;  // key chunks 0 .. qb; chunk qb is the diagonal
   const uint32_t base = (ptx::smem_addr(at_smem) + 1023u) & ~1023u;
-  const uint32_t bar0 = base + PF_BAR_OFF;
-  // cache row of token t of this sequence is b * seq + t (fits: checked on the host)
-  const int krow0 = (int)(b * seq);
-  const int x0 = kh * AT_D;
-  auto issue = [&](int c) {
-    const uint32_t st = base + (c % PF_STAGES) * PF_STAGE;
-    const uint32_t bar = bar0 + (c % PF_STAGES) * 8;
-    ptx::mbar_arrive_expect_tx(bar, PF_STAGE);
-    ptx::tma_load_2d(st, &tm_k, bar, x0, krow0 + c * PF_KEYS);
-    ptx::tma_load_2d(st + PF_TILE, &tm_v, bar, x0, krow0 + c * PF_KEYS);
-  };
+  uint8_t* gbase = at_smem + (base - ptx::smem_addr(at_smem));
+  const uint32_t bar0 = base + PT_OFF_BAR;
+  const uint32_t q_full = bar0;
+  auto kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto kv_empty = [&](int s) { return bar0 + 8u * (3 + s); };   // S MMA commit + 2 converter warps
+  auto s_full = [&](int s) { return bar0 + 8u * (5 + s); };
+  auto s_empty = [&](int s) { return bar0 + 8u * (7 + s); };    // 4 softmax warps
+  auto vt_full = [&](int s) { return bar0 + 8u * (9 + s); };    // 2 converter warps
+  auto vt_empty = [&](int s) { return bar0 + 8u * (11 + s); };  // PV MMA commit
+  const uint32_t p_full = bar0 + 8u * 13;                         // 4 softmax warps
+  const uint32_t p_empty = bar0 + 8u * 14;                        // PV MMA commit
+  const uint32_t pv_full = bar0 + 8u * 15;                        // PV MMA commit
+  const uint32_t pv_empty = bar0 + 8u * 16;                       // 4 softmax warps
+  const uint32_t mma_done = bar0 + 8u * 17;                       // the last MMAs completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + PT_OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + PT_OFF_MISC + 4);
+  const int krow0 = (int)(b * seq);  // cache row of the sequence's token 0 (checked on the host)
+
   if (threadIdx.x == 0) {
-    for (int s = 0; s < PF_STAGES; ++s) ptx::mbar_init(bar0 + s * 8, 1);
+    ptx::mbar_init(q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(kv_full(s), 1);
+      ptx::mbar_init(kv_empty(s), 3);
+      ptx::mbar_init(s_full(s), 1);
+      ptx::mbar_init(s_empty(s), 4);
+      ptx::mbar_init(vt_full(s), 2);
+      ptx::mbar_init(vt_empty(s), 1);
+    }
+    ptx::mbar_init(p_full, 4);
+    ptx::mbar_init(p_empty, 1);
+    ptx::mbar_init(pv_full, 1);
+    ptx::mbar_init(pv_empty, 4);
+    ptx::mbar_init(mma_done, 1);
+    *abort_flag = 0;
     ptx::fence_mbar_init();
-    for (int c = 0; c < PF_STAGES && c < nch; ++c) issue(c);
   }
-  __syncthreads();  // the barriers are initialised before any thread polls them
-
-  // Q as the A operand of S = Q K^T (raw E4M3 codes): rows g and g + 8 are
-  // query tokens r0 + g and r0 + g + 8 (zero past the sequence); k step ks
-  // covers dims 32 ks .. 32 ks + 31
-  uint32_t qa[4][4];
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    const int tok = r0 + g + 8 * hh;
-    const uint8_t* qp = q + (((b * seq + tok) * hq) + h) * (int64_t)AT_D + 4 * tig;
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      qa[ks][hh] = tok < seq ? *reinterpret_cast<const uint32_t*>(qp + 32 * ks) : 0u;
-      qa[ks][2 + hh] = tok < seq ? *reinterpret_cast<const uint32_t*>(qp + 32 * ks + 16) : 0u;
-    }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), 512);
+    ptx::tmem_relinquish();
   }
-  const float qk = softmax_scale * sq_p[0] * sk_p[0] * 1.4426950408889634f;
-  // online-softmax state of rows g (index 0) and g + 8 (index 1): the 4
-  // lanes of a row agree on m, each sums its own keys into l; O[row, d] for
-  // d = 16 s + 4 tig + e + 2 i: acc[s][e][i] (row g), acc[s][e][2 + i] (row g + 8)
-  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f};
-  float acc[8][2][4];
-#pragma unroll
-  for (int s = 0; s < 8; ++s)
-#pragma unroll
-    for (int e = 0; e < 2; ++e)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc[s][e][i] = 0.0f;
-  // ldmatrix row address of this lane inside a tile (as in the decode kernel)
-  const int mrow = (lane & 7) + ((lane >> 3) & 1) * 8;
-  const int mseg = lane >> 4;
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t tS0 = tmem_base, tPV = tmem_base + 256;
 
-  int c = 0;
-  bool ok = true;
-  for (; c < nch; ++c) {
-    const int s = c % PF_STAGES;
-    const bool landed = ptx::mbar_wait(bar0 + s * 8, (uint32_t)(c / PF_STAGES) & 1u, AT_WAIT_LIMIT_NS);
-    if (!__syncthreads_and(landed ? 1 : 0)) {
-      ok = false;
-      break;
-    }
-    const uint32_t tk = base + s * PF_STAGE, tv = tk + PF_TILE;
-    const bool diag = c == qb;
-    // S for the chunk: n tile j holds keys 64 c + 8 j + 0..7; this lane gets
-    // keys 64 c + 8 j + 2 tig + {0, 1} of rows g and g + 8
-    float sp[PF_KEYS / 8][4];
-#pragma unroll
-    for (int j = 0; j < PF_KEYS / 8; ++j)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) sp[j][i] = 0.0f;
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks)
-#pragma unroll
-      for (int tb = 0; tb < PF_KEYS / 16; ++tb) {
-        uint32_t r[4];
-        const int row = 16 * tb + mrow;
-        ldsm_x4(tk + row * AT_D + (((2 * ks + mseg) ^ (row & 7)) << 4), r);
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) mma_e4m3_rows16(sp[2 * tb + jj], qa[ks], r[jj], r[jj + 2]);
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA
+    if (lane == 0) {
+      ptx::mbar_arrive_expect_tx(q_full, PT_TILE);
+      ptx::tma_load_2d(base + PT_OFF_Q, &tm_q, q_full, h * AT_D, krow0 + q0);
+      int issued = 0;
+      for (int c = 0; c < nch; ++c) {
+        const int s = c & 1;
+        if (!pt_wait(kv_empty(s), (uint32_t)(((c >> 1) & 1) ^ 1), abort_flag)) break;
+        const uint32_t st = base + PT_OFF_KV + s * 2 * PT_TILE;
+        ptx::mbar_arrive_expect_tx(kv_full(s), 2 * PT_TILE);
+        ptx::tma_load_2d(st, &tm_k, kv_full(s), kh * AT_D, krow0 + c * PT_KEYS);
+        ptx::tma_load_2d(st + PT_TILE, &tm_v, kv_full(s), kh * AT_D, krow0 + c * PT_KEYS);
+        ++issued;
       }
-    // one online-softmax step per row: scores in log2 units, keys after the
-    // query weigh nothing (the diagonal chunk only); every row has key 0 in
-    // chunk 0, so its maximum is finite from the first step on
-    float mx[2] = {m[0], m[1]};
-#pragma unroll
-    for (int j = 0; j < PF_KEYS / 8; ++j)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int key = c * PF_KEYS + 8 * j + 2 * tig + (i & 1);
-        const int row = r0 + g + 8 * (i >> 1);
-        const float x = diag && key > row ? -INFINITY : sp[j][i] * qk;
-        sp[j][i] = x;
-        mx[i >> 1] = fmaxf(mx[i >> 1], x);
+      // no copy may still be landing when the CTA retires
+      const uint64_t t0 = ptx::globaltimer();
+      while (!ptx::mbar_try_wait(q_full, 0))
+        if (ptx::globaltimer() - t0 > AT_WAIT_LIMIT_NS) { atomicCAS(&g_w8a8_attn_error, 0, 23); break; }
+      for (int c = issued > 2 ? issued - 2 : 0; c < issued; ++c) {
+        const uint64_t t1 = ptx::globaltimer();
+        while (!ptx::mbar_try_wait(kv_full(c & 1), (uint32_t)((c >> 1) & 1)))
+          if (ptx::globaltimer() - t1 > AT_WAIT_LIMIT_NS) { atomicCAS(&g_w8a8_attn_error, 0, 23); break; }
       }
-    float cr[2];
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xFFFFFFFFu, mx[hh], 1));
-      mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xFFFFFFFFu, mx[hh], 2));
-      // 0 for the first step, exactly 1 while the maximum holds
-      cr[hh] = m[hh] == mx[hh] ? 1.0f : ex2_approx(m[hh] - mx[hh]);
     }
-    float ps[2] = {0.0f, 0.0f};
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA
+    if (lane == 0) {
+      bool ok = pt_wait(q_full, 0, abort_flag);
+      const uint64_t qdesc = ptx::smem_desc_kmajor_sw128(base + PT_OFF_Q);
+      auto issue_s = [&](int c) {
+        const int s = c & 1;
+        if (!pt_wait(kv_full(s), (uint32_t)((c >> 1) & 1), abort_flag)) return false;
+        if (!pt_wait(s_empty(s), (uint32_t)(((c >> 1) & 1) ^ 1), abort_flag)) return false;
+        ptx::tc_fence_after();
+        const uint64_t kdesc = ptx::smem_desc_kmajor_sw128(base + PT_OFF_KV + s * 2 * PT_TILE);
 #pragma unroll
-    for (int j = 0; j < PF_KEYS / 8; ++j)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        sp[j][i] = ex2_approx(sp[j][i] - mx[i >> 1] + AT_P_LOG2);
-        ps[i >> 1] += sp[j][i];
-      }
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      l[hh] = __fmaf_rn(l[hh], cr[hh], ps[hh]);
-      m[hh] = mx[hh];
-    }
-    if (__any_sync(0xFFFFFFFFu, cr[0] != 1.0f || cr[1] != 1.0f)) {
-#pragma unroll
-      for (int s2 = 0; s2 < 8; ++s2)
-#pragma unroll
-        for (int e = 0; e < 2; ++e)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) acc[s2][e][i] *= cr[i >> 1];
-    }
-    // O += P V, one k16 step per 16 keys: P in the A layout (rows g, g + 8;
-    // k slots = the keys, where the S tiles left them), as high and low f16
-    // parts, each one MMA against the same V fragments
-#pragma unroll
-    for (int kk = 0; kk < PF_KEYS / 16; ++kk) {
-      uint32_t ah[4], al[4];  // a0: row g keys 0-7 of the step, a1: row g + 8, a2 / a3: keys 8-15
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const float p0 = sp[2 * kk + t][2 * hh], p1 = sp[2 * kk + t][2 * hh + 1];
-          const uint32_t hi = pack_f16x2(p0, p1);
-          const float2 f = unpack_f16x2(hi);
-          ah[2 * t + hh] = hi;
-          al[2 * t + hh] = pack_f16x2(p0 - f.x, p1 - f.y);
+        for (int kk = 0; kk < 4; ++kk)  // 32 dims (bytes) per MMA
+          ptx::mma_f8f6f4(tS0 + s * 128, qdesc + 2u * kk, kdesc + 2u * kk, PT_IDESC, kk > 0 ? 1u : 0u);
+        ptx::mma_commit(s_full(s));
+        ptx::mma_commit(kv_empty(s));
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int c = 0; c < nch && ok; ++c) {
+        if (c + 1 < nch && !issue_s(c + 1)) { ok = false; break; }
+        // PV(c): the weights of chunk c in shared memory, V_c^T widened,
+        // the PV buffer read out
+        const int s = c & 1;
+        if (!pt_wait(p_full, (uint32_t)(c & 1), abort_flag) ||
+            !pt_wait(vt_full(s), (uint32_t)((c >> 1) & 1), abort_flag) ||
+            !pt_wait(pv_empty, (uint32_t)((c & 1) ^ 1), abort_flag)) {
+          ok = false;
+          break;
         }
+        ptx::tc_fence_after();
+        const uint32_t vt = base + PT_OFF_VT + s * 2 * PT_HALF;
 #pragma unroll
-      for (int spg = 0; spg < 8; spg += 2) {
-        // transposed: keys 16 kk + 2 tig + {0, 1} (+ 8) of dims 2 g, 2 g + 1 of a segment
-        uint32_t r[4];
-        const int row = 16 * kk + mrow;
-        ldsm_x4_trans(tv + row * AT_D + (((spg + mseg) ^ (row & 7)) << 4), r);
+        for (int part = 0; part < 2; ++part) {  // the weights' high, then low f16 parts
+          const uint32_t pa = base + PT_OFF_P + part * 2 * PT_HALF;
 #pragma unroll
-        for (int hs = 0; hs < 2; ++hs) {
-          const int seg = spg + hs;
-          const uint32_t x0v = __byte_perm(r[2 * hs], 0u, 0x3120u);
-          const uint32_t x1v = __byte_perm(r[2 * hs + 1], 0u, 0x3120u);
-          uint32_t b0[2], b1[2];  // [e]: n tile of dims 16 seg + 2 n + e
-          e4m3x4_f16x2x2(x0v, b0[0], b0[1]);
-          e4m3x4_f16x2x2(x1v, b1[0], b1[1]);
+          for (int kk = 0; kk < 8; ++kk) {  // 16 keys (32 bytes) per MMA
+            const uint32_t hoff = (uint32_t)(kk >> 2) * PT_HALF;
+            const uint64_t adesc = ptx::smem_desc_kmajor_sw128(pa + hoff) + 2u * (kk & 3);
+            const uint64_t bdesc = ptx::smem_desc_kmajor_sw128(vt + hoff) + 2u * (kk & 3);
+            mma_f16(tPV, adesc, bdesc, PT_IDESC, (part | kk) ? 1u : 0u);
+          }
+        }
+        ptx::mma_commit(pv_full);
+        ptx::mma_commit(p_empty);
+        ptx::mma_commit(vt_empty(s));
+      }
+      // every MMA issued has completed before the CTA frees TMEM
+      ptx::mma_commit(mma_done);
+      const uint64_t t0 = ptx::globaltimer();
+      while (!ptx::mbar_try_wait(mma_done, 0))
+        if (ptx::globaltimer() - t0 > AT_WAIT_LIMIT_NS) { atomicCAS(&g_w8a8_attn_error, 0, 23); break; }
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ------------------------------------------------------ V -> V^T (f16)
+    // a block is 16 dims x 8 keys: 8 LDS.128 from key rows (128-byte swizzle
+    // of the TMA tile), transposed with byte permutes, widened exactly to
+    // f16, 16 STS.128 into V^T rows (128-byte swizzle of the K-major operand:
+    // 16-byte chunk c of row d at c ^ (d & 7)). Lane l of converter warp wv
+    // takes key octet (l & 7) + 8 wv and dim groups l >> 3, (l >> 3) + 4:
+    // the stores of a warp fill whole 128-byte lines, the loads two-way.
+    const int wv = warp - 2;
+    const int ko = (lane & 7) + 8 * wv;
+    for (int c = 0; c < nch; ++c) {
+      const int s = c & 1;
+      bool okl = pt_wait(kv_full(s), (uint32_t)((c >> 1) & 1), abort_flag) &&
+                 pt_wait(vt_empty(s), (uint32_t)(((c >> 1) & 1) ^ 1), abort_flag);
+      if (!__all_sync(0xFFFFFFFFu, okl)) break;
+      const uint32_t vsrc = base + PT_OFF_KV + s * 2 * PT_TILE + PT_TILE;
+      const uint32_t vt = base + PT_OFF_VT + s * 2 * PT_HALF + (uint32_t)wv * PT_HALF;
+#pragma unroll 1
+      for (int i = 0; i < 2; ++i) {
+        const int g = (lane >> 3) + 4 * i;  // dims 16 g .. 16 g + 15
+        uint4 w[8];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            mma_rows16(acc[seg][e], ah[0], ah[1], ah[2], ah[3], b0[e], b1[e]);
-            mma_rows16(acc[seg][e], al[0], al[1], al[2], al[3], b0[e], b1[e]);
+        for (int kk = 0; kk < 8; ++kk)
+          w[kk] = ptx::lds128(vsrc + (8 * ko + kk) * 128 + ((g ^ kk) << 4));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t x[8];
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            x[kk] = j == 0 ? w[kk].x : j == 1 ? w[kk].y : j == 2 ? w[kk].z : w[kk].w;
+#pragma unroll
+          for (int dd = 0; dd < 4; ++dd) {
+            // dim 16 g + 4 j + dd of keys 8 ko .. 8 ko + 7: byte dd of each
+            // word (low two bytes: byte dd of the first word, then of the second)
+            const uint32_t sel = (uint32_t)dd | ((uint32_t)(dd + 4) << 4);
+            const uint32_t k01 = __byte_perm(x[0], x[1], sel);
+            const uint32_t k23 = __byte_perm(x[2], x[3], sel);
+            const uint32_t k45 = __byte_perm(x[4], x[5], sel);
+            const uint32_t k67 = __byte_perm(x[6], x[7], sel);
+            const uint32_t k0123 = __byte_perm(k01, k23, 0x5410u);
+            const uint32_t k4567 = __byte_perm(k45, k67, 0x5410u);
+            uint32_t f[4];
+            e4m3x4_f16x2x2(k0123, f[0], f[1]);
+            e4m3x4_f16x2x2(k4567, f[2], f[3]);
+            const int d = 16 * g + 4 * j + dd;
+            ptx::sts128(vt + d * 128 + ((((ko & 7) ^ (d & 7))) << 4), f[0], f[1], f[2], f[3]);
           }
         }
       }
-    }
-    // every warp has used this stage (each ldmatrix result has fed an MMA
-    // above): refill it with chunk c + PF_STAGES
-    __syncthreads();
-    if (threadIdx.x == 0 && c + PF_STAGES < nch) issue(c + PF_STAGES);
-  }
-  if (!ok && threadIdx.x == 0) {
-    // chunks c .. c + PF_STAGES - 1 may still be in flight: let them land
-    // (bounded) before the shared memory is given up
-    atomicCAS(&g_w8a8_attn_error, 0, 23);
-    for (int j = c; j < nch && j < c + PF_STAGES; ++j)
-      if (!ptx::mbar_wait(bar0 + (j % PF_STAGES) * 8, (uint32_t)(j / PF_STAGES) & 1u,
-                          AT_WAIT_LIMIT_NS))
-        atomicCAS(&g_w8a8_attn_error, 0, 24);
-  }
-  if (!ok) return;
-  const float sv = sv_p[0];
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    float lt = l[hh];
-    lt += __shfl_xor_sync(0xFFFFFFFFu, lt, 1);
-    lt += __shfl_xor_sync(0xFFFFFFFFu, lt, 2);
-    const int tok = r0 + g + 8 * hh;
-    if (tok >= seq) continue;
-    const float f = sv / lt;
-    uint16_t* o = out + (((b * seq + tok) * hq) + h) * (int64_t)AT_D;
-#pragma unroll
-    for (int s2 = 0; s2 < 8; ++s2)
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        // dims 16 s2 + 4 tig + 2 i + {0, 1}
-        const uint32_t v2 = (uint32_t)bf16_rn(acc[s2][0][2 * hh + i] * f) |
-                            ((uint32_t)bf16_rn(acc[s2][1][2 * hh + i] * f) << 16);
-        *reinterpret_cast<uint32_t*>(o + 16 * s2 + 4 * tig + 2 * i) = v2;
+      ptx::fence_proxy_async_smem();  // generic writes -> the MMA's reads
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive(vt_full(s));
+        ptx::mbar_arrive(kv_empty(s));
       }
+    }
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int quarter = warp & 3;
+    const int rrow = quarter * 32 + lane;  // query row in the block (TMEM lane)
+    const int tok = q0 + rrow;
+    const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
+    const float qk = softmax_scale * sq_p[0] * sk_p[0] * 1.4426950408889634f;
+    float o[128];
+#pragma unroll
+    for (int i = 0; i < 128; ++i) o[i] = 0.0f;
+    float m = -INFINITY, l = 0.0f;
+    bool ok = true;
+    // pass 1 of chunk c: the row's new maximum and the correction of what
+    // came before (keys after the query masked)
+    auto pass1 = [&](int c, float& mx, float& cr) {
+      const int s = c & 1;
+      uint32_t okw = lane == 0 ? (pt_wait(s_full(s), (uint32_t)((c >> 1) & 1), abort_flag) ? 1u : 0u) : 0u;
+      okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+      if (!okw) return false;
+      ptx::tc_fence_after();
+      const bool diag = c == qb;
+      const uint32_t ts = tS0 + s * 128 + lanes;
+      mx = m;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t r[32];
+        ptx::tmem_ld_32x32b_x32(ts + 32 * cc, r);
+        ptx::tmem_wait_ld_dep32(r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int key = c * PT_KEYS + 32 * cc + i;
+          const float x = diag && key > tok ? -INFINITY : __uint_as_float(r[i]) * qk;
+          mx = fmaxf(mx, x);
+        }
+      }
+      cr = m == mx ? 1.0f : ex2_approx(m - mx);
+      m = mx;
+      return true;
+    };
+    // Software pipelined: pass 1 of chunk c + 1 runs while the tensor cores
+    // compute PV(c); the correction of O for chunk c is applied with PV(c).
+    float mx_c = 0.0f, cr_c = 0.0f;
+    ok = nch > 0 && pass1(0, mx_c, cr_c);
+    for (int c = 0; c < nch && ok; ++c) {
+      const int s = c & 1;
+      const bool diag = c == qb;
+      const uint32_t ts = tS0 + s * 128 + lanes;
+      // the PV MMA of the previous chunk has read P: overwrite it
+      uint32_t okw = lane == 0 ? (pt_wait(p_empty, (uint32_t)((c & 1) ^ 1), abort_flag) ? 1u : 0u) : 0u;
+      okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+      if (!okw) { ok = false; break; }
+      // pass 2: the weights, as high and low f16 parts, into this row of P
+      float ps = 0.0f;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t r[32];
+        ptx::tmem_ld_32x32b_x32(ts + 32 * cc, r);
+        ptx::tmem_wait_ld_dep32(r);
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {  // 8 keys: one 16-byte chunk of each part
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float pv[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int i = 8 * q8 + 2 * e + u;
+              const int key = c * PT_KEYS + 32 * cc + i;
+              pv[u] = diag && key > tok ? 0.0f
+                                        : ex2_approx(__uint_as_float(r[i]) * qk - mx_c + AT_P_LOG2);
+              ps += pv[u];
+            }
+            hi[e] = pack_f16x2(pv[0], pv[1]);
+            const float2 fh = unpack_f16x2(hi[e]);
+            lo[e] = pack_f16x2(pv[0] - fh.x, pv[1] - fh.y);
+          }
+          const int chunk = 4 * cc + q8;  // 8-key chunk 0..15 of the row
+          const uint32_t off = (uint32_t)(chunk >> 3) * PT_HALF + rrow * 128 +
+                               (((chunk & 7) ^ (rrow & 7)) << 4);
+          ptx::sts128(base + PT_OFF_P + off, hi[0], hi[1], hi[2], hi[3]);
+          ptx::sts128(base + PT_OFF_P + 2 * PT_HALF + off, lo[0], lo[1], lo[2], lo[3]);
+        }
+      }
+      l = __fmaf_rn(l, cr_c, ps);
+      // S(c) read out; P(c) written (generic writes -> the MMA's async reads)
+      ptx::tc_fence_before();
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive(s_empty(s));
+        ptx::mbar_arrive(p_full);
+      }
+      float mx_n = 0.0f, cr_n = 0.0f;
+      if (c + 1 < nch && !pass1(c + 1, mx_n, cr_n)) { ok = false; break; }
+      // O = O * correction + PV(c)
+      okw = lane == 0 ? (pt_wait(pv_full, (uint32_t)(c & 1), abort_flag) ? 1u : 0u) : 0u;
+      okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+      if (!okw) { ok = false; break; }
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t r[32];
+        ptx::tmem_ld_32x32b_x32(tPV + lanes + 32 * cc, r);
+        ptx::tmem_wait_ld_dep32(r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[32 * cc + i] = __fmaf_rn(o[32 * cc + i], cr_c, __uint_as_float(r[i]));
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(pv_empty);
+      mx_c = mx_n;
+      cr_c = cr_n;
+    }
+    if (ok && tok < seq) {
+      const float f = sv_p[0] / l;
+      uint4* dst = reinterpret_cast<uint4*>(out + (((b * seq + tok) * hq) + h) * (int64_t)AT_D);
+#pragma unroll
+      for (int v8 = 0; v8 < 16; ++v8) {
+        uint4 w;
+        w.x = (uint32_t)bf16_rn(o[8 * v8 + 0] * f) | ((uint32_t)bf16_rn(o[8 * v8 + 1] * f) << 16);
+        w.y = (uint32_t)bf16_rn(o[8 * v8 + 2] * f) | ((uint32_t)bf16_rn(o[8 * v8 + 3] * f) << 16);
+        w.z = (uint32_t)bf16_rn(o[8 * v8 + 4] * f) | ((uint32_t)bf16_rn(o[8 * v8 + 5] * f) << 16);
+        w.w = (uint32_t)bf16_rn(o[8 * v8 + 6] * f) | ((uint32_t)bf16_rn(o[8 * v8 + 7] * f) << 16);
+        dst[v8] = w;
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, 512);
   }
 }
 
@@ -794,30 +959,29 @@ cudaError_t launch_prefill_attention(const uint8_t* q, const float* sq, const ui
                                      int64_t batch, int64_t seq, int hq, int hkv,
                                      float softmax_scale, uint16_t* out, cudaStream_t st) {
   if (batch == 0 || seq == 0) return cudaSuccess;
-  const int64_t nqb = (seq + PF_ROWS - 1) / PF_ROWS;
-  // grid y / z limits; TMA row coordinates are 32-bit: the last chunk may
-  // run PF_KEYS rows past batch * seq (those rows read as zero)
+  const int64_t nqb = (seq + PT_ROWS - 1) / PT_ROWS;
   if (hq > 65535 || batch > 65535 || nqb > 0x7FFFFFFFLL ||
-      batch * seq > 0x7FFFFFFFLL - PF_KEYS)
+      batch * seq > 0x7FFFFFFFLL - PT_KEYS)
     return cudaErrorInvalidValue;
-  CUtensorMap tm_k, tm_v;
-  const uint64_t rows = (uint64_t)(batch * seq), cols = (uint64_t)hkv * AT_D;
-  if (!make_tmap_2d(&tm_k, k, 1, rows, cols, PF_KEYS, AT_D, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap_2d(&tm_v, v, 1, rows, cols, PF_KEYS, AT_D, CU_TENSOR_MAP_SWIZZLE_128B))
+  CUtensorMap tm_q, tm_k, tm_v;
+  const uint64_t rows = (uint64_t)(batch * seq);
+  if (!make_tmap_2d(&tm_q, q, 1, rows, (uint64_t)hq * AT_D, PT_ROWS, AT_D, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d(&tm_k, k, 1, rows, (uint64_t)hkv * AT_D, PT_KEYS, AT_D, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d(&tm_v, v, 1, rows, (uint64_t)hkv * AT_D, PT_KEYS, AT_D, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(prefill_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             PF_DYN_SMEM);
+    e = cudaFuncSetAttribute(prefill_attention_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, PT_DYN_SMEM);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
   const dim3 grid((unsigned)nqb, (unsigned)hq, (unsigned)batch);
-  prefill_attention_kernel<<<grid, AT_THREADS, PF_DYN_SMEM, st>>>(
-      tm_k, tm_v, q, sq, sk, sv, (int)seq, hq, hkv, (int)nqb, softmax_scale, out);
+  prefill_attention_kernel<<<grid, PT_THREADS, PT_DYN_SMEM, st>>>(
+      tm_q, tm_k, tm_v, sq, sk, sv, (int)seq, hq, hkv, (int)nqb, softmax_scale, out);
   return cudaGetLastError();
 }
 
