@@ -549,21 +549,24 @@ cudaError_t launch_decode_attention(const uint8_t* q, const float* sq, const uin
 // (sequence, query head); keys come in chunks of 128 tokens, so chunk qb is
 // the diagonal one; query blocks are launched longest (most keys) first.
 //   warp 0     TMA: the Q tile once, then K and V tiles (E4M3, 128-byte
-//              swizzle) into a 2-stage ring;
-//   warp 1     allocates 512 TMEM columns; lane 0 issues S(j) = Q K_j^T on
-//              the raw E4M3 codes (kind::f8f6f4, M = 128 queries, N = 128
-//              keys, f32 accumulation) into one of two S buffers, and
-//              PV(j) = P_j V_j (kind::f16, M = 128 queries, N = 128 dims,
-//              K = 128 keys, the weights' high and low f16 parts in turn)
-//              into the PV buffer;
+//              swizzle) into a 3-stage ring;
+//   warp 1     allocates 512 TMEM columns: two S buffers, two PV buffers.
+//              Lane 0 issues S(j) = Q K_j^T on the raw E4M3 codes
+//              (kind::f8f6f4, M = 128 queries, N = 128 keys, f32
+//              accumulation) into S buffer j % 2, and PV(j) = P_j V_j
+//              (kind::f16, M = 128 queries, N = 128 dims, K = 128 keys, A
+//              read from tensor memory, the weights' high then low f16
+//              parts) into PV buffer j % 2;
 //   warps 2-3  widen each V tile to f16, transposed (V^T [dim][key], the
 //              K-major B operand), exactly;
-//   warps 4-7  one query row per thread: the row of S(j) out of TMEM, its
-//              maximum and weights P = 2^15 p (online softmax in log2 units,
-//              later keys masked in the diagonal chunk) as high and low f16
-//              parts (together 22 bits of each weight) into shared memory
-//              (the A operand), then the row of PV(j):
-//              O = O * correction + PV(j) in FP32 registers.
+//   warps 4-7  one query row per thread: the row's maximum over S(j), then
+//              the weights P = 2^15 p (online softmax in log2 units, later
+//              keys masked in the diagonal chunk) as high and low f16 parts
+//              (together 22 bits of each weight), written over the row of
+//              S(j) in tensor memory, where PV(j) reads them; then, one
+//              chunk behind, O = O * correction + PV(j - 1) in FP32
+//              registers, so that PV(j) runs while the next chunk's
+//              weights are formed.
 // The softmax passes keep their 32-column loops rolled: fully unrolled, the
 // loop body outgrew the instruction cache and the kernel ran ~30% slower.
 // Every mbarrier wait is bounded; a wait that gives up records error 23 and
@@ -573,34 +576,41 @@ constexpr int PT_ROWS = 128;                        // query tokens per CTA
 constexpr int PT_KEYS = 128;                        // keys per chunk
 constexpr int PT_TILE = PT_KEYS * AT_D;             // 16 KB: a Q, K or V tile (E4M3)
 constexpr int PT_HALF = 128 * 128;                  // 16 KB: 128 rows x 64 f16 (128 bytes)
+constexpr int PT_STAGES = 3;                        // K/V ring
 constexpr int PT_OFF_Q = 0;
-constexpr int PT_OFF_KV = PT_OFF_Q + PT_TILE;       // 2 stages of (K, V)
-constexpr int PT_OFF_VT = PT_OFF_KV + 4 * PT_TILE;  // 2 buffers of V^T f16 (2 halves each)
-constexpr int PT_OFF_P = PT_OFF_VT + 4 * PT_HALF;   // P high (2 halves), P low (2 halves)
-constexpr int PT_OFF_BAR = PT_OFF_P + 4 * PT_HALF;
-constexpr int PT_NBAR = 18;
+constexpr int PT_OFF_KV = PT_OFF_Q + PT_TILE;                   // stages of (K, V)
+constexpr int PT_OFF_VT = PT_OFF_KV + 2 * PT_STAGES * PT_TILE;  // 2 buffers of V^T f16 (2 halves each)
+constexpr int PT_OFF_BAR = PT_OFF_VT + 4 * PT_HALF;
+constexpr int PT_NBAR = 2 * PT_STAGES + 14;
 constexpr int PT_OFF_MISC = PT_OFF_BAR + PT_NBAR * 8;
 constexpr int PT_DYN_SMEM = PT_OFF_MISC + 16 + 1024;
 constexpr int PT_THREADS = 256;
 constexpr uint32_t PT_IDESC = ptx::idesc_e4m3_f32(128, 128);  // also kind::f16 with F16 A, B
-static_assert(PT_OFF_KV % 1024 == 0 && PT_OFF_VT % 1024 == 0 && PT_OFF_P % 1024 == 0,
+static_assert(PT_OFF_KV % 1024 == 0 && PT_OFF_VT % 1024 == 0,
               "swizzled tiles start on 1024-byte boundaries");
 static_assert(PT_DYN_SMEM <= 232448, "shared memory");
 
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
+// D (TMEM) (+)= A (TMEM, 128 lanes = rows, two f16 per 32-bit column along
+// K) x B (shared memory descriptor), kind::f16
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// 32 lanes x 4 consecutive 32-bit columns from registers
+__device__ __forceinline__ void tmem_st_x4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2,
+                                           uint32_t v3) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+               "r"(v0), "r"(v1), "r"(v2), "r"(v3)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // bounded mbarrier wait that also gives up once another role has
@@ -619,15 +629,22 @@ __device__ __forceinline__ bool pt_wait(uint32_t bar, uint32_t parity, volatile 
     }
   }
 }
+
+// the same wait taken by lane 0 and broadcast to the warp
+__device__ __forceinline__ bool pt_wait_warp(uint32_t bar, uint32_t parity,
+                                             volatile int* abort_flag, int lane) {
+  uint32_t okw = lane == 0 ? (pt_wait(bar, parity, abort_flag) ? 1u : 0u) : 0u;
+  return __shfl_sync(0xFFFFFFFFu, okw, 0) != 0u;
+}
 }  // namespace
 
 __global__ void __launch_bounds__(PT_THREADS, 1)
     prefill_attention_kernel(const __grid_constant__ CUtensorMap tm_q,
-                                const __grid_constant__ CUtensorMap tm_k,
-                                const __grid_constant__ CUtensorMap tm_v,
-                                const float* __restrict__ sq_p, const float* __restrict__ sk_p,
-                                const float* __restrict__ sv_p, int seq, int hq, int hkv, int nqb,
-                                float softmax_scale, uint16_t* __restrict__ out) {
+                             const __grid_constant__ CUtensorMap tm_k,
+                             const __grid_constant__ CUtensorMap tm_v,
+                             const float* __restrict__ sq_p, const float* __restrict__ sk_p,
+                             const float* __restrict__ sv_p, int seq, int hq, int hkv, int nqb,
+                             float softmax_scale, uint16_t* __restrict__ out) {
   extern __shared__ __align__(16) uint8_t at_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qb = nqb - 1 - (int)blockIdx.x;  // the longest blocks first
@@ -640,35 +657,34 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
   uint8_t* gbase = at_smem + (base - ptx::smem_addr(at_smem));
   const uint32_t bar0 = base + PT_OFF_BAR;
   const uint32_t q_full = bar0;
-  auto kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto kv_empty = [&](int s) { return bar0 + 8u * (3 + s); };   // S MMA commit + 2 converter warps
-  auto s_full = [&](int s) { return bar0 + 8u * (5 + s); };
-  auto s_empty = [&](int s) { return bar0 + 8u * (7 + s); };    // 4 softmax warps
-  auto vt_full = [&](int s) { return bar0 + 8u * (9 + s); };    // 2 converter warps
-  auto vt_empty = [&](int s) { return bar0 + 8u * (11 + s); };  // PV MMA commit
-  const uint32_t p_full = bar0 + 8u * 13;                         // 4 softmax warps
-  const uint32_t p_empty = bar0 + 8u * 14;                        // PV MMA commit
-  const uint32_t pv_full = bar0 + 8u * 15;                        // PV MMA commit
-  const uint32_t pv_empty = bar0 + 8u * 16;                       // 4 softmax warps
-  const uint32_t mma_done = bar0 + 8u * 17;                       // the last MMAs completed
+  auto kv_full = [&](int t) { return bar0 + 8u * (1 + t); };
+  auto kv_empty = [&](int t) { return bar0 + 8u * (1 + PT_STAGES + t); };  // S commit + 2 converter warps
+  const uint32_t bar2 = bar0 + 8u * (1 + 2 * PT_STAGES);  // then pairs, indexed by chunk % 2
+  auto s_full = [&](int s) { return bar2 + 8u * (0 + s); };    // S MMA commit
+  auto p_full = [&](int s) { return bar2 + 8u * (2 + s); };    // 4 softmax warps
+  auto vt_full = [&](int s) { return bar2 + 8u * (4 + s); };   // 2 converter warps
+  auto vt_empty = [&](int s) { return bar2 + 8u * (6 + s); };  // PV MMA commit
+  auto pv_full = [&](int s) { return bar2 + 8u * (8 + s); };   // PV MMA commit
+  auto pv_empty = [&](int s) { return bar2 + 8u * (10 + s); }; // 4 softmax warps
+  const uint32_t mma_done = bar2 + 8u * 12;                     // the last MMAs completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + PT_OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + PT_OFF_MISC + 4);
   const int krow0 = (int)(b * seq);  // cache row of the sequence's token 0 (checked on the host)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
+    for (int t = 0; t < PT_STAGES; ++t) {
+      ptx::mbar_init(kv_full(t), 1);
+      ptx::mbar_init(kv_empty(t), 3);
+    }
     for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(kv_full(s), 1);
-      ptx::mbar_init(kv_empty(s), 3);
       ptx::mbar_init(s_full(s), 1);
-      ptx::mbar_init(s_empty(s), 4);
+      ptx::mbar_init(p_full(s), 4);
       ptx::mbar_init(vt_full(s), 2);
       ptx::mbar_init(vt_empty(s), 1);
+      ptx::mbar_init(pv_full(s), 1);
+      ptx::mbar_init(pv_empty(s), 4);
     }
-    ptx::mbar_init(p_full, 4);
-    ptx::mbar_init(p_empty, 1);
-    ptx::mbar_init(pv_full, 1);
-    ptx::mbar_init(pv_empty, 4);
     ptx::mbar_init(mma_done, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -681,7 +697,8 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const uint32_t tS0 = tmem_base, tPV = tmem_base + 256;
+  auto tS = [&](int s) { return tmem_base + 128u * (uint32_t)s; };         // S(j), then P(j)
+  auto tPV = [&](int s) { return tmem_base + 256u + 128u * (uint32_t)s; };  // PV(j)
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA
@@ -690,21 +707,21 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
       ptx::tma_load_2d(base + PT_OFF_Q, &tm_q, q_full, h * AT_D, krow0 + q0);
       int issued = 0;
       for (int c = 0; c < nch; ++c) {
-        const int s = c & 1;
-        if (!pt_wait(kv_empty(s), (uint32_t)(((c >> 1) & 1) ^ 1), abort_flag)) break;
-        const uint32_t st = base + PT_OFF_KV + s * 2 * PT_TILE;
-        ptx::mbar_arrive_expect_tx(kv_full(s), 2 * PT_TILE);
-        ptx::tma_load_2d(st, &tm_k, kv_full(s), kh * AT_D, krow0 + c * PT_KEYS);
-        ptx::tma_load_2d(st + PT_TILE, &tm_v, kv_full(s), kh * AT_D, krow0 + c * PT_KEYS);
+        const int t = c % PT_STAGES;
+        if (!pt_wait(kv_empty(t), (uint32_t)(((c / PT_STAGES) & 1) ^ 1), abort_flag)) break;
+        const uint32_t st = base + PT_OFF_KV + t * 2 * PT_TILE;
+        ptx::mbar_arrive_expect_tx(kv_full(t), 2 * PT_TILE);
+        ptx::tma_load_2d(st, &tm_k, kv_full(t), kh * AT_D, krow0 + c * PT_KEYS);
+        ptx::tma_load_2d(st + PT_TILE, &tm_v, kv_full(t), kh * AT_D, krow0 + c * PT_KEYS);
         ++issued;
       }
       // no copy may still be landing when the CTA retires
       const uint64_t t0 = ptx::globaltimer();
       while (!ptx::mbar_try_wait(q_full, 0))
         if (ptx::globaltimer() - t0 > AT_WAIT_LIMIT_NS) { atomicCAS(&g_w8a8_attn_error, 0, 23); break; }
-      for (int c = issued > 2 ? issued - 2 : 0; c < issued; ++c) {
+      for (int c = issued > PT_STAGES ? issued - PT_STAGES : 0; c < issued; ++c) {
         const uint64_t t1 = ptx::globaltimer();
-        while (!ptx::mbar_try_wait(kv_full(c & 1), (uint32_t)((c >> 1) & 1)))
+        while (!ptx::mbar_try_wait(kv_full(c % PT_STAGES), (uint32_t)((c / PT_STAGES) & 1)))
           if (ptx::globaltimer() - t1 > AT_WAIT_LIMIT_NS) { atomicCAS(&g_w8a8_attn_error, 0, 23); break; }
       }
     }
@@ -715,27 +732,26 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
       bool ok = pt_wait(q_full, 0, abort_flag);
       const uint64_t qdesc = ptx::smem_desc_kmajor_sw128(base + PT_OFF_Q);
       auto issue_s = [&](int c) {
-        const int s = c & 1;
-        if (!pt_wait(kv_full(s), (uint32_t)((c >> 1) & 1), abort_flag)) return false;
-        if (!pt_wait(s_empty(s), (uint32_t)(((c >> 1) & 1) ^ 1), abort_flag)) return false;
+        const int t = c % PT_STAGES;
+        if (!pt_wait(kv_full(t), (uint32_t)((c / PT_STAGES) & 1), abort_flag)) return false;
         ptx::tc_fence_after();
-        const uint64_t kdesc = ptx::smem_desc_kmajor_sw128(base + PT_OFF_KV + s * 2 * PT_TILE);
+        const uint64_t kdesc = ptx::smem_desc_kmajor_sw128(base + PT_OFF_KV + t * 2 * PT_TILE);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // 32 dims (bytes) per MMA
-          ptx::mma_f8f6f4(tS0 + s * 128, qdesc + 2u * kk, kdesc + 2u * kk, PT_IDESC, kk > 0 ? 1u : 0u);
-        ptx::mma_commit(s_full(s));
-        ptx::mma_commit(kv_empty(s));
+          ptx::mma_f8f6f4(tS(c & 1), qdesc + 2u * kk, kdesc + 2u * kk, PT_IDESC, kk > 0 ? 1u : 0u);
+        ptx::mma_commit(s_full(c & 1));
+        ptx::mma_commit(kv_empty(t));
         return true;
       };
       if (ok) ok = issue_s(0);
+      if (ok && nch > 1) ok = issue_s(1);
       for (int c = 0; c < nch && ok; ++c) {
-        if (c + 1 < nch && !issue_s(c + 1)) { ok = false; break; }
-        // PV(c): the weights of chunk c in shared memory, V_c^T widened,
-        // the PV buffer read out
+        // PV(c): the weights of chunk c in S buffer s, V_c^T widened, PV
+        // buffer s read out (chunk c - 2)
         const int s = c & 1;
-        if (!pt_wait(p_full, (uint32_t)(c & 1), abort_flag) ||
-            !pt_wait(vt_full(s), (uint32_t)((c >> 1) & 1), abort_flag) ||
-            !pt_wait(pv_empty, (uint32_t)((c & 1) ^ 1), abort_flag)) {
+        const uint32_t ph = (uint32_t)((c >> 1) & 1);
+        if (!pt_wait(p_full(s), ph, abort_flag) || !pt_wait(vt_full(s), ph, abort_flag) ||
+            !pt_wait(pv_empty(s), ph ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
@@ -743,18 +759,23 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
         const uint32_t vt = base + PT_OFF_VT + s * 2 * PT_HALF;
 #pragma unroll
         for (int part = 0; part < 2; ++part) {  // the weights' high, then low f16 parts
-          const uint32_t pa = base + PT_OFF_P + part * 2 * PT_HALF;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {  // 16 keys (32 bytes) per MMA
-            const uint32_t hoff = (uint32_t)(kk >> 2) * PT_HALF;
-            const uint64_t adesc = ptx::smem_desc_kmajor_sw128(pa + hoff) + 2u * (kk & 3);
-            const uint64_t bdesc = ptx::smem_desc_kmajor_sw128(vt + hoff) + 2u * (kk & 3);
-            mma_f16(tPV, adesc, bdesc, PT_IDESC, (part | kk) ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk) {  // 16 keys per MMA: 8 columns of P
+            const uint32_t a = tS(s) + 32u * (uint32_t)(kk >> 1) + 16u * (uint32_t)part +
+                               8u * (uint32_t)(kk & 1);
+            const uint64_t bdesc = ptx::smem_desc_kmajor_sw128(vt + (uint32_t)(kk >> 2) * PT_HALF) +
+                                   2u * (kk & 3);
+            mma_f16_tmem_a(tPV(s), a, bdesc, PT_IDESC, (part | kk) ? 1u : 0u);
           }
         }
-        ptx::mma_commit(pv_full);
-        ptx::mma_commit(p_empty);
+        ptx::mma_commit(pv_full(s));
         ptx::mma_commit(vt_empty(s));
+        if (c + 2 < nch) {
+          // S(c + 2) goes where P(c) is: after PV(c) has completed
+          if (!pt_wait(pv_full(s), ph, abort_flag)) { ok = false; break; }
+          ptx::tc_fence_after();
+          ok = issue_s(c + 2);
+        }
       }
       // every MMA issued has completed before the CTA frees TMEM
       ptx::mma_commit(mma_done);
@@ -774,11 +795,11 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
     const int wv = warp - 2;
     const int ko = (lane & 7) + 8 * wv;
     for (int c = 0; c < nch; ++c) {
-      const int s = c & 1;
-      bool okl = pt_wait(kv_full(s), (uint32_t)((c >> 1) & 1), abort_flag) &&
+      const int t = c % PT_STAGES, s = c & 1;
+      bool okl = pt_wait(kv_full(t), (uint32_t)((c / PT_STAGES) & 1), abort_flag) &&
                  pt_wait(vt_empty(s), (uint32_t)(((c >> 1) & 1) ^ 1), abort_flag);
       if (!__all_sync(0xFFFFFFFFu, okl)) break;
-      const uint32_t vsrc = base + PT_OFF_KV + s * 2 * PT_TILE + PT_TILE;
+      const uint32_t vsrc = base + PT_OFF_KV + t * 2 * PT_TILE + PT_TILE;
       const uint32_t vt = base + PT_OFF_VT + s * 2 * PT_HALF + (uint32_t)wv * PT_HALF;
 #pragma unroll 1
       for (int i = 0; i < 2; ++i) {
@@ -816,7 +837,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
       __syncwarp();
       if (lane == 0) {
         ptx::mbar_arrive(vt_full(s));
-        ptx::mbar_arrive(kv_empty(s));
+        ptx::mbar_arrive(kv_empty(t));
       }
     }
   } else {
@@ -830,17 +851,13 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
 #pragma unroll
     for (int i = 0; i < 128; ++i) o[i] = 0.0f;
     float m = -INFINITY, l = 0.0f;
-    bool ok = true;
     // pass 1 of chunk c: the row's new maximum and the correction of what
     // came before (keys after the query masked)
     auto pass1 = [&](int c, float& mx, float& cr) {
-      const int s = c & 1;
-      uint32_t okw = lane == 0 ? (pt_wait(s_full(s), (uint32_t)((c >> 1) & 1), abort_flag) ? 1u : 0u) : 0u;
-      okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
-      if (!okw) return false;
+      if (!pt_wait_warp(s_full(c & 1), (uint32_t)((c >> 1) & 1), abort_flag, lane)) return false;
       ptx::tc_fence_after();
       const bool diag = c == qb;
-      const uint32_t ts = tS0 + s * 128 + lanes;
+      const uint32_t ts = tS(c & 1) + lanes;
       mx = m;
 #pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
@@ -858,19 +875,31 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
       m = mx;
       return true;
     };
-    // Software pipelined: pass 1 of chunk c + 1 runs while the tensor cores
-    // compute PV(c); the correction of O for chunk c is applied with PV(c).
-    float mx_c = 0.0f, cr_c = 0.0f;
-    ok = nch > 0 && pass1(0, mx_c, cr_c);
+    // O = O * cr + PV(c), then PV buffer c % 2 is free again
+    auto o_update = [&](int c, float cr) {
+      if (!pt_wait_warp(pv_full(c & 1), (uint32_t)((c >> 1) & 1), abort_flag, lane)) return false;
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t r[32];
+        ptx::tmem_ld_32x32b_x32(tPV(c & 1) + lanes + 32 * cc, r);
+        ptx::tmem_wait_ld_dep32(r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[32 * cc + i] = __fmaf_rn(o[32 * cc + i], cr, __uint_as_float(r[i]));
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(pv_empty(c & 1));
+      return true;
+    };
+    float mx_c = 0.0f, cr_c = 0.0f, cr_lag = 0.0f;
+    bool ok = nch > 0 && pass1(0, mx_c, cr_c);
     for (int c = 0; c < nch && ok; ++c) {
-      const int s = c & 1;
       const bool diag = c == qb;
-      const uint32_t ts = tS0 + s * 128 + lanes;
-      // the PV MMA of the previous chunk has read P: overwrite it
-      uint32_t okw = lane == 0 ? (pt_wait(p_empty, (uint32_t)((c & 1) ^ 1), abort_flag) ? 1u : 0u) : 0u;
-      okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
-      if (!okw) { ok = false; break; }
-      // pass 2: the weights, as high and low f16 parts, into this row of P
+      const uint32_t ts = tS(c & 1) + lanes;
+      // pass 2: the weights, as high and low f16 parts, over the row of S(c):
+      // columns 32 cc .. 32 cc + 15 the high parts of keys 32 cc .. 32 cc + 31
+      // (two per column), 32 cc + 16 .. 32 cc + 31 the low parts
       float ps = 0.0f;
 #pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
@@ -878,7 +907,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
         ptx::tmem_ld_32x32b_x32(ts + 32 * cc, r);
         ptx::tmem_wait_ld_dep32(r);
 #pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8) {  // 8 keys: one 16-byte chunk of each part
+        for (int q8 = 0; q8 < 4; ++q8) {  // 8 keys: 4 columns of each part
           uint32_t hi[4], lo[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -895,43 +924,21 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
             const float2 fh = unpack_f16x2(hi[e]);
             lo[e] = pack_f16x2(pv[0] - fh.x, pv[1] - fh.y);
           }
-          const int chunk = 4 * cc + q8;  // 8-key chunk 0..15 of the row
-          const uint32_t off = (uint32_t)(chunk >> 3) * PT_HALF + rrow * 128 +
-                               (((chunk & 7) ^ (rrow & 7)) << 4);
-          ptx::sts128(base + PT_OFF_P + off, hi[0], hi[1], hi[2], hi[3]);
-          ptx::sts128(base + PT_OFF_P + 2 * PT_HALF + off, lo[0], lo[1], lo[2], lo[3]);
+          tmem_st_x4(ts + 32 * cc + 4 * q8, hi[0], hi[1], hi[2], hi[3]);
+          tmem_st_x4(ts + 32 * cc + 16 + 4 * q8, lo[0], lo[1], lo[2], lo[3]);
         }
       }
       l = __fmaf_rn(l, cr_c, ps);
-      // S(c) read out; P(c) written (generic writes -> the MMA's async reads)
-      ptx::tc_fence_before();
-      ptx::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        ptx::mbar_arrive(s_empty(s));
-        ptx::mbar_arrive(p_full);
-      }
-      float mx_n = 0.0f, cr_n = 0.0f;
-      if (c + 1 < nch && !pass1(c + 1, mx_n, cr_n)) { ok = false; break; }
-      // O = O * correction + PV(c)
-      okw = lane == 0 ? (pt_wait(pv_full, (uint32_t)(c & 1), abort_flag) ? 1u : 0u) : 0u;
-      okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
-      if (!okw) { ok = false; break; }
-      ptx::tc_fence_after();
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t r[32];
-        ptx::tmem_ld_32x32b_x32(tPV + lanes + 32 * cc, r);
-        ptx::tmem_wait_ld_dep32(r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[32 * cc + i] = __fmaf_rn(o[32 * cc + i], cr_c, __uint_as_float(r[i]));
-      }
+      tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(pv_empty);
-      mx_c = mx_n;
-      cr_c = cr_n;
+      if (lane == 0) ptx::mbar_arrive(p_full(c & 1));
+      // one chunk behind: O += PV(c - 1) while the tensor cores compute PV(c)
+      if (c > 0 && !o_update(c - 1, cr_lag)) { ok = false; break; }
+      cr_lag = cr_c;
+      if (c + 1 < nch && !pass1(c + 1, mx_c, cr_c)) { ok = false; break; }
     }
+    if (ok) ok = o_update(nch - 1, cr_lag);
     if (ok && tok < seq) {
       const float f = sv_p[0] / l;
       uint4* dst = reinterpret_cast<uint4*>(out + (((b * seq + tok) * hq) + h) * (int64_t)AT_D);
