@@ -36,6 +36,8 @@
 // shared memory), are merged at the end.
 #include <math.h>
 
+#include <type_traits>
+
 #include <cuda.h>
 
 #include "common.cuh"
@@ -856,21 +858,26 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
     auto pass1 = [&](int c, float& mx, float& cr) {
       if (!pt_wait_warp(s_full(c & 1), (uint32_t)((c >> 1) & 1), abort_flag, lane)) return false;
       ptx::tc_fence_after();
-      const bool diag = c == qb;
       const uint32_t ts = tS(c & 1) + lanes;
-      mx = m;
+      // four running maxima (independent chains); the diagonal chunk's
+      // keys after the query are left out
+      const int lim = c == qb ? tok - c * PT_KEYS : PT_KEYS;
+      float mq[4] = {m, m, m, m};
 #pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t r[32];
         ptx::tmem_ld_32x32b_x32(ts + 32 * cc, r);
         ptx::tmem_wait_ld_dep32(r);
+        if (!__any_sync(0xFFFFFFFFu, lim < 32 * cc + 31)) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int key = c * PT_KEYS + 32 * cc + i;
-          const float x = diag && key > tok ? -INFINITY : __uint_as_float(r[i]) * qk;
-          mx = fmaxf(mx, x);
+          for (int i = 0; i < 32; ++i) mq[i & 3] = fmaxf(mq[i & 3], __uint_as_float(r[i]) * qk);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (32 * cc + i <= lim) mq[i & 3] = fmaxf(mq[i & 3], __uint_as_float(r[i]) * qk);
         }
       }
+      mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
       cr = m == mx ? 1.0f : ex2_approx(m - mx);
       m = mx;
       return true;
@@ -894,40 +901,49 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
     };
     float mx_c = 0.0f, cr_c = 0.0f, cr_lag = 0.0f;
     bool ok = nch > 0 && pass1(0, mx_c, cr_c);
+    // the weights of 32 keys (one 32-column block of S) as high and low f16
+    // parts over the block: columns 0 .. 15 the high parts (two keys per
+    // column), 16 .. 31 the low parts; keys past lim weigh 0
+    auto weights = [&](uint32_t taddr, const uint32_t (&r)[32], float mxc, int lim,
+                       float (&psq)[4], auto masked) {
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) {  // 8 keys: 4 columns of each part
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float pv[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int i = 8 * q8 + 2 * e + u;
+            pv[u] = ex2_approx(__uint_as_float(r[i]) * qk - mxc + AT_P_LOG2);
+            if (decltype(masked)::value && i > lim) pv[u] = 0.0f;
+            psq[e] += pv[u];
+          }
+          hi[e] = pack_f16x2(pv[0], pv[1]);
+          const float2 fh = unpack_f16x2(hi[e]);
+          lo[e] = pack_f16x2(pv[0] - fh.x, pv[1] - fh.y);
+        }
+        tmem_st_x4(taddr + 4 * q8, hi[0], hi[1], hi[2], hi[3]);
+        tmem_st_x4(taddr + 16 + 4 * q8, lo[0], lo[1], lo[2], lo[3]);
+      }
+    };
     for (int c = 0; c < nch && ok; ++c) {
-      const bool diag = c == qb;
       const uint32_t ts = tS(c & 1) + lanes;
-      // pass 2: the weights, as high and low f16 parts, over the row of S(c):
-      // columns 32 cc .. 32 cc + 15 the high parts of keys 32 cc .. 32 cc + 31
-      // (two per column), 32 cc + 16 .. 32 cc + 31 the low parts
-      float ps = 0.0f;
+      const int lim = c == qb ? tok - c * PT_KEYS : PT_KEYS;
+      // pass 2: the weights over the row of S(c), four partial sums
+      float psq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t r[32];
         ptx::tmem_ld_32x32b_x32(ts + 32 * cc, r);
         ptx::tmem_wait_ld_dep32(r);
-#pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8) {  // 8 keys: 4 columns of each part
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float pv[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int i = 8 * q8 + 2 * e + u;
-              const int key = c * PT_KEYS + 32 * cc + i;
-              pv[u] = diag && key > tok ? 0.0f
-                                        : ex2_approx(__uint_as_float(r[i]) * qk - mx_c + AT_P_LOG2);
-              ps += pv[u];
-            }
-            hi[e] = pack_f16x2(pv[0], pv[1]);
-            const float2 fh = unpack_f16x2(hi[e]);
-            lo[e] = pack_f16x2(pv[0] - fh.x, pv[1] - fh.y);
-          }
-          tmem_st_x4(ts + 32 * cc + 4 * q8, hi[0], hi[1], hi[2], hi[3]);
-          tmem_st_x4(ts + 32 * cc + 16 + 4 * q8, lo[0], lo[1], lo[2], lo[3]);
-        }
+        // tcgen05.st is warp-collective: the choice of path is the warp's
+        if (!__any_sync(0xFFFFFFFFu, lim < 32 * cc + 31))
+          weights(ts + 32 * cc, r, mx_c, 0, psq, std::false_type{});
+        else
+          weights(ts + 32 * cc, r, mx_c, lim - 32 * cc, psq, std::true_type{});
       }
+      const float ps = (psq[0] + psq[1]) + (psq[2] + psq[3]);
       l = __fmaf_rn(l, cr_c, ps);
       tmem_wait_st();
       ptx::tc_fence_before();
