@@ -346,12 +346,12 @@ w8a8_status fp8_decode_attention(const uint8_t *q, const float *q_scale,
  * Rules: head_dim == 128 (else W8A8_ERR_UNSUPPORTED); num_q_heads and
  * batch at most 65535, seq and batch * seq below 2^31 - 128 (grid and TMA
  * coordinate limits; over-size inputs give W8A8_ERR_UNSUPPORTED); q, k, v
- * and out_bf16 16-byte aligned, the scales 4-byte aligned.  A CTA takes 128
- * query tokens of one (sequence, query head) and streams the keys and
- * values up to them in chunks of 128 tokens (TMA tiles); both products run
- * on the tcgen05 tensor cores with the accumulators in tensor memory (E4M3
- * for Q K^T, f16 for P V).  A bounded wait that gives up records device
- * error 23.
+ * and out_bf16 16-byte aligned, the scales 4-byte aligned.  One persistent
+ * CTA per SM takes blocks of 128 query tokens of one (sequence, query head)
+ * in turn and streams the keys and values up to each block in chunks of
+ * 128 tokens (TMA tiles); both products run on the tcgen05 tensor cores
+ * with the accumulators in tensor memory (E4M3 for Q K^T, f16 for P V).  A
+ * bounded wait that gives up records device error 23.
  * ---------------------------------------------------------------------- */
 w8a8_status fp8_prefill_attention(const uint8_t *q, const float *q_scale,
                                   const uint8_t *k, const float *k_scale,

@@ -547,9 +547,10 @@ cudaError_t launch_decode_attention(const uint8_t* q, const float* sq, const uin
 // layout), out [batch, seq, hq, 128] BF16.
 //
 // Both contractions run on the 5th-generation tensor cores with the
-// accumulators in tensor memory.  A CTA takes 128 query tokens of one
-// (sequence, query head); keys come in chunks of 128 tokens, so chunk qb is
-// the diagonal one; query blocks are launched longest (most keys) first.
+// accumulators in tensor memory.  A query block is 128 query tokens of one
+// (sequence, query head); keys come in chunks of 128 tokens, so chunk qb of
+// block qb is the diagonal one.  The kernel is persistent: one CTA per SM
+// takes its share of the blocks in turn, longest (most keys) first.
 //   warp 0     TMA: the Q tile once, then K and V tiles (E4M3, 128-byte
 //              swizzle) into a 3-stage ring;
 //   warp 1     allocates 512 TMEM columns: two S buffers, two PV buffers.
@@ -583,7 +584,7 @@ constexpr int PT_OFF_Q = 0;
 constexpr int PT_OFF_KV = PT_OFF_Q + PT_TILE;                   // stages of (K, V)
 constexpr int PT_OFF_VT = PT_OFF_KV + 2 * PT_STAGES * PT_TILE;  // 2 buffers of V^T f16 (2 halves each)
 constexpr int PT_OFF_BAR = PT_OFF_VT + 4 * PT_HALF;
-constexpr int PT_NBAR = 2 * PT_STAGES + 14;
+constexpr int PT_NBAR = 2 * PT_STAGES + 15;
 constexpr int PT_OFF_MISC = PT_OFF_BAR + PT_NBAR * 8;
 constexpr int PT_DYN_SMEM = PT_OFF_MISC + 16 + 1024;
 constexpr int PT_THREADS = 256;
@@ -640,21 +641,37 @@ __device__ __forceinline__ bool pt_wait_warp(uint32_t bar, uint32_t parity,
 }
 }  // namespace
 
+// The k-th query block of CTA x (of G): blocks are numbered longest first
+// (then sequence, then query head, so the query heads of one KV head are
+// neighbours), dealt in rounds of G, every other round in reverse order so
+// that the CTAs' totals even out.
+struct PtBlock {
+  int qb, h, b;
+};
+__device__ __forceinline__ bool pt_block(int k, int x, int G, int64_t total, int nqb, int hq,
+                                         int batch, PtBlock& blk) {
+  const int64_t u = (int64_t)k * G + ((k & 1) ? G - 1 - x : x);
+  if (u >= total) return false;
+  const int64_t per = (int64_t)hq * batch;
+  blk.qb = nqb - 1 - (int)(u / per);
+  const int64_t rem = u % per;
+  blk.h = (int)(rem % hq);
+  blk.b = (int)(rem / hq);
+  return true;
+}
+
 __global__ void __launch_bounds__(PT_THREADS, 1)
     prefill_attention_kernel(const __grid_constant__ CUtensorMap tm_q,
                              const __grid_constant__ CUtensorMap tm_k,
                              const __grid_constant__ CUtensorMap tm_v,
                              const float* __restrict__ sq_p, const float* __restrict__ sk_p,
                              const float* __restrict__ sv_p, int seq, int hq, int hkv, int nqb,
-                             float softmax_scale, uint16_t* __restrict__ out) {
+                             int batch, float softmax_scale, uint16_t* __restrict__ out) {
   extern __shared__ __align__(16) uint8_t at_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qb = nqb - 1 - (int)blockIdx.x;  // the longest blocks first
-  const int h = (int)blockIdx.y;
-  const int64_t b = blockIdx.z;
-  const int kh = h / (hq / hkv);
-  const int q0 = qb * PT_ROWS;
-  const int nch = qb + 1;  // key chunks 0 .. qb; chunk qb is the diagonal
+  const int G = (int)gridDim.x, x = (int)blockIdx.x;
+  const int64_t total = (int64_t)nqb * hq * batch;
+  const int group = hq / hkv;
   const uint32_t base = (ptx::smem_addr(at_smem) + 1023u) & ~1023u;
   uint8_t* gbase = at_smem + (base - ptx::smem_addr(at_smem));
   const uint32_t bar0 = base + PT_OFF_BAR;
@@ -669,12 +686,16 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
   auto pv_full = [&](int s) { return bar2 + 8u * (8 + s); };   // PV MMA commit
   auto pv_empty = [&](int s) { return bar2 + 8u * (10 + s); }; // 4 softmax warps
   const uint32_t mma_done = bar2 + 8u * 12;                     // the last MMAs completed
+  const uint32_t q_empty = bar2 + 8u * 13;                      // a block's last S MMA completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + PT_OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + PT_OFF_MISC + 4);
-  const int krow0 = (int)(b * seq);  // cache row of the sequence's token 0 (checked on the host)
+  auto next_block = [&](int k, PtBlock& blk) {
+    return pt_block(k, x, G, total, nqb, hq, batch, blk);
+  };
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
+    ptx::mbar_init(q_empty, 1);
     for (int t = 0; t < PT_STAGES; ++t) {
       ptx::mbar_init(kv_full(t), 1);
       ptx::mbar_init(kv_empty(t), 3);
@@ -702,28 +723,44 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
   auto tS = [&](int s) { return tmem_base + 128u * (uint32_t)s; };         // S(j), then P(j)
   auto tPV = [&](int s) { return tmem_base + 256u + 128u * (uint32_t)s; };  // PV(j)
 
+  // Chunks are counted over all of the CTA's blocks (g): the rings, the
+  // TMEM buffers and their barriers' phases follow g, so one block's first
+  // loads and MMAs overlap the previous block's last steps.
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA
     if (lane == 0) {
-      ptx::mbar_arrive_expect_tx(q_full, PT_TILE);
-      ptx::tma_load_2d(base + PT_OFF_Q, &tm_q, q_full, h * AT_D, krow0 + q0);
-      int issued = 0;
-      for (int c = 0; c < nch; ++c) {
-        const int t = c % PT_STAGES;
-        if (!pt_wait(kv_empty(t), (uint32_t)(((c / PT_STAGES) & 1) ^ 1), abort_flag)) break;
-        const uint32_t st = base + PT_OFF_KV + t * 2 * PT_TILE;
-        ptx::mbar_arrive_expect_tx(kv_full(t), 2 * PT_TILE);
-        ptx::tma_load_2d(st, &tm_k, kv_full(t), kh * AT_D, krow0 + c * PT_KEYS);
-        ptx::tma_load_2d(st + PT_TILE, &tm_v, kv_full(t), kh * AT_D, krow0 + c * PT_KEYS);
-        ++issued;
+      int g = 0, nblk = 0;
+      bool ok = true;
+      PtBlock blk;
+      for (int k = 0; ok && next_block(k, blk); ++k) {
+        const int krow0 = blk.b * seq;  // cache row of the sequence's token 0 (checked on the host)
+        const int kh = blk.h / group;
+        for (int c = 0; c <= blk.qb; ++c) {
+          const int t = g % PT_STAGES;
+          if (!pt_wait(kv_empty(t), (uint32_t)(((g / PT_STAGES) & 1) ^ 1), abort_flag)) { ok = false; break; }
+          const uint32_t st = base + PT_OFF_KV + t * 2 * PT_TILE;
+          ptx::mbar_arrive_expect_tx(kv_full(t), 2 * PT_TILE);
+          ptx::tma_load_2d(st, &tm_k, kv_full(t), kh * AT_D, krow0 + c * PT_KEYS);
+          ptx::tma_load_2d(st + PT_TILE, &tm_v, kv_full(t), kh * AT_D, krow0 + c * PT_KEYS);
+          ++g;
+          if (c == 0) {
+            // Q of this block, once the previous block's S MMAs are done with the tile
+            if (!pt_wait(q_empty, (uint32_t)((k & 1) ^ 1), abort_flag)) { ok = false; break; }
+            ptx::mbar_arrive_expect_tx(q_full, PT_TILE);
+            ptx::tma_load_2d(base + PT_OFF_Q, &tm_q, q_full, blk.h * AT_D, krow0 + blk.qb * PT_ROWS);
+            ++nblk;
+          }
+        }
       }
       // no copy may still be landing when the CTA retires
-      const uint64_t t0 = ptx::globaltimer();
-      while (!ptx::mbar_try_wait(q_full, 0))
-        if (ptx::globaltimer() - t0 > AT_WAIT_LIMIT_NS) { atomicCAS(&g_w8a8_attn_error, 0, 23); break; }
-      for (int c = issued > PT_STAGES ? issued - PT_STAGES : 0; c < issued; ++c) {
+      if (nblk > 0) {
+        const uint64_t t0 = ptx::globaltimer();
+        while (!ptx::mbar_try_wait(q_full, (uint32_t)((nblk - 1) & 1)))
+          if (ptx::globaltimer() - t0 > AT_WAIT_LIMIT_NS) { atomicCAS(&g_w8a8_attn_error, 0, 23); break; }
+      }
+      for (int j = g > PT_STAGES ? g - PT_STAGES : 0; j < g; ++j) {
         const uint64_t t1 = ptx::globaltimer();
-        while (!ptx::mbar_try_wait(kv_full(c % PT_STAGES), (uint32_t)((c / PT_STAGES) & 1)))
+        while (!ptx::mbar_try_wait(kv_full(j % PT_STAGES), (uint32_t)((j / PT_STAGES) & 1)))
           if (ptx::globaltimer() - t1 > AT_WAIT_LIMIT_NS) { atomicCAS(&g_w8a8_attn_error, 0, 23); break; }
       }
     }
@@ -731,27 +768,42 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA
     if (lane == 0) {
-      bool ok = pt_wait(q_full, 0, abort_flag);
+      bool ok = true;
       const uint64_t qdesc = ptx::smem_desc_kmajor_sw128(base + PT_OFF_Q);
-      auto issue_s = [&](int c) {
-        const int t = c % PT_STAGES;
-        if (!pt_wait(kv_full(t), (uint32_t)((c / PT_STAGES) & 1), abort_flag)) return false;
+      // S cursor: block ks, its chunk cs, overall chunk gs
+      int ks = 0, cs = 0, gs = 0;
+      PtBlock bs;
+      bool s_more = next_block(0, bs);
+      auto issue_s = [&]() {
+        if (cs == 0 && !pt_wait(q_full, (uint32_t)(ks & 1), abort_flag)) return false;
+        const int t = gs % PT_STAGES;
+        if (!pt_wait(kv_full(t), (uint32_t)((gs / PT_STAGES) & 1), abort_flag)) return false;
         ptx::tc_fence_after();
         const uint64_t kdesc = ptx::smem_desc_kmajor_sw128(base + PT_OFF_KV + t * 2 * PT_TILE);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // 32 dims (bytes) per MMA
-          ptx::mma_f8f6f4(tS(c & 1), qdesc + 2u * kk, kdesc + 2u * kk, PT_IDESC, kk > 0 ? 1u : 0u);
-        ptx::mma_commit(s_full(c & 1));
+          ptx::mma_f8f6f4(tS(gs & 1), qdesc + 2u * kk, kdesc + 2u * kk, PT_IDESC, kk > 0 ? 1u : 0u);
+        ptx::mma_commit(s_full(gs & 1));
         ptx::mma_commit(kv_empty(t));
+        ++gs;
+        if (++cs > bs.qb) {  // the block's last S: its Q tile may be replaced once it completes
+          ptx::mma_commit(q_empty);
+          cs = 0;
+          s_more = next_block(++ks, bs);
+        }
         return true;
       };
-      if (ok) ok = issue_s(0);
-      if (ok && nch > 1) ok = issue_s(1);
-      for (int c = 0; c < nch && ok; ++c) {
-        // PV(c): the weights of chunk c in S buffer s, V_c^T widened, PV
-        // buffer s read out (chunk c - 2)
-        const int s = c & 1;
-        const uint32_t ph = (uint32_t)((c >> 1) & 1);
+      // PV cursor: block kp, its chunk cp, overall chunk gp (two behind S)
+      int kp = 0, cp = 0, gp = 0;
+      PtBlock bp;
+      bool p_more = next_block(0, bp);
+      if (s_more) ok = issue_s();
+      if (ok && s_more) ok = issue_s();
+      while (ok && p_more) {
+        // PV(gp): the weights of chunk gp in S buffer s, V^T widened, PV
+        // buffer s read out (chunk gp - 2)
+        const int s = gp & 1;
+        const uint32_t ph = (uint32_t)((gp >> 1) & 1);
         if (!pt_wait(p_full(s), ph, abort_flag) || !pt_wait(vt_full(s), ph, abort_flag) ||
             !pt_wait(pv_empty(s), ph ^ 1u, abort_flag)) {
           ok = false;
@@ -772,11 +824,16 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
         }
         ptx::mma_commit(pv_full(s));
         ptx::mma_commit(vt_empty(s));
-        if (c + 2 < nch) {
-          // S(c + 2) goes where P(c) is: after PV(c) has completed
+        if (s_more) {
+          // S(gp + 2) goes where P(gp) is: after PV(gp) has completed
           if (!pt_wait(pv_full(s), ph, abort_flag)) { ok = false; break; }
           ptx::tc_fence_after();
-          ok = issue_s(c + 2);
+          ok = issue_s();
+        }
+        ++gp;
+        if (++cp > bp.qb) {
+          cp = 0;
+          p_more = next_block(++kp, bp);
         }
       }
       // every MMA issued has completed before the CTA frees TMEM
@@ -796,71 +853,74 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
     // the stores of a warp fill whole 128-byte lines, the loads two-way.
     const int wv = warp - 2;
     const int ko = (lane & 7) + 8 * wv;
-    for (int c = 0; c < nch; ++c) {
-      const int t = c % PT_STAGES, s = c & 1;
-      bool okl = pt_wait(kv_full(t), (uint32_t)((c / PT_STAGES) & 1), abort_flag) &&
-                 pt_wait(vt_empty(s), (uint32_t)(((c >> 1) & 1) ^ 1), abort_flag);
-      if (!__all_sync(0xFFFFFFFFu, okl)) break;
-      const uint32_t vsrc = base + PT_OFF_KV + t * 2 * PT_TILE + PT_TILE;
-      const uint32_t vt = base + PT_OFF_VT + s * 2 * PT_HALF + (uint32_t)wv * PT_HALF;
+    int g = 0;
+    bool okc = true;
+    PtBlock blk;
+    for (int k = 0; okc && next_block(k, blk); ++k) {
+      for (int c = 0; c <= blk.qb; ++c, ++g) {
+        const int t = g % PT_STAGES, s = g & 1;
+        bool okl = pt_wait(kv_full(t), (uint32_t)((g / PT_STAGES) & 1), abort_flag) &&
+                   pt_wait(vt_empty(s), (uint32_t)(((g >> 1) & 1) ^ 1), abort_flag);
+        if (!__all_sync(0xFFFFFFFFu, okl)) { okc = false; break; }
+        const uint32_t vsrc = base + PT_OFF_KV + t * 2 * PT_TILE + PT_TILE;
+        const uint32_t vt = base + PT_OFF_VT + s * 2 * PT_HALF + (uint32_t)wv * PT_HALF;
 #pragma unroll 1
-      for (int i = 0; i < 2; ++i) {
-        const int g = (lane >> 3) + 4 * i;  // dims 16 g .. 16 g + 15
-        uint4 w[8];
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          w[kk] = ptx::lds128(vsrc + (8 * ko + kk) * 128 + ((g ^ kk) << 4));
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t x[8];
+        for (int i = 0; i < 2; ++i) {
+          const int gq = (lane >> 3) + 4 * i;  // dims 16 gq .. 16 gq + 15
+          uint4 w[8];
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            x[kk] = j == 0 ? w[kk].x : j == 1 ? w[kk].y : j == 2 ? w[kk].z : w[kk].w;
+            w[kk] = ptx::lds128(vsrc + (8 * ko + kk) * 128 + ((gq ^ kk) << 4));
 #pragma unroll
-          for (int dd = 0; dd < 4; ++dd) {
-            // dim 16 g + 4 j + dd of keys 8 ko .. 8 ko + 7: byte dd of each
-            // word (low two bytes: byte dd of the first word, then of the second)
-            const uint32_t sel = (uint32_t)dd | ((uint32_t)(dd + 4) << 4);
-            const uint32_t k01 = __byte_perm(x[0], x[1], sel);
-            const uint32_t k23 = __byte_perm(x[2], x[3], sel);
-            const uint32_t k45 = __byte_perm(x[4], x[5], sel);
-            const uint32_t k67 = __byte_perm(x[6], x[7], sel);
-            const uint32_t k0123 = __byte_perm(k01, k23, 0x5410u);
-            const uint32_t k4567 = __byte_perm(k45, k67, 0x5410u);
-            uint32_t f[4];
-            e4m3x4_f16x2x2(k0123, f[0], f[1]);
-            e4m3x4_f16x2x2(k4567, f[2], f[3]);
-            const int d = 16 * g + 4 * j + dd;
-            ptx::sts128(vt + d * 128 + ((((ko & 7) ^ (d & 7))) << 4), f[0], f[1], f[2], f[3]);
+          for (int j = 0; j < 4; ++j) {
+            uint32_t xw[8];
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              xw[kk] = j == 0 ? w[kk].x : j == 1 ? w[kk].y : j == 2 ? w[kk].z : w[kk].w;
+#pragma unroll
+            for (int dd = 0; dd < 4; ++dd) {
+              // dim 16 gq + 4 j + dd of keys 8 ko .. 8 ko + 7: byte dd of each
+              // word (low two bytes: byte dd of the first word, then of the second)
+              const uint32_t sel = (uint32_t)dd | ((uint32_t)(dd + 4) << 4);
+              const uint32_t k01 = __byte_perm(xw[0], xw[1], sel);
+              const uint32_t k23 = __byte_perm(xw[2], xw[3], sel);
+              const uint32_t k45 = __byte_perm(xw[4], xw[5], sel);
+              const uint32_t k67 = __byte_perm(xw[6], xw[7], sel);
+              const uint32_t k0123 = __byte_perm(k01, k23, 0x5410u);
+              const uint32_t k4567 = __byte_perm(k45, k67, 0x5410u);
+              uint32_t f[4];
+              e4m3x4_f16x2x2(k0123, f[0], f[1]);
+              e4m3x4_f16x2x2(k4567, f[2], f[3]);
+              const int d = 16 * gq + 4 * j + dd;
+              ptx::sts128(vt + d * 128 + ((((ko & 7) ^ (d & 7))) << 4), f[0], f[1], f[2], f[3]);
+            }
           }
         }
-      }
-      ptx::fence_proxy_async_smem();  // generic writes -> the MMA's reads
-      __syncwarp();
-      if (lane == 0) {
-        ptx::mbar_arrive(vt_full(s));
-        ptx::mbar_arrive(kv_empty(t));
+        ptx::fence_proxy_async_smem();  // generic writes -> the MMA's reads
+        __syncwarp();
+        if (lane == 0) {
+          ptx::mbar_arrive(vt_full(s));
+          ptx::mbar_arrive(kv_empty(t));
+        }
       }
     }
   } else {
     // ------------------------------------------------------------- softmax
     const int quarter = warp & 3;
     const int rrow = quarter * 32 + lane;  // query row in the block (TMEM lane)
-    const int tok = q0 + rrow;
     const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
     const float qk = softmax_scale * sq_p[0] * sk_p[0] * 1.4426950408889634f;
+    const float fv = sv_p[0];
     float o[128];
-#pragma unroll
-    for (int i = 0; i < 128; ++i) o[i] = 0.0f;
-    float m = -INFINITY, l = 0.0f;
-    // pass 1 of chunk c: the row's new maximum and the correction of what
-    // came before (keys after the query masked)
-    auto pass1 = [&](int c, float& mx, float& cr) {
-      if (!pt_wait_warp(s_full(c & 1), (uint32_t)((c >> 1) & 1), abort_flag, lane)) return false;
+    float m, l;
+    int qb = 0, tok = 0;
+    // pass 1 of chunk c (overall gc): the row's new maximum and the
+    // correction of what came before; four running maxima (independent
+    // chains); the diagonal chunk's keys after the query are left out
+    auto pass1 = [&](int c, int gc, float& mx, float& cr) {
+      if (!pt_wait_warp(s_full(gc & 1), (uint32_t)((gc >> 1) & 1), abort_flag, lane)) return false;
       ptx::tc_fence_after();
-      const uint32_t ts = tS(c & 1) + lanes;
-      // four running maxima (independent chains); the diagonal chunk's
-      // keys after the query are left out
+      const uint32_t ts = tS(gc & 1) + lanes;
       const int lim = c == qb ? tok - c * PT_KEYS : PT_KEYS;
       float mq[4] = {m, m, m, m};
 #pragma unroll 1
@@ -882,25 +942,23 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
       m = mx;
       return true;
     };
-    // O = O * cr + PV(c), then PV buffer c % 2 is free again
-    auto o_update = [&](int c, float cr) {
-      if (!pt_wait_warp(pv_full(c & 1), (uint32_t)((c >> 1) & 1), abort_flag, lane)) return false;
+    // O = O * cr + PV(gc), then PV buffer gc % 2 is free again
+    auto o_update = [&](int gc, float cr) {
+      if (!pt_wait_warp(pv_full(gc & 1), (uint32_t)((gc >> 1) & 1), abort_flag, lane)) return false;
       ptx::tc_fence_after();
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t r[32];
-        ptx::tmem_ld_32x32b_x32(tPV(c & 1) + lanes + 32 * cc, r);
+        ptx::tmem_ld_32x32b_x32(tPV(gc & 1) + lanes + 32 * cc, r);
         ptx::tmem_wait_ld_dep32(r);
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[32 * cc + i] = __fmaf_rn(o[32 * cc + i], cr, __uint_as_float(r[i]));
       }
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(pv_empty(c & 1));
+      if (lane == 0) ptx::mbar_arrive(pv_empty(gc & 1));
       return true;
     };
-    float mx_c = 0.0f, cr_c = 0.0f, cr_lag = 0.0f;
-    bool ok = nch > 0 && pass1(0, mx_c, cr_c);
     // the weights of 32 keys (one 32-column block of S) as high and low f16
     // parts over the block: columns 0 .. 15 the high parts (two keys per
     // column), 16 .. 31 the low parts; keys past lim weigh 0
@@ -927,45 +985,62 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
         tmem_st_x4(taddr + 16 + 4 * q8, lo[0], lo[1], lo[2], lo[3]);
       }
     };
-    for (int c = 0; c < nch && ok; ++c) {
-      const uint32_t ts = tS(c & 1) + lanes;
-      const int lim = c == qb ? tok - c * PT_KEYS : PT_KEYS;
-      // pass 2: the weights over the row of S(c), four partial sums
-      float psq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t r[32];
-        ptx::tmem_ld_32x32b_x32(ts + 32 * cc, r);
-        ptx::tmem_wait_ld_dep32(r);
-        // tcgen05.st is warp-collective: the choice of path is the warp's
-        if (!__any_sync(0xFFFFFFFFu, lim < 32 * cc + 31))
-          weights(ts + 32 * cc, r, mx_c, 0, psq, std::false_type{});
-        else
-          weights(ts + 32 * cc, r, mx_c, lim - 32 * cc, psq, std::true_type{});
-      }
-      const float ps = (psq[0] + psq[1]) + (psq[2] + psq[3]);
-      l = __fmaf_rn(l, cr_c, ps);
-      tmem_wait_st();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(p_full(c & 1));
-      // one chunk behind: O += PV(c - 1) while the tensor cores compute PV(c)
-      if (c > 0 && !o_update(c - 1, cr_lag)) { ok = false; break; }
-      cr_lag = cr_c;
-      if (c + 1 < nch && !pass1(c + 1, mx_c, cr_c)) { ok = false; break; }
-    }
-    if (ok) ok = o_update(nch - 1, cr_lag);
-    if (ok && tok < seq) {
-      const float f = sv_p[0] / l;
-      uint4* dst = reinterpret_cast<uint4*>(out + (((b * seq + tok) * hq) + h) * (int64_t)AT_D);
+    int g = 0;
+    bool ok = true;
+    PtBlock blk;
+    for (int k = 0; ok && next_block(k, blk); ++k) {
+      qb = blk.qb;
+      tok = qb * PT_ROWS + rrow;
+      const int nch = qb + 1;  // key chunks 0 .. qb; chunk qb is the diagonal
 #pragma unroll
-      for (int v8 = 0; v8 < 16; ++v8) {
-        uint4 w;
-        w.x = (uint32_t)bf16_rn(o[8 * v8 + 0] * f) | ((uint32_t)bf16_rn(o[8 * v8 + 1] * f) << 16);
-        w.y = (uint32_t)bf16_rn(o[8 * v8 + 2] * f) | ((uint32_t)bf16_rn(o[8 * v8 + 3] * f) << 16);
-        w.z = (uint32_t)bf16_rn(o[8 * v8 + 4] * f) | ((uint32_t)bf16_rn(o[8 * v8 + 5] * f) << 16);
-        w.w = (uint32_t)bf16_rn(o[8 * v8 + 6] * f) | ((uint32_t)bf16_rn(o[8 * v8 + 7] * f) << 16);
-        dst[v8] = w;
+      for (int i = 0; i < 128; ++i) o[i] = 0.0f;
+      m = -INFINITY;
+      l = 0.0f;
+      float mx_c = 0.0f, cr_c = 0.0f, cr_lag = 0.0f;
+      ok = pass1(0, g, mx_c, cr_c);
+      for (int c = 0; c < nch && ok; ++c) {
+        const int gc = g + c;
+        const uint32_t ts = tS(gc & 1) + lanes;
+        const int lim = c == qb ? tok - c * PT_KEYS : PT_KEYS;
+        // pass 2: the weights over the row of S(c), four partial sums
+        float psq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t r[32];
+          ptx::tmem_ld_32x32b_x32(ts + 32 * cc, r);
+          ptx::tmem_wait_ld_dep32(r);
+          // tcgen05.st is warp-collective: the choice of path is the warp's
+          if (!__any_sync(0xFFFFFFFFu, lim < 32 * cc + 31))
+            weights(ts + 32 * cc, r, mx_c, 0, psq, std::false_type{});
+          else
+            weights(ts + 32 * cc, r, mx_c, lim - 32 * cc, psq, std::true_type{});
+        }
+        const float ps = (psq[0] + psq[1]) + (psq[2] + psq[3]);
+        l = __fmaf_rn(l, cr_c, ps);
+        tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(p_full(gc & 1));
+        // one chunk behind: O += PV(c - 1) while the tensor cores compute PV(c)
+        if (c > 0 && !o_update(gc - 1, cr_lag)) { ok = false; break; }
+        cr_lag = cr_c;
+        if (c + 1 < nch && !pass1(c + 1, gc + 1, mx_c, cr_c)) { ok = false; break; }
+      }
+      if (ok) ok = o_update(g + nch - 1, cr_lag);
+      g += nch;
+      if (ok && tok < seq) {
+        const float f = fv / l;
+        uint4* dst = reinterpret_cast<uint4*>(
+            out + ((((int64_t)blk.b * seq + tok) * hq) + blk.h) * (int64_t)AT_D);
+#pragma unroll
+        for (int v8 = 0; v8 < 16; ++v8) {
+          uint4 w;
+          w.x = (uint32_t)bf16_rn(o[8 * v8 + 0] * f) | ((uint32_t)bf16_rn(o[8 * v8 + 1] * f) << 16);
+          w.y = (uint32_t)bf16_rn(o[8 * v8 + 2] * f) | ((uint32_t)bf16_rn(o[8 * v8 + 3] * f) << 16);
+          w.z = (uint32_t)bf16_rn(o[8 * v8 + 4] * f) | ((uint32_t)bf16_rn(o[8 * v8 + 5] * f) << 16);
+          w.w = (uint32_t)bf16_rn(o[8 * v8 + 6] * f) | ((uint32_t)bf16_rn(o[8 * v8 + 7] * f) << 16);
+          dst[v8] = w;
+        }
       }
     }
   }
@@ -1002,9 +1077,11 @@ cudaError_t launch_prefill_attention(const uint8_t* q, const float* sq, const ui
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  const dim3 grid((unsigned)nqb, (unsigned)hq, (unsigned)batch);
+  // persistent: one CTA per SM walks its share of the query blocks
+  const int64_t blocks = nqb * hq * batch;
+  const unsigned grid = (unsigned)std::min<int64_t>(blocks, sm_count());
   prefill_attention_kernel<<<grid, PT_THREADS, PT_DYN_SMEM, st>>>(
-      tm_q, tm_k, tm_v, sq, sk, sv, (int)seq, hq, hkv, (int)nqb, softmax_scale, out);
+      tm_q, tm_k, tm_v, sq, sk, sv, (int)seq, hq, hkv, (int)nqb, (int)batch, softmax_scale, out);
   return cudaGetLastError();
 }
 
