@@ -562,14 +562,16 @@ cudaError_t launch_decode_attention(const uint8_t* q, const float* sq, const uin
 //              parts) into PV buffer j % 2;
 //   warps 2-3  widen each V tile to f16, transposed (V^T [dim][key], the
 //              K-major B operand), exactly;
-//   warps 4-7  one query row per thread: the row's maximum over S(j), then
-//              the weights P = 2^15 p (online softmax in log2 units, later
-//              keys masked in the diagonal chunk) as high and low f16 parts
-//              (together 22 bits of each weight), written over the row of
-//              S(j) in tensor memory, where PV(j) reads them; then, one
-//              chunk behind, O = O * correction + PV(j - 1) in FP32
-//              registers, so that PV(j) runs while the next chunk's
-//              weights are formed.
+//   warps 4-11 two threads per query row (one in each of two warps on the
+//              same TMEM lanes), each with half of the keys and half of the
+//              output dims: the row's maximum over S(j) (the pair's partial
+//              maxima exchanged), then the weights P = 2^15 p (online
+//              softmax in log2 units, later keys masked in the diagonal
+//              chunk) as high and low f16 parts (together 22 bits of each
+//              weight), written over the row of S(j) in tensor memory, where
+//              PV(j) reads them; then, one chunk behind,
+//              O = O * correction + PV(j - 1) in FP32 registers, so that
+//              PV(j) runs while the next chunk's weights are formed.
 // The softmax passes keep their 32-column loops rolled: fully unrolled, the
 // loop body outgrew the instruction cache and the kernel ran ~30% slower.
 // Every mbarrier wait is bounded; a wait that gives up records error 23 and
@@ -584,10 +586,11 @@ constexpr int PT_OFF_Q = 0;
 constexpr int PT_OFF_KV = PT_OFF_Q + PT_TILE;                   // stages of (K, V)
 constexpr int PT_OFF_VT = PT_OFF_KV + 2 * PT_STAGES * PT_TILE;  // 2 buffers of V^T f16 (2 halves each)
 constexpr int PT_OFF_BAR = PT_OFF_VT + 4 * PT_HALF;
-constexpr int PT_NBAR = 2 * PT_STAGES + 15;
+constexpr int PT_NBAR = 2 * PT_STAGES + 23;
 constexpr int PT_OFF_MISC = PT_OFF_BAR + PT_NBAR * 8;
-constexpr int PT_DYN_SMEM = PT_OFF_MISC + 16 + 1024;
-constexpr int PT_THREADS = 256;
+constexpr int PT_OFF_X = PT_OFF_MISC + 16;  // row maxima and sums exchanged by warp pairs
+constexpr int PT_DYN_SMEM = PT_OFF_X + 2 * 2 * PT_ROWS * 4 + 1024;
+constexpr int PT_THREADS = 384;
 constexpr uint32_t PT_IDESC = ptx::idesc_e4m3_f32(128, 128);  // also kind::f16 with F16 A, B
 static_assert(PT_OFF_KV % 1024 == 0 && PT_OFF_VT % 1024 == 0,
               "swizzled tiles start on 1024-byte boundaries");
@@ -680,13 +683,15 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
   auto kv_empty = [&](int t) { return bar0 + 8u * (1 + PT_STAGES + t); };  // S commit + 2 converter warps
   const uint32_t bar2 = bar0 + 8u * (1 + 2 * PT_STAGES);  // then pairs, indexed by chunk % 2
   auto s_full = [&](int s) { return bar2 + 8u * (0 + s); };    // S MMA commit
-  auto p_full = [&](int s) { return bar2 + 8u * (2 + s); };    // 4 softmax warps
+  auto p_full = [&](int s) { return bar2 + 8u * (2 + s); };    // 8 softmax warps
   auto vt_full = [&](int s) { return bar2 + 8u * (4 + s); };   // 2 converter warps
   auto vt_empty = [&](int s) { return bar2 + 8u * (6 + s); };  // PV MMA commit
   auto pv_full = [&](int s) { return bar2 + 8u * (8 + s); };   // PV MMA commit
-  auto pv_empty = [&](int s) { return bar2 + 8u * (10 + s); }; // 4 softmax warps
+  auto pv_empty = [&](int s) { return bar2 + 8u * (10 + s); }; // 8 softmax warps
   const uint32_t mma_done = bar2 + 8u * 12;                     // the last MMAs completed
   const uint32_t q_empty = bar2 + 8u * 13;                      // a block's last S MMA completed
+  // exchange e of the softmax warp pair of TMEM lane quarter q: buffer e % 2
+  auto xbar = [&](int e, int q) { return bar2 + 8u * (14 + 4 * (e & 1) + q); };  // 64 threads
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + PT_OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + PT_OFF_MISC + 4);
   auto next_block = [&](int k, PtBlock& blk) {
@@ -702,12 +707,13 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(s_full(s), 1);
-      ptx::mbar_init(p_full(s), 4);
+      ptx::mbar_init(p_full(s), 8);
       ptx::mbar_init(vt_full(s), 2);
       ptx::mbar_init(vt_empty(s), 1);
       ptx::mbar_init(pv_full(s), 1);
-      ptx::mbar_init(pv_empty(s), 4);
+      ptx::mbar_init(pv_empty(s), 8);
     }
+    for (int q = 0; q < 8; ++q) ptx::mbar_init(xbar(q >> 2, q & 3), 64);
     ptx::mbar_init(mma_done, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -906,17 +912,35 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------- softmax
-    const int quarter = warp & 3;
+    // Two warps per TMEM lane quarter: thread rrow of half hf takes keys
+    // 64 hf .. 64 hf + 63 of each chunk of query row rrow and dims
+    // 64 hf .. 64 hf + 63 of its output.  The pair exchanges its partial
+    // row maxima once per chunk and its sums once per block, through shared
+    // memory and an mbarrier per exchange (bounded waits).
+    const int quarter = warp & 3, hf = (warp - 4) >> 2;
     const int rrow = quarter * 32 + lane;  // query row in the block (TMEM lane)
     const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
     const float qk = softmax_scale * sq_p[0] * sk_p[0] * 1.4426950408889634f;
     const float fv = sv_p[0];
-    float o[128];
+    float* xv = reinterpret_cast<float*>(gbase + PT_OFF_X);  // [buffer][half][row]
+    float o[64];
     float m, l;
-    int qb = 0, tok = 0;
+    int qb = 0, tok = 0, ex = 0;
+    // the partner's value of exchange ex (this thread's own is v)
+    auto exchange = [&](float v, float& other) {
+      const int bx = ex & 1;
+      xv[(bx * 2 + hf) * PT_ROWS + rrow] = v;
+      ptx::mbar_arrive(xbar(ex, quarter));  // releases the store above
+      const bool okx = pt_wait(xbar(ex, quarter), (uint32_t)((ex >> 1) & 1), abort_flag);
+      if (!__all_sync(0xFFFFFFFFu, okx)) return false;
+      other = xv[(bx * 2 + (hf ^ 1)) * PT_ROWS + rrow];
+      ++ex;
+      return true;
+    };
     // pass 1 of chunk c (overall gc): the row's new maximum and the
     // correction of what came before; four running maxima (independent
-    // chains); the diagonal chunk's keys after the query are left out
+    // chains) over this half's keys, the diagonal chunk's keys after the
+    // query left out, then the pair's two maxima
     auto pass1 = [&](int c, int gc, float& mx, float& cr) {
       if (!pt_wait_warp(s_full(gc & 1), (uint32_t)((gc >> 1) & 1), abort_flag, lane)) return false;
       ptx::tc_fence_after();
@@ -924,7 +948,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
       const int lim = c == qb ? tok - c * PT_KEYS : PT_KEYS;
       float mq[4] = {m, m, m, m};
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 2 * hf; cc < 2 * hf + 2; ++cc) {
         uint32_t r[32];
         ptx::tmem_ld_32x32b_x32(ts + 32 * cc, r);
         ptx::tmem_wait_ld_dep32(r);
@@ -937,19 +961,23 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
             if (32 * cc + i <= lim) mq[i & 3] = fmaxf(mq[i & 3], __uint_as_float(r[i]) * qk);
         }
       }
-      mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+      const float mh = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+      float mo;
+      if (!exchange(mh, mo)) return false;
+      mx = fmaxf(mh, mo);
       cr = m == mx ? 1.0f : ex2_approx(m - mx);
       m = mx;
       return true;
     };
-    // O = O * cr + PV(gc), then PV buffer gc % 2 is free again
+    // O = O * cr + PV(gc) over this half's dims, then PV buffer gc % 2 is
+    // free again (once both halves have read it)
     auto o_update = [&](int gc, float cr) {
       if (!pt_wait_warp(pv_full(gc & 1), (uint32_t)((gc >> 1) & 1), abort_flag, lane)) return false;
       ptx::tc_fence_after();
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t r[32];
-        ptx::tmem_ld_32x32b_x32(tPV(gc & 1) + lanes + 32 * cc, r);
+        ptx::tmem_ld_32x32b_x32(tPV(gc & 1) + lanes + 64 * hf + 32 * cc, r);
         ptx::tmem_wait_ld_dep32(r);
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[32 * cc + i] = __fmaf_rn(o[32 * cc + i], cr, __uint_as_float(r[i]));
@@ -993,7 +1021,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
       tok = qb * PT_ROWS + rrow;
       const int nch = qb + 1;  // key chunks 0 .. qb; chunk qb is the diagonal
 #pragma unroll
-      for (int i = 0; i < 128; ++i) o[i] = 0.0f;
+      for (int i = 0; i < 64; ++i) o[i] = 0.0f;
       m = -INFINITY;
       l = 0.0f;
       float mx_c = 0.0f, cr_c = 0.0f, cr_lag = 0.0f;
@@ -1002,10 +1030,11 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
         const int gc = g + c;
         const uint32_t ts = tS(gc & 1) + lanes;
         const int lim = c == qb ? tok - c * PT_KEYS : PT_KEYS;
-        // pass 2: the weights over the row of S(c), four partial sums
+        // pass 2: the weights over this half of the row of S(c), four
+        // partial sums
         float psq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 2 * hf; cc < 2 * hf + 2; ++cc) {
           uint32_t r[32];
           ptx::tmem_ld_32x32b_x32(ts + 32 * cc, r);
           ptx::tmem_wait_ld_dep32(r);
@@ -1028,12 +1057,14 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
       }
       if (ok) ok = o_update(g + nch - 1, cr_lag);
       g += nch;
+      float lo_sum = 0.0f;
+      if (ok) ok = exchange(l, lo_sum);
       if (ok && tok < seq) {
-        const float f = fv / l;
+        const float f = fv / (l + lo_sum);
         uint4* dst = reinterpret_cast<uint4*>(
-            out + ((((int64_t)blk.b * seq + tok) * hq) + blk.h) * (int64_t)AT_D);
+            out + ((((int64_t)blk.b * seq + tok) * hq) + blk.h) * (int64_t)AT_D + 64 * hf);
 #pragma unroll
-        for (int v8 = 0; v8 < 16; ++v8) {
+        for (int v8 = 0; v8 < 8; ++v8) {
           uint4 w;
           w.x = (uint32_t)bf16_rn(o[8 * v8 + 0] * f) | ((uint32_t)bf16_rn(o[8 * v8 + 1] * f) << 16);
           w.y = (uint32_t)bf16_rn(o[8 * v8 + 2] * f) | ((uint32_t)bf16_rn(o[8 * v8 + 3] * f) << 16);
