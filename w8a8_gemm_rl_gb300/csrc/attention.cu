@@ -939,14 +939,16 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
     };
     // pass 1 of chunk c (overall gc): the row's new maximum and the
     // correction of what came before; four running maxima (independent
-    // chains) over this half's keys, the diagonal chunk's keys after the
-    // query left out, then the pair's two maxima
+    // chains) of this half's raw scores, the diagonal chunk's keys after the
+    // query left out, scaled once (rounding is monotone and qk >= 0, so this
+    // is the maximum of the scaled scores; an empty half gives NaN, which
+    // fmaxf passes over), then the pair's two maxima
     auto pass1 = [&](int c, int gc, float& mx, float& cr) {
       if (!pt_wait_warp(s_full(gc & 1), (uint32_t)((gc >> 1) & 1), abort_flag, lane)) return false;
       ptx::tc_fence_after();
       const uint32_t ts = tS(gc & 1) + lanes;
       const int lim = c == qb ? tok - c * PT_KEYS : PT_KEYS;
-      float mq[4] = {m, m, m, m};
+      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
       for (int cc = 2 * hf; cc < 2 * hf + 2; ++cc) {
         uint32_t r[32];
@@ -954,14 +956,14 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
         ptx::tmem_wait_ld_dep32(r);
         if (!__any_sync(0xFFFFFFFFu, lim < 32 * cc + 31)) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mq[i & 3] = fmaxf(mq[i & 3], __uint_as_float(r[i]) * qk);
+          for (int i = 0; i < 32; ++i) mq[i & 3] = fmaxf(mq[i & 3], __uint_as_float(r[i]));
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if (32 * cc + i <= lim) mq[i & 3] = fmaxf(mq[i & 3], __uint_as_float(r[i]) * qk);
+            if (32 * cc + i <= lim) mq[i & 3] = fmaxf(mq[i & 3], __uint_as_float(r[i]));
         }
       }
-      const float mh = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+      const float mh = fmaxf(m, fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * qk);
       float mo;
       if (!exchange(mh, mo)) return false;
       mx = fmaxf(mh, mo);
@@ -989,8 +991,9 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
     };
     // the weights of 32 keys (one 32-column block of S) as high and low f16
     // parts over the block: columns 0 .. 15 the high parts (two keys per
-    // column), 16 .. 31 the low parts; keys past lim weigh 0
-    auto weights = [&](uint32_t taddr, const uint32_t (&r)[32], float mxc, int lim,
+    // column), 16 .. 31 the low parts; keys past lim weigh 0.  bias is
+    // log2(2^15) minus the row's maximum.
+    auto weights = [&](uint32_t taddr, const uint32_t (&r)[32], float bias, int lim,
                        float (&psq)[4], auto masked) {
 #pragma unroll
       for (int q8 = 0; q8 < 4; ++q8) {  // 8 keys: 4 columns of each part
@@ -1001,7 +1004,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int i = 8 * q8 + 2 * e + u;
-            pv[u] = ex2_approx(__uint_as_float(r[i]) * qk - mxc + AT_P_LOG2);
+            pv[u] = ex2_approx(__fmaf_rn(__uint_as_float(r[i]), qk, bias));
             if (decltype(masked)::value && i > lim) pv[u] = 0.0f;
             psq[e] += pv[u];
           }
@@ -1033,6 +1036,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
         // pass 2: the weights over this half of the row of S(c), four
         // partial sums
         float psq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        const float bias = AT_P_LOG2 - mx_c;
 #pragma unroll 1
         for (int cc = 2 * hf; cc < 2 * hf + 2; ++cc) {
           uint32_t r[32];
@@ -1040,9 +1044,9 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
           ptx::tmem_wait_ld_dep32(r);
           // tcgen05.st is warp-collective: the choice of path is the warp's
           if (!__any_sync(0xFFFFFFFFu, lim < 32 * cc + 31))
-            weights(ts + 32 * cc, r, mx_c, 0, psq, std::false_type{});
+            weights(ts + 32 * cc, r, bias, 0, psq, std::false_type{});
           else
-            weights(ts + 32 * cc, r, mx_c, lim - 32 * cc, psq, std::true_type{});
+            weights(ts + 32 * cc, r, bias, lim - 32 * cc, psq, std::true_type{});
         }
         const float ps = (psq[0] + psq[1]) + (psq[2] + psq[3]);
         l = __fmaf_rn(l, cr_c, ps);
