@@ -873,7 +873,8 @@ def measure_prefill_attention(W, peaks, reps=10):
     return {"workload": "4 sequences x 2048 tokens, causal, 32 query heads over 8 KV heads, "
                         "head dim 128", "us": round(sec * 1e6, 1), "tflops": round(tf, 1),
             "pct_roofline": round(100 * tf / fp8_peak_tflops(peaks), 2), "flops_per_call": f,
-            "note": "mma.sync tensor path (E4M3 Q K^T, f16 P V with two-part weights)"}
+            "note": "tcgen05 path: E4M3 Q K^T and two-part f16 P V into tensor memory, "
+                    "persistent CTAs over 128-token query blocks"}
 
 
 def single_linear_work():

@@ -132,14 +132,16 @@ def _dropped_bound(v, sv, hq):
     return abs(sv) * 2.0 ** -39 * cum[..., None]
 
 PREFILL_CASES = [  # batch, tokens per sequence, q heads, kv heads
-    (1, 1, 4, 4), (2, 63, 8, 2), (1, 64, 4, 1), (2, 65, 4, 4), (1, 200, 8, 2),
-    (3, 130, 32, 8), (1, 700, 8, 8)]
+    (1, 1, 4, 4), (2, 63, 8, 2), (1, 64, 4, 1), (2, 65, 4, 4), (1, 128, 4, 2), (2, 129, 8, 8),
+    (1, 200, 8, 2), (1, 256, 4, 4), (3, 130, 32, 8), (1, 700, 8, 8),
+    (2, 520, 16, 4)]  # 160 query blocks: some CTAs take two
 
 
 @pytest.mark.parametrize("B,S,Hq,Hkv", PREFILL_CASES)
 def test_prefill_attention_matches_oracle(W, B, S, Hq, Hkv):
     """Causal prefill over random E4M3 codes (every finite code): a single
-    token, partial and whole 64-token query blocks, grouped heads."""
+    token, partial and whole 128-token query blocks and key chunks, grouped
+    heads, more query blocks than SMs (a persistent CTA takes several)."""
     g = torch.Generator().manual_seed(B * 100 + S + Hq)
     q, k, v = _codes((B, S, Hq, 128), g), _codes((B, S, Hkv, 128), g), _codes((B, S, Hkv, 128), g)
     scales = torch.tensor([0.02, 0.03, 0.5], dtype=torch.float32)
@@ -172,3 +174,28 @@ def test_prefill_attention_over_quantized_activations(W):
     drop = _dropped_bound(qkv[2][0].cpu().numpy(), sc[2], Hq)
     _check(out, ref, ab, 1e-3, drop)
     _check(out, ref, ab, 2.0 ** -14, drop)
+
+
+def test_prefill_attention_full_size_sampled(W):
+    """The bench's workload and launch: 4 sequences x 2048 tokens, 32 query
+    heads over 8 KV heads, Q, K and V per-tensor-quantized N(0, 1)
+    activations with outliers (the same seeds).  The oracle computes sampled
+    (sequence, query head) slices one by one: first and last, and heads of
+    different KV groups."""
+    B, S, Hq, Hkv = 4, 2048, 32, 8
+    x = [synth.activations(B * S * h, 128, seed=95 + i, device="cuda").reshape(B, S, h, 128)
+         for i, h in enumerate((Hq, Hkv, Hkv))]
+    qkv = [W.kv_amax_quantize(t) for t in x]
+    out = W.fp8_prefill_attention(qkv[0][0], qkv[0][1], qkv[1][0], qkv[1][1], qkv[2][0], qkv[2][1])
+    torch.cuda.synchronize()
+    assert W.consume_device_error() == 0
+    sc = [t[1].item() for t in qkv]
+    q, k, v = (t[0].cpu().numpy() for t in qkv)
+    for b, h in [(0, 0), (1, 13), (2, 22), (3, 31)]:
+        kh = h // (Hq // Hkv)
+        qs, ks, vs = (np.ascontiguousarray(a[b:b + 1, :, j:j + 1]) for a, j in ((q, h), (k, kh), (v, kh)))
+        ref, ab = O.prefill_attention(qs, sc[0], ks, sc[1], vs, sc[2], 1 / math.sqrt(128))
+        drop = _dropped_bound(vs, sc[2], 1)
+        got = out[b:b + 1, :, h:h + 1].contiguous()
+        _check(got, ref, ab, 1e-3, drop)
+        _check(got, ref, ab, 2.0 ** -14, drop)
