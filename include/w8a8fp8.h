@@ -79,11 +79,13 @@ const char *w8a8_last_cuda_error(void);
 w8a8_status w8a8_consume_device_error(int *code);
 
 /* Test hook for the abort paths: while `on` is nonzero, every later launch
- * of the GEMMs and of the weight quantizer behaves as if one of its bounded
- * waits had run out of time at once (the GEMMs' MMA issuer before its first
- * slab: code 5, 35 for m <= 256, 55 for fp8_block_gemm_pow2; the weight
- * quantizer's consumers on
- * their first block: code 13).  The kernel then stops as it would after a
+ * of the GEMMs, of the weight quantizer and of the attention kernels
+ * behaves as if one of its bounded waits had run out of time at once (the
+ * GEMMs' MMA issuer before its first slab: code 5, 35 for m <= 256, 55 for
+ * fp8_block_gemm_pow2; the weight quantizer's consumers on their first
+ * block: code 13; each warp of fp8_decode_attention on its first chunk:
+ * code 21; the MMA issuer of fp8_prefill_attention before its first MMA:
+ * code 23).  The kernel then stops as it would after a
  * real time-out -- the other roles stop, copies and MMAs in flight are
  * drained, tensor memory is freed -- and its output is incomplete.  Nothing
  * faults or hangs.  Synchronous; call with 0 to return to normal. */

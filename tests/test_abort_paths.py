@@ -7,8 +7,10 @@ import numpy as np
 import pytest
 import torch
 
+import math
+
 import oracle as O
-from parity_util import assert_gemm_close, bits16
+from parity_util import assert_gemm_close, bf16_to_f64, bits16, ulp_bf16
 from w8a8_gemm_rl_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -103,3 +105,73 @@ def test_weight_quant_abort_then_recover(W):
     assert W.consume_device_error() == 0
     wq_ref, ws_ref = O.quantize_weight_blockwise(synth.bf16_bits(w))
     assert (wq.cpu().numpy() == wq_ref).all() and (ws.cpu().numpy() == ws_ref).all()
+
+
+def _attention_case(B, S, Hq, Hkv, seed, query_tokens):
+    g = torch.Generator().manual_seed(seed)
+
+    def codes(shape):
+        c = torch.randint(0, 256, shape, generator=g, dtype=torch.int32)
+        c[(c & 0x7F) == 0x7F] = 0x7E  # every finite E4M3 code
+        return c.to(torch.uint8)
+
+    q = codes((B, S, Hq, 128) if query_tokens else (B, Hq, 128))
+    return q, codes((B, S, Hkv, 128)), codes((B, S, Hkv, 128)), [0.02, 0.03, 0.5]
+
+
+def _attention_close(out, ref, ab, dropped):
+    """The documented accuracy: 1e-3 * sv * sum p |dec(v)| plus half a BF16
+    ulp plus what the weights f16 cannot hold (below 2^-39 of a row's
+    largest) can carry."""
+    got = bf16_to_f64(bits16(out)).reshape(ref.shape)
+    bad = np.abs(got - ref) > 1e-3 * ab + 0.5 * ulp_bf16(ref) + dropped
+    assert not bad.any(), int(bad.sum())
+
+
+def _vmax(v):
+    return np.abs(O.e4m3_decode(v.numpy())).max(axis=3)  # [B, S, Hkv]
+
+
+def test_decode_attention_abort_then_recover(W):
+    q, k, v, sc = _attention_case(2, 300, 8, 2, seed=21, query_tokens=False)
+    lens = torch.tensor([300, 123], dtype=torch.int32)
+    dev = [t.cuda() for t in (q, k, v, lens)] + [torch.tensor([x]).cuda() for x in sc]
+    args = (dev[0], dev[4], dev[1], dev[5], dev[2], dev[6], dev[3])
+    assert W.consume_device_error() == 0
+    W.debug_force_wait_timeout(True)
+    try:
+        W.fp8_decode_attention(*args)
+        torch.cuda.synchronize()
+    finally:
+        W.debug_force_wait_timeout(False)
+    assert W.consume_device_error() == 21
+    out = W.fp8_decode_attention(*args)
+    torch.cuda.synchronize()
+    assert W.consume_device_error() == 0
+    ref, ab = O.decode_attention(q.numpy(), sc[0], k.numpy(), sc[1], v.numpy(), sc[2],
+                                 lens.numpy(), 1 / math.sqrt(128))
+    vm = _vmax(v)
+    per_bh = np.stack([vm[b, :L].sum(axis=0) for b, L in enumerate(lens.tolist())])  # [B, Hkv]
+    dropped = sc[2] * 2.0 ** -39 * np.repeat(per_bh, 4, axis=1)[..., None]  # [B, Hq, 1]
+    _attention_close(out, ref, ab, dropped)
+
+
+def test_prefill_attention_abort_then_recover(W):
+    q, k, v, sc = _attention_case(2, 300, 8, 2, seed=23, query_tokens=True)
+    dev = [t.cuda() for t in (q, k, v)] + [torch.tensor([x]).cuda() for x in sc]
+    args = (dev[0], dev[3], dev[1], dev[4], dev[2], dev[5])
+    assert W.consume_device_error() == 0
+    W.debug_force_wait_timeout(True)
+    try:
+        W.fp8_prefill_attention(*args)
+        torch.cuda.synchronize()
+    finally:
+        W.debug_force_wait_timeout(False)
+    assert W.consume_device_error() == 23
+    out = W.fp8_prefill_attention(*args)
+    torch.cuda.synchronize()
+    assert W.consume_device_error() == 0
+    ref, ab = O.prefill_attention(q.numpy(), sc[0], k.numpy(), sc[1], v.numpy(), sc[2],
+                                  1 / math.sqrt(128))
+    cum = np.repeat(np.cumsum(_vmax(v), axis=1), 4, axis=2)  # keys 0..i, per query head
+    _attention_close(out, ref, ab, sc[2] * 2.0 ** -39 * cum[..., None])

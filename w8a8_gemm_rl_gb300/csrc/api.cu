@@ -17,6 +17,7 @@ cudaError_t set_pow2_gemm_force_timeout(int on);
 cudaError_t set_gemm_force_timeout(int on);
 cudaError_t set_small_gemm_force_timeout(int on);
 cudaError_t set_quant_force_timeout(int on);
+cudaError_t set_attn_force_timeout(int on);
 cudaError_t consume_batch_error(int* code);
 cudaError_t consume_quant_error(int* code);
 cudaError_t consume_attention_error(int* code);
@@ -456,6 +457,8 @@ W8A8_API w8a8_status w8a8_debug_force_wait_timeout(int on) {
   st = from_cuda(w8a8::set_small_gemm_force_timeout(v));
   if (st != W8A8_OK) return st;
   st = from_cuda(w8a8::set_pow2_gemm_force_timeout(v));
+  if (st != W8A8_OK) return st;
+  st = from_cuda(w8a8::set_attn_force_timeout(v));
   if (st != W8A8_OK) return st;
   return from_cuda(w8a8::set_quant_force_timeout(v));
 }

@@ -47,10 +47,20 @@
 
 namespace w8a8 {
 
-// Set (first code wins) when a bounded wait of the decode attention kernel
-// gives up: 21 = a chunk's TMA loads did not land in time, 22 = the drain
-// of the loads still in flight after that also timed out.
+// Set (first code wins) when a bounded wait of an attention kernel gives
+// up: 21 = a decode chunk's TMA loads did not land in time, 22 = the drain
+// of the loads still in flight after that also timed out, 23 = a wait of
+// the prefill kernel.
 __device__ int g_w8a8_attn_error = 0;
+
+// Test hook (w8a8_debug_force_wait_timeout): when set, each decode warp's
+// wait for its first chunk, and the prefill MMA issuer before its first
+// MMA, behave as if they had run out of time.
+__device__ int g_w8a8_attn_force_timeout = 0;
+
+cudaError_t set_attn_force_timeout(int on) {
+  return cudaMemcpyToSymbol(g_w8a8_attn_force_timeout, &on, sizeof(int));
+}
 
 cudaError_t consume_attention_error(int* code) {
   int v = 0;
@@ -267,7 +277,8 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
   bool ok = true;
   for (; c < nch; ++c) {
     const int s = c % AT_STAGES;
-    const bool landed = ptx::mbar_wait(bar0 + s * 8, (uint32_t)(c / AT_STAGES) & 1u, AT_WAIT_LIMIT_NS);
+    bool landed = ptx::mbar_wait(bar0 + s * 8, (uint32_t)(c / AT_STAGES) & 1u, AT_WAIT_LIMIT_NS);
+    if (c == 0 && *reinterpret_cast<volatile int*>(&g_w8a8_attn_force_timeout) != 0) landed = false;
     if (!__all_sync(0xFFFFFFFFu, landed)) {
       ok = false;
       break;
@@ -775,6 +786,11 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
     // ------------------------------------------------------------------ MMA
     if (lane == 0) {
       bool ok = true;
+      if (*reinterpret_cast<volatile int*>(&g_w8a8_attn_force_timeout) != 0) {
+        atomicCAS(&g_w8a8_attn_error, 0, 23);
+        *abort_flag = 1;
+        ok = false;
+      }
       const uint64_t qdesc = ptx::smem_desc_kmajor_sw128(base + PT_OFF_Q);
       // S cursor: block ks, its chunk cs, overall chunk gs
       int ks = 0, cs = 0, gs = 0;
@@ -803,7 +819,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
       int kp = 0, cp = 0, gp = 0;
       PtBlock bp;
       bool p_more = next_block(0, bp);
-      if (s_more) ok = issue_s();
+      if (ok && s_more) ok = issue_s();
       if (ok && s_more) ok = issue_s();
       while (ok && p_more) {
         // PV(gp): the weights of chunk gp in S buffer s, V^T widened, PV
