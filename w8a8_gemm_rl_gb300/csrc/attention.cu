@@ -235,6 +235,8 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
     ptx::tma_load_2d(st, &tm_k, bar, x0, row0 + c * AT_CHUNK);
     ptx::tma_load_2d(st + AT_TILE, &tm_v, bar, x0, row0 + c * AT_CHUNK);
   };
+  // the test hook, read while the first loads are in flight
+  const bool force_timeout = *reinterpret_cast<volatile int*>(&g_w8a8_attn_force_timeout) != 0;
   if (lane == 0) {
 #pragma unroll
     for (int s = 0; s < AT_STAGES; ++s) ptx::mbar_init(bar0 + s * 8, 1);
@@ -278,7 +280,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
   for (; c < nch; ++c) {
     const int s = c % AT_STAGES;
     bool landed = ptx::mbar_wait(bar0 + s * 8, (uint32_t)(c / AT_STAGES) & 1u, AT_WAIT_LIMIT_NS);
-    if (c == 0 && *reinterpret_cast<volatile int*>(&g_w8a8_attn_force_timeout) != 0) landed = false;
+    if (c == 0 && force_timeout) landed = false;
     if (!__all_sync(0xFFFFFFFFu, landed)) {
       ok = false;
       break;
