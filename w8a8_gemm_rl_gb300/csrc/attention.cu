@@ -564,8 +564,9 @@ cudaError_t launch_decode_attention(const uint8_t* q, const float* sq, const uin
 // (sequence, query head); keys come in chunks of 128 tokens, so chunk qb of
 // block qb is the diagonal one.  The kernel is persistent: one CTA per SM
 // takes its share of the blocks in turn, longest (most keys) first.
-//   warp 0     TMA: the Q tile once, then K and V tiles (E4M3, 128-byte
-//              swizzle) into a 3-stage ring;
+//   warp 0     TMA: each block's Q tile (once the previous block's S MMAs
+//              are done with the buffer), then its K and V tiles (E4M3,
+//              128-byte swizzle) into a 3-stage ring;
 //   warp 1     allocates 512 TMEM columns: two S buffers, two PV buffers.
 //              Lane 0 issues S(j) = Q K_j^T on the raw E4M3 codes
 //              (kind::f8f6f4, M = 128 queries, N = 128 keys, f32
@@ -590,7 +591,7 @@ cudaError_t launch_decode_attention(const uint8_t* q, const float* sq, const uin
 // Every mbarrier wait is bounded; a wait that gives up records error 23 and
 // stops the CTA's roles.
 namespace {
-constexpr int PT_ROWS = 128;                        // query tokens per CTA
+constexpr int PT_ROWS = 128;                        // query tokens per block
 constexpr int PT_KEYS = 128;                        // keys per chunk
 constexpr int PT_TILE = PT_KEYS * AT_D;             // 16 KB: a Q, K or V tile (E4M3)
 constexpr int PT_HALF = 128 * 128;                  // 16 KB: 128 rows x 64 f16 (128 bytes)
